@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Throughput of the ReplaySSM decode path on GB300.
+
+Workload: one Mamba-2-shaped SSM layer. B=256 sequences, H=128 value heads,
+P=64, N=128 (a 4 MiB FP32 checkpoint per sequence), G=8 groups, window L=16,
+bf16 v/k/q. One bench step is one full window of L decode launches over the
+batch: L-1 non-flush steps plus the flush step. The metric is seq-steps/s,
+that is, (sequence, decode step) pairs per second.
+
+Prints one JSON line. Keys beyond the driver contract:
+  roofline      achieved HBM GB/s of the decode kernel (algorithmic bytes per
+                launch / mean launch time from CUDA events on its stream)
+                against the measured copy bandwidth
+  cpu_baseline  the float64 CPU oracle on a bounded sample of the same workload
+  e2e           the same metric with inputs copied from pinned host memory and
+                outputs copied back inside the timed region
+  comparison    the conventional read-update-write kernel on the same workload
+
+`--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "SSM decode seq-steps/s at B=256, L=16; achieved HBM GB/s vs GB300 peak"
+UNIT = "seq-steps/s"
+WORKLOAD = synth.PRESETS["mamba2_layer_b256_l16"]
+FALLBACK_HBM_GBS = 6800.0
+DECODE_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_decode.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_step_b256_l16.md")
+
+
+# ----------------------------------------------------------------- analytic bytes
+def record_bytes(s) -> int:
+    """Bytes of one input record (alpha, v, k) of one sequence."""
+    es = 2 if s.in_dtype == "bf16" else 4
+    return 4 * s.H + es * s.H * s.P + es * s.G * s.N
+
+
+def window_bytes(s) -> dict:
+    """Algorithmic HBM bytes of one sequence over one window of L decode steps.
+
+    Each step reads the checkpoint |S| and its inputs (record + q) and writes its
+    output. Step t of the window (t = 0..L-1) also reads the t buffered records,
+    and every non-flush step appends its record. The flush step writes the
+    checkpoint once.
+    """
+    es = 2 if s.in_dtype == "bf16" else 4
+    S = 4 * s.H * s.P * s.N
+    r = record_bytes(s)
+    inp = r + es * s.G * s.N
+    out = 4 * s.H * s.P
+    L = s.L
+    total = L * S + S + r * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * r
+    conv = L * (2 * S + inp + out)
+    return {"replay_window": total, "replay_per_seq_step": total / L, "conventional_per_seq_step": conv / L,
+            "state": S}
+
+
+# ----------------------------------------------------------------- environment
+def measured_peak_gbs() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic() -> float | None:
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on this kernel source."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict | None:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (every rank gets it)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+def time_oracle(shape, n_seq: int, n_steps: int, seed: int = 0) -> tuple[float, int]:
+    """Seconds for n_steps conventional float64 steps of the oracle on n_seq sequences."""
+    import oracle
+    s = shape.with_(B=n_seq)
+    gen = synth.make_generator(seed)
+    S = oracle.to_f64(synth.initial_state(s, gen))
+    steps = [tuple(oracle.to_f64(x) for x in synth.decode_step_inputs(s, gen)) for _ in range(min(n_steps, 4))]
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        S, o = oracle.conventional_step(S, *steps[i % len(steps)])
+    return time.perf_counter() - t0, n_seq * n_steps
+
+
+def cpu_baseline_line(shape, budget_s: float = 12.0) -> dict:
+    n_seq = 4
+    t, units = time_oracle(shape, n_seq, 2)  # calibrate
+    per_step = t / 2
+    steps = max(4, int(budget_s / max(per_step, 1e-6)))
+    t, units = time_oracle(shape, n_seq, steps)
+    return {"value": units / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"float64 conventional recurrence, {n_seq} of {shape.B} sequences x all {shape.H} heads, "
+                      f"{steps} steps ({t:.1f} s); numpy elementwise, one thread"}
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args, world, rank, local):
+    from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM, conventional_step
+
+    torch.cuda.set_device(local)
+    s = WORKLOAD
+    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(s.seed + 1000 * rank)
+    ckpt = (torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev, dtype=torch.float32) * 0.1)
+    model = ReplaySSM(ls, ckpt)
+    pool = []
+    sc = 1.0 / math.sqrt(s.N)
+    for _ in range(16):  # 16 resident steps of inputs, cycled
+        u = torch.randn((s.B, s.H), generator=gen, device=dev)
+        alpha = torch.exp(-torch.nn.functional.softplus(u)).float()
+        v = (torch.randn((s.B, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
+        k = (torch.randn((s.B, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
+        q = (torch.randn((s.B, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
+        pool.append((alpha, v, k, q))
+    out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=dev)
+    L = s.L
+
+    def window(i0: int, ev: list | None = None):
+        for j in range(L):
+            a, v, k, q = pool[(i0 + j) % len(pool)]
+            if ev is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                model.decode_step(a, v, k, q, out=out)
+                e1.record(stream)
+                ev.append((e0, e1))
+            else:
+                model.decode_step(a, v, k, q, out=out)
+
+    # warm-up (whole windows keep every sequence aligned on the window)
+    for w in range(args.warmup):
+        window(w * L)
+    torch.cuda.synchronize()
+    model.read_pointers()  # raises on any device error
+
+    # timed region: K windows
+    evs: list = []
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            window(i * L, evs)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed = t0.elapsed_time(t1) / 1e3
+    launch_s = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    start, count, err = model.read_pointers()
+    elapsed_max = max_over_ranks(elapsed, world)
+    seq_steps = world * s.B * L * args.steps
+    value = seq_steps / elapsed_max
+    mean_launch = sum(launch_s) / len(launch_s)
+    wb = window_bytes(s)
+    alg_bytes_launch = wb["replay_per_seq_step"] * s.B
+    achieved = alg_bytes_launch / mean_launch / 1e9
+    peak, peak_kind = measured_peak_gbs()
+
+    # flush launch vs non-flush launches (launch index within the window)
+    flush_s = [launch_s[i] for i in range(len(launch_s)) if i % L == L - 1]
+    nonflush_s = [launch_s[i] for i in range(len(launch_s)) if i % L != L - 1]
+
+    # in-run comparison: the conventional kernel on the same workload
+    comp = None
+    if not args.no_conventional:
+        state = ckpt.clone()
+        n_conv = max(1, min(args.steps, 50))
+        for i in range(L):
+            a, v, k, q = pool[i % len(pool)]
+            conventional_step(ls, state, a, v, k, q, out=out)
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(n_conv * L):
+            a, v, k, q = pool[i % len(pool)]
+            conventional_step(ls, state, a, v, k, q, out=out)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        conv_t = c0.elapsed_time(c1) / 1e3
+        conv_value = s.B * L * n_conv / conv_t
+        conv_bytes = wb["conventional_per_seq_step"] * s.B * L * n_conv
+        comp = {"conventional_seq_steps_per_s": conv_value,
+                "conventional_hbm_gbs": conv_bytes / conv_t / 1e9,
+                "replay_speedup": value / world / conv_value,
+                "replay_state_bytes_per_window_over_conventional": (L + 1) / (2 * L),
+                "windows_timed": n_conv}
+        del state
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_pool = [tuple(x.cpu().pin_memory() for x in step) for step in pool]
+        dpool = [tuple(torch.empty_like(x) for x in step) for step in pool[:2]]
+        host_out = torch.empty((s.B, s.H, s.P), dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host_pool[0])
+        d2h = host_out.numel() * host_out.element_size()
+        n_e2e = max(1, min(args.steps, 60))
+        torch.cuda.synchronize()
+        barrier(world)
+        tw0 = time.perf_counter()
+        for i in range(n_e2e * L):
+            hs = host_pool[i % len(host_pool)]
+            ds = dpool[i % 2]
+            for d, h in zip(ds, hs):
+                d.copy_(h, non_blocking=True)
+            model.decode_step(*ds, out=out)
+            host_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        tw = max_over_ranks(time.perf_counter() - tw0, world)
+        e2e = {"value": world * s.B * L * n_e2e / tw, "unit": UNIT, "h2d_bytes_per_step": h2d * L,
+               "d2h_bytes_per_step": d2h * L, "windows_timed": n_e2e,
+               "note": "pinned host inputs copied in and outputs copied out every decode step, one stream"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_line(s)
+
+    if rank != 0:
+        return None
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"ReplaySSM decode, one Mamba-2-shaped layer: B={s.B} H={s.H} P={s.P} N={s.N} "
+                               f"G={s.G} L={L}, bf16 v/k/q, fp32 checkpoint and outputs; one step = one window "
+                               f"of {L} decode launches ({L - 1} non-flush + 1 flush)",
+                   "global_batch": s.B * world, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush needed: the 1 GiB checkpoint per replica is 8x the 129 MB L2",
+                   "inputs": "16 resident steps of seeded inputs, cycled"},
+        "hbm_gbs_achieved": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": alg_bytes_launch,
+                     "mean_launch_ms": mean_launch * 1e3,
+                     "mean_nonflush_launch_ms": 1e3 * sum(nonflush_s) / max(1, len(nonflush_s)),
+                     "mean_flush_launch_ms": 1e3 * sum(flush_s) / max(1, len(flush_s)),
+                     "frac_of_nominal_8tbs": achieved / 8000.0},
+        "comparison": comp,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": len(evs),
+        "device_error_word": err,
+    }
+    return line
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step is one window of L decode
+    steps on a sample of the batch (rank 0 only)."""
+    if rank != 0:
+        return None
+    s = WORKLOAD
+    import oracle
+    n_seq = 2
+    sub = s.with_(B=n_seq)
+    gen = synth.make_generator(s.seed)
+    S = oracle.to_f64(synth.initial_state(sub, gen))
+    steps = [tuple(oracle.to_f64(x) for x in synth.decode_step_inputs(sub, gen)) for _ in range(4)]
+    for w in range(args.warmup):
+        for j in range(s.L):
+            S, _ = oracle.conventional_step(S, *steps[j % 4])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        for j in range(s.L):
+            S, _ = oracle.conventional_step(S, *steps[j % 4])
+    t = time.perf_counter() - t0
+    value = n_seq * s.L * args.steps / t
+    sample = (f"float64 oracle (conventional recurrence), {n_seq} of {s.B} sequences x {s.H} heads, "
+              f"one window of {s.L} decode steps per bench step")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"ReplaySSM decode, B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
+                                   f"(oracle sample of {n_seq} sequences)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300, help="timed windows of L decode steps")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-conventional", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,388 @@
+// rssm_api.cu - the C ABI of librssm.so (declared in include/rssm.h).
+//
+// Host side only: it validates arguments, derives buffer layouts and launch
+// shapes, and enqueues kernels on the caller's stream. It never allocates
+// device memory. Errors are returned as rssm_status. The message is kept per
+// thread for rssm_last_error().
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "../../include/rssm.h"
+#include "rssm_launch.cuh"
+
+namespace {
+
+thread_local std::string g_msg = "no error";
+
+rssm_status fail(rssm_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
+rssm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RSSM_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Geom {
+  int R = 0, Rp = 0, esize = 0;
+  size_t v_off = 0, k_off = 0, ring_bytes = 0;
+  size_t off_count = 0, off_ticket = 0, off_err = 0, ptr_bytes = 0;
+  size_t head_stride = 0, bsc_off = 0, rsc_off = 0, copy_bytes = 0;
+};
+
+// Validate a configuration and derive the buffer layouts.
+rssm_status derive(const rssm_config* c, Geom* g) {
+  if (!c) return fail(RSSM_EINVAL, "config is NULL");
+  if (c->B < 1 || c->H < 1 || c->P < 1 || c->N < 1 || c->G < 1 || c->L < 1 || c->T_max < 1)
+    return fail(RSSM_EINVAL, "sizes must be positive (B=%d H=%d P=%d N=%d G=%d L=%d T_max=%d)", c->B, c->H,
+                c->P, c->N, c->G, c->L, c->T_max);
+  if (c->H % c->G) return fail(RSSM_EINVAL, "H=%d is not a multiple of G=%d", c->H, c->G);
+  if (c->in_dtype != RSSM_F32 && c->in_dtype != RSSM_BF16) return fail(RSSM_EINVAL, "in_dtype %d", c->in_dtype);
+  if (c->read_fmt < RSSM_READ_NONE || c->read_fmt > RSSM_READ_E2M1_B16)
+    return fail(RSSM_EINVAL, "read_fmt %d", c->read_fmt);
+  if (c->N != 16 && c->N != 32 && c->N != 64 && c->N != 128)
+    return fail(RSSM_EUNSUPPORTED, "N=%d (supported: 16, 32, 64, 128)", c->N);
+  if (c->P % 8) return fail(RSSM_EUNSUPPORTED, "P=%d must be a multiple of 8", c->P);
+  if ((size_t)c->P * c->N * 4 > 64 * 1024) return fail(RSSM_EUNSUPPORTED, "P*N*4 > 64 KiB");
+  if (c->T_max > rssm::kTMax) return fail(RSSM_EUNSUPPORTED, "T_max=%d > %d", c->T_max, rssm::kTMax);
+  const int R = c->L + c->T_max - 1;
+  if (R > rssm::kRMax) return fail(RSSM_EUNSUPPORTED, "R = L + T_max - 1 = %d > %d", R, rssm::kRMax);
+  if (c->read_fmt != RSSM_READ_NONE && c->N < 64)
+    return fail(RSSM_EUNSUPPORTED, "read copies need N in {64, 128}");
+  if ((long long)c->B * c->H > (1ll << 30)) return fail(RSSM_EUNSUPPORTED, "B*H too large");
+  g->R = R;
+  g->Rp = (R + 3) / 4 * 4;
+  g->esize = c->in_dtype == RSSM_F32 ? 4 : 2;
+  const size_t B = c->B, H = c->H, P = c->P, N = c->N, G = c->G;
+  const size_t a_bytes = B * H * g->Rp * 4;
+  g->v_off = align_up(a_bytes, 256);
+  g->k_off = align_up(g->v_off + B * H * R * P * g->esize, 256);
+  g->ring_bytes = align_up(g->k_off + B * G * R * N * g->esize, 256);
+  const size_t pb = align_up(B * 4, 256);
+  g->off_count = pb;
+  g->off_ticket = 2 * pb;
+  g->off_err = 3 * pb;
+  g->ptr_bytes = 3 * pb + 256;
+  if (c->read_fmt == RSSM_READ_E4M3_ROW) {
+    g->bsc_off = P * N;
+    g->rsc_off = P * N;
+    g->head_stride = align_up(P * N + 4 * P, 16);
+  } else if (c->read_fmt == RSSM_READ_E2M1_B16) {
+    g->bsc_off = P * N / 2;
+    g->rsc_off = align_up(g->bsc_off + P * N / 16, 16);
+    g->head_stride = align_up(g->rsc_off + 4 * P, 16);
+  }
+  g->copy_bytes = B * H * g->head_stride;
+  return RSSM_OK;
+}
+
+struct Plan {
+  int stages = 0;
+  size_t smem = 0;
+  rssm::Params p{};
+};
+
+// Shared-memory carve for one launch (see Params in rssm_device.cuh).
+rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
+  using namespace rssm;
+  auto a128 = [](size_t x) { return align_up(x, 128); };
+  const size_t stage = a128((size_t)c->P * c->N * 4);
+  const size_t kt = a128((size_t)g.R * c->N * 4);
+  const size_t qt = a128((size_t)kTMax * c->N * 4);
+  const size_t skq = a128((size_t)kTMax * g.R * 4);
+  const int rpi = 128 / c->N;
+  const int wsc_floats = (int)align_up(std::max(g.R * rpi * kKR, kTMax * kRMax + kTMax), 4);
+  const size_t wsc = a128((size_t)kNCW * wsc_floats * 4);
+  const size_t bars = a128((2 * kMaxStages + 2) * 8 + 16);
+  const size_t fixed = kt + qt + skq + wsc + bars;
+  if (fixed + 2 * stage > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
+  const int stages = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage);
+  rssm::Params& p = pl->p;
+  p.stages = stages;
+  p.stage_bytes = (int)stage;
+  size_t off = (size_t)stages * stage;
+  p.kt_off = (int)off; off += kt;
+  p.qt_off = (int)off; off += qt;
+  p.skq_off = (int)off; off += skq;
+  p.wsc_off = (int)off; off += wsc;
+  p.wsc_floats = wsc_floats;
+  p.bar_off = (int)off; off += bars;
+  pl->stages = stages;
+  pl->smem = off;
+  return RSSM_OK;
+}
+
+int sm_count() {
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+}  // namespace
+
+struct rssm_ctx {
+  rssm_config cfg;
+  Geom g;
+  float* ckpt;
+  uint8_t* ring;
+  uint8_t* ptrs;
+  uint8_t* copy;
+  int last_T;  // draft count of the last verify, 0 when none is pending
+};
+
+namespace {
+
+void fill_common(const rssm_ctx* h, rssm::Params* p) {
+  const rssm_config& c = h->cfg;
+  p->B = c.B; p->H = c.H; p->P = c.P; p->N = c.N; p->G = c.G; p->L = c.L;
+  p->R = h->g.R; p->Rp = h->g.Rp; p->HPG = c.H / c.G; p->T = 1; p->min_count = 1;
+  p->ckpt = h->ckpt;
+  p->copy = h->copy;
+  p->head_stride = (int)h->g.head_stride;
+  p->bsc_off = (int)h->g.bsc_off;
+  p->rsc_off = (int)h->g.rsc_off;
+  p->ring_a = reinterpret_cast<float*>(h->ring);
+  p->ring_v = h->ring + h->g.v_off;
+  p->ring_k = h->ring + h->g.k_off;
+  p->start = reinterpret_cast<int32_t*>(h->ptrs);
+  p->count = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_count);
+  p->ticket = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_ticket);
+  p->err = reinterpret_cast<uint32_t*>(h->ptrs + h->g.off_err);
+}
+
+int persistent_grid(long long heads) {
+  const int sms = sm_count();
+  return (int)std::max(1ll, std::min<long long>(heads, sms > 0 ? sms : 1));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rssm_last_error(void) { return g_msg.c_str(); }
+
+rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* ring_bytes, size_t* ptr_bytes,
+                                size_t* read_copy_bytes) {
+  Geom g;
+  const rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (ring_bytes) *ring_bytes = g.ring_bytes;
+  if (ptr_bytes) *ptr_bytes = g.ptr_bytes;
+  if (read_copy_bytes) *read_copy_bytes = g.copy_bytes;
+  return RSSM_OK;
+}
+
+rssm_status rssm_ring_offsets(const rssm_config* cfg, size_t* v_off, size_t* k_off) {
+  Geom g;
+  const rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (v_off) *v_off = g.v_off;
+  if (k_off) *k_off = g.k_off;
+  return RSSM_OK;
+}
+
+rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, size_t* bscale_off,
+                                  size_t* rscale_off) {
+  Geom g;
+  const rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (cfg->read_fmt == RSSM_READ_NONE) return fail(RSSM_EINVAL, "configuration has no read copy");
+  if (head_stride) *head_stride = g.head_stride;
+  if (bscale_off) *bscale_off = g.bsc_off;
+  if (rscale_off) *rscale_off = g.rsc_off;
+  return RSSM_OK;
+}
+
+rssm_status rssm_create(const rssm_config* cfg, float* ckpt, void* ring, void* ptrs, void* read_copy,
+                        void* stream, rssm_handle* out) {
+  if (!out) return fail(RSSM_EINVAL, "out is NULL");
+  *out = nullptr;
+  Geom g;
+  rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (!ckpt || !ring || !ptrs) return fail(RSSM_EINVAL, "ckpt, ring and ptrs must be non-NULL");
+  if (!aligned16(ckpt) || !aligned16(ring) || !aligned16(ptrs))
+    return fail(RSSM_EINVAL, "ckpt, ring and ptrs must be 16-byte aligned");
+  if (cfg->read_fmt != RSSM_READ_NONE && (!read_copy || !aligned16(read_copy)))
+    return fail(RSSM_EINVAL, "read_copy must be a non-NULL 16-byte aligned buffer for this read format");
+  rssm_ctx* h = new (std::nothrow) rssm_ctx;
+  if (!h) return fail(RSSM_EINVAL, "out of host memory");
+  h->cfg = *cfg;
+  h->g = g;
+  h->ckpt = ckpt;
+  h->ring = static_cast<uint8_t*>(ring);
+  h->ptrs = static_cast<uint8_t*>(ptrs);
+  h->copy = cfg->read_fmt != RSSM_READ_NONE ? static_cast<uint8_t*>(read_copy) : nullptr;
+  h->last_T = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ptrs, 0, g.ptr_bytes, st);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "cudaMemsetAsync(ptrs)");
+  }
+  if (h->copy) {
+    Plan pl;
+    s = plan_smem(cfg, g, &pl);
+    if (s != RSSM_OK) {
+      delete h;
+      return s;
+    }
+    fill_common(h, &pl.p);
+    const long long heads = (long long)cfg->B * cfg->H;
+    e = rssm::launch_quant(pl.p, persistent_grid(heads), pl.smem, st, cfg->N, cfg->read_fmt);
+    if (e != cudaSuccess) {
+      delete h;
+      return cuda_fail(e, "read-copy quantize launch");
+    }
+  }
+  *out = h;
+  return RSSM_OK;
+}
+
+rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, const void* k, const void* q,
+                             float* o, void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
+  if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
+    return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
+  Plan pl;
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  if (s != RSSM_OK) return s;
+  fill_common(h, &pl.p);
+  pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
+  const long long heads = (long long)h->cfg.B * h->cfg.H;
+  const cudaError_t e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
+                                            h->cfg.N, h->cfg.in_dtype, h->cfg.read_fmt);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  h->last_T = 0;
+  return RSSM_OK;
+}
+
+rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k, const void* q,
+                        float* o, void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (T < 1 || T > h->cfg.T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, h->cfg.T_max);
+  if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
+  if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
+    return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
+  Plan pl;
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  if (s != RSSM_OK) return s;
+  fill_common(h, &pl.p);
+  pl.p.T = T;
+  pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
+  const long long heads = (long long)h->cfg.B * h->cfg.H;
+  const cudaError_t e = rssm::launch_verify(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
+                                            h->cfg.N, h->cfg.in_dtype);
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  h->last_T = T;
+  return RSSM_OK;
+}
+
+rssm_status rssm_commit(rssm_handle h, const int32_t* accepted, void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (!accepted) return fail(RSSM_EINVAL, "accepted is NULL");
+  if (h->last_T < 1) return fail(RSSM_EINVAL, "commit without a pending verify");
+  rssm::Params p{};
+  fill_common(h, &p);
+  const cudaError_t e = rssm::launch_commit(h->cfg.B, h->last_T, h->g.R, accepted, p.count, p.err,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  h->last_T = 0;
+  return RSSM_OK;
+}
+
+rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (min_count < 1) return fail(RSSM_EINVAL, "min_count=%d must be >= 1", min_count);
+  Plan pl;
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  if (s != RSSM_OK) return s;
+  fill_common(h, &pl.p);
+  pl.p.min_count = min_count;
+  // one CTA per (sequence, group): CTAs of sequences that do not flush exit at once
+  const int grid = h->cfg.B * h->cfg.G;
+  const cudaError_t e = rssm::launch_flush(pl.p, grid, pl.smem, static_cast<cudaStream_t>(stream), h->cfg.N,
+                                           h->cfg.in_dtype, h->cfg.read_fmt);
+  if (e != cudaSuccess) return cuda_fail(e, "flush launch");
+  h->last_T = 0;
+  return RSSM_OK;
+}
+
+rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* count_host, uint32_t* err_host,
+                               void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t nb = (size_t)h->cfg.B * 4;
+  uint32_t err = 0;
+  cudaError_t e = cudaSuccess;
+  if (start_host && e == cudaSuccess) e = cudaMemcpyAsync(start_host, h->ptrs, nb, cudaMemcpyDeviceToHost, st);
+  if (count_host && e == cudaSuccess)
+    e = cudaMemcpyAsync(count_host, h->ptrs + h->g.off_count, nb, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&err, h->ptrs + h->g.off_err, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "read pointers");
+  if (err_host) *err_host = err;
+  if (err & rssm::kErrTimeout) return fail(RSSM_ETIMEOUT, "a bounded wait inside a kernel expired (error word 0x%x)", err);
+  if (err & (rssm::kErrCapacity | rssm::kErrAccept))
+    return fail(RSSM_ECAPACITY, "ring overflow or bad accepted length (error word 0x%x)", err);
+  return RSSM_OK;
+}
+
+rssm_status rssm_clear_error(rssm_handle h, void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  const cudaError_t e = cudaMemsetAsync(h->ptrs + h->g.off_err, 0, 4, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "clear error");
+  return RSSM_OK;
+}
+
+rssm_status rssm_destroy(rssm_handle h) {
+  delete h;
+  return RSSM_OK;
+}
+
+rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const float* alpha, const void* v,
+                                   const void* k, const void* q, float* o, void* stream) {
+  Geom g;
+  rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (!state || !alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
+  if (!aligned16(state) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
+    return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
+  Plan pl;
+  s = plan_smem(cfg, g, &pl);
+  if (s != RSSM_OK) return s;
+  rssm::Params& p = pl.p;
+  p.B = cfg->B; p.H = cfg->H; p.P = cfg->P; p.N = cfg->N; p.G = cfg->G; p.L = cfg->L;
+  p.R = g.R; p.Rp = g.Rp; p.HPG = cfg->H / cfg->G; p.T = 1; p.min_count = 1;
+  p.ckpt = state;
+  p.alpha = alpha; p.v = v; p.k = k; p.q = q; p.o = o;
+  const long long heads = (long long)cfg->B * cfg->H;
+  const cudaError_t e = rssm::launch_conv(p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
+                                          cfg->N, cfg->in_dtype);
+  if (e != cudaSuccess) return cuda_fail(e, "conventional launch");
+  return RSSM_OK;
+}
+
+}  // extern "C"

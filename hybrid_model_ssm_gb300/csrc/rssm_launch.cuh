@@ -1,0 +1,57 @@
+// rssm_launch.cuh - host-side dispatch from runtime sizes to kernel instantiations.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "rssm_device.cuh"
+
+namespace rssm {
+
+constexpr int kSmemMax = 227 * 1024;  // largest dynamic shared memory per CTA on sm_103a
+
+template <int MODE, int N, typename TIn, int RF>
+cudaError_t launch_one(const Params& p, int grid, size_t smem, cudaStream_t st) {
+  auto kern = head_kernel<MODE, N, TIn, RF>;
+  static bool attr_set = false;  // one GPU per process: set the opt-in size once
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// N in {16,32,64,128}; dtype 0 = f32, 1 = bf16; rf 0/1/2 (1,2 only for N >= 64).
+template <int MODE, typename TIn>
+cudaError_t dispatch_n(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf) {
+  if (rf == kRfNone) {
+    if constexpr (MODE != kQuant) {
+      switch (N) {
+        case 16: return launch_one<MODE, 16, TIn, kRfNone>(p, grid, smem, st);
+        case 32: return launch_one<MODE, 32, TIn, kRfNone>(p, grid, smem, st);
+        case 64: return launch_one<MODE, 64, TIn, kRfNone>(p, grid, smem, st);
+        case 128: return launch_one<MODE, 128, TIn, kRfNone>(p, grid, smem, st);
+      }
+    }
+  } else if constexpr (MODE == kDecode || MODE == kFlush || MODE == kQuant) {
+    if (rf == kRfE4m3) {
+      if (N == 64) return launch_one<MODE, 64, TIn, kRfE4m3>(p, grid, smem, st);
+      if (N == 128) return launch_one<MODE, 128, TIn, kRfE4m3>(p, grid, smem, st);
+    } else if (rf == kRfE2m1) {
+      if (N == 64) return launch_one<MODE, 64, TIn, kRfE2m1>(p, grid, smem, st);
+      if (N == 128) return launch_one<MODE, 128, TIn, kRfE2m1>(p, grid, smem, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
+cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
+cudaError_t launch_flush(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
+cudaError_t launch_quant(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf);
+cudaError_t launch_conv(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
+cudaError_t launch_commit(int B, int T, int R, const int32_t* accepted, int32_t* count, uint32_t* err,
+                          cudaStream_t st);
+
+}  // namespace rssm

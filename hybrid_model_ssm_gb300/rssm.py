@@ -1,0 +1,262 @@
+"""ctypes binding of librssm.so: argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels. This module
+checks tensor shapes, dtypes and devices, allocates the caller-owned workspace
+with PyTorch (which provides device memory and streams), and passes raw
+pointers through the C ABI declared in ``include/rssm.h``. No computation of
+the method happens here. No CPU fallback exists: if the library is missing,
+the import raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librssm.so")
+
+RSSM_OK, RSSM_EINVAL, RSSM_ECAPACITY, RSSM_ECUDA, RSSM_EUNSUPPORTED, RSSM_ETIMEOUT = range(6)
+STATUS_NAMES = {0: "RSSM_OK", 1: "RSSM_EINVAL", 2: "RSSM_ECAPACITY", 3: "RSSM_ECUDA", 4: "RSSM_EUNSUPPORTED",
+                5: "RSSM_ETIMEOUT"}
+DTYPES = {"f32": 0, "bf16": 1}
+READ_FMTS = {None: 0, "none": 0, "e4m3": 1, "e2m1": 2}
+ERR_CAPACITY, ERR_ACCEPT, ERR_TIMEOUT = 1, 2, 4
+
+# The C ABI functions, with their argument types.
+_c_size_p = ctypes.POINTER(ctypes.c_size_t)
+_c_i32_p = ctypes.POINTER(ctypes.c_int32)
+_c_u32_p = ctypes.POINTER(ctypes.c_uint32)
+_vp = ctypes.c_void_p
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "H", "P", "N", "G", "L", "T_max", "in_dtype", "read_fmt")]
+
+
+_Cfg_p = ctypes.POINTER(Config)
+SIGNATURES = {
+    "rssm_workspace_size": [_Cfg_p, _c_size_p, _c_size_p, _c_size_p],
+    "rssm_ring_offsets": [_Cfg_p, _c_size_p, _c_size_p],
+    "rssm_read_copy_layout": [_Cfg_p, _c_size_p, _c_size_p, _c_size_p],
+    "rssm_create": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)],
+    "rssm_decode_step": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_verify": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_commit": [_vp, _vp, _vp],
+    "rssm_flush": [_vp, ctypes.c_int32, _vp],
+    "rssm_read_pointers": [_vp, _c_i32_p, _c_i32_p, _c_u32_p, _vp],
+    "rssm_clear_error": [_vp, _vp],
+    "rssm_destroy": [_vp],
+    "rssm_last_error": [],
+    "rssm_conventional_step": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+}
+
+
+class RssmError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load librssm.so. Raises if it has not been built (no fallback exists)."""
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m hybrid_model_ssm_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, args in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "rssm_last_error" else ctypes.c_int
+    return lib
+
+
+_LIB: ctypes.CDLL | None = None
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = load_library()
+    return _LIB
+
+
+def _check(status: int):
+    if status != RSSM_OK:
+        raise RssmError(status, lib().rssm_last_error().decode())
+
+
+@dataclass(frozen=True)
+class LayerShape:
+    """Sizes of one SSM layer (see include/rssm.h for their meaning)."""
+
+    B: int
+    H: int
+    P: int
+    N: int
+    G: int
+    L: int
+    T_max: int = 1
+    in_dtype: str = "bf16"
+    read_fmt: str | None = None
+
+    @property
+    def R(self) -> int:
+        return self.L + self.T_max - 1
+
+    @property
+    def torch_in_dtype(self) -> torch.dtype:
+        return {"bf16": torch.bfloat16, "f32": torch.float32}[self.in_dtype]
+
+    def config(self) -> Config:
+        return Config(self.B, self.H, self.P, self.N, self.G, self.L, self.T_max, DTYPES[self.in_dtype],
+                      READ_FMTS[self.read_fmt])
+
+
+def workspace_size(shape: LayerShape) -> tuple[int, int, int]:
+    c = shape.config()
+    r, p, q = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().rssm_workspace_size(ctypes.byref(c), ctypes.byref(r), ctypes.byref(p), ctypes.byref(q)))
+    return r.value, p.value, q.value
+
+
+def ring_offsets(shape: LayerShape) -> tuple[int, int]:
+    c = shape.config()
+    v, k = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().rssm_ring_offsets(ctypes.byref(c), ctypes.byref(v), ctypes.byref(k)))
+    return v.value, k.value
+
+
+def read_copy_layout(shape: LayerShape) -> tuple[int, int, int]:
+    c = shape.config()
+    a, b, d = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().rssm_read_copy_layout(ctypes.byref(c), ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
+    return a.value, b.value, d.value
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _expect(t: torch.Tensor, shape, dtype, name: str):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype} != {dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+
+
+class ReplaySSM:
+    """One SSM layer's replay decoding state, bound to caller (PyTorch) memory.
+
+    ``ckpt`` [B,H,P,N] fp32 on the GPU is the initial state. It is updated in
+    place at every flush. The ring, the pointer block and the optional read copy
+    are allocated here as plain uint8 CUDA tensors and then belong to this object.
+    """
+
+    def __init__(self, shape: LayerShape, ckpt: torch.Tensor, stream=None):
+        _expect(ckpt, (shape.B, shape.H, shape.P, shape.N), torch.float32, "ckpt")
+        self.shape = shape
+        self.ckpt = ckpt
+        ring_b, ptr_b, copy_b = workspace_size(shape)
+        dev = ckpt.device
+        self.ring = torch.empty(ring_b, dtype=torch.uint8, device=dev)
+        self.ptrs = torch.empty(ptr_b, dtype=torch.uint8, device=dev)
+        self.copy = torch.empty(copy_b, dtype=torch.uint8, device=dev) if copy_b else None
+        self._cfg = shape.config()
+        h = ctypes.c_void_p()
+        _check(lib().rssm_create(ctypes.byref(self._cfg), _ptr(ckpt), _ptr(self.ring), _ptr(self.ptrs),
+                                 _ptr(self.copy), _stream_ptr(stream), ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _LIB is not None:
+            _LIB.rssm_destroy(h)
+            self._h = None
+
+    # ------------------------------------------------------------ decode path
+    def decode_step(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+        s = self.shape
+        _expect(alpha, (s.B, s.H), torch.float32, "alpha")
+        _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v")
+        _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k")
+        _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q")
+        if out is None:
+            out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=alpha.device)
+        _expect(out, (s.B, s.H, s.P), torch.float32, "out")
+        _check(lib().rssm_decode_step(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
+                                      _stream_ptr(stream)))
+        return out
+
+    def verify(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+        s = self.shape
+        T = alpha.shape[1]
+        _expect(alpha, (s.B, T, s.H), torch.float32, "alpha")
+        _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v")
+        _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k")
+        _expect(q, (s.B, T, s.G, s.N), s.torch_in_dtype, "q")
+        if out is None:
+            out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=alpha.device)
+        _expect(out, (s.B, T, s.H, s.P), torch.float32, "out")
+        _check(lib().rssm_verify(self._h, T, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
+                                 _stream_ptr(stream)))
+        return out
+
+    def commit(self, accepted: torch.Tensor, stream=None):
+        _expect(accepted, (self.shape.B,), torch.int32, "accepted")
+        _check(lib().rssm_commit(self._h, _ptr(accepted), _stream_ptr(stream)))
+
+    def flush(self, min_count: int | None = None, stream=None):
+        _check(lib().rssm_flush(self._h, self.shape.L if min_count is None else int(min_count), _stream_ptr(stream)))
+
+    def read_pointers(self, stream=None, check: bool = True):
+        """(start, count, error word) as host int32 tensors and an int; synchronizes the stream."""
+        B = self.shape.B
+        start = (ctypes.c_int32 * B)()
+        count = (ctypes.c_int32 * B)()
+        err = ctypes.c_uint32()
+        st = lib().rssm_read_pointers(self._h, start, count, ctypes.byref(err), _stream_ptr(stream))
+        if check:
+            _check(st)
+        return (torch.tensor(list(start), dtype=torch.int32), torch.tensor(list(count), dtype=torch.int32),
+                int(err.value))
+
+    def clear_error(self, stream=None):
+        _check(lib().rssm_clear_error(self._h, _stream_ptr(stream)))
+
+    # ------------------------------------------------------- ring inspection
+    def ring_views(self):
+        """(alpha [B,H,Rp] f32, V [B,H,R,P], K [B,G,R,N]) views of the ring buffer (for tests)."""
+        s = self.shape
+        R, Rp = s.R, (s.R + 3) // 4 * 4
+        v_off, k_off = ring_offsets(s)
+        es = 4 if s.in_dtype == "f32" else 2
+        a = self.ring[: s.B * s.H * Rp * 4].view(torch.float32).view(s.B, s.H, Rp)
+        V = self.ring[v_off: v_off + s.B * s.H * R * s.P * es].view(s.torch_in_dtype).view(s.B, s.H, R, s.P)
+        K = self.ring[k_off: k_off + s.B * s.G * R * s.N * es].view(s.torch_in_dtype).view(s.B, s.G, R, s.N)
+        return a, V, K
+
+
+def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+    """The comparison kernel: S <- alpha S + v k^T, o = S q, state read and written in full."""
+    s = shape
+    _expect(state, (s.B, s.H, s.P, s.N), torch.float32, "state")
+    _expect(alpha, (s.B, s.H), torch.float32, "alpha")
+    _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v")
+    _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k")
+    _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q")
+    if out is None:
+        out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=state.device)
+    cfg = s.config()
+    _check(lib().rssm_conventional_step(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(v), _ptr(k), _ptr(q),
+                                        _ptr(out), _stream_ptr(stream)))
+    return out

@@ -1,0 +1,191 @@
+/*
+ * rssm.h - C ABI of the ReplaySSM decode library (librssm.so), sm_103a.
+ *
+ * The library implements decoding for the gated outer-product SSM recurrence
+ *     S_t = alpha_t S_{t-1} + v_t k_t^T,   o_t = S_t q_t
+ * (aikraft.ru, "ReplaySSM: Революция в декодировании гибридных моделей", §01,
+ * recurrence). The state of each (sequence, value head) is an FP32 checkpoint
+ * plus a ring buffer of the records (alpha_j, v_j, k_j) that arrived since the
+ * checkpoint (same page §03; ai.cheesepanini.fun,
+ * "知识卡片：ReplaySSM——重新思考混合模型解码的状态存储", 方法/产品要点, core
+ * representation). k and q are shared by the H/G consecutive value heads of a
+ * group.
+ *
+ * Conventions for every call:
+ *  - All tensors are caller-owned device memory in row-major layout with the
+ *    last index contiguous. Base pointers must be 16-byte aligned. The library
+ *    never allocates device memory. Its only allocation is the small host
+ *    handle.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *    void*; NULL means the legacy default stream). The one exception is
+ *    rssm_read_pointers, which synchronizes the stream.
+ *  - Argument errors (shapes, alignment, NULL pointers, unsupported sizes) are
+ *    detected on the host before anything is enqueued. They return a status,
+ *    and rssm_last_error() describes them.
+ *  - Per-sequence errors found on the device (ring overflow, a bad accepted
+ *    length, a wait that ran out of time) set bits in a device error word and
+ *    skip the affected sequence. Other sequences proceed. rssm_read_pointers
+ *    reports the word.
+ *  - No C++ exception crosses this boundary. A handle is not thread safe: use
+ *    one stream per handle at a time.
+ *
+ * Supported sizes: N in {16, 32, 64, 128}; P a multiple of 8 with P*N*4 <= 64 KiB;
+ * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8. Read copies need
+ * N in {64, 128}.
+ */
+#ifndef RSSM_H_
+#define RSSM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RSSM_OK = 0,
+  RSSM_EINVAL = 1,        /* bad argument (shape, pointer, alignment, value) */
+  RSSM_ECAPACITY = 2,     /* device error word: ring overflow or bad accepted length */
+  RSSM_ECUDA = 3,         /* a CUDA runtime call failed */
+  RSSM_EUNSUPPORTED = 4,  /* valid but unsupported size or format */
+  RSSM_ETIMEOUT = 5       /* device error word: a bounded wait inside a kernel expired */
+} rssm_status;
+
+typedef enum { RSSM_F32 = 0, RSSM_BF16 = 1 } rssm_dtype;
+
+/* Low-precision read copy of the checkpoint, refreshed at every flush and read
+ * by non-flush decode steps. The recurrence always stays in FP32 (aikraft.ru
+ * page §06; sitech.ge, "NVIDIA و Dao AI Lab يقدّمان ReplaySSM…", section
+ * "الحد من خطأ التكميم"). Byte layout per (sequence, head): see
+ * rssm_read_copy_layout. */
+typedef enum {
+  RSSM_READ_NONE = 0,
+  RSSM_READ_E4M3_ROW = 1,  /* E4M3 codes, one fp32 scale per row of N */
+  RSSM_READ_E2M1_B16 = 2   /* E2M1 codes (2 per byte, low nibble first), one E4M3
+                              scale per 16 elements along N, one fp32 scale per row */
+} rssm_read_fmt;
+
+/* Problem sizes. B sequences, H value heads, P head dim of v and o, N state dim
+ * of k and q, G groups, L flush window, T_max largest draft count of a verify
+ * (1 for plain decoding). The ring has R = L + T_max - 1 slots per head.
+ * in_dtype is the storage type of v, k and q (rssm_dtype); alpha, the
+ * checkpoint and all outputs are fp32. read_fmt is an rssm_read_fmt. */
+typedef struct {
+  int32_t B, H, P, N, G, L, T_max;
+  int32_t in_dtype;
+  int32_t read_fmt;
+} rssm_config;
+
+typedef struct rssm_ctx* rssm_handle;
+
+/* Byte sizes of the three caller-allocated buffers that rssm_create binds.
+ *  ring_bytes: the record ring, made of
+ *      alpha [B,H,Rp] fp32 (Rp = R rounded up to 4) at offset 0,
+ *      V     [B,H,R,P] in_dtype at offset v_off,
+ *      K     [B,G,R,N] in_dtype at offset k_off (see rssm_ring_offsets).
+ *  ptr_bytes: pointer block of int32 start[B], count[B], ticket[B] and one
+ *      uint32 error word, padded to 256 bytes.
+ *  read_copy_bytes: B*H*head_stride for a read copy, else 0.
+ * Any output pointer may be NULL. Returns RSSM_EINVAL or RSSM_EUNSUPPORTED for
+ * a bad configuration. */
+rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* ring_bytes, size_t* ptr_bytes,
+                                size_t* read_copy_bytes);
+
+/* Byte offsets of the V and K arrays inside the ring buffer (both 256-aligned). */
+rssm_status rssm_ring_offsets(const rssm_config* cfg, size_t* v_off, size_t* k_off);
+
+/* Read-copy layout. Each (sequence, head) owns head_stride bytes at
+ * (b*H + h)*head_stride. Inside it:
+ *   codes at 0: [P][N] bytes (E4M3) or [P][N/2] bytes (E2M1, element 2i in the low nibble);
+ *   block scales at bscale_off: [P][N/16] E4M3 bytes (E2M1 only);
+ *   row scales at rscale_off: [P] fp32.
+ * Quantizer (both formats), with rn32 IEEE round-to-nearest-even binary32 and
+ * the FP8/FP4 conversions rounding to nearest even with saturation:
+ *   E4M3: a = max|x| over the row; a <= 2^-100 gives an all-zero row;
+ *         inv = rn32(448/a), s = rn32(a/448), code = E4M3(rn32(x*inv)).
+ *   E2M1: s_r = rn32(a/2688), d6 = rn32(6*s_r); per block of 16:
+ *         sb = E4M3(rn32(max|x|_blk / d6)), d = rn32(value(sb)*s_r),
+ *         r = d > 0 ? rn32(1/d) : 0, code = E2M1(rn32(x*r)).
+ * Returns RSSM_EINVAL when cfg has no read copy. */
+rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, size_t* bscale_off,
+                                  size_t* rscale_off);
+
+/* Bind a decoding context to caller memory.
+ *  ckpt      [B,H,P,N] fp32 device: the initial state. It becomes the checkpoint
+ *            and is updated in place at every flush.
+ *  ring      device buffer of ring_bytes; contents need not be initialised.
+ *  ptrs      device buffer of ptr_bytes; zeroed here (start = count = 0).
+ *  read_copy device buffer of read_copy_bytes, or NULL when read_fmt is NONE;
+ *            filled here by quantizing ckpt.
+ * The buffers must stay valid until rssm_destroy. Enqueues a memset and,
+ * with a read copy, one kernel on the stream. *out receives the handle. */
+rssm_status rssm_create(const rssm_config* cfg, float* ckpt, void* ring, void* ptrs, void* read_copy,
+                        void* stream, rssm_handle* out);
+
+/* One decode step for all B sequences (aikraft.ru page §03, "non-flush" and
+ * "flush" steps). Inputs: alpha [B,H] fp32, v [B,H,P], k [B,G,N], q [B,G,N] in
+ * in_dtype. Output o [B,H,P] fp32.
+ * Per sequence with c committed records the step appends its record as record
+ * h = c+1. If h < L it computes only the output, from the checkpoint (or
+ * its read copy) and the ring (same page §05, output-only evaluation):
+ *     o = gamma_{1:h} (S_ckpt q) + sum_j gamma_{j+1:h} (k_j^T q) v_j
+ * and writes no state. If h >= L it folds all h records into the checkpoint,
+ * writes it once (and refreshes the read copy), outputs o = S_new q, and
+ * clears the buffer (start += h mod R, count = 0). A sequence with h > R sets
+ * RSSM_ECAPACITY in the error word and is left untouched. */
+rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, const void* k,
+                             const void* q, float* o, void* stream);
+
+/* Speculative verify of T <= T_max drafts (aikraft.ru page §05;
+ * ai.cheesepanini.fun card, 方法/产品要点, verify formula). Inputs: alpha
+ * [B,T,H] fp32, v [B,T,H,P], k [B,T,G,N], q [B,T,G,N]. Output o [B,T,H,P] fp32.
+ * The T draft records are appended after the c committed ones. Pointers do
+ * not move. Each draft's output uses the checkpoint once for all T queries:
+ *     O = S_ckpt Q D + V (W ⊙ (K^T Q)),  D = diag(gamma_{1:c+tau}),
+ *     W[j,tau] = gamma_{j+1:c+tau} for j <= c+tau, else 0.
+ * Verify always reads the FP32 checkpoint. A sequence with c + T > R sets
+ * RSSM_ECAPACITY and is skipped. */
+rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k,
+                        const void* q, float* o, void* stream);
+
+/* Commit the accepted prefix of the last verify: count[b] += accepted[b]
+ * (aikraft.ru page §05; records past the pointer are ignored and later
+ * overwritten). accepted [B] int32 device, each in 0..T of the last verify.
+ * A value outside that range sets RSSM_ECAPACITY and leaves the sequence
+ * unchanged. Nothing else moves. */
+rssm_status rssm_commit(rssm_handle h, const int32_t* accepted, void* stream);
+
+/* Fold every sequence that holds count >= min_count records (min_count >= 1)
+ * into its checkpoint, write it once, refresh the read copy, and clear its
+ * buffer. Pass min_count = L after a commit. Other sequences are not touched. */
+rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream);
+
+/* Copy start[B], count[B] (int32) and the error word to host memory,
+ * synchronizing the stream first. Any output may be NULL. Returns RSSM_OK,
+ * RSSM_ECAPACITY (bits 1|2 set) or RSSM_ETIMEOUT (bit 4 set). */
+rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* count_host,
+                               uint32_t* err_host, void* stream);
+
+/* Clear the device error word (asynchronous). */
+rssm_status rssm_clear_error(rssm_handle h, void* stream);
+
+/* Release the host handle. Caller memory is not touched. */
+rssm_status rssm_destroy(rssm_handle h);
+
+/* Message of the last error on the calling thread (never NULL). */
+const char* rssm_last_error(void);
+
+/* Comparison kernel (not part of the replay path): the conventional fused
+ * read-update-write step S <- alpha S + v k^T, o = S q on a full state
+ * [B,H,P,N] fp32, read and written every step (aikraft.ru page §01). cfg's
+ * L, T_max and read_fmt are ignored. */
+rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const float* alpha,
+                                   const void* v, const void* k, const void* q, float* o,
+                                   void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSSM_H_ */

@@ -29,14 +29,15 @@ Policy (readings where the pages leave it open):
 
 With a read copy (``read_fmt`` = "e4m3" or "e2m1"), the checkpoint is also
 quantized at every flush (and at creation), from its fp32 rounding. Non-flush
-and verify outputs then use the dequantized copy in the output-only formula.
+decode outputs then use the dequantized copy in the output-only formula.
+Verify outputs and flush-step outputs use the FP32 checkpoint.
 The recurrence itself stays exact ([RU] §06; [AR] quantization section).
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .recurrence import conventional_step, head_groups, replay_output, verify_outputs
+from .recurrence import conventional_step, head_groups, replay_output
 from . import quant
 
 
@@ -121,21 +122,17 @@ class ReplayOracle:
         """Speculative verify of T drafts: alpha [B,T,H], v [B,T,H,P], k,q [B,T,G,N].
 
         Output-only: the drafts run on a scratch copy of the exact state, so
-        the real state and the pointers stay unchanged. Returns O [B,T,H,P].
+        the real state and the pointers stay unchanged. Verify reads the FP32
+        checkpoint even when a read copy exists (reading: the pages tie the
+        copy to non-flush decode reads, [RU] §06). Returns O [B,T,H,P].
         """
         T = alpha.shape[1]
         if np.any(self.count + T > self.R):
             raise CapacityError("verify would exceed the ring capacity")
         O = np.empty((self.B, T, self.H, self.P))
-        if self.read_fmt is None:
-            Sc = self.S.copy()
-            for t in range(T):
-                Sc, O[:, t] = conventional_step(Sc, alpha[:, t], v[:, t], k[:, t], q[:, t])
-        else:
-            for b in range(self.B):
-                recs = self.records[b] + [(alpha[b, t], v[b, t], k[b, t]) for t in range(T)]
-                a_, v_, k_ = (np.stack(x) for x in zip(*recs))
-                O[b] = verify_outputs(self.copy[b], a_, v_, k_, q[b], int(self.count[b]))
+        Sc = self.S.copy()
+        for t in range(T):
+            Sc, O[:, t] = conventional_step(Sc, alpha[:, t], v[:, t], k[:, t], q[:, t])
         self._drafts = (alpha.copy(), v.copy(), k.copy(), q.copy(), T)
         self.events += 1
         return O

@@ -1,0 +1,95 @@
+"""The C-ABI library, checked without a GPU.
+
+librssm.so must load and export every function declared in include/rssm.h.
+The host-side validation and the buffer layouts are checked here too (no
+compute call runs).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from hybrid_model_ssm_gb300 import LayerShape, RssmError, read_copy_layout, ring_offsets, workspace_size
+from hybrid_model_ssm_gb300 import build as build_mod
+from hybrid_model_ssm_gb300.rssm import RSSM_EINVAL, RSSM_EUNSUPPORTED, SIGNATURES
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rssm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_mod.build()  # nvcc cross-compiles without a GPU; a no-op when up to date
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rssm_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in rssm.h but not exported"
+
+
+def test_binding_covers_the_header():
+    assert set(declared_functions()) == set(SIGNATURES)
+
+
+def test_workspace_layout_of_the_layer_workload(lib):
+    s = LayerShape(B=256, H=128, P=64, N=128, G=8, L=16)
+    ring, ptrs, copy = workspace_size(s)
+    v_off, k_off = ring_offsets(s)
+    R, Rp = 16, 16
+    assert v_off == 256 * 128 * Rp * 4
+    assert k_off == v_off + 256 * 128 * R * 64 * 2
+    assert ring == k_off + 256 * 8 * R * 128 * 2
+    assert v_off % 256 == 0 and k_off % 256 == 0
+    assert ptrs == 3 * 1024 + 256
+    assert copy == 0
+
+
+def test_read_copy_layouts(lib):
+    e4 = LayerShape(B=2, H=4, P=64, N=128, G=2, L=16, read_fmt="e4m3")
+    stride, bsc, rsc = read_copy_layout(e4)
+    assert (stride, rsc) == (64 * 128 + 4 * 64, 64 * 128)
+    e2 = LayerShape(B=2, H=4, P=64, N=128, G=2, L=16, read_fmt="e2m1")
+    stride, bsc, rsc = read_copy_layout(e2)
+    assert bsc == 64 * 64 and rsc == bsc + 64 * 8 and stride == rsc + 256
+    assert workspace_size(e2)[2] == 2 * 4 * stride
+    with pytest.raises(RssmError):
+        read_copy_layout(LayerShape(B=2, H=4, P=64, N=128, G=2, L=16))
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H=3, G=2), RSSM_EINVAL),
+    (dict(N=48), RSSM_EUNSUPPORTED),
+    (dict(N=256), RSSM_EUNSUPPORTED),
+    (dict(P=12), RSSM_EUNSUPPORTED),
+    (dict(B=0), RSSM_EINVAL),
+    (dict(L=30, T_max=4), RSSM_EUNSUPPORTED),
+    (dict(T_max=9), RSSM_EUNSUPPORTED),
+    (dict(N=32, read_fmt="e2m1"), RSSM_EUNSUPPORTED),
+    (dict(P=256, N=128), RSSM_EUNSUPPORTED),
+])
+def test_invalid_configurations_are_rejected(lib, kw, status):
+    base = dict(B=2, H=4, P=16, N=64, G=2, L=4, T_max=1)
+    base.update(kw)
+    with pytest.raises(RssmError) as ei:
+        workspace_size(LayerShape(**base))
+    assert ei.value.status == status
+
+
+def test_null_config_and_handle(lib):
+    lib.rssm_workspace_size.restype = ctypes.c_int
+    assert lib.rssm_workspace_size(None, None, None, None) == RSSM_EINVAL
+    lib.rssm_decode_step.restype = ctypes.c_int
+    assert lib.rssm_decode_step(None, None, None, None, None, None, None) == RSSM_EINVAL
+    lib.rssm_last_error.restype = ctypes.c_char_p
+    assert b"NULL" in lib.rssm_last_error()
+    assert lib.rssm_destroy(None) == 0
