@@ -54,21 +54,35 @@ def record_bytes(s) -> int:
     return 4 * s.H + es * s.H * s.P + es * s.G * s.N
 
 
-def window_bytes(s) -> dict:
+def copy_bytes_per_head(s, read_fmt) -> int:
+    """Bytes of one head's read copy (codes + scales, padded to 16)."""
+    if read_fmt is None:
+        return 0
+    P, N = s.P, s.N
+    if read_fmt == "e4m3":
+        return -(-(P * N + 4 * P) // 16) * 16
+    rsc = -(-(P * N // 2 + P * N // 16) // 16) * 16
+    return -(-(rsc + 4 * P) // 16) * 16
+
+
+def window_bytes(s, read_fmt=None) -> dict:
     """Algorithmic HBM bytes of one sequence over one window of L decode steps.
 
-    Each step reads the checkpoint |S| and its inputs (record + q) and writes its
-    output. Step t of the window (t = 0..L-1) also reads the t buffered records,
-    and every non-flush step appends its record. The flush step writes the
-    checkpoint once.
+    Every step reads its inputs (record + q) and writes its output. Step t of
+    the window (t = 0..L-1) also reads the t buffered records, and every
+    non-flush step appends its record. The L-1 non-flush steps each read the
+    checkpoint |S|, or its read copy |C| when there is one. The flush step
+    reads |S| and writes it once, plus the refreshed copy.
     """
     es = 2 if s.in_dtype == "bf16" else 4
     S = 4 * s.H * s.P * s.N
+    C = s.H * copy_bytes_per_head(s, read_fmt)
     r = record_bytes(s)
     inp = r + es * s.G * s.N
     out = 4 * s.H * s.P
     L = s.L
-    total = L * S + S + r * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * r
+    reads = (L - 1) * (C if read_fmt else S) + S
+    total = reads + S + C + r * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * r
     conv = L * (2 * S + inp + out)
     return {"replay_window": total, "replay_per_seq_step": total / L, "conventional_per_seq_step": conv / L,
             "state": S}
@@ -224,8 +238,8 @@ def run_ours(args, world, rank, local):
     from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM, conventional_step
 
     torch.cuda.set_device(local)
-    s = WORKLOAD
-    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype)
+    s = WORKLOAD if args.batch is None else WORKLOAD.with_(B=args.batch)
+    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype, read_fmt=args.read_fmt)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev)
@@ -283,7 +297,7 @@ def run_ours(args, world, rank, local):
     seq_steps = world * s.B * L * args.steps
     value = seq_steps / elapsed_max
     mean_launch = sum(launch_s) / len(launch_s)
-    wb = window_bytes(s)
+    wb = window_bytes(s, args.read_fmt)
     alg_bytes_launch = wb["replay_per_seq_step"] * s.B
     achieved = alg_bytes_launch / mean_launch / 1e9
     peak, peak_kind = measured_peak_gbs()
@@ -421,6 +435,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-conventional", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (smaller cases for ncu captures; not a bench line)")
+    ap.add_argument("--read-fmt", choices=["e4m3", "e2m1"], default=None,
+                    help="non-flush steps read a low-precision copy of the checkpoint")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

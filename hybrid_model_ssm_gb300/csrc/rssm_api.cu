@@ -96,28 +96,68 @@ struct Plan {
   rssm::Params p{};
 };
 
-// Shared-memory carve for one launch (see Params in rssm_device.cuh).
+// Row units, stage ring and shared-memory carve for one launch (see Params in rssm_device.cuh).
 rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
   using namespace rssm;
   auto a128 = [](size_t x) { return align_up(x, 128); };
-  const size_t stage = a128((size_t)c->P * c->N * 4);
-  const size_t kt = a128((size_t)g.R * c->N * 4);
-  const size_t qt = a128((size_t)kTMax * c->N * 4);
-  const size_t skq = a128((size_t)kTMax * g.R * 4);
-  const int rpi = 128 / c->N;
-  const int wsc_floats = (int)align_up(std::max(g.R * rpi * kKR, kTMax * kRMax + kTMax), 4);
+  const int P = c->P, N = c->N;
+  const size_t es = (size_t)g.esize;
+  const int rpi = 128 / N, sub_rows = kKR * rpi;
+  // U in {1,2,4,8}: the fewest units of at most two sub-passes each; UR a multiple of 8
+  int U = 1;
+  while (U < 8 && (P + U - 1) / U > 2 * sub_rows) U *= 2;
+  auto rows_per_unit = [&](int u) { return (int)align_up((size_t)((P + u - 1) / u), 8); };
+  int UR = rows_per_unit(U);
+  while (U > 1 && (U - 1) * UR >= P) {
+    U /= 2;
+    UR = rows_per_unit(U);
+  }
+  const int vchunks = UR * g.esize / 16;
+  int vcp_lg = 0;
+  while ((1 << vcp_lg) < vchunks) ++vcp_lg;
+  if (vcp_lg > 5) return fail(RSSM_EUNSUPPORTED, "unit value rows too long");
+  const size_t tile = (size_t)UR * N * 4;
+  const size_t sm_off = align_up(tile, 16);
+  const size_t sa_off = sm_off + 64;  // unit descriptor
+  const size_t sv_off = sa_off + (size_t)kRMax * 4;
+  const size_t stage = a128(sv_off + (size_t)g.R * UR * es);
+  size_t cbs_off = 0, crs_off = 0;
+  if (c->read_fmt == RSSM_READ_E4M3_ROW) {
+    crs_off = align_up((size_t)UR * N, 16);
+  } else if (c->read_fmt == RSSM_READ_E2M1_B16) {
+    cbs_off = (size_t)UR * N / 2;
+    crs_off = align_up(cbs_off + (size_t)UR * N / 16, 16);
+  }
+  const size_t gq_off = (size_t)g.R * N * es;
+  const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
+  const int wsc_floats = (int)align_up((size_t)2 * kTMax * kRMax + 16 + (size_t)g.R * rpi * kKR, 4);
   const size_t wsc = a128((size_t)kNCW * wsc_floats * 4);
-  const size_t bars = a128((2 * kMaxStages + 2) * 8 + 16);
-  const size_t fixed = kt + qt + skq + wsc + bars;
+  const size_t bars = a128((2 * kMaxStages + 8) * 8 + (size_t)kRMax * 8);  // barriers, flag, producer table
+  const size_t fixed = 2 * gb + wsc + bars;
   if (fixed + 2 * stage > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
-  const int stages = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage);
+  int stages = 2;
+  while (stages * 2 <= kMaxStages && fixed + (size_t)stages * 2 * stage <= (size_t)kSmemMax) stages *= 2;
+  int lgS = 0;
+  while ((1 << lgS) < stages) ++lgS;
+  int lgU = 0;
+  while ((1 << lgU) < U) ++lgU;
   rssm::Params& p = pl->p;
+  p.U = U;
+  p.lgU = lgU;
+  p.UR = UR;
   p.stages = stages;
+  p.lgS = lgS;
   p.stage_bytes = (int)stage;
+  p.sm_off = (int)sm_off;
+  p.sa_off = (int)sa_off;
+  p.sv_off = (int)sv_off;
+  p.cbs_off = (int)cbs_off;
+  p.crs_off = (int)crs_off;
+  p.vcp_lg = vcp_lg;
   size_t off = (size_t)stages * stage;
-  p.kt_off = (int)off; off += kt;
-  p.qt_off = (int)off; off += qt;
-  p.skq_off = (int)off; off += skq;
+  p.gb_off = (int)off; off += 2 * gb;
+  p.gb_bytes = (int)gb;
+  p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
   p.wsc_floats = wsc_floats;
   p.bar_off = (int)off; off += bars;

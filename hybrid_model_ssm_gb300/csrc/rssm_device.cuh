@@ -1,13 +1,14 @@
 // rssm_device.cuh - device code of the ReplaySSM decode library (sm_103a).
 //
 // One kernel template serves every mode. Each CTA owns a contiguous range of
-// (sequence, head) pairs. One producer warp streams the 32 KiB FP32
-// checkpoint tile of each head (or its read copy) into a ring of shared-memory
-// stages with bulk TMA copies (cp.async.bulk + mbarrier transaction counts).
-// Eight consumer warps compute from the staged tile while the next tiles
-// are in flight. The small per-group data (the buffered keys K, the queries,
-// the dot products k_j^T q) sits in shared memory. The per-head decays and
-// coefficients stay in registers and are exchanged with warp shuffles.
+// (sequence, head) pairs. A producer warp feeds a ring of shared-memory
+// stages. For each head, one bulk TMA copy (cp.async.bulk + mbarrier
+// transaction count) brings the 32 KiB FP32 checkpoint tile, or its read copy.
+// The producer lanes also gather that head's buffered records in record order
+// with cp.async: the decays alpha_j and the value rows v_j. For each group of
+// H/G heads, they gather the buffered keys k_j and the queries into a
+// double-buffered group area. Eight consumer warps therefore read only
+// shared memory, and the next stages stay in flight while they compute.
 //
 // Math (aikraft.ru, "ReplaySSM: Революция в декодировании гибридных моделей",
 // §01 recurrence, §03 unrolled window, §05 output-only evaluation;
@@ -34,7 +35,7 @@ constexpr int kKR = 8;                     // FP32-tile row-instructions per war
 constexpr int kTQ = 4;                     // verify queries per pass over the tile
 constexpr int kTMax = 8;                   // largest draft count
 constexpr int kRMax = 32;                  // largest ring (records per head)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -59,27 +60,43 @@ struct Params {
   const void* k;       // decode/conv [B,G,N]; verify [B,T,G,N]
   const void* q;       // decode/conv [B,G,N]; verify [B,T,G,N]
   float* o;            // decode/conv [B,H,P]; verify [B,T,H,P]
-  int stages, stage_bytes;
-  int kt_off, qt_off, skq_off, wsc_off, wsc_floats, bar_off;  // shared-memory carve (bytes / floats)
+  // Each head is split into U (1, 2, 4 or 8) row units of UR rows (the last may
+  // be shorter); one consumer warp owns a whole unit.
+  int U, lgU, UR;
+  // Shared memory (bytes). `stages` (a power of two) stages of
+  // [unit tile | unit descriptor | alpha_j (kRMax fp32) | v_j rows of the unit (R x UR)];
+  // a read-copy tile keeps its block scales at cbs_off and row scales at crs_off.
+  int stages, lgS, stage_bytes, sm_off, sa_off, sv_off, cbs_off, crs_off;
+  int vcp_lg;  // log2 of the power of two >= 16-byte chunks per unit value row
+  // Two group areas of [k_j rows (R x N) | queries (kTMax x N)].
+  int gb_off, gb_bytes, gq_off;
+  int wsc_off, wsc_floats, bar_off;  // per-warp scratch (floats each), barriers
 };
 
 // ----------------------------------------------------------------- input types
+// Loads of v/k/q elements (fp32 or bf16) as fp32 from shared memory.
 template <typename T> struct In;
 template <> struct In<float> {
-  using raw = uint32_t;
-  static __device__ __forceinline__ float ld(const void* p, size_t i) { return reinterpret_cast<const float*>(p)[i]; }
-};
-template <> struct In<__nv_bfloat16> {
-  using raw = uint16_t;
-  static __device__ __forceinline__ float ld(const void* p, size_t i) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  static constexpr int kBytes = 4;
+  static __device__ __forceinline__ float lds(const uint8_t* base, int i) {
+    return reinterpret_cast<const float*>(base)[i];
+  }
+  static __device__ __forceinline__ float4 lds4(const uint8_t* base, int i) {  // i multiple of 4
+    return *reinterpret_cast<const float4*>(base + 4 * i);
   }
 };
-template <typename T>
-__device__ __forceinline__ void copy_raw(void* dst, size_t di, const void* src, size_t si) {
-  using R = typename In<T>::raw;
-  reinterpret_cast<R*>(dst)[di] = reinterpret_cast<const R*>(src)[si];
-}
+template <> struct In<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  static __device__ __forceinline__ float lds(const uint8_t* base, int i) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+  }
+  static __device__ __forceinline__ float4 lds4(const uint8_t* base, int i) {  // i multiple of 4
+    const uint2 w = *reinterpret_cast<const uint2*>(base + 2 * i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+};
 
 // ------------------------------------------------------------ PTX primitives
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -93,6 +110,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
@@ -114,10 +134,23 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       : "memory");
 }
 
+// Small asynchronous copies global -> shared (the record gathers).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once all earlier cp.async of this thread have landed (counted in the init count).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Bounded wait on an mbarrier phase. Returns false (after flagging the CTA and
 // the device error word) when the wait runs out or another thread aborted.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
-  if (mbar_try(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   uint32_t* err) {
   const unsigned long long t0 = gtimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try(bar, parity)) return true;
@@ -130,6 +163,25 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
   atomicOr(err, kErrTimeout);
   return false;
 }
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, err);
+}
+
+// (sequence, head, group) of consecutive flattened heads, advanced without divisions.
+struct HeadIter {
+  int b, hh, g, gpos;
+  __device__ __forceinline__ void init(long long h0, int H, int HPG) {
+    b = (int)(h0 / H);
+    hh = (int)(h0 - (long long)b * H);
+    g = hh / HPG;
+    gpos = hh - g * HPG;
+  }
+  __device__ __forceinline__ void next(int H, int HPG) {
+    ++hh;
+    if (++gpos == HPG) { gpos = 0; ++g; }
+    if (hh == H) { hh = 0; g = 0; gpos = 0; ++b; }
+  }
+};
 
 // ------------------------------------------------------------ FP8/FP4 codes
 // cvt packs the value converted from the first source into the upper half.
@@ -236,6 +288,11 @@ __device__ __forceinline__ float suffix_prod(float x, int lane) {
   return x;
 }
 
+// Ring slot of record j (0-based) for a buffer starting at slot st < R, with j < R.
+__device__ __forceinline__ int ring_slot(int st, int j, int R) {
+  const int x = st + j;
+  return x >= R ? x - R : x;
+}
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ float dot4(const float4 a, const float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
@@ -277,49 +334,86 @@ __device__ __forceinline__ void quantize_store(const float4 x, bool live_row, in
   }
 }
 
+
+
+// Identity of one unit, written by the producer into its stage.
+struct UnitDesc {
+  long long gh;  // flattened (sequence, head)
+  int b, hh, g;
+  int c, st, J;  // committed records, ring start, records used by this unit's head
+  int r0, ur;    // first row and row count of the unit
+  int gi;        // index of the unit's group among the groups this CTA loaded
+  int flags;
+};
+constexpr int kUnitFlush = 1;     // fold path (decode flush step, flush, quantize, conventional)
+constexpr int kUnitEnd = 2;       // sentinel: no more units
+constexpr int kUnitFirst = 4;     // unit 0 of its head: appends the decays
+constexpr int kUnitKeyOwner = 8;  // unit 0 of its group's first head: appends the keys
+
 // ============================================================================
 // The head kernel.
 // ============================================================================
+// Records are numbered j = 0..J-1 in arrival order after the checkpoint:
+// committed records j < c live in the ring at slot (start + j) mod R; the
+// decode step's own record is j = c; verify drafts are j = c..c+T-1.
+// Work is cut into units (one head, rows r0..r0+ur-1). The producer loads
+// units in order into the stage ring. Consumer warps claim units in that
+// order from a shared counter, so all stages form one pool.
 template <int MODE, int N, typename TIn, int RF>
 __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
-  constexpr int LPR = N / 4;    // lanes per FP32 row (4 columns per lane)
+  constexpr int LPR = N / 4;     // lanes per FP32 row (4 columns per lane)
   constexpr int RPI = 32 / LPR;  // rows per warp instruction
   static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "N must be 4..128, power of two");
+  constexpr int ES = In<TIn>::kBytes;
+  constexpr int CHN = N * ES / 16;  // 16-byte chunks per k or q row
+  constexpr int kSubRows = kKR * RPI;  // rows of one sub-pass
   constexpr bool kAppendMode = (MODE == kDecode || MODE == kVerify);
+  constexpr bool kGroupData = (MODE != kQuant);
+  constexpr bool kQuery = (MODE == kDecode || MODE == kVerify || MODE == kConv);
+  constexpr int kFullCount = 1 + 32;  // producer lane 0 (tile bytes) + 32 gather arrivals
 
   extern __shared__ __align__(128) uint8_t smem[];
-  float* Kt = reinterpret_cast<float*>(smem + p.kt_off);    // [J][N] keys of the current group
-  float* Qt = reinterpret_cast<float*>(smem + p.qt_off);    // [nq][N] queries of the current group
-  float* sKQ = reinterpret_cast<float*>(smem + p.skq_off);  // [nq][R] k_j^T q_tau
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  // bars: full[stages], empty[stages], group, end; then the abort flag
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 2);
+  // bars: full[kMaxStages], empty[kMaxStages], gfull[2], gempty[2], end, then the
+  // abort flag and the claim counter, then the producer's table of value rows.
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 5);
+  int* claim = reinterpret_cast<int*>(bars + 2 * kMaxStages + 6);
+  const uint8_t** vtab = reinterpret_cast<const uint8_t**>(bars + 2 * kMaxStages + 8);  // [kRMax] v_j row 0
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+  const uint32_t gfull0 = smem_u32(bars + 2 * kMaxStages), gempty0 = smem_u32(bars + 2 * kMaxStages + 2);
+  const uint32_t end_bar = smem_u32(bars + 2 * kMaxStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = (long long)p.B * p.H;
   const long long h0 = (long long)blockIdx.x * total / gridDim.x;
   const long long h1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
-  const uint32_t grp_bar = smem_u32(bars + 2 * kMaxStages), end_bar = smem_u32(bars + 2 * kMaxStages + 1);
+  const int nq = (MODE == kVerify) ? p.T : 1;
+  const int gcap = p.HPG * p.U;  // units of a whole group
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kNCW);
+      mbar_init(full0 + 8 * s, kFullCount);
+      mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(grp_bar, kNCW * 32);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(gfull0 + 8 * s, 32);
+      mbar_init(gempty0 + 8 * s, gcap);
+    }
     mbar_init(end_bar, kThreads);
     *abort_flag = 0;
+    *claim = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // Per-sequence decision shared by producer and consumers (both read the same
-  // count[b]; no thread writes pointers before every CTA of b is done).
-  //   returns records J to use (>=0) and whether the head tile is loaded.
+  // Per-sequence plan: the producer uses it per unit, thread 0 again for the
+  // pointer update. Nobody writes pointers before every CTA of b has finished.
   auto seq_plan = [&](int b, int& c, int& st, bool& load, bool& flush, bool& bad) {
     c = 0; st = 0; flush = false; bad = false; load = true;
-    if constexpr (MODE == kConv || MODE == kQuant) return;
+    if constexpr (MODE == kConv || MODE == kQuant) {
+      flush = true;
+      return;
+    }
     c = p.count[b];
     st = p.start[b];
     if constexpr (MODE == kDecode) {
@@ -334,208 +428,290 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       load = flush;
     }
   };
+  auto records = [&](int c) -> int {
+    if constexpr (MODE == kDecode) return c + 1;
+    else if constexpr (MODE == kVerify) return c + p.T;
+    else if constexpr (MODE == kFlush) return c;
+    else if constexpr (MODE == kConv) return 1;
+    else return 0;
+  };
 
   if (warp == kNCW) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int li = 0, cur_b = -1, c = 0, st = 0;
-      bool load = false, flush = false, bad = false;
-      bool ok = true;
-      const uint32_t f32_bytes = (uint32_t)p.P * N * 4;
-      for (long long gh = h0; gh < h1 && ok; ++gh) {
-        const int b = (int)(gh / p.H);
-        if (b != cur_b) {
-          cur_b = b;
-          seq_plan(b, c, st, load, flush, bad);
+    // ====================================================================== producer
+    int li = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
+    long long cur_gg = -1;
+    bool load = false, flush = false, bad = false, ok = true;
+    const int vcp = 1 << p.vcp_lg;              // lanes per value row (power of two)
+    const int vch = lane & (vcp - 1);            // this lane's chunk within a value row
+    const int vj0 = lane >> p.vcp_lg, vdj = 32 >> p.vcp_lg;
+    long long gfirst = 0;
+    // acquire the next stage (bounded wait, warp-uniform result)
+    auto acquire = [&](int& s) -> bool {
+      s = li & (p.stages - 1);
+      const int use = li >> p.lgS;
+      const bool w = use == 0 || mbar_wait(empty0 + 8 * s, (use - 1) & 1, abort_flag, p.err);
+      return __all_sync(kFull, w);
+    };
+    HeadIter it;
+    it.init(h0, p.H, p.HPG);
+    for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
+      const int b = it.b, hh = it.hh, g = it.g;
+      const long long gg = (long long)b * p.G + g;
+      const size_t hrow = (size_t)gh;
+      if (b != cur_b) {
+        cur_b = b;
+        seq_plan(b, c, st, load, flush, bad);
+        if (bad && lane == 0) atomicOr(p.err, kErrCapacity);
+        J = records(c);
+        cur_gg = -1;
+      }
+      if (!load) continue;
+      if constexpr (kGroupData) {
+        if (gg != cur_gg) {
+          cur_gg = gg;
+          gfirst = (long long)b * p.H + (long long)g * p.HPG;
+          const int gs = gi & 1, guse = gi >> 1;
+          const bool w = guse == 0 || mbar_wait(gempty0 + 8 * gs, (guse - 1) & 1, abort_flag, p.err);
+          if (!__all_sync(kFull, w)) { ok = false; break; }
+          if (lane == 0) {  // arrive for the units of this group that other CTAs own
+            const long long nh = min(h1, gfirst + p.HPG) - max(h0, gfirst);
+            const int extra = gcap - (int)nh * p.U;
+            if (extra > 0) mbar_arrive_n(gempty0 + 8 * gs, extra);
+          }
+          const uint32_t gdst = smem_u32(smem + p.gb_off + gs * p.gb_bytes);
+          const size_t grow = (size_t)b * p.G + g;
+          for (int idx = lane; idx < J * CHN; idx += 32) {
+            const int j = idx / CHN, ch = idx % CHN;  // CHN is a power of two
+            const uint8_t* src;
+            if (MODE == kConv || (MODE == kDecode && j >= c))
+              src = reinterpret_cast<const uint8_t*>(p.k) + grow * N * ES;
+            else if (j < c)
+              src = reinterpret_cast<const uint8_t*>(p.ring_k) + (grow * p.R + ring_slot(st, j, p.R)) * N * ES;
+            else  // verify draft j - c
+              src = reinterpret_cast<const uint8_t*>(p.k) + (((size_t)b * p.T + (j - c)) * p.G + g) * N * ES;
+            cp_async16(gdst + j * N * ES + ch * 16, src + ch * 16);
+          }
+          if constexpr (kQuery) {
+            for (int idx = lane; idx < nq * CHN; idx += 32) {
+              const int t = idx / CHN, ch = idx % CHN;
+              const size_t row = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
+              cp_async16(gdst + p.gq_off + t * N * ES + ch * 16,
+                         reinterpret_cast<const uint8_t*>(p.q) + row * N * ES + ch * 16);
+            }
+          }
+          cp_async_arrive(gfull0 + 8 * gs);
+          ++gi;
         }
-        if (!load) continue;
-        const int s = li % p.stages, use = li / p.stages;
-        if (use > 0 && !mbar_wait(empty0 + 8 * s, (use - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
-        const void* src = from_copy ? (const void*)(p.copy + (size_t)gh * p.head_stride)
-                                    : (const void*)(p.ckpt + (size_t)gh * p.P * N);
-        const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : f32_bytes;
-        const uint32_t dst = smem_u32(smem + (size_t)s * p.stage_bytes);
-        mbar_arrive_tx(full0 + 8 * s, bytes);
-        tma_load_1d(dst, src, bytes, full0 + 8 * s);
+      }
+      // record sources of this head: lane j keeps alpha_j's address and publishes
+      // the address of v_j's row 0 in the shared table used by every unit
+      const float* asrc = nullptr;
+      __syncwarp();  // the previous head's units have read the table
+      if (lane < J) {
+        const int j = lane;
+        const uint8_t* vsrc;
+        if (MODE == kConv) {
+          asrc = p.alpha + hrow;
+          vsrc = reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
+        } else if (j < c) {
+          const int slot = ring_slot(st, j, p.R);
+          asrc = p.ring_a + hrow * p.Rp + slot;
+          vsrc = reinterpret_cast<const uint8_t*>(p.ring_v) + (hrow * p.R + slot) * p.P * ES;
+        } else if (MODE == kVerify) {
+          asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
+          vsrc = reinterpret_cast<const uint8_t*>(p.v) + (((size_t)b * p.T + (j - c)) * p.H + hh) * p.P * ES;
+        } else {
+          asrc = p.alpha + hrow;
+          vsrc = reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
+        }
+        vtab[j] = vsrc;
+      }
+      __syncwarp();
+      const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
+      for (int u = 0; u < p.U; ++u) {
+        const int r0 = u * p.UR, ur = min(p.UR, p.P - r0);
+        int s;
+        if (!acquire(s)) { ok = false; break; }
+        uint8_t* stg = smem + (size_t)s * p.stage_bytes;
+        const uint32_t sdst = smem_u32(stg);
+        if (lane == 0) {
+          UnitDesc* d = reinterpret_cast<UnitDesc*>(stg + p.sm_off);
+          d->gh = gh; d->b = b; d->hh = hh; d->g = g;
+          d->c = c; d->st = st; d->J = J; d->r0 = r0; d->ur = ur; d->gi = gi - 1;
+          d->flags = (flush ? kUnitFlush : 0) | (u == 0 ? kUnitFirst : 0) |
+                     ((u == 0 && gh == gfirst) ? kUnitKeyOwner : 0);
+          if (!from_copy) {
+            const uint32_t bytes = (uint32_t)ur * N * 4;
+            mbar_arrive_tx(full0 + 8 * s, bytes);
+            tma_load_1d(sdst, p.ckpt + (hrow * p.P + r0) * N, bytes, full0 + 8 * s);
+          } else {
+            const uint8_t* hc = p.copy + hrow * p.head_stride;
+            const uint32_t rs_bytes = (uint32_t)ur * 4;
+            if constexpr (RF == kRfE4m3) {
+              const uint32_t cb = (uint32_t)ur * N;
+              mbar_arrive_tx(full0 + 8 * s, cb + rs_bytes);
+              tma_load_1d(sdst, hc + (size_t)r0 * N, cb, full0 + 8 * s);
+            } else {
+              const uint32_t cb = (uint32_t)ur * (N / 2), bb = (uint32_t)ur * (N / 16);
+              mbar_arrive_tx(full0 + 8 * s, cb + bb + rs_bytes);
+              tma_load_1d(sdst, hc + (size_t)r0 * (N / 2), cb, full0 + 8 * s);
+              tma_load_1d(sdst + p.cbs_off, hc + p.bsc_off + (size_t)r0 * (N / 16), bb, full0 + 8 * s);
+            }
+            tma_load_1d(sdst + p.crs_off, hc + p.rsc_off + (size_t)r0 * 4, rs_bytes, full0 + 8 * s);
+          }
+        }
+        if (lane < J) cp_async4(sdst + p.sa_off + 4 * lane, asrc);
+        // value rows r0..r0+ur-1 of every record: lane copies chunk vch of records vj0, vj0+vdj, ...
+        if (vch < ur * ES / 16) {
+          const int soff = r0 * ES + vch * 16;
+          for (int j = vj0; j < J; j += vdj)
+            cp_async16(sdst + p.sv_off + j * p.UR * ES + vch * 16, vtab[j] + soff);
+        }
+        cp_async_arrive(full0 + 8 * s);
         ++li;
       }
-      if (!ok) {  // drain the copies still in flight (bounded), then leave
-        for (int i = (li > p.stages ? li - p.stages : 0); i < li; ++i) {
-          volatile int dummy = 0;
-          mbar_wait(full0 + 8 * (i % p.stages), (i / p.stages) & 1, &dummy, p.err);
-        }
+    }
+    // one end marker per consumer warp
+    for (int k = 0; k < kNCW && ok; ++k) {
+      int s;
+      if (!acquire(s)) { ok = false; break; }
+      if (lane == 0) {
+        reinterpret_cast<UnitDesc*>(smem + (size_t)s * p.stage_bytes + p.sm_off)->flags = kUnitEnd;
+        mbar_arrive(full0 + 8 * s);
       }
+      cp_async_arrive(full0 + 8 * s);
+      ++li;
+    }
+    cp_async_wait_all();
+    if (!ok && lane == 0) {  // drain the bulk copies still in flight (bounded), then leave
+      volatile int dummy = 0;
+      for (int i = (li > p.stages ? li - p.stages : 0); i < li; ++i)
+        mbar_wait(full0 + 8 * (i & (p.stages - 1)), (i >> p.lgS) & 1, &dummy, p.err);
     }
   } else {
-    // ---------------------------------------------------------------- consumers
-    const int ct = threadIdx.x;  // 0..255
+    // ====================================================================== consumers
     const int col4 = lane % LPR, rsub = lane / LPR;
     float* wsc = reinterpret_cast<float*>(smem + p.wsc_off) + warp * p.wsc_floats;  // per-warp scratch
-    int li = 0, gphase = 0;
-    long long cur_gg = -1;
-    int cur_b = -1, c = 0, st = 0, J = 0;
-    bool load = false, flush = false, bad = false;
+    float* skq_w = wsc;                          // [kTMax][kRMax] k_j^T q_t of the current group
+    float* cw = wsc + kTMax * kRMax;             // [kTMax][kRMax] coefficients of the current unit
+    float* gw = cw + kTMax * kRMax;              // [kTMax] cumulative decays g_{1:c+t+1}
+    float* uwork = gw + 16;                      // [R][RPI][kKR] scaled values of the fold
+    int last_gi = -1;
+    const uint8_t* gK = nullptr;  // keys of the current group (input dtype), rows j
+    const uint8_t* gQ = nullptr;  // queries of the current group
+    float sj = 0.f;               // decode: lane j holds k_j^T q
     float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
     constexpr int CPL = (RF == kRfE2m1) ? 32 : 16;  // copy-tile columns per lane
     constexpr int LPRc = (N / CPL) > 0 ? (N / CPL) : 1;
     constexpr int RPIc = 32 / LPRc;
     constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
     float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
-    const int nq = (MODE == kVerify) ? p.T : 1;
-    const int rows_pass = kNCW * kKR * RPI;
-    const int npass = (p.P + rows_pass - 1) / rows_pass;
 
-    auto group_sync = [&]() -> bool {
-      mbar_arrive(grp_bar);
-      const bool r = mbar_wait(grp_bar, gphase, abort_flag, p.err);
-      gphase ^= 1;
-      return r;
-    };
-
-    bool ok = true;
-    for (long long gh = h0; gh < h1 && ok; ++gh) {
-      const int b = (int)(gh / p.H), hh = (int)(gh % p.H), g = hh / p.HPG;
-      const long long gg = (long long)b * p.G + g;
-      if (b != cur_b) {
-        cur_b = b;
-        seq_plan(b, c, st, load, flush, bad);
-        if (bad && ct == 0) atomicOr(p.err, kErrCapacity);
-        if constexpr (MODE == kDecode) J = c + 1;
-        else if constexpr (MODE == kVerify) J = c + p.T;
-        else if constexpr (MODE == kFlush) J = c;
-        else if constexpr (MODE == kConv) J = 1;
-        else J = 0;
-        cur_gg = -1;
-      }
-      if (!load) continue;
-      if (gg != cur_gg) {
-        // ------------------------------------------------ group set-up
-        cur_gg = gg;
-        if (!group_sync()) { ok = false; break; }
-        const size_t kbase = (size_t)(b * p.G + g) * p.R;  // ring row of this group
-        const bool first_cta_of_group = ((long long)b * p.H + (long long)g * p.HPG) >= h0;
-        for (int idx = ct; idx < J * N; idx += kNCW * 32) {
-          const int j = idx / N, n = idx % N;
-          float val;
-          if constexpr (MODE == kConv) {
-            val = In<TIn>::ld(p.k, (size_t)(b * p.G + g) * N + n);
-          } else if (j < c) {
-            val = In<TIn>::ld(p.ring_k, (kbase + (st + j) % p.R) * N + n);
-          } else if constexpr (MODE == kDecode) {
-            val = In<TIn>::ld(p.k, (size_t)(b * p.G + g) * N + n);
-            if (first_cta_of_group && !flush) copy_raw<TIn>(p.ring_k, (kbase + (st + j) % p.R) * N + n, p.k, (size_t)(b * p.G + g) * N + n);
-          } else if constexpr (MODE == kVerify) {
-            const size_t si = ((size_t)(b * p.T + (j - c)) * p.G + g) * N + n;
-            val = In<TIn>::ld(p.k, si);
-            if (first_cta_of_group) copy_raw<TIn>(p.ring_k, (kbase + (st + j) % p.R) * N + n, p.k, si);
-          } else {
-            val = 0.f;
-          }
-          Kt[idx] = val;
-        }
-        if constexpr (MODE == kDecode || MODE == kConv || MODE == kVerify) {
-          for (int idx = ct; idx < nq * N; idx += kNCW * 32) {
-            const int t = idx / N, n = idx % N;
-            const size_t si = (MODE == kVerify) ? ((size_t)(b * p.T + t) * p.G + g) * N + n : (size_t)(b * p.G + g) * N + n;
-            Qt[idx] = In<TIn>::ld(p.q, si);
-          }
-        }
-        if (!group_sync()) { ok = false; break; }
-        if constexpr (MODE == kDecode || MODE == kVerify) {
-          // k_j^T q_tau for all pairs: 8 threads per pair, strided over N
-          const int npair = J * nq;
-          for (int base = 0; base < npair * 8; base += kNCW * 32) {
-            const int idx = base + ct;
-            const int pr = idx >> 3, sub = idx & 7;
-            float acc = 0.f;
-            if (pr < npair) {
-              const int t = pr / J, j = pr % J;
-              for (int n = sub; n < N; n += 8) acc = fmaf(Kt[j * N + n], Qt[t * N + n], acc);
-            }
-            acc += __shfl_xor_sync(kFull, acc, 4);
-            acc += __shfl_xor_sync(kFull, acc, 2);
-            acc += __shfl_xor_sync(kFull, acc, 1);
-            if (pr < npair && sub == 0) sKQ[(pr / J) * p.R + (pr % J)] = acc;
-          }
-          if (!group_sync()) { ok = false; break; }
-        }
-        if constexpr (MODE == kDecode || MODE == kConv) q4 = lds4(Qt + col4 * 4);
-        if constexpr (RF != kRfNone && MODE == kDecode) {
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) qc[i] = Qt[(lane % LPRc) * CPL + i];
-        }
-      }
-
-      // ---------------------------------------------------- wait for the tile
-      const int s = li % p.stages;
-      if (!mbar_wait(full0 + 8 * s, (li / p.stages) & 1, abort_flag, p.err)) { ok = false; break; }
+    while (true) {
+      int li = 0;
+      if (lane == 0) li = atomicAdd(claim, 1);
+      li = __shfl_sync(kFull, li, 0);
+      const int s = li & (p.stages - 1);
+      if (!__all_sync(kFull, mbar_wait(full0 + 8 * s, (li >> p.lgS) & 1, abort_flag, p.err))) break;
       const uint8_t* tile = smem + (size_t)s * p.stage_bytes;
-      const float* tf = reinterpret_cast<const float*>(tile);
-      const size_t hrow = (size_t)b * p.H + hh;  // (b, h) index
+      const UnitDesc d = *reinterpret_cast<const UnitDesc*>(tile + p.sm_off);
+      if (d.flags & kUnitEnd) break;
+      const int b = d.b, hh = d.hh, c = d.c, st = d.st, J = d.J, r0 = d.r0, ur = d.ur;
+      const size_t hrow = (size_t)d.gh;
+      const bool flush = (d.flags & kUnitFlush) != 0;
 
-      // record accessors: decays a(j), values v(j,row) for record j (0-based)
-      auto rec_v = [&](int j, int row) -> float {
-        if constexpr (MODE == kConv) return In<TIn>::ld(p.v, hrow * p.P + row);
-        if (j < c) return In<TIn>::ld(p.ring_v, (hrow * p.R + (st + j) % p.R) * p.P + row);
-        if constexpr (MODE == kVerify) return In<TIn>::ld(p.v, ((size_t)(b * p.T + (j - c)) * p.H + hh) * p.P + row);
-        return In<TIn>::ld(p.v, hrow * p.P + row);
-      };
-      float aj = 1.f;  // lane j holds alpha_{j+1}
-      if (lane < J) {
-        if constexpr (MODE == kConv) aj = p.alpha[hrow];
-        else if (lane < c) aj = p.ring_a[hrow * p.Rp + (st + lane) % p.R];
-        else if constexpr (MODE == kVerify) aj = p.alpha[((size_t)b * p.T + (lane - c)) * p.H + hh];
-        else aj = p.alpha[hrow];
-      }
-
-      // ---------------------------------------------------- appends
-      if constexpr (kAppendMode) {
-        const bool do_append = (MODE == kVerify) || !flush;
-        if (do_append) {
-          const int na = (MODE == kVerify) ? p.T : 1;
-          for (int idx = ct; idx < na * p.P; idx += kNCW * 32) {
-            const int t = idx / p.P, row = idx % p.P;
-            const size_t dst = (hrow * p.R + (st + c + t) % p.R) * p.P + row;
-            const size_t src = (MODE == kVerify) ? ((size_t)(b * p.T + t) * p.H + hh) * p.P + row : hrow * p.P + row;
-            copy_raw<TIn>(p.ring_v, dst, p.v, src);
+      if constexpr (kGroupData) {
+        if (d.gi != last_gi) {
+          // ---------------------------------------------- this warp enters the unit's group
+          last_gi = d.gi;
+          const int gs = d.gi & 1;
+          if (!__all_sync(kFull, mbar_wait(gfull0 + 8 * gs, (d.gi >> 1) & 1, abort_flag, p.err))) break;
+          gK = smem + p.gb_off + gs * p.gb_bytes;
+          gQ = gK + p.gq_off;
+          if constexpr (MODE == kDecode || MODE == kVerify) {
+            // k_j^T q_t: one pair per lane, N/4 chunks visited from a lane-dependent start
+            const int npair = J * nq;
+            for (int pr = lane; pr < ((npair + 31) & ~31); pr += 32) {
+              float acc = 0.f;
+              const int t = (nq == 1) ? 0 : pr / J;
+              const int j = pr - t * J;
+              if (pr < npair) {
+#pragma unroll 8
+                for (int i = 0; i < N / 4; ++i) {
+                  const int c4 = (i + lane) & (N / 4 - 1);
+                  acc += dot4(In<TIn>::lds4(gK, j * N + 4 * c4), In<TIn>::lds4(gQ, t * N + 4 * c4));
+                }
+              }
+              if constexpr (MODE == kDecode) {
+                sj = acc;  // npair = J <= 32: one pass, lane j holds k_j^T q
+              } else {
+                if (pr < npair) skq_w[t * kRMax + j] = acc;
+              }
+            }
+            __syncwarp();
           }
-          if (ct < na) {
-            const size_t src = (MODE == kVerify) ? ((size_t)b * p.T + ct) * p.H + hh : hrow;
-            p.ring_a[hrow * p.Rp + (st + c + ct) % p.R] = p.alpha[src];
+          if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
+          if constexpr (RF != kRfNone && MODE == kDecode) {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) qc[i] = In<TIn>::lds(gQ, (lane % LPRc) * CPL + i);
           }
         }
       }
 
-      const bool fold = (MODE == kConv) || (MODE == kQuant) || (MODE == kFlush) || (MODE == kDecode && flush);
+      const float* tf = reinterpret_cast<const float*>(tile);
+      const float* sa = reinterpret_cast<const float*>(tile + p.sa_off);  // alpha_j, record order
+      const uint8_t* sv = tile + p.sv_off;                                // v_j rows r0.., stride UR
+      const float aj = (lane < J) ? sa[lane] : 1.f;                        // lane j holds alpha of record j
+      const int nsp = (ur + kSubRows - 1) / kSubRows;                      // sub-passes of this unit
+
+      // ---------------------------------------------------- appends (from shared memory)
+      if constexpr (kAppendMode) {
+        const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
+        const int cu = ur * ES / 16;  // <= 32 chunks per value row of the unit
+        for (int t = 0; t < na; ++t) {
+          if (lane < cu) {
+            const uint4 val = *reinterpret_cast<const uint4*>(sv + ((c + t) * p.UR) * ES + lane * 16);
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_v) +
+                                      ((hrow * p.R + ring_slot(st, c + t, p.R)) * p.P + r0) * ES + lane * 16) = val;
+          }
+        }
+        if ((d.flags & kUnitFirst) && lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[c + lane];
+        if (d.flags & kUnitKeyOwner) {  // the group's first head appends the new keys
+          const size_t grow = (size_t)b * p.G + d.g;
+          for (int idx = lane; idx < na * CHN; idx += 32) {
+            const int t = idx / CHN, ch = idx % CHN;
+            const uint4 val = *reinterpret_cast<const uint4*>(gK + (c + t) * N * ES + ch * 16);
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_k) +
+                                      (grow * p.R + ring_slot(st, c + t, p.R)) * N * ES + ch * 16) = val;
+          }
+        }
+      }
+
       if constexpr (MODE == kVerify) {
         // ================================================ verify (T queries)
-        // per query tau: x_j = alpha_j for j < c+tau+1 else 1
-        float* cw = wsc;                 // [kTMax][kRMax] coefficients
-        float* gw = wsc + kTMax * kRMax;  // [kTMax] g_{1:c+tau+1}
         for (int t = 0; t < p.T; ++t) {
           const int ht = c + t + 1;
           const float x = (lane < ht) ? aj : 1.f;
           const float incl = suffix_prod(x, lane);
           const float nxt = __shfl_down_sync(kFull, incl, 1);
           const float w = (lane < 31) ? nxt : 1.f;
-          cw[t * kRMax + lane] = (lane < ht) ? w * sKQ[t * p.R + lane] : 0.f;
+          cw[t * kRMax + lane] = (lane < ht) ? w * skq_w[t * kRMax + lane] : 0.f;
           if (lane == 0) gw[t] = incl;
         }
         __syncwarp();
-        for (int pass = 0; pass < npass; ++pass) {
-          const int rbase = (pass * kNCW + warp) * kKR;
+        for (int sp = 0; sp < nsp; ++sp) {
           for (int t0 = 0; t0 < p.T; t0 += kTQ) {
             float4 qv[kTQ];
 #pragma unroll
-            for (int t = 0; t < kTQ; ++t) qv[t] = (t0 + t < p.T) ? lds4(Qt + (t0 + t) * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int t = 0; t < kTQ; ++t)
+              qv[t] = (t0 + t < p.T) ? In<TIn>::lds4(gQ, (t0 + t) * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
             float part[kKR * kTQ];
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
-              const int row = (rbase + kk) * RPI + rsub;
-              const float4 sv = (row < p.P) ? lds4(tf + ((size_t)row * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const int lr = (sp * kKR + kk) * RPI + rsub;
+              const float4 x4 = (lr < ur) ? lds4(tf + ((size_t)lr * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-              for (int t = 0; t < kTQ; ++t) part[kk * kTQ + t] = dot4(sv, qv[t]);
+              for (int t = 0; t < kTQ; ++t) part[kk * kTQ + t] = dot4(x4, qv[t]);
             }
             int off = 0;
             TRed<kKR * kTQ, LPR / 2>::run(part, lane, off);
@@ -545,28 +721,26 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
               const int kk = (off + i) / kTQ, t = t0 + (off + i) % kTQ;
-              const int row = (rbase + kk) * RPI + rsub;
-              const bool valid = row < p.P && t < p.T;
+              const int lr = (sp * kKR + kk) * RPI + rsub;
+              const bool valid = lr < ur && t < p.T;
               float ov = 0.f;
               if (valid) {
-                for (int j = dup; j < J; j += D) ov = fmaf(cw[t * kRMax + j], rec_v(j, row), ov);
+                for (int j = dup; j < J; j += D) ov = fmaf(cw[t * kRMax + j], In<TIn>::lds(sv, j * p.UR + lr), ov);
               }
               ov = low_sum<D>(ov);
-              if (dup == 0 && valid) p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = fmaf(gw[t], part[i], ov);
+              if (dup == 0 && valid) p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + r0 + lr] = fmaf(gw[t], part[i], ov);
             }
           }
         }
-        __syncwarp();
-      } else if (fold) {
+      } else if (flush) {
         // ================================================ fold path
-        // S_new = g_{1:J} S + sum_j (g_{j+1:J} v_j) k_j^T ; store ; o = S_new q
+        // S_new = g_{1:J} S + sum_j (g_{j+2:J} v_j) k_j^T ; store ; o = S_new q (decode, conv)
         const float incl = suffix_prod(aj, lane);
         const float nxt = __shfl_down_sync(kFull, incl, 1);
-        const float wj = (lane < 31) ? nxt : 1.f;  // lane j: g_{j+2:J}, the weight of record j+1
+        const float wj = (lane < 31) ? nxt : 1.f;  // lane j: weight of record j
         const float gam = __shfl_sync(kFull, incl, 0);
-        for (int pass = 0; pass < npass; ++pass) {
-          const int rbase = (pass * kNCW + warp) * kKR;  // first row-instruction of this warp
-          // u[(j*RPI + rs)*KR + k] = w_j * v_j[row]
+        for (int sp = 0; sp < nsp; ++sp) {
+          // uwork[(j*RPI + rs)*KR + k] = w_j * v_j[row]
           const int nu = J * RPI * kKR;
           for (int base = 0; base < nu; base += 32) {
             const int idx = base + lane;
@@ -574,25 +748,25 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             const float wsel = __shfl_sync(kFull, wj, j);
             if (idx < nu) {
               const int rem = idx % (RPI * kKR), rs = rem / kKR, kk = rem % kKR;
-              const int row = (rbase + kk) * RPI + rs;
-              wsc[idx] = (row < p.P) ? wsel * rec_v(j, row) : 0.f;
+              const int lr = (sp * kKR + kk) * RPI + rs;
+              uwork[idx] = (lr < ur) ? wsel * In<TIn>::lds(sv, j * p.UR + lr) : 0.f;
             }
           }
           __syncwarp();
           float4 acc[kKR];
 #pragma unroll
           for (int kk = 0; kk < kKR; ++kk) {
-            const int row = (rbase + kk) * RPI + rsub;
-            if (row < p.P) {
-              const float4 sv = lds4(tf + ((size_t)row * LPR + col4) * 4);
-              acc[kk] = make_float4(gam * sv.x, gam * sv.y, gam * sv.z, gam * sv.w);
+            const int lr = (sp * kKR + kk) * RPI + rsub;
+            if (lr < ur) {
+              const float4 x = lds4(tf + ((size_t)lr * LPR + col4) * 4);
+              acc[kk] = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
             } else {
               acc[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
           for (int j = 0; j < J; ++j) {
-            const float4 kv = lds4(Kt + j * N + col4 * 4);
-            const float* uj = wsc + (j * RPI + rsub) * kKR;
+            const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
+            const float* uj = uwork + (j * RPI + rsub) * kKR;
             const float4 u0 = lds4(uj), u1 = lds4(uj + 4);
             const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
@@ -603,16 +777,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               acc[kk].w = fmaf(uu[kk], kv.w, acc[kk].w);
             }
           }
-          // store the new checkpoint (or state) and refresh the read copy
 #pragma unroll
           for (int kk = 0; kk < kKR; ++kk) {
-            const int row = (rbase + kk) * RPI + rsub;
-            const bool live_row = row < p.P;
+            const int lr = (sp * kKR + kk) * RPI + rsub;
+            const bool live_row = lr < ur;
+            const int row = r0 + lr;
             if constexpr (MODE != kQuant) {
               if (live_row) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
             }
             if constexpr (RF != kRfNone && MODE != kConv) {
-              // rows beyond P still join the shuffles with zeros
+              // rows beyond the unit still join the shuffles, with zeros
               quantize_store<RF, LPR>(acc[kk], live_row, row, col4, N, p.copy + hrow * p.head_stride, p.bsc_off,
                                       p.rsc_off);
             }
@@ -627,8 +801,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             constexpr int D = (LPR / kKR) > 0 ? (LPR / kKR) : 1;
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
-              const int row = (rbase + off + i) * RPI + rsub;
-              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = part[i];
+              const int lr = (sp * kKR + off + i) * RPI + rsub;
+              if ((lane & (D - 1)) == 0 && lr < ur) p.o[hrow * p.P + r0 + lr] = part[i];
             }
           }
           __syncwarp();
@@ -639,15 +813,15 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const float nxt = __shfl_down_sync(kFull, incl, 1);
         const float w = (lane < 31) ? nxt : 1.f;
         const float gam = __shfl_sync(kFull, incl, 0);
-        const float cj = (lane < J) ? w * sKQ[lane] : 0.f;  // g_{j+2:J} * k_{j+1}^T q
-        for (int pass = 0; pass < npass; ++pass) {
+        cw[lane] = (lane < J) ? w * sj : 0.f;  // coefficient of record j: g_{j+2:J} k_j^T q
+        __syncwarp();
+        for (int sp = 0; sp < nsp; ++sp) {
           if constexpr (RF == kRfNone) {
-            const int rbase = (pass * kNCW + warp) * kKR;
             float part[kKR];
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
-              const int row = (rbase + kk) * RPI + rsub;
-              part[kk] = (row < p.P) ? dot4(lds4(tf + ((size_t)row * LPR + col4) * 4), q4) : 0.f;
+              const int lr = (sp * kKR + kk) * RPI + rsub;
+              part[kk] = (lr < ur) ? dot4(lds4(tf + ((size_t)lr * LPR + col4) * 4), q4) : 0.f;
             }
             int off = 0;
             TRed<kKR, LPR / 2>::run(part, lane, off);
@@ -656,29 +830,26 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             const int dup = lane & (D - 1);
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
-              const int row = (rbase + off + i) * RPI + rsub;
+              const int lr = (sp * kKR + off + i) * RPI + rsub;
               float ov = 0.f;
-              for (int j = 0; j < J; ++j) {
-                const float cjj = __shfl_sync(kFull, cj, j);
-                if ((j & (D - 1)) == dup && row < p.P) ov = fmaf(cjj, rec_v(j, row), ov);
-              }
+              if (lr < ur)
+                for (int j = dup; j < J; j += D) ov = fmaf(cw[j], In<TIn>::lds(sv, j * p.UR + lr), ov);
               ov = low_sum<D>(ov);
-              if (dup == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[i], ov);
+              if (dup == 0 && lr < ur) p.o[hrow * p.P + r0 + lr] = fmaf(gam, part[i], ov);
             }
           } else {
             // read copy: lanes own CPL consecutive codes of a row
-            const int rows0 = (pass * kNCW + warp) * kKR * RPI;  // first row of this warp
             const int colc = lane % LPRc, rsc = lane / LPRc;
-            const float* rscale = reinterpret_cast<const float*>(tile + p.rsc_off);
+            const float* rscale = reinterpret_cast<const float*>(tile + p.crs_off);
             float part[KRc];
 #pragma unroll
             for (int kk = 0; kk < KRc; ++kk) {
-              const int row = rows0 + kk * RPIc + rsc;
+              const int lr = sp * kSubRows + kk * RPIc + rsc;
               float acc = 0.f;
-              if (row < p.P) {
+              if (lr < ur) {
                 if constexpr (RF == kRfE4m3) {
-                  const uint4 cw = *reinterpret_cast<const uint4*>(tile + (size_t)row * N + colc * 16);
-                  const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
+                  const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)lr * N + colc * 16);
+                  const uint32_t ws[4] = {cwd.x, cwd.y, cwd.z, cwd.w};
 #pragma unroll
                   for (int qd = 0; qd < 4; ++qd) {
                     float f[4];
@@ -687,9 +858,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                     for (int e = 0; e < 4; ++e) acc = fmaf(f[e], qc[qd * 4 + e], acc);
                   }
                 } else {
-                  const uint4 cw = *reinterpret_cast<const uint4*>(tile + (size_t)row * (N / 2) + colc * 16);
-                  const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
-                  const uint8_t* bsp = tile + p.bsc_off + row * (N / 16) + colc * 2;
+                  const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)lr * (N / 2) + colc * 16);
+                  const uint32_t ws[4] = {cwd.x, cwd.y, cwd.z, cwd.w};
+                  const uint8_t* bsp = tile + p.cbs_off + lr * (N / 16) + colc * 2;
                   float blk[2] = {0.f, 0.f};
 #pragma unroll
                   for (int qd = 0; qd < 4; ++qd) {
@@ -700,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                   }
                   acc = fmaf(dec_e4m3(bsp[0]), blk[0], dec_e4m3(bsp[1]) * blk[1]);
                 }
-                acc *= rscale[row];
+                acc *= rscale[lr];
               }
               part[kk] = acc;
             }
@@ -711,23 +882,23 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             const int dup = lane & (D - 1);
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
-              const int row = rows0 + (off + i) * RPIc + rsc;
+              const int lr = sp * kSubRows + (off + i) * RPIc + rsc;
               float ov = 0.f;
-              for (int j = 0; j < J; ++j) {
-                const float cjj = __shfl_sync(kFull, cj, j);
-                if ((j & (D - 1)) == dup && row < p.P) ov = fmaf(cjj, rec_v(j, row), ov);
-              }
+              if (lr < ur)
+                for (int j = dup; j < J; j += D) ov = fmaf(cw[j], In<TIn>::lds(sv, j * p.UR + lr), ov);
               ov = low_sum<D>(ov);
-              if (dup == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[i], ov);
+              if (dup == 0 && lr < ur) p.o[hrow * p.P + r0 + lr] = fmaf(gam, part[i], ov);
             }
           }
         }
       }
 
-      // ---------------------------------------------------- release the stage
+      // ---------------------------------------------------- release the stage and the group unit
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      ++li;
+      if (lane == 0) {
+        mbar_arrive(empty0 + 8 * s);
+        if constexpr (kGroupData) mbar_arrive(gempty0 + 8 * (d.gi & 1));
+      }
     }
   }
 
