@@ -58,6 +58,7 @@ rssm_status derive(const rssm_config* c, Geom* g) {
     return fail(RSSM_EUNSUPPORTED, "N=%d (supported: 16, 32, 64, 128)", c->N);
   if (c->P % 8) return fail(RSSM_EUNSUPPORTED, "P=%d must be a multiple of 8", c->P);
   if ((size_t)c->P * c->N * 4 > 64 * 1024) return fail(RSSM_EUNSUPPORTED, "P*N*4 > 64 KiB");
+  if (c->P > 128) return fail(RSSM_EUNSUPPORTED, "P=%d > 128", c->P);
   if (c->T_max > rssm::kTMax) return fail(RSSM_EUNSUPPORTED, "T_max=%d > %d", c->T_max, rssm::kTMax);
   const int R = c->L + c->T_max - 1;
   if (R > rssm::kRMax) return fail(RSSM_EUNSUPPORTED, "R = L + T_max - 1 = %d > %d", R, rssm::kRMax);
@@ -96,70 +97,35 @@ struct Plan {
   rssm::Params p{};
 };
 
-// Row units, stage ring and shared-memory carve for one launch (see Params in rssm_device.cuh).
+// Stage ring and shared-memory carve for one launch (see Params in rssm_device.cuh).
 rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
   using namespace rssm;
   auto a128 = [](size_t x) { return align_up(x, 128); };
-  const int P = c->P, N = c->N;
-  const size_t es = (size_t)g.esize;
-  const int rpi = 128 / N, sub_rows = kKR * rpi;
-  // U in {1,2,4,8}: the fewest units of at most two sub-passes each; UR a multiple of 8
-  int U = 1;
-  while (U < 8 && (P + U - 1) / U > 2 * sub_rows) U *= 2;
-  auto rows_per_unit = [&](int u) { return (int)align_up((size_t)((P + u - 1) / u), 8); };
-  int UR = rows_per_unit(U);
-  while (U > 1 && (U - 1) * UR >= P) {
-    U /= 2;
-    UR = rows_per_unit(U);
-  }
-  const int vchunks = UR * g.esize / 16;
-  int vcp_lg = 0;
-  while ((1 << vcp_lg) < vchunks) ++vcp_lg;
-  if (vcp_lg > 5) return fail(RSSM_EUNSUPPORTED, "unit value rows too long");
-  const size_t tile = (size_t)UR * N * 4;
-  const size_t sm_off = align_up(tile, 16);
-  const size_t sa_off = sm_off + 64;  // unit descriptor
+  const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
+  const size_t tile = P * N * 4;  // a read copy (head_stride bytes) is smaller
+  const size_t sa_off = align_up(tile, 16);
   const size_t sv_off = sa_off + (size_t)kRMax * 4;
-  const size_t stage = a128(sv_off + (size_t)g.R * UR * es);
-  size_t cbs_off = 0, crs_off = 0;
-  if (c->read_fmt == RSSM_READ_E4M3_ROW) {
-    crs_off = align_up((size_t)UR * N, 16);
-  } else if (c->read_fmt == RSSM_READ_E2M1_B16) {
-    cbs_off = (size_t)UR * N / 2;
-    crs_off = align_up(cbs_off + (size_t)UR * N / 16, 16);
-  }
-  const size_t gq_off = (size_t)g.R * N * es;
+  const size_t sc_off = align_up(sv_off + R * P * es, 16);
+  const size_t sc_floats = 16 + std::max({P, R * P, (size_t)kTMax * kRMax});
+  const size_t stage = a128(sc_off + sc_floats * 4);
+  const size_t gq_off = R * N * es;
   const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
-  const int wsc_floats = (int)align_up((size_t)2 * kTMax * kRMax + 16 + (size_t)g.R * rpi * kKR, 4);
-  const size_t wsc = a128((size_t)kNCW * wsc_floats * 4);
-  const size_t bars = a128((2 * kMaxStages + 8) * 8 + (size_t)kRMax * 8);  // barriers, flag, producer table
+  const size_t wsc = a128((size_t)kTMax * kRMax * 4);
+  const size_t bars = a128((4 * kMaxStages + 6) * 8);
   const size_t fixed = 2 * gb + wsc + bars;
   if (fixed + 2 * stage > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
-  int stages = 2;
-  while (stages * 2 <= kMaxStages && fixed + (size_t)stages * 2 * stage <= (size_t)kSmemMax) stages *= 2;
-  int lgS = 0;
-  while ((1 << lgS) < stages) ++lgS;
-  int lgU = 0;
-  while ((1 << lgU) < U) ++lgU;
+  const int stages = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage);
   rssm::Params& p = pl->p;
-  p.U = U;
-  p.lgU = lgU;
-  p.UR = UR;
   p.stages = stages;
-  p.lgS = lgS;
   p.stage_bytes = (int)stage;
-  p.sm_off = (int)sm_off;
   p.sa_off = (int)sa_off;
   p.sv_off = (int)sv_off;
-  p.cbs_off = (int)cbs_off;
-  p.crs_off = (int)crs_off;
-  p.vcp_lg = vcp_lg;
+  p.sc_off = (int)sc_off;
   size_t off = (size_t)stages * stage;
   p.gb_off = (int)off; off += 2 * gb;
   p.gb_bytes = (int)gb;
   p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
-  p.wsc_floats = wsc_floats;
   p.bar_off = (int)off; off += bars;
   pl->stages = stages;
   pl->smem = off;

@@ -29,13 +29,15 @@
 
 namespace rssm {
 
-constexpr int kNCW = 8;                    // consumer warps per CTA
-constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
+constexpr int kNDW = 8;                    // dot warps per CTA (stream the checkpoint tile)
+constexpr int kProducer = kNDW;            // warp that issues the copies
+constexpr int kCoef = kNDW + 1;            // warp that computes the per-head decay terms
+constexpr int kThreads = (kNDW + 2) * 32;
 constexpr int kKR = 8;                     // FP32-tile row-instructions per warp per pass
 constexpr int kTQ = 4;                     // verify queries per pass over the tile
 constexpr int kTMax = 8;                   // largest draft count
 constexpr int kRMax = 32;                  // largest ring (records per head)
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 8;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -60,17 +62,14 @@ struct Params {
   const void* k;       // decode/conv [B,G,N]; verify [B,T,G,N]
   const void* q;       // decode/conv [B,G,N]; verify [B,T,G,N]
   float* o;            // decode/conv [B,H,P]; verify [B,T,H,P]
-  // Each head is split into U (1, 2, 4 or 8) row units of UR rows (the last may
-  // be shorter); one consumer warp owns a whole unit.
-  int U, lgU, UR;
-  // Shared memory (bytes). `stages` (a power of two) stages of
-  // [unit tile | unit descriptor | alpha_j (kRMax fp32) | v_j rows of the unit (R x UR)];
-  // a read-copy tile keeps its block scales at cbs_off and row scales at crs_off.
-  int stages, lgS, stage_bytes, sm_off, sa_off, sv_off, cbs_off, crs_off;
-  int vcp_lg;  // log2 of the power of two >= 16-byte chunks per unit value row
+  // Shared memory (bytes). `stages` stages of
+  // [head tile (P x N fp32, or the read copy) | alpha_j (kRMax fp32) | v_j rows (R x P) | coefficients];
+  // coefficients: g (or g_t) at 0..15, then the value term [P], the scaled values
+  // [R][P] of a fold, or the verify weights [kTMax][kRMax].
+  int stages, stage_bytes, sa_off, sv_off, sc_off;
   // Two group areas of [k_j rows (R x N) | queries (kTMax x N)].
   int gb_off, gb_bytes, gq_off;
-  int wsc_off, wsc_floats, bar_off;  // per-warp scratch (floats each), barriers
+  int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
 };
 
 // ----------------------------------------------------------------- input types
@@ -336,29 +335,22 @@ __device__ __forceinline__ void quantize_store(const float4 x, bool live_row, in
 
 
 
-// Identity of one unit, written by the producer into its stage.
-struct UnitDesc {
-  long long gh;  // flattened (sequence, head)
-  int b, hh, g;
-  int c, st, J;  // committed records, ring start, records used by this unit's head
-  int r0, ur;    // first row and row count of the unit
-  int gi;        // index of the unit's group among the groups this CTA loaded
-  int flags;
-};
-constexpr int kUnitFlush = 1;     // fold path (decode flush step, flush, quantize, conventional)
-constexpr int kUnitEnd = 2;       // sentinel: no more units
-constexpr int kUnitFirst = 4;     // unit 0 of its head: appends the decays
-constexpr int kUnitKeyOwner = 8;  // unit 0 of its group's first head: appends the keys
-
 // ============================================================================
 // The head kernel.
 // ============================================================================
 // Records are numbered j = 0..J-1 in arrival order after the checkpoint:
 // committed records j < c live in the ring at slot (start + j) mod R; the
 // decode step's own record is j = c; verify drafts are j = c..c+T-1.
-// Work is cut into units (one head, rows r0..r0+ur-1). The producer loads
-// units in order into the stage ring. Consumer warps claim units in that
-// order from a shared counter, so all stages form one pool.
+//
+// Warp roles, all walking the CTA's heads in the same order over a ring of
+// stages:
+//   producer      bulk TMA of the head tile; cp.async gathers of alpha_j and v_j
+//                 into the stage, of k_j and the queries into the group area
+//   coefficients  per head: the decay scan g_{j+1:h}, and the value term
+//                 sum_j c_j v_j (non-flush), the scaled values g v_j (fold) or
+//                 the verify weights; published in the stage
+//   dot warps     stream the tile: rows . q, the reduction, the output (and the
+//                 fold's rank-J update, store and read-copy refresh)
 template <int MODE, int N, typename TIn, int RF>
 __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr int LPR = N / 4;     // lanes per FP32 row (4 columns per lane)
@@ -366,48 +358,45 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "N must be 4..128, power of two");
   constexpr int ES = In<TIn>::kBytes;
   constexpr int CHN = N * ES / 16;  // 16-byte chunks per k or q row
-  constexpr int kSubRows = kKR * RPI;  // rows of one sub-pass
   constexpr bool kAppendMode = (MODE == kDecode || MODE == kVerify);
   constexpr bool kGroupData = (MODE != kQuant);
   constexpr bool kQuery = (MODE == kDecode || MODE == kVerify || MODE == kConv);
-  constexpr int kFullCount = 1 + 32;  // producer lane 0 (tile bytes) + 32 gather arrivals
+  constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  // bars: full[kMaxStages], empty[kMaxStages], gfull[2], gempty[2], end, then the
-  // abort flag and the claim counter, then the producer's table of value rows.
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 5);
-  int* claim = reinterpret_cast<int*>(bars + 2 * kMaxStages + 6);
-  const uint8_t** vtab = reinterpret_cast<const uint8_t**>(bars + 2 * kMaxStages + 8);  // [kRMax] v_j row 0
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
-  const uint32_t gfull0 = smem_u32(bars + 2 * kMaxStages), gempty0 = smem_u32(bars + 2 * kMaxStages + 2);
-  const uint32_t end_bar = smem_u32(bars + 2 * kMaxStages + 4);
+  // bars: full[S] (tile), small[S] (gathers), coef[S], empty[S], gfull[2], gempty[2], end; abort flag
+  const uint32_t full0 = smem_u32(bars), small0 = smem_u32(bars + kMaxStages);
+  const uint32_t coef0 = smem_u32(bars + 2 * kMaxStages), empty0 = smem_u32(bars + 3 * kMaxStages);
+  const uint32_t gfull0 = smem_u32(bars + 4 * kMaxStages), gempty0 = smem_u32(bars + 4 * kMaxStages + 2);
+  const uint32_t end_bar = smem_u32(bars + 4 * kMaxStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kMaxStages + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = (long long)p.B * p.H;
   const long long h0 = (long long)blockIdx.x * total / gridDim.x;
   const long long h1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
   const int nq = (MODE == kVerify) ? p.T : 1;
-  const int gcap = p.HPG * p.U;  // units of a whole group
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(full0 + 8 * s, kFullCount);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(small0 + 8 * s, 32);
+      mbar_init(coef0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kNDW + 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(gfull0 + 8 * s, 32);
-      mbar_init(gempty0 + 8 * s, gcap);
+      mbar_init(gempty0 + 8 * s, kNDW + 1);
     }
     mbar_init(end_bar, kThreads);
     *abort_flag = 0;
-    *claim = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // Per-sequence plan: the producer uses it per unit, thread 0 again for the
-  // pointer update. Nobody writes pointers before every CTA of b has finished.
+  // Per-sequence plan, identical in every role: all read the same count[b], and
+  // nobody writes pointers before every CTA of b has finished.
   auto seq_plan = [&](int b, int& c, int& st, bool& load, bool& flush, bool& bad) {
     c = 0; st = 0; flush = false; bad = false; load = true;
     if constexpr (MODE == kConv || MODE == kQuant) {
@@ -435,23 +424,29 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     else if constexpr (MODE == kConv) return 1;
     else return 0;
   };
+  // Source of record j's value row 0 for head (b, hh).
+  auto vrow_src = [&](int j, int c, int st, int b, int hh, size_t hrow) -> const uint8_t* {
+    if (MODE == kConv) return reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
+    if (j < c) return reinterpret_cast<const uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, j, p.R)) * p.P * ES;
+    if (MODE == kVerify)
+      return reinterpret_cast<const uint8_t*>(p.v) + (((size_t)b * p.T + (j - c)) * p.H + hh) * p.P * ES;
+    return reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
+  };
 
-  if (warp == kNCW) {
+  // Stage bookkeeping shared by all roles: stage index and its phase parity.
+  int stg_i = 0, stg_ph = 0;
+  auto stage_next = [&]() {
+    if (++stg_i == p.stages) { stg_i = 0; stg_ph ^= 1; }
+  };
+
+  bool ok = true;
+  if (warp == kProducer) {
     // ====================================================================== producer
     int li = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
     long long cur_gg = -1;
-    bool load = false, flush = false, bad = false, ok = true;
-    const int vcp = 1 << p.vcp_lg;              // lanes per value row (power of two)
-    const int vch = lane & (vcp - 1);            // this lane's chunk within a value row
-    const int vj0 = lane >> p.vcp_lg, vdj = 32 >> p.vcp_lg;
-    long long gfirst = 0;
-    // acquire the next stage (bounded wait, warp-uniform result)
-    auto acquire = [&](int& s) -> bool {
-      s = li & (p.stages - 1);
-      const int use = li >> p.lgS;
-      const bool w = use == 0 || mbar_wait(empty0 + 8 * s, (use - 1) & 1, abort_flag, p.err);
-      return __all_sync(kFull, w);
-    };
+    bool load = false, flush = false, bad = false;
+    const int chp = p.P * ES / 16;  // 16-byte chunks per value row
+    const int vj0 = lane / chp, vch0 = lane % chp, vdj = 32 / chp, vdch = 32 % chp;
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
@@ -469,15 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       if constexpr (kGroupData) {
         if (gg != cur_gg) {
           cur_gg = gg;
-          gfirst = (long long)b * p.H + (long long)g * p.HPG;
           const int gs = gi & 1, guse = gi >> 1;
           const bool w = guse == 0 || mbar_wait(gempty0 + 8 * gs, (guse - 1) & 1, abort_flag, p.err);
           if (!__all_sync(kFull, w)) { ok = false; break; }
-          if (lane == 0) {  // arrive for the units of this group that other CTAs own
-            const long long nh = min(h1, gfirst + p.HPG) - max(h0, gfirst);
-            const int extra = gcap - (int)nh * p.U;
-            if (extra > 0) mbar_arrive_n(gempty0 + 8 * gs, extra);
-          }
           const uint32_t gdst = smem_u32(smem + p.gb_off + gs * p.gb_bytes);
           const size_t grow = (size_t)b * p.G + g;
           for (int idx = lane; idx < J * CHN; idx += 32) {
@@ -503,131 +492,77 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      // record sources of this head: lane j keeps alpha_j's address and publishes
-      // the address of v_j's row 0 in the shared table used by every unit
-      const float* asrc = nullptr;
-      __syncwarp();  // the previous head's units have read the table
+      const int s = stg_i;
+      const bool w = li < p.stages || mbar_wait(empty0 + 8 * s, stg_ph ^ 1, abort_flag, p.err);
+      if (!__all_sync(kFull, w)) { ok = false; break; }
+      uint8_t* stg = smem + (size_t)s * p.stage_bytes;
+      const uint32_t sdst = smem_u32(stg);
+      if (lane == 0) {
+        const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
+        const void* src = from_copy ? (const void*)(p.copy + hrow * p.head_stride)
+                                    : (const void*)(p.ckpt + hrow * p.P * N);
+        const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)p.P * N * 4;
+        mbar_arrive_tx(full0 + 8 * s, bytes);
+        tma_load_1d(sdst, src, bytes, full0 + 8 * s);
+      }
       if (lane < J) {
         const int j = lane;
-        const uint8_t* vsrc;
-        if (MODE == kConv) {
-          asrc = p.alpha + hrow;
-          vsrc = reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
-        } else if (j < c) {
-          const int slot = ring_slot(st, j, p.R);
-          asrc = p.ring_a + hrow * p.Rp + slot;
-          vsrc = reinterpret_cast<const uint8_t*>(p.ring_v) + (hrow * p.R + slot) * p.P * ES;
-        } else if (MODE == kVerify) {
-          asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
-          vsrc = reinterpret_cast<const uint8_t*>(p.v) + (((size_t)b * p.T + (j - c)) * p.H + hh) * p.P * ES;
-        } else {
-          asrc = p.alpha + hrow;
-          vsrc = reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
-        }
-        vtab[j] = vsrc;
+        const float* asrc;
+        if (MODE == kConv) asrc = p.alpha + hrow;
+        else if (j < c) asrc = p.ring_a + hrow * p.Rp + ring_slot(st, j, p.R);
+        else if (MODE == kVerify) asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
+        else asrc = p.alpha + hrow;
+        cp_async4(sdst + p.sa_off + 4 * j, asrc);
       }
-      __syncwarp();
-      const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
-      for (int u = 0; u < p.U; ++u) {
-        const int r0 = u * p.UR, ur = min(p.UR, p.P - r0);
-        int s;
-        if (!acquire(s)) { ok = false; break; }
-        uint8_t* stg = smem + (size_t)s * p.stage_bytes;
-        const uint32_t sdst = smem_u32(stg);
-        if (lane == 0) {
-          UnitDesc* d = reinterpret_cast<UnitDesc*>(stg + p.sm_off);
-          d->gh = gh; d->b = b; d->hh = hh; d->g = g;
-          d->c = c; d->st = st; d->J = J; d->r0 = r0; d->ur = ur; d->gi = gi - 1;
-          d->flags = (flush ? kUnitFlush : 0) | (u == 0 ? kUnitFirst : 0) |
-                     ((u == 0 && gh == gfirst) ? kUnitKeyOwner : 0);
-          if (!from_copy) {
-            const uint32_t bytes = (uint32_t)ur * N * 4;
-            mbar_arrive_tx(full0 + 8 * s, bytes);
-            tma_load_1d(sdst, p.ckpt + (hrow * p.P + r0) * N, bytes, full0 + 8 * s);
-          } else {
-            const uint8_t* hc = p.copy + hrow * p.head_stride;
-            const uint32_t rs_bytes = (uint32_t)ur * 4;
-            if constexpr (RF == kRfE4m3) {
-              const uint32_t cb = (uint32_t)ur * N;
-              mbar_arrive_tx(full0 + 8 * s, cb + rs_bytes);
-              tma_load_1d(sdst, hc + (size_t)r0 * N, cb, full0 + 8 * s);
-            } else {
-              const uint32_t cb = (uint32_t)ur * (N / 2), bb = (uint32_t)ur * (N / 16);
-              mbar_arrive_tx(full0 + 8 * s, cb + bb + rs_bytes);
-              tma_load_1d(sdst, hc + (size_t)r0 * (N / 2), cb, full0 + 8 * s);
-              tma_load_1d(sdst + p.cbs_off, hc + p.bsc_off + (size_t)r0 * (N / 16), bb, full0 + 8 * s);
-            }
-            tma_load_1d(sdst + p.crs_off, hc + p.rsc_off + (size_t)r0 * 4, rs_bytes, full0 + 8 * s);
-          }
-        }
-        if (lane < J) cp_async4(sdst + p.sa_off + 4 * lane, asrc);
-        // value rows r0..r0+ur-1 of every record: lane copies chunk vch of records vj0, vj0+vdj, ...
-        if (vch < ur * ES / 16) {
-          const int soff = r0 * ES + vch * 16;
-          for (int j = vj0; j < J; j += vdj)
-            cp_async16(sdst + p.sv_off + j * p.UR * ES + vch * 16, vtab[j] + soff);
-        }
-        cp_async_arrive(full0 + 8 * s);
-        ++li;
+      for (int j = vj0, ch = vch0; j < J;) {
+        cp_async16(sdst + p.sv_off + j * p.P * ES + ch * 16, vrow_src(j, c, st, b, hh, hrow) + ch * 16);
+        j += vdj;
+        ch += vdch;
+        if (ch >= chp) { ch -= chp; ++j; }
       }
-    }
-    // one end marker per consumer warp
-    for (int k = 0; k < kNCW && ok; ++k) {
-      int s;
-      if (!acquire(s)) { ok = false; break; }
-      if (lane == 0) {
-        reinterpret_cast<UnitDesc*>(smem + (size_t)s * p.stage_bytes + p.sm_off)->flags = kUnitEnd;
-        mbar_arrive(full0 + 8 * s);
-      }
-      cp_async_arrive(full0 + 8 * s);
+      cp_async_arrive(small0 + 8 * s);
+      stage_next();
       ++li;
     }
     cp_async_wait_all();
     if (!ok && lane == 0) {  // drain the bulk copies still in flight (bounded), then leave
       volatile int dummy = 0;
-      for (int i = (li > p.stages ? li - p.stages : 0); i < li; ++i)
-        mbar_wait(full0 + 8 * (i & (p.stages - 1)), (i >> p.lgS) & 1, &dummy, p.err);
+      for (int k = 0; k < p.stages && k < li; ++k) {
+        const int i = li - 1 - k;
+        mbar_wait(full0 + 8 * (i % p.stages), (i / p.stages) & 1, &dummy, p.err);
+      }
     }
-  } else {
-    // ====================================================================== consumers
-    const int col4 = lane % LPR, rsub = lane / LPR;
-    float* wsc = reinterpret_cast<float*>(smem + p.wsc_off) + warp * p.wsc_floats;  // per-warp scratch
-    float* skq_w = wsc;                          // [kTMax][kRMax] k_j^T q_t of the current group
-    float* cw = wsc + kTMax * kRMax;             // [kTMax][kRMax] coefficients of the current unit
-    float* gw = cw + kTMax * kRMax;              // [kTMax] cumulative decays g_{1:c+t+1}
-    float* uwork = gw + 16;                      // [R][RPI][kKR] scaled values of the fold
-    int last_gi = -1;
-    const uint8_t* gK = nullptr;  // keys of the current group (input dtype), rows j
-    const uint8_t* gQ = nullptr;  // queries of the current group
-    float sj = 0.f;               // decode: lane j holds k_j^T q
-    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    constexpr int CPL = (RF == kRfE2m1) ? 32 : 16;  // copy-tile columns per lane
-    constexpr int LPRc = (N / CPL) > 0 ? (N / CPL) : 1;
-    constexpr int RPIc = 32 / LPRc;
-    constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
-    float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
-
-    while (true) {
-      int li = 0;
-      if (lane == 0) li = atomicAdd(claim, 1);
-      li = __shfl_sync(kFull, li, 0);
-      const int s = li & (p.stages - 1);
-      if (!__all_sync(kFull, mbar_wait(full0 + 8 * s, (li >> p.lgS) & 1, abort_flag, p.err))) break;
-      const uint8_t* tile = smem + (size_t)s * p.stage_bytes;
-      const UnitDesc d = *reinterpret_cast<const UnitDesc*>(tile + p.sm_off);
-      if (d.flags & kUnitEnd) break;
-      const int b = d.b, hh = d.hh, c = d.c, st = d.st, J = d.J, r0 = d.r0, ur = d.ur;
-      const size_t hrow = (size_t)d.gh;
-      const bool flush = (d.flags & kUnitFlush) != 0;
-
+  } else if (warp == kCoef) {
+    // ====================================================================== coefficients
+    float* skq_w = reinterpret_cast<float*>(smem + p.wsc_off);  // [kTMax][kRMax] k_j^T q_t (verify)
+    int gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
+    long long cur_gg = -1;
+    bool load = false, flush = false, bad = false;
+    float sj = 0.f;  // decode: lane j holds k_j^T q
+    HeadIter it;
+    it.init(h0, p.H, p.HPG);
+    for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
+      const int b = it.b, hh = it.hh, g = it.g;
+      const long long gg = (long long)b * p.G + g;
+      const size_t hrow = (size_t)gh;
+      if (b != cur_b) {
+        cur_b = b;
+        seq_plan(b, c, st, load, flush, bad);
+        J = records(c);
+        cur_gg = -1;
+      }
+      if (!load) continue;
       if constexpr (kGroupData) {
-        if (d.gi != last_gi) {
-          // ---------------------------------------------- this warp enters the unit's group
-          last_gi = d.gi;
-          const int gs = d.gi & 1;
-          if (!__all_sync(kFull, mbar_wait(gfull0 + 8 * gs, (d.gi >> 1) & 1, abort_flag, p.err))) break;
-          gK = smem + p.gb_off + gs * p.gb_bytes;
-          gQ = gK + p.gq_off;
+        if (gg != cur_gg) {
+          cur_gg = gg;
+          if (gi > 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gempty0 + 8 * ((gi - 1) & 1));
+          }
+          const int gs = gi & 1;
+          if (!__all_sync(kFull, mbar_wait(gfull0 + 8 * gs, (gi >> 1) & 1, abort_flag, p.err))) { ok = false; break; }
+          const uint8_t* gK = smem + p.gb_off + gs * p.gb_bytes;
+          const uint8_t* gQ = gK + p.gq_off;
           if constexpr (MODE == kDecode || MODE == kVerify) {
             // k_j^T q_t: one pair per lane, N/4 chunks visited from a lane-dependent start
             const int npair = J * nq;
@@ -650,56 +585,154 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             }
             __syncwarp();
           }
-          if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
-          if constexpr (RF != kRfNone && MODE == kDecode) {
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) qc[i] = In<TIn>::lds(gQ, (lane % LPRc) * CPL + i);
+          if constexpr (kAppendMode) {  // the group's first head (if this CTA owns it) appends the new keys
+            const long long gfirst = (long long)b * p.H + (long long)g * p.HPG;
+            const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
+            if (gfirst >= h0 && na > 0) {
+              const size_t grow = (size_t)b * p.G + g;
+              for (int idx = lane; idx < na * CHN; idx += 32) {
+                const int t = idx / CHN, ch = idx % CHN;
+                const uint4 val = *reinterpret_cast<const uint4*>(gK + (c + t) * N * ES + ch * 16);
+                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_k) +
+                                          (grow * p.R + ring_slot(st, c + t, p.R)) * N * ES + ch * 16) = val;
+              }
+            }
           }
+          ++gi;
         }
       }
-
-      const float* tf = reinterpret_cast<const float*>(tile);
-      const float* sa = reinterpret_cast<const float*>(tile + p.sa_off);  // alpha_j, record order
-      const uint8_t* sv = tile + p.sv_off;                                // v_j rows r0.., stride UR
-      const float aj = (lane < J) ? sa[lane] : 1.f;                        // lane j holds alpha of record j
-      const int nsp = (ur + kSubRows - 1) / kSubRows;                      // sub-passes of this unit
-
-      // ---------------------------------------------------- appends (from shared memory)
-      if constexpr (kAppendMode) {
-        const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
-        const int cu = ur * ES / 16;  // <= 32 chunks per value row of the unit
-        for (int t = 0; t < na; ++t) {
-          if (lane < cu) {
-            const uint4 val = *reinterpret_cast<const uint4*>(sv + ((c + t) * p.UR) * ES + lane * 16);
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_v) +
-                                      ((hrow * p.R + ring_slot(st, c + t, p.R)) * p.P + r0) * ES + lane * 16) = val;
-          }
-        }
-        if ((d.flags & kUnitFirst) && lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[c + lane];
-        if (d.flags & kUnitKeyOwner) {  // the group's first head appends the new keys
-          const size_t grow = (size_t)b * p.G + d.g;
-          for (int idx = lane; idx < na * CHN; idx += 32) {
-            const int t = idx / CHN, ch = idx % CHN;
-            const uint4 val = *reinterpret_cast<const uint4*>(gK + (c + t) * N * ES + ch * 16);
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_k) +
-                                      (grow * p.R + ring_slot(st, c + t, p.R)) * N * ES + ch * 16) = val;
-          }
-        }
-      }
-
+      const int s = stg_i;
+      if (!__all_sync(kFull, mbar_wait(small0 + 8 * s, stg_ph, abort_flag, p.err))) { ok = false; break; }
+      uint8_t* stg = smem + (size_t)s * p.stage_bytes;
+      const float* sa = reinterpret_cast<const float*>(stg + p.sa_off);  // alpha_j, record order
+      const uint8_t* sv = stg + p.sv_off;                                // v_j rows, record order
+      float* sc = reinterpret_cast<float*>(stg + p.sc_off);             // coefficients
+      const float aj = (lane < J) ? sa[lane] : 1.f;                      // lane j holds alpha of record j
       if constexpr (MODE == kVerify) {
-        // ================================================ verify (T queries)
         for (int t = 0; t < p.T; ++t) {
           const int ht = c + t + 1;
           const float x = (lane < ht) ? aj : 1.f;
           const float incl = suffix_prod(x, lane);
           const float nxt = __shfl_down_sync(kFull, incl, 1);
           const float w = (lane < 31) ? nxt : 1.f;
-          cw[t * kRMax + lane] = (lane < ht) ? w * skq_w[t * kRMax + lane] : 0.f;
-          if (lane == 0) gw[t] = incl;
+          sc[kCoefOff + t * kRMax + lane] = (lane < ht) ? w * skq_w[t * kRMax + lane] : 0.f;
+          if (lane == 0) sc[t] = incl;
         }
-        __syncwarp();
-        for (int sp = 0; sp < nsp; ++sp) {
+      } else {
+        const float incl = suffix_prod(aj, lane);
+        const float nxt = __shfl_down_sync(kFull, incl, 1);
+        const float wj = (lane < 31) ? nxt : 1.f;  // lane j: weight g_{j+2:J} of record j
+        if (lane == 0) sc[0] = incl;               // g_{1:J}
+        if (flush) {
+          // fold: scaled values u_j[p] = g_{j+2:J} v_j[p]
+          for (int j = 0; j < J; ++j) {
+            const float wjj = __shfl_sync(kFull, wj, j);
+            for (int r = lane; r < p.P; r += 32) sc[kCoefOff + j * p.P + r] = wjj * In<TIn>::lds(sv, j * p.P + r);
+          }
+        } else if constexpr (MODE == kDecode) {
+          // non-flush: value term sum_j g_{j+2:J} (k_j^T q) v_j[p]
+          const float cj = (lane < J) ? wj * sj : 0.f;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows lane + 32 m (P <= 128)
+          for (int j = 0; j < J; ++j) {
+            const float cjj = __shfl_sync(kFull, cj, j);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int r = lane + 32 * m;
+              if (r < p.P) acc[m] = fmaf(cjj, In<TIn>::lds(sv, j * p.P + r), acc[m]);
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int r = lane + 32 * m;
+            if (r < p.P) sc[kCoefOff + r] = acc[m];
+          }
+        }
+      }
+      if constexpr (kAppendMode) {  // the new decays go to the ring
+        const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
+        if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[c + lane];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(coef0 + 8 * s);   // coefficients published
+        mbar_arrive(empty0 + 8 * s);  // this warp is done with the stage
+      }
+      stage_next();
+    }
+  } else {
+    // ====================================================================== dot warps
+    const int ct = threadIdx.x;  // 0..255
+    const int col4 = lane % LPR, rsub = lane / LPR;
+    int gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
+    long long cur_gg = -1;
+    bool load = false, flush = false, bad = false;
+    const uint8_t* gK = smem + p.gb_off;
+    const uint8_t* gQ = gK + p.gq_off;
+    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int CPL = (RF == kRfE2m1) ? 32 : 16;  // copy-tile columns per lane
+    constexpr int LPRc = (N / CPL) > 0 ? (N / CPL) : 1;
+    constexpr int RPIc = 32 / LPRc;
+    constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
+    float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
+    const int rows_pass = kNDW * kKR * RPI;
+    const int npass = (p.P + rows_pass - 1) / rows_pass;
+    const int chp = p.P * ES / 16;
+    HeadIter it;
+    it.init(h0, p.H, p.HPG);
+    for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
+      const int b = it.b, hh = it.hh, g = it.g;
+      const long long gg = (long long)b * p.G + g;
+      const size_t hrow = (size_t)gh;
+      if (b != cur_b) {
+        cur_b = b;
+        seq_plan(b, c, st, load, flush, bad);
+        J = records(c);
+        cur_gg = -1;
+      }
+      if (!load) continue;
+      if constexpr (kGroupData) {
+        if (gg != cur_gg) {
+          cur_gg = gg;
+          if (gi > 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gempty0 + 8 * ((gi - 1) & 1));
+          }
+          const int gs = gi & 1;
+          if (!__all_sync(kFull, mbar_wait(gfull0 + 8 * gs, (gi >> 1) & 1, abort_flag, p.err))) { ok = false; break; }
+          gK = smem + p.gb_off + gs * p.gb_bytes;
+          gQ = gK + p.gq_off;
+          if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
+          if constexpr (RF != kRfNone && MODE == kDecode) {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) qc[i] = In<TIn>::lds(gQ, (lane % LPRc) * CPL + i);
+          }
+          ++gi;
+        }
+      }
+      const int s = stg_i;
+      const bool got = mbar_wait(full0 + 8 * s, stg_ph, abort_flag, p.err) &&
+                       mbar_wait(small0 + 8 * s, stg_ph, abort_flag, p.err) &&
+                       mbar_wait(coef0 + 8 * s, stg_ph, abort_flag, p.err);
+      if (!__all_sync(kFull, got)) { ok = false; break; }
+      const uint8_t* tile = smem + (size_t)s * p.stage_bytes;
+      const float* tf = reinterpret_cast<const float*>(tile);
+      const uint8_t* sv = tile + p.sv_off;
+      const float* sc = reinterpret_cast<const float*>(tile + p.sc_off);
+
+      if constexpr (kAppendMode) {  // new value rows go to the ring (16-byte chunks over the dot threads)
+        const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
+        for (int idx = ct; idx < na * chp; idx += kNDW * 32) {
+          const int t = idx / chp, ch = idx - t * chp;
+          const uint4 val = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_v) +
+                                    (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES + ch * 16) = val;
+        }
+      }
+
+      if constexpr (MODE == kVerify) {
+        // ================================================ verify (T queries)
+        for (int pass = 0; pass < npass; ++pass) {
+          const int rbase = (pass * kNDW + warp) * kKR;
           for (int t0 = 0; t0 < p.T; t0 += kTQ) {
             float4 qv[kTQ];
 #pragma unroll
@@ -708,8 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             float part[kKR * kTQ];
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
-              const int lr = (sp * kKR + kk) * RPI + rsub;
-              const float4 x4 = (lr < ur) ? lds4(tf + ((size_t)lr * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const int row = (rbase + kk) * RPI + rsub;
+              const float4 x4 = (row < p.P) ? lds4(tf + ((size_t)row * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
               for (int t = 0; t < kTQ; ++t) part[kk * kTQ + t] = dot4(x4, qv[t]);
             }
@@ -721,72 +754,69 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
               const int kk = (off + i) / kTQ, t = t0 + (off + i) % kTQ;
-              const int lr = (sp * kKR + kk) * RPI + rsub;
-              const bool valid = lr < ur && t < p.T;
+              const int row = (rbase + kk) * RPI + rsub;
+              const bool valid = row < p.P && t < p.T;
               float ov = 0.f;
               if (valid) {
-                for (int j = dup; j < J; j += D) ov = fmaf(cw[t * kRMax + j], In<TIn>::lds(sv, j * p.UR + lr), ov);
+                const float* cwt = sc + kCoefOff + t * kRMax;
+                for (int j = dup; j < J; j += D) ov = fmaf(cwt[j], In<TIn>::lds(sv, j * p.P + row), ov);
               }
               ov = low_sum<D>(ov);
-              if (dup == 0 && valid) p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + r0 + lr] = fmaf(gw[t], part[i], ov);
+              if (dup == 0 && valid) p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = fmaf(sc[t], part[i], ov);
             }
           }
         }
       } else if (flush) {
         // ================================================ fold path
-        // S_new = g_{1:J} S + sum_j (g_{j+2:J} v_j) k_j^T ; store ; o = S_new q (decode, conv)
-        const float incl = suffix_prod(aj, lane);
-        const float nxt = __shfl_down_sync(kFull, incl, 1);
-        const float wj = (lane < 31) ? nxt : 1.f;  // lane j: weight of record j
-        const float gam = __shfl_sync(kFull, incl, 0);
-        for (int sp = 0; sp < nsp; ++sp) {
-          // uwork[(j*RPI + rs)*KR + k] = w_j * v_j[row]
-          const int nu = J * RPI * kKR;
-          for (int base = 0; base < nu; base += 32) {
-            const int idx = base + lane;
-            const int j = min(idx / (RPI * kKR), J > 0 ? J - 1 : 0);
-            const float wsel = __shfl_sync(kFull, wj, j);
-            if (idx < nu) {
-              const int rem = idx % (RPI * kKR), rs = rem / kKR, kk = rem % kKR;
-              const int lr = (sp * kKR + kk) * RPI + rs;
-              uwork[idx] = (lr < ur) ? wsel * In<TIn>::lds(sv, j * p.UR + lr) : 0.f;
-            }
-          }
-          __syncwarp();
+        // S_new = g_{1:J} S + sum_j u_j k_j^T with u_j = g_{j+2:J} v_j ; store ; o = S_new q
+        const float gam = sc[0];
+        const float* su = sc + kCoefOff;  // [J][P]
+        for (int pass = 0; pass < npass; ++pass) {
+          const int rbase = (pass * kNDW + warp) * kKR;
           float4 acc[kKR];
 #pragma unroll
           for (int kk = 0; kk < kKR; ++kk) {
-            const int lr = (sp * kKR + kk) * RPI + rsub;
-            if (lr < ur) {
-              const float4 x = lds4(tf + ((size_t)lr * LPR + col4) * 4);
+            const int row = (rbase + kk) * RPI + rsub;
+            if (row < p.P) {
+              const float4 x = lds4(tf + ((size_t)row * LPR + col4) * 4);
               acc[kk] = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
             } else {
               acc[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
-          for (int j = 0; j < J; ++j) {
-            const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
-            const float* uj = uwork + (j * RPI + rsub) * kKR;
-            const float4 u0 = lds4(uj), u1 = lds4(uj + 4);
-            const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          if (rbase * RPI < p.P) {
+            for (int j = 0; j < J; ++j) {
+              const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
+              float uu[kKR];
+              if constexpr (RPI == 1) {  // the warp's 8 rows are consecutive: two vector loads
+                const float4 u0 = lds4(su + j * p.P + rbase), u1 = lds4(su + j * p.P + rbase + 4);
+                uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
+                uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
+              } else {
 #pragma unroll
-            for (int kk = 0; kk < kKR; ++kk) {
-              acc[kk].x = fmaf(uu[kk], kv.x, acc[kk].x);
-              acc[kk].y = fmaf(uu[kk], kv.y, acc[kk].y);
-              acc[kk].z = fmaf(uu[kk], kv.z, acc[kk].z);
-              acc[kk].w = fmaf(uu[kk], kv.w, acc[kk].w);
+                for (int kk = 0; kk < kKR; ++kk) {
+                  const int row = (rbase + kk) * RPI + rsub;
+                  uu[kk] = (row < p.P) ? su[j * p.P + row] : 0.f;
+                }
+              }
+#pragma unroll
+              for (int kk = 0; kk < kKR; ++kk) {
+                acc[kk].x = fmaf(uu[kk], kv.x, acc[kk].x);
+                acc[kk].y = fmaf(uu[kk], kv.y, acc[kk].y);
+                acc[kk].z = fmaf(uu[kk], kv.z, acc[kk].z);
+                acc[kk].w = fmaf(uu[kk], kv.w, acc[kk].w);
+              }
             }
           }
 #pragma unroll
           for (int kk = 0; kk < kKR; ++kk) {
-            const int lr = (sp * kKR + kk) * RPI + rsub;
-            const bool live_row = lr < ur;
-            const int row = r0 + lr;
+            const int row = (rbase + kk) * RPI + rsub;
+            const bool live_row = row < p.P;
             if constexpr (MODE != kQuant) {
               if (live_row) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
             }
             if constexpr (RF != kRfNone && MODE != kConv) {
-              // rows beyond the unit still join the shuffles, with zeros
+              // rows beyond P still join the shuffles, with zeros
               quantize_store<RF, LPR>(acc[kk], live_row, row, col4, N, p.copy + hrow * p.head_stride, p.bsc_off,
                                       p.rsc_off);
             }
@@ -801,54 +831,46 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             constexpr int D = (LPR / kKR) > 0 ? (LPR / kKR) : 1;
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
-              const int lr = (sp * kKR + off + i) * RPI + rsub;
-              if ((lane & (D - 1)) == 0 && lr < ur) p.o[hrow * p.P + r0 + lr] = part[i];
+              const int row = (rbase + off + i) * RPI + rsub;
+              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = part[i];
             }
           }
-          __syncwarp();
         }
       } else if constexpr (MODE == kDecode) {
-        // ================================================ non-flush decode
-        const float incl = suffix_prod(aj, lane);
-        const float nxt = __shfl_down_sync(kFull, incl, 1);
-        const float w = (lane < 31) ? nxt : 1.f;
-        const float gam = __shfl_sync(kFull, incl, 0);
-        cw[lane] = (lane < J) ? w * sj : 0.f;  // coefficient of record j: g_{j+2:J} k_j^T q
-        __syncwarp();
-        for (int sp = 0; sp < nsp; ++sp) {
+        // ================================================ non-flush decode: o = g (S q) + value term
+        const float gam = sc[0];
+        const float* sov = sc + kCoefOff;  // [P]
+        for (int pass = 0; pass < npass; ++pass) {
           if constexpr (RF == kRfNone) {
+            const int rbase = (pass * kNDW + warp) * kKR;
             float part[kKR];
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
-              const int lr = (sp * kKR + kk) * RPI + rsub;
-              part[kk] = (lr < ur) ? dot4(lds4(tf + ((size_t)lr * LPR + col4) * 4), q4) : 0.f;
+              const int row = (rbase + kk) * RPI + rsub;
+              part[kk] = (row < p.P) ? dot4(lds4(tf + ((size_t)row * LPR + col4) * 4), q4) : 0.f;
             }
             int off = 0;
             TRed<kKR, LPR / 2>::run(part, lane, off);
             constexpr int KF = (kKR / LPR) > 0 ? (kKR / LPR) : 1;
             constexpr int D = (LPR / kKR) > 0 ? (LPR / kKR) : 1;
-            const int dup = lane & (D - 1);
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
-              const int lr = (sp * kKR + off + i) * RPI + rsub;
-              float ov = 0.f;
-              if (lr < ur)
-                for (int j = dup; j < J; j += D) ov = fmaf(cw[j], In<TIn>::lds(sv, j * p.UR + lr), ov);
-              ov = low_sum<D>(ov);
-              if (dup == 0 && lr < ur) p.o[hrow * p.P + r0 + lr] = fmaf(gam, part[i], ov);
+              const int row = (rbase + off + i) * RPI + rsub;
+              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[i], sov[row]);
             }
           } else {
             // read copy: lanes own CPL consecutive codes of a row
+            const int rows0 = (pass * kNDW + warp) * kKR * RPI;  // first row of this warp
             const int colc = lane % LPRc, rsc = lane / LPRc;
-            const float* rscale = reinterpret_cast<const float*>(tile + p.crs_off);
+            const float* rscale = reinterpret_cast<const float*>(tile + p.rsc_off);
             float part[KRc];
 #pragma unroll
             for (int kk = 0; kk < KRc; ++kk) {
-              const int lr = sp * kSubRows + kk * RPIc + rsc;
+              const int row = rows0 + kk * RPIc + rsc;
               float acc = 0.f;
-              if (lr < ur) {
+              if (row < p.P) {
                 if constexpr (RF == kRfE4m3) {
-                  const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)lr * N + colc * 16);
+                  const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)row * N + colc * 16);
                   const uint32_t ws[4] = {cwd.x, cwd.y, cwd.z, cwd.w};
 #pragma unroll
                   for (int qd = 0; qd < 4; ++qd) {
@@ -858,9 +880,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                     for (int e = 0; e < 4; ++e) acc = fmaf(f[e], qc[qd * 4 + e], acc);
                   }
                 } else {
-                  const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)lr * (N / 2) + colc * 16);
+                  const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)row * (N / 2) + colc * 16);
                   const uint32_t ws[4] = {cwd.x, cwd.y, cwd.z, cwd.w};
-                  const uint8_t* bsp = tile + p.cbs_off + lr * (N / 16) + colc * 2;
+                  const uint8_t* bsp = tile + p.bsc_off + row * (N / 16) + colc * 2;
                   float blk[2] = {0.f, 0.f};
 #pragma unroll
                   for (int qd = 0; qd < 4; ++qd) {
@@ -871,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                   }
                   acc = fmaf(dec_e4m3(bsp[0]), blk[0], dec_e4m3(bsp[1]) * blk[1]);
                 }
-                acc *= rscale[lr];
+                acc *= rscale[row];
               }
               part[kk] = acc;
             }
@@ -879,26 +901,19 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             TRed<KRc, LPRc / 2>::run(part, lane, off);
             constexpr int KF = (KRc / LPRc) > 0 ? (KRc / LPRc) : 1;
             constexpr int D = (LPRc / KRc) > 0 ? (LPRc / KRc) : 1;
-            const int dup = lane & (D - 1);
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
-              const int lr = sp * kSubRows + (off + i) * RPIc + rsc;
-              float ov = 0.f;
-              if (lr < ur)
-                for (int j = dup; j < J; j += D) ov = fmaf(cw[j], In<TIn>::lds(sv, j * p.UR + lr), ov);
-              ov = low_sum<D>(ov);
-              if (dup == 0 && lr < ur) p.o[hrow * p.P + r0 + lr] = fmaf(gam, part[i], ov);
+              const int row = rows0 + (off + i) * RPIc + rsc;
+              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[i], sov[row]);
             }
           }
         }
       }
 
-      // ---------------------------------------------------- release the stage and the group unit
+      // ---------------------------------------------------- release the stage
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty0 + 8 * s);
-        if constexpr (kGroupData) mbar_arrive(gempty0 + 8 * (d.gi & 1));
-      }
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      stage_next();
     }
   }
 

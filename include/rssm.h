@@ -29,7 +29,7 @@
  *  - No C++ exception crosses this boundary. A handle is not thread safe: use
  *    one stream per handle at a time.
  *
- * Supported sizes: N in {16, 32, 64, 128}; P a multiple of 8 with P*N*4 <= 64 KiB;
+ * Supported sizes: N in {16, 32, 64, 128}; P a multiple of 8, at most 128;
  * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8. Read copies need
  * N in {64, 128}.
  */
