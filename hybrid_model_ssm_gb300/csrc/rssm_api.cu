@@ -97,36 +97,40 @@ struct Plan {
   rssm::Params p{};
 };
 
-// Stage ring and shared-memory carve for one launch (see Params in rssm_device.cuh).
+// Tile stages, record slots and shared-memory carve for one launch (see Params in rssm_device.cuh).
 rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
   using namespace rssm;
   auto a128 = [](size_t x) { return align_up(x, 128); };
   const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
-  const size_t tile = P * N * 4;  // a read copy (head_stride bytes) is smaller
-  const size_t sa_off = align_up(tile, 16);
-  const size_t sv_off = sa_off + (size_t)kRMax * 4;
+  const size_t tile = a128(P * N * 4);  // a read copy (head_stride bytes) is smaller
+  const size_t sv_off = (size_t)kRMax * 4;
   const size_t sc_off = align_up(sv_off + R * P * es, 16);
   const size_t sc_floats = 16 + std::max({P, R * P, (size_t)kTMax * kRMax});
-  const size_t stage = a128(sc_off + sc_floats * 4);
+  const size_t slot = a128(sc_off + sc_floats * 4);
   const size_t gq_off = R * N * es;
   const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
-  const size_t wsc = a128((size_t)kTMax * kRMax * 4);
-  const size_t bars = a128((4 * kMaxStages + 6) * 8);
+  const size_t wsc = a128((size_t)kNCoef * kTMax * kRMax * 4);
+  const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6) * 8);
   const size_t fixed = 2 * gb + wsc + bars;
-  if (fixed + 2 * stage > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
-  const int stages = (int)std::min<size_t>(kMaxStages, (kSmemMax - fixed) / stage);
+  if (fixed + 2 * tile + 2 * slot > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
+  const size_t budget = kSmemMax - fixed;
+  const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, budget / (tile + 3 * slot)));
+  const int slots = (int)std::max<size_t>(2, std::min<size_t>(kMaxSlots, (budget - stages * tile) / slot));
   rssm::Params& p = pl->p;
   p.stages = stages;
-  p.stage_bytes = (int)stage;
-  p.sa_off = (int)sa_off;
+  p.stage_bytes = (int)tile;
+  p.slots = slots;
+  p.slot_bytes = (int)slot;
   p.sv_off = (int)sv_off;
   p.sc_off = (int)sc_off;
-  size_t off = (size_t)stages * stage;
+  size_t off = (size_t)stages * tile;
+  p.slot_off = (int)off; off += (size_t)slots * slot;
   p.gb_off = (int)off; off += 2 * gb;
   p.gb_bytes = (int)gb;
   p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
   p.bar_off = (int)off; off += bars;
+  if (off > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
   pl->stages = stages;
   pl->smem = off;
   return RSSM_OK;

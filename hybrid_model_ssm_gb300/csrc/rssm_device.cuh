@@ -29,11 +29,24 @@
 
 namespace rssm {
 
-constexpr int kNDW = 8;                    // dot warps per CTA (stream the checkpoint tile)
-constexpr int kProducer = kNDW;            // warp that issues the copies
-constexpr int kCoef = kNDW + 1;            // warp that computes the per-head decay terms
-constexpr int kThreads = (kNDW + 2) * 32;
-constexpr int kKR = 8;                     // FP32-tile row-instructions per warp per pass
+#ifndef RSSM_DOT_WARPS
+#define RSSM_DOT_WARPS 8
+#endif
+#ifndef RSSM_ROWS_PER_WARP
+#define RSSM_ROWS_PER_WARP 8
+#endif
+constexpr int kNDW = RSSM_DOT_WARPS;       // dot warps per CTA (stream the checkpoint tile)
+#ifndef RSSM_COEF_WARPS
+#define RSSM_COEF_WARPS 2
+#endif
+constexpr int kNCoef = RSSM_COEF_WARPS;    // warps computing the per-head decay terms (alternate heads)
+constexpr int kTileWarp = kNDW;            // warp that issues the bulk tile copies
+constexpr int kCoef0 = kNDW + 1;           // first coefficient warp
+constexpr int kGatherWarp = kNDW + 1 + kNCoef;  // warp that gathers the records, keys and queries
+constexpr int kThreads = (kNDW + 2 + kNCoef) * 32;
+constexpr int kMaxSlots = 16;              // largest record-slot ring
+constexpr int kKR = RSSM_ROWS_PER_WARP;    // FP32-tile row-instructions per warp per pass (multiple of 4)
+static_assert(kKR % 4 == 0, "rows per warp must be a multiple of 4");
 constexpr int kTQ = 4;                     // verify queries per pass over the tile
 constexpr int kTMax = 8;                   // largest draft count
 constexpr int kRMax = 32;                  // largest ring (records per head)
@@ -62,12 +75,13 @@ struct Params {
   const void* k;       // decode/conv [B,G,N]; verify [B,T,G,N]
   const void* q;       // decode/conv [B,G,N]; verify [B,T,G,N]
   float* o;            // decode/conv [B,H,P]; verify [B,T,H,P]
-  // Shared memory (bytes). `stages` stages of
-  // [head tile (P x N fp32, or the read copy) | alpha_j (kRMax fp32) | v_j rows (R x P) | coefficients];
-  // coefficients: g (or g_t) at 0..15, then the value term [P], the scaled values
-  // [R][P] of a fold, or the verify weights [kTMax][kRMax].
-  int stages, stage_bytes, sa_off, sv_off, sc_off;
-  // Two group areas of [k_j rows (R x N) | queries (kTMax x N)].
+  // Shared memory (bytes).
+  //   `stages` tile stages: the head tile (P x N fp32, or the read copy);
+  //   `slots` record slots: [alpha_j (kRMax fp32) | v_j rows (R x P) | coefficients],
+  //   coefficients: g (or g_t) at 0..15, then the value term [P], the scaled
+  //   values [R][P] of a fold, or the verify weights [kTMax][kRMax];
+  //   two group areas of [k_j rows (R x N) | queries (kTMax x N)].
+  int stages, stage_bytes, slots, slot_bytes, slot_off, sv_off, sc_off;
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
 };
@@ -83,6 +97,9 @@ template <> struct In<float> {
   static __device__ __forceinline__ float4 lds4(const uint8_t* base, int i) {  // i multiple of 4
     return *reinterpret_cast<const float4*>(base + 4 * i);
   }
+  static __device__ __forceinline__ float2 lds2(const uint8_t* base, int i) {  // i even
+    return *reinterpret_cast<const float2*>(base + 4 * i);
+  }
 };
 template <> struct In<__nv_bfloat16> {
   static constexpr int kBytes = 2;
@@ -94,6 +111,10 @@ template <> struct In<__nv_bfloat16> {
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
     return make_float4(a.x, a.y, b.x, b.y);
+  }
+  static __device__ __forceinline__ float2 lds2(const uint8_t* base, int i) {  // i even
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(base + 2 * i);
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
   }
 };
 
@@ -148,11 +169,26 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // Bounded wait on an mbarrier phase. Returns false (after flagging the CTA and
 // the device error word) when the wait runs out or another thread aborted.
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes
+// or about `ns` nanoseconds pass, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+#ifndef RSSM_WAIT_HINT_NS
+#define RSSM_WAIT_HINT_NS 0  // 0: plain try_wait (the hardware's own suspend limit)
+#endif
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                    uint32_t* err) {
   const unsigned long long t0 = gtimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try(bar, parity)) return true;
+    if (RSSM_WAIT_HINT_NS ? mbar_try_sleep(bar, parity, RSSM_WAIT_HINT_NS) : mbar_try(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (gtimer() - t0 > kWaitLimitNs) break;
@@ -296,6 +332,28 @@ __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cas
 __device__ __forceinline__ float dot4(const float4 a, const float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
+// Packed pairs of fp32 for fma.rn.f32x2 (two independent IEEE fmas per instruction).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo2(f32x2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a;
+}
+__device__ __forceinline__ float hi2(f32x2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return b;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 
 // ------------------------------------------------------------ quantize a row slice
 // Lane holds 4 consecutive elements (x) of a row covered by LPR lanes.
@@ -342,13 +400,14 @@ __device__ __forceinline__ void quantize_store(const float4 x, bool live_row, in
 // committed records j < c live in the ring at slot (start + j) mod R; the
 // decode step's own record is j = c; verify drafts are j = c..c+T-1.
 //
-// Warp roles, all walking the CTA's heads in the same order over a ring of
-// stages:
-//   producer      bulk TMA of the head tile; cp.async gathers of alpha_j and v_j
-//                 into the stage, of k_j and the queries into the group area
+// Warp roles, all walking the CTA's heads in the same order:
+//   tile warp     bulk TMA of each head tile into a ring of `stages` tile stages
+//   gather warp   cp.async of alpha_j and v_j into a deeper ring of `slots`
+//                 record slots, and of k_j and the queries into two group areas;
+//                 it runs ahead of the tiles so record latency stays hidden
 //   coefficients  per head: the decay scan g_{j+1:h}, and the value term
 //                 sum_j c_j v_j (non-flush), the scaled values g v_j (fold) or
-//                 the verify weights; published in the stage
+//                 the verify weights, published in the record slot; the appends
 //   dot warps     stream the tile: rows . q, the reduction, the output (and the
 //                 fold's rank-J update, store and read-copy refresh)
 template <int MODE, int N, typename TIn, int RF>
@@ -365,12 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-  // bars: full[S] (tile), small[S] (gathers), coef[S], empty[S], gfull[2], gempty[2], end; abort flag
-  const uint32_t full0 = smem_u32(bars), small0 = smem_u32(bars + kMaxStages);
-  const uint32_t coef0 = smem_u32(bars + 2 * kMaxStages), empty0 = smem_u32(bars + 3 * kMaxStages);
-  const uint32_t gfull0 = smem_u32(bars + 4 * kMaxStages), gempty0 = smem_u32(bars + 4 * kMaxStages + 2);
-  const uint32_t end_bar = smem_u32(bars + 4 * kMaxStages + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kMaxStages + 5);
+  // bars: tfull[kMaxStages], tempty[kMaxStages], sfull[kMaxSlots], scoef[kMaxSlots],
+  //       sempty[kMaxSlots], gfull[2], gempty[2], end; then the abort flag
+  const uint32_t tfull0 = smem_u32(bars), tempty0 = smem_u32(bars + kMaxStages);
+  const uint32_t sfull0 = smem_u32(bars + 2 * kMaxStages), scoef0 = sfull0 + 8 * kMaxSlots;
+  const uint32_t sempty0 = scoef0 + 8 * kMaxSlots;
+  const uint32_t gfull0 = sempty0 + 8 * kMaxSlots, gempty0 = gfull0 + 16;
+  const uint32_t end_bar = gempty0 + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 3 * kMaxSlots + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = (long long)p.B * p.H;
@@ -380,14 +441,17 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(small0 + 8 * s, 32);
-      mbar_init(coef0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kNDW + 1);
+      mbar_init(tfull0 + 8 * s, 1);
+      mbar_init(tempty0 + 8 * s, kNDW);
+    }
+    for (int s = 0; s < p.slots; ++s) {
+      mbar_init(sfull0 + 8 * s, 32);
+      mbar_init(scoef0 + 8 * s, 1);
+      mbar_init(sempty0 + 8 * s, kNDW + 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(gfull0 + 8 * s, 32);
-      mbar_init(gempty0 + 8 * s, kNDW + 1);
+      mbar_init(gempty0 + 8 * s, kNDW + kNCoef);
     }
     mbar_init(end_bar, kThreads);
     *abort_flag = 0;
@@ -433,15 +497,50 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     return reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
   };
 
-  // Stage bookkeeping shared by all roles: stage index and its phase parity.
-  int stg_i = 0, stg_ph = 0;
-  auto stage_next = [&]() {
-    if (++stg_i == p.stages) { stg_i = 0; stg_ph ^= 1; }
+  // Ring positions (index, phase parity) of the tile stages and record slots.
+  int ts = 0, tph = 0, rs = 0, rph = 0;
+  auto tile_next = [&]() {
+    if (++ts == p.stages) { ts = 0; tph ^= 1; }
+  };
+  auto slot_next = [&]() {
+    if (++rs == p.slots) { rs = 0; rph ^= 1; }
   };
 
   bool ok = true;
-  if (warp == kProducer) {
-    // ====================================================================== producer
+  if (warp == kTileWarp) {
+    // ====================================================================== tile warp
+    if (lane == 0) {
+      int li = 0, cur_b = -1, c = 0, st = 0;
+      bool load = false, flush = false, bad = false;
+      HeadIter it;
+      it.init(h0, p.H, p.HPG);
+      for (long long gh = h0; gh < h1; ++gh, it.next(p.H, p.HPG)) {
+        const int b = it.b;
+        if (b != cur_b) {
+          cur_b = b;
+          seq_plan(b, c, st, load, flush, bad);
+        }
+        if (!load) continue;
+        if (li >= p.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
+        const void* src = from_copy ? (const void*)(p.copy + (size_t)gh * p.head_stride)
+                                    : (const void*)(p.ckpt + (size_t)gh * p.P * N);
+        const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)p.P * N * 4;
+        mbar_arrive_tx(tfull0 + 8 * ts, bytes);
+        tma_load_1d(smem_u32(smem + (size_t)ts * p.stage_bytes), src, bytes, tfull0 + 8 * ts);
+        tile_next();
+        ++li;
+      }
+      if (!ok) {  // drain the bulk copies still in flight (bounded), then leave
+        volatile int dummy = 0;
+        for (int k = 0; k < p.stages && k < li; ++k) {
+          const int i = li - 1 - k;
+          mbar_wait(tfull0 + 8 * (i % p.stages), (i / p.stages) & 1, &dummy, p.err);
+        }
+      }
+    }
+  } else if (warp == kGatherWarp) {
+    // ====================================================================== gather warp
     int li = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
     long long cur_gg = -1;
     bool load = false, flush = false, bad = false;
@@ -492,19 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      const int s = stg_i;
-      const bool w = li < p.stages || mbar_wait(empty0 + 8 * s, stg_ph ^ 1, abort_flag, p.err);
+      const bool w = li < p.slots || mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err);
       if (!__all_sync(kFull, w)) { ok = false; break; }
-      uint8_t* stg = smem + (size_t)s * p.stage_bytes;
-      const uint32_t sdst = smem_u32(stg);
-      if (lane == 0) {
-        const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
-        const void* src = from_copy ? (const void*)(p.copy + hrow * p.head_stride)
-                                    : (const void*)(p.ckpt + hrow * p.P * N);
-        const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)p.P * N * 4;
-        mbar_arrive_tx(full0 + 8 * s, bytes);
-        tma_load_1d(sdst, src, bytes, full0 + 8 * s);
-      }
+      const uint32_t sdst = smem_u32(smem + p.slot_off + (size_t)rs * p.slot_bytes);
       if (lane < J) {
         const int j = lane;
         const float* asrc;
@@ -512,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         else if (j < c) asrc = p.ring_a + hrow * p.Rp + ring_slot(st, j, p.R);
         else if (MODE == kVerify) asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
         else asrc = p.alpha + hrow;
-        cp_async4(sdst + p.sa_off + 4 * j, asrc);
+        cp_async4(sdst + 4 * j, asrc);
       }
       for (int j = vj0, ch = vch0; j < J;) {
         cp_async16(sdst + p.sv_off + j * p.P * ES + ch * 16, vrow_src(j, c, st, b, hh, hrow) + ch * 16);
@@ -520,29 +609,23 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         ch += vdch;
         if (ch >= chp) { ch -= chp; ++j; }
       }
-      cp_async_arrive(small0 + 8 * s);
-      stage_next();
+      cp_async_arrive(sfull0 + 8 * rs);
+      slot_next();
       ++li;
     }
     cp_async_wait_all();
-    if (!ok && lane == 0) {  // drain the bulk copies still in flight (bounded), then leave
-      volatile int dummy = 0;
-      for (int k = 0; k < p.stages && k < li; ++k) {
-        const int i = li - 1 - k;
-        mbar_wait(full0 + 8 * (i % p.stages), (i / p.stages) & 1, &dummy, p.err);
-      }
-    }
-  } else if (warp == kCoef) {
+  } else if (warp >= kCoef0 && warp < kCoef0 + kNCoef) {
     // ====================================================================== coefficients
-    float* skq_w = reinterpret_cast<float*>(smem + p.wsc_off);  // [kTMax][kRMax] k_j^T q_t (verify)
-    int gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
+    const int cwi = warp - kCoef0;  // this warp takes the loaded heads with index = cwi (mod kNCoef)
+    float* skq_w = reinterpret_cast<float*>(smem + p.wsc_off) + cwi * kTMax * kRMax;  // [kTMax][kRMax] (verify)
+    int lh = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
     long long cur_gg = -1;
     bool load = false, flush = false, bad = false;
     float sj = 0.f;  // decode: lane j holds k_j^T q
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
-      const int b = it.b, hh = it.hh, g = it.g;
+      const int b = it.b, g = it.g;
       const long long gg = (long long)b * p.G + g;
       const size_t hrow = (size_t)gh;
       if (b != cur_b) {
@@ -588,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if constexpr (kAppendMode) {  // the group's first head (if this CTA owns it) appends the new keys
             const long long gfirst = (long long)b * p.H + (long long)g * p.HPG;
             const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
-            if (gfirst >= h0 && na > 0) {
+            if (cwi == 0 && gfirst >= h0 && na > 0) {
               const size_t grow = (size_t)b * p.G + g;
               for (int idx = lane; idx < na * CHN; idx += 32) {
                 const int t = idx / CHN, ch = idx % CHN;
@@ -601,13 +684,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      const int s = stg_i;
-      if (!__all_sync(kFull, mbar_wait(small0 + 8 * s, stg_ph, abort_flag, p.err))) { ok = false; break; }
-      uint8_t* stg = smem + (size_t)s * p.stage_bytes;
-      const float* sa = reinterpret_cast<const float*>(stg + p.sa_off);  // alpha_j, record order
-      const uint8_t* sv = stg + p.sv_off;                                // v_j rows, record order
-      float* sc = reinterpret_cast<float*>(stg + p.sc_off);             // coefficients
-      const float aj = (lane < J) ? sa[lane] : 1.f;                      // lane j holds alpha of record j
+      if ((lh++ % kNCoef) != cwi) {  // another coefficient warp takes this head
+        slot_next();
+        continue;
+      }
+      if (!__all_sync(kFull, mbar_wait(sfull0 + 8 * rs, rph, abort_flag, p.err))) { ok = false; break; }
+      uint8_t* slot = smem + p.slot_off + (size_t)rs * p.slot_bytes;
+      const float* sa = reinterpret_cast<const float*>(slot);  // alpha_j, record order
+      const uint8_t* sv = slot + p.sv_off;                      // v_j rows, record order
+      float* sc = reinterpret_cast<float*>(slot + p.sc_off);    // coefficients
+      const float aj = (lane < J) ? sa[lane] : 1.f;             // lane j holds alpha of record j
       if constexpr (MODE == kVerify) {
         for (int t = 0; t < p.T; ++t) {
           const int ht = c + t + 1;
@@ -624,44 +710,57 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const float wj = (lane < 31) ? nxt : 1.f;  // lane j: weight g_{j+2:J} of record j
         if (lane == 0) sc[0] = incl;               // g_{1:J}
         if (flush) {
-          // fold: scaled values u_j[p] = g_{j+2:J} v_j[p]
+          // fold: scaled values u_j[p] = g_{j+2:J} v_j[p]; lane handles row pairs 2*lane + 64 m
+#pragma unroll 4
           for (int j = 0; j < J; ++j) {
             const float wjj = __shfl_sync(kFull, wj, j);
-            for (int r = lane; r < p.P; r += 32) sc[kCoefOff + j * p.P + r] = wjj * In<TIn>::lds(sv, j * p.P + r);
+            for (int r = 2 * lane; r < p.P; r += 64) {
+              const float2 v2 = In<TIn>::lds2(sv, j * p.P + r);
+              *reinterpret_cast<float2*>(sc + kCoefOff + j * p.P + r) = make_float2(wjj * v2.x, wjj * v2.y);
+            }
           }
         } else if constexpr (MODE == kDecode) {
-          // non-flush: value term sum_j g_{j+2:J} (k_j^T q) v_j[p]
+          // non-flush: value term sum_j g_{j+2:J} (k_j^T q) v_j[p] for row pairs 2*lane + 64 m (P <= 128)
           const float cj = (lane < J) ? wj * sj : 0.f;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows lane + 32 m (P <= 128)
+          float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 4
           for (int j = 0; j < J; ++j) {
             const float cjj = __shfl_sync(kFull, cj, j);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int r = lane + 32 * m;
-              if (r < p.P) acc[m] = fmaf(cjj, In<TIn>::lds(sv, j * p.P + r), acc[m]);
+            for (int m = 0; m < 2; ++m) {
+              const int r = 2 * lane + 64 * m;
+              if (r < p.P) {
+                const float2 v2 = In<TIn>::lds2(sv, j * p.P + r);
+                acc[m].x = fmaf(cjj, v2.x, acc[m].x);
+                acc[m].y = fmaf(cjj, v2.y, acc[m].y);
+              }
             }
           }
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int r = lane + 32 * m;
-            if (r < p.P) sc[kCoefOff + r] = acc[m];
+          for (int m = 0; m < 2; ++m) {
+            const int r = 2 * lane + 64 * m;
+            if (r < p.P) *reinterpret_cast<float2*>(sc + kCoefOff + r) = acc[m];
           }
         }
       }
-      if constexpr (kAppendMode) {  // the new decays go to the ring
+      __syncwarp();
+      if (lane == 0) mbar_arrive(scoef0 + 8 * rs);  // coefficients published
+      if constexpr (kAppendMode) {                   // the new decays and value rows go to the ring
         const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[c + lane];
+        const int chp = p.P * ES / 16;
+        for (int t = 0; t < na; ++t) {
+          uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
+          for (int ch = lane; ch < chp; ch += 32)
+            *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
+        }
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(coef0 + 8 * s);   // coefficients published
-        mbar_arrive(empty0 + 8 * s);  // this warp is done with the stage
-      }
-      stage_next();
+      if (lane == 0) mbar_arrive(sempty0 + 8 * rs);  // this warp is done with the slot
+      slot_next();
     }
   } else {
     // ====================================================================== dot warps
-    const int ct = threadIdx.x;  // 0..255
     const int col4 = lane % LPR, rsub = lane / LPR;
     int gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
     long long cur_gg = -1;
@@ -676,7 +775,6 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
     const int rows_pass = kNDW * kKR * RPI;
     const int npass = (p.P + rows_pass - 1) / rows_pass;
-    const int chp = p.P * ES / 16;
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
@@ -709,25 +807,17 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      const int s = stg_i;
-      const bool got = mbar_wait(full0 + 8 * s, stg_ph, abort_flag, p.err) &&
-                       mbar_wait(small0 + 8 * s, stg_ph, abort_flag, p.err) &&
-                       mbar_wait(coef0 + 8 * s, stg_ph, abort_flag, p.err);
+      // the coefficient warp arrives only after the record gathers landed, so
+      // its barrier also covers alpha_j and v_j
+      const bool got = mbar_wait(tfull0 + 8 * ts, tph, abort_flag, p.err) &&
+                       mbar_wait(scoef0 + 8 * rs, rph, abort_flag, p.err) &&
+                       (MODE != kVerify || mbar_wait(sfull0 + 8 * rs, rph, abort_flag, p.err));
       if (!__all_sync(kFull, got)) { ok = false; break; }
-      const uint8_t* tile = smem + (size_t)s * p.stage_bytes;
+      const uint8_t* tile = smem + (size_t)ts * p.stage_bytes;
       const float* tf = reinterpret_cast<const float*>(tile);
-      const uint8_t* sv = tile + p.sv_off;
-      const float* sc = reinterpret_cast<const float*>(tile + p.sc_off);
-
-      if constexpr (kAppendMode) {  // new value rows go to the ring (16-byte chunks over the dot threads)
-        const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
-        for (int idx = ct; idx < na * chp; idx += kNDW * 32) {
-          const int t = idx / chp, ch = idx - t * chp;
-          const uint4 val = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
-          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_v) +
-                                    (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES + ch * 16) = val;
-        }
-      }
+      const uint8_t* slot = smem + p.slot_off + (size_t)rs * p.slot_bytes;
+      const uint8_t* sv = slot + p.sv_off;
+      const float* sc = reinterpret_cast<const float*>(slot + p.sc_off);
 
       if constexpr (MODE == kVerify) {
         // ================================================ verify (T queries)
@@ -773,31 +863,63 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const float* su = sc + kCoefOff;  // [J][P]
         for (int pass = 0; pass < npass; ++pass) {
           const int rbase = (pass * kNDW + warp) * kKR;
+          if (rbase * RPI >= p.P) break;  // warp-uniform: no rows left for this warp
           float4 acc[kKR];
+          if constexpr (RPI == 1) {
+            // The warp's 8 rows are consecutive and all valid (P is a multiple of 8).
+            // Accumulate row pairs with packed fp32x2 fmas: A[kp][col] = {row 2kp, row 2kp+1}.
+            f32x2 A[kKR / 2][4];
 #pragma unroll
-          for (int kk = 0; kk < kKR; ++kk) {
-            const int row = (rbase + kk) * RPI + rsub;
-            if (row < p.P) {
-              const float4 x = lds4(tf + ((size_t)row * LPR + col4) * 4);
-              acc[kk] = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
-            } else {
-              acc[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int kp = 0; kp < kKR / 2; ++kp) {
+              const float4 x0 = lds4(tf + ((size_t)(rbase + 2 * kp) * LPR + col4) * 4);
+              const float4 x1 = lds4(tf + ((size_t)(rbase + 2 * kp + 1) * LPR + col4) * 4);
+              A[kp][0] = pk2(gam * x0.x, gam * x1.x);
+              A[kp][1] = pk2(gam * x0.y, gam * x1.y);
+              A[kp][2] = pk2(gam * x0.z, gam * x1.z);
+              A[kp][3] = pk2(gam * x0.w, gam * x1.w);
             }
-          }
-          if (rbase * RPI < p.P) {
+#pragma unroll 2
+            for (int j = 0; j < J; ++j) {
+              const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
+              const f32x2 kx = pk2(kv.x, kv.x), ky = pk2(kv.y, kv.y), kz = pk2(kv.z, kv.z), kw = pk2(kv.w, kv.w);
+              f32x2 U[kKR / 2];
+#pragma unroll
+              for (int qd = 0; qd < kKR / 4; ++qd) {
+                const ulonglong2 uq = *reinterpret_cast<const ulonglong2*>(su + j * p.P + rbase + 4 * qd);
+                U[2 * qd] = uq.x;
+                U[2 * qd + 1] = uq.y;
+              }
+#pragma unroll
+              for (int kp = 0; kp < kKR / 2; ++kp) {
+                A[kp][0] = fma2(U[kp], kx, A[kp][0]);
+                A[kp][1] = fma2(U[kp], ky, A[kp][1]);
+                A[kp][2] = fma2(U[kp], kz, A[kp][2]);
+                A[kp][3] = fma2(U[kp], kw, A[kp][3]);
+              }
+            }
+#pragma unroll
+            for (int kp = 0; kp < kKR / 2; ++kp) {
+              acc[2 * kp] = make_float4(lo2(A[kp][0]), lo2(A[kp][1]), lo2(A[kp][2]), lo2(A[kp][3]));
+              acc[2 * kp + 1] = make_float4(hi2(A[kp][0]), hi2(A[kp][1]), hi2(A[kp][2]), hi2(A[kp][3]));
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kKR; ++kk) {
+              const int row = (rbase + kk) * RPI + rsub;
+              if (row < p.P) {
+                const float4 x = lds4(tf + ((size_t)row * LPR + col4) * 4);
+                acc[kk] = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
+              } else {
+                acc[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
             for (int j = 0; j < J; ++j) {
               const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
               float uu[kKR];
-              if constexpr (RPI == 1) {  // the warp's 8 rows are consecutive: two vector loads
-                const float4 u0 = lds4(su + j * p.P + rbase), u1 = lds4(su + j * p.P + rbase + 4);
-                uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
-                uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
-              } else {
 #pragma unroll
-                for (int kk = 0; kk < kKR; ++kk) {
-                  const int row = (rbase + kk) * RPI + rsub;
-                  uu[kk] = (row < p.P) ? su[j * p.P + row] : 0.f;
-                }
+              for (int kk = 0; kk < kKR; ++kk) {
+                const int row = (rbase + kk) * RPI + rsub;
+                uu[kk] = (row < p.P) ? su[j * p.P + row] : 0.f;
               }
 #pragma unroll
               for (int kk = 0; kk < kKR; ++kk) {
@@ -910,10 +1032,14 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         }
       }
 
-      // ---------------------------------------------------- release the stage
+      // ---------------------------------------------------- release the stage and the slot
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      stage_next();
+      if (lane == 0) {
+        mbar_arrive(tempty0 + 8 * ts);
+        mbar_arrive(sempty0 + 8 * rs);
+      }
+      tile_next();
+      slot_next();
     }
   }
 
