@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <mutex>
 #include <string>
 
 #include "../../include/rssm.h"
@@ -392,6 +393,69 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
   const cudaError_t e = rssm::launch_conv(p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
                                           cfg->N, cfg->in_dtype);
   if (e != cudaSuccess) return cuda_fail(e, "conventional launch");
+  return RSSM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Decode step with library-owned scratch.
+//
+// Some callers cannot hand the library any more device memory once decoding
+// has started: engines that carve one fixed arena at start-up, code that runs
+// while another component owns the device allocator, or paths that are being
+// captured into a CUDA graph, where cudaMalloc is not allowed. The decode
+// kernel needs one piece of scratch, the per-sequence ticket counters that
+// tell the last CTA of a sequence to advance its pointers. This variant keeps
+// those counters in a static device array of this file instead of the
+// caller's pointer block, so it allocates nothing.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kStaticTicketSeqs = 8192;  // 32 KiB held by every GPU that loads the library
+__device__ __align__(256) int32_t g_static_tickets[kStaticTicketSeqs];
+constexpr int kMaxDevices = 64;
+int32_t* g_static_ticket_addr[kMaxDevices] = {};  // device address of the array, per device
+std::mutex g_static_ticket_mu;
+}  // namespace
+
+rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, const void* v, const void* k,
+                                            const void* q, float* o, void* stream) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
+  if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
+    return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
+  if (h->cfg.B > kStaticTicketSeqs)
+    return fail(RSSM_EUNSUPPORTED, "B=%d exceeds the %d sequences of the library-owned scratch", h->cfg.B,
+                kStaticTicketSeqs);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(RSSM_EUNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
+  int32_t* tickets = nullptr;
+  {
+    // Set-up, once per device with that device current: the host-side name of
+    // the array is not a device address, so ask the runtime for the real one.
+    std::lock_guard<std::mutex> lock(g_static_ticket_mu);
+    if (!g_static_ticket_addr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_tickets);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static tickets)");
+      g_static_ticket_addr[dev] = static_cast<int32_t*>(ptr);
+    }
+    tickets = g_static_ticket_addr[dev];
+  }
+  Plan pl;
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  if (s != RSSM_OK) return s;
+  fill_common(h, &pl.p);
+  pl.p.ticket = tickets;
+  pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps the last call's contents; the tickets must start at zero.
+  e = cudaMemsetAsync(tickets, 0, (size_t)h->cfg.B * sizeof(int32_t), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static tickets)");
+  const long long heads = (long long)h->cfg.B * h->cfg.H;
+  e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, st, h->cfg.N, h->cfg.in_dtype, h->cfg.read_fmt);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");
+  h->last_T = 0;
   return RSSM_OK;
 }
 

@@ -44,6 +44,7 @@ SIGNATURES = {
     "rssm_read_copy_layout": [_Cfg_p, _c_size_p, _c_size_p, _c_size_p],
     "rssm_create": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)],
     "rssm_decode_step": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_decode_step_static_scratch": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_verify": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_commit": [_vp, _vp, _vp],
     "rssm_flush": [_vp, ctypes.c_int32, _vp],

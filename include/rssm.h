@@ -176,6 +176,25 @@ rssm_status rssm_destroy(rssm_handle h);
 /* Message of the last error on the calling thread (never NULL). */
 const char* rssm_last_error(void);
 
+/* Decode step that allocates nothing (no counterpart in the paper: a library
+ * convenience). Same arguments, results and error behaviour as
+ * rssm_decode_step. The decode kernel's only scratch, one ticket counter per
+ * sequence, lives in a static device array of the library (8192 sequences,
+ * 32 KiB, held by every GPU that loads the library until the process exits)
+ * instead of the caller's pointer block. It is for callers that cannot provide
+ * more device memory once decoding runs: a fixed arena planned at start-up, an
+ * allocator owned by another component, or a stream being captured.
+ *  - B above 8192 returns RSSM_EUNSUPPORTED.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress). Make that first call before any
+ *    stream capture.
+ *  - Each call clears the counters it uses with cudaMemsetAsync on `stream`.
+ *    It calls no cudaMalloc or cudaFree.
+ *  - Every call shares the one array: calls that overlap on the GPU (other
+ *    streams, other handles) race on it. Serialize them on one stream. */
+rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, const void* v, const void* k,
+                                            const void* q, float* o, void* stream);
+
 /* Comparison kernel (not part of the replay path): the conventional fused
  * read-update-write step S <- alpha S + v k^T, o = S q on a full state
  * [B,H,P,N] fp32, read and written every step (aikraft.ru page §01). cfg's
