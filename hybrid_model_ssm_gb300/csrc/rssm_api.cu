@@ -368,6 +368,13 @@ rssm_status rssm_clear_error(rssm_handle h, void* stream) {
   return RSSM_OK;
 }
 
+rssm_status rssm_selftest_bounded_wait(uint32_t* err_word, void* stream) {
+  if (!err_word) return fail(RSSM_EINVAL, "err_word is NULL");
+  const cudaError_t e = rssm::launch_wait_selftest(err_word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test launch");
+  return RSSM_OK;
+}
+
 rssm_status rssm_destroy(rssm_handle h) {
   delete h;
   return RSSM_OK;

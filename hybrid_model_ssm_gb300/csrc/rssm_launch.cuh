@@ -51,6 +51,7 @@ cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t s
 cudaError_t launch_flush(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
 cudaError_t launch_quant(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf);
 cudaError_t launch_conv(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
+cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t st);
 cudaError_t launch_commit(int B, int T, int R, const int32_t* accepted, int32_t* count, uint32_t* err,
                           cudaStream_t st);
 

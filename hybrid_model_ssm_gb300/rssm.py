@@ -50,6 +50,7 @@ SIGNATURES = {
     "rssm_flush": [_vp, ctypes.c_int32, _vp],
     "rssm_read_pointers": [_vp, _c_i32_p, _c_i32_p, _c_u32_p, _vp],
     "rssm_clear_error": [_vp, _vp],
+    "rssm_selftest_bounded_wait": [_vp, _vp],
     "rssm_destroy": [_vp],
     "rssm_last_error": [],
     "rssm_conventional_step": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp],

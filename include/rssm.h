@@ -170,6 +170,13 @@ rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* coun
 /* Clear the device error word (asynchronous). */
 rssm_status rssm_clear_error(rssm_handle h, void* stream);
 
+/* Self-test of the kernels' bounded waits (no counterpart in the paper). It
+ * launches one warp that waits on an mbarrier nothing completes. After the
+ * wait limit (about 1 s) the warp gives up, ORs the timeout bit (4) into
+ * *err_word (a device uint32 the caller owns) and returns. No trap, no
+ * fault: the context stays usable. Asynchronous on `stream`. */
+rssm_status rssm_selftest_bounded_wait(uint32_t* err_word, void* stream);
+
 /* Release the host handle. Caller memory is not touched. */
 rssm_status rssm_destroy(rssm_handle h);
 

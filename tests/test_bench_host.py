@@ -1,0 +1,74 @@
+"""Host logic of bench.py, checked without a GPU.
+
+- The analytic HBM bytes per window, against the closed forms worked out by hand.
+- The multi-rank timing path: two gloo ranks on the CPU take the max over ranks,
+  the way torchrun replicas do on GPUs.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import synth
+
+
+def test_window_bytes_of_the_layer_workload():
+    s = synth.PRESETS["mamba2_layer_b256_l16"]
+    S = 4 * 128 * 64 * 128
+    r = 4 * 128 + 2 * 128 * 64 + 2 * 8 * 128
+    assert (S, r) == (4194304, 18944)
+    inp, out = r + 2 * 8 * 128, 4 * 128 * 64
+    expect = 16 * S + S + r * 16 * 15 // 2 + 16 * (inp + out) + 15 * r
+    wb = bench.window_bytes(s)
+    assert wb["replay_window"] == expect == 74720768
+    assert wb["replay_per_seq_step"] == 4670048
+    assert wb["conventional_per_seq_step"] == 2 * S + inp + out == 8442368
+    # read copies: (L-1) non-flush reads of the copy, one flush read of S and one write of S + copy
+    c4 = 128 * (64 * 128 + 4 * 64)
+    e4 = bench.window_bytes(s, "e4m3")["replay_window"]
+    assert e4 == 15 * c4 + S + S + c4 + r * 120 + 16 * (inp + out) + 15 * r
+    assert bench.copy_bytes_per_head(s, "e2m1") == 64 * 64 + 64 * 8 + 64 * 4
+
+
+def _free_port():
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def _rank(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        results[rank] = bench.max_over_ranks(float(10 * (rank + 1)), world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    world = 2
+    results = mp.Manager().dict()
+    mp.start_processes(_rank, args=(world, _free_port(), results), nprocs=world, start_method="spawn")
+    assert dict(results) == {0: 20.0, 1: 20.0}
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    bench.barrier(1)
+
+
+def test_reference_arm_runs_on_cpu(capsys):
+    """The reference arm (the float64 oracle) prints one JSON line with its own e2e and cpu_baseline."""
+    import json
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
+    if not torch.cuda.is_available():
+        with pytest.raises(SystemExit):
+            bench.main(["--steps", "1", "--warmup", "3"])

@@ -101,3 +101,29 @@ def test_ring_overflow_sets_error_and_leaves_sequence_untouched():
     start3, count3, err3 = model.read_pointers()
     assert count3.tolist() == [0, 0] and err3 == 0
     assert start3.tolist() == [6 % 6, 3]
+
+
+def test_bounded_wait_expires_and_reports():
+    """A wait that nothing completes gives up after its limit, sets the timeout
+    bit in the error word and returns; the context keeps working afterwards."""
+    import ctypes
+    import time
+
+    from hybrid_model_ssm_gb300 import lib
+    from hybrid_model_ssm_gb300.rssm import ERR_TIMEOUT, RSSM_OK
+
+    require_gpu()
+    word = torch.zeros(4, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    st = lib().rssm_selftest_bounded_wait(word.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == RSSM_OK
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(word[0]) & ERR_TIMEOUT
+    assert 0.5 < elapsed < 10.0
+    shape = S(B=2, H=4, P=16, N=32, G=2, L=4, seed=43)
+    model, gen = _model(shape)
+    a, v, k, q = (dev(x) for x in synth.decode_step_inputs(shape, gen))
+    model.decode_step(a, v, k, q)
+    assert model.read_pointers()[2] == 0

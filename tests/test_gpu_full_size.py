@@ -1,0 +1,96 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+Mamba-2 layer decode: B=256, H=128, P=64, N=128, G=8, L=16, bf16 inputs, 256
+steps from an N(0, 0.1^2) state. Speculative verify: the same layer at B=512,
+T=4, 64 rounds with seeded accepted lengths in 0..4, flushing every sequence
+that reaches 16 records. The GPU runs the whole batch; the float64 oracle
+follows a sample of sequences (all heads) through every step. The pointers
+of every sequence are compared bit for bit against the oracle's bookkeeping.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from hybrid_model_ssm_gb300 import ReplaySSM
+from tests.gpu_helpers import REL_TOL, PointerShadow, dev, f64, layer_shape, require_gpu, slice_rel_err
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _sample(B, n=8):
+    return np.unique(np.linspace(0, B - 1, n).round().astype(int))
+
+
+def test_mamba2_layer_decode_b256_256_steps():
+    require_gpu()
+    shape = synth.PRESETS["mamba2_layer_b256_l16"]
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    model = ReplaySSM(layer_shape(shape), dev(S0))
+    sample = _sample(shape.B)
+    orc = oracle.ReplayOracle(f64(S0[sample]), L=shape.L, R=shape.R, G=shape.G)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    del S0
+    worst_o = worst_s = 0.0
+    for t in range(256):
+        a, v, k, q = synth.decode_step_inputs(shape, gen)
+        o = model.decode_step(dev(a), dev(v), dev(k), dev(q))
+        o_s = o[torch.as_tensor(sample, device="cuda")].cpu()
+        o_ref, flushed = orc.decode(f64(a[sample]), f64(v[sample]), f64(k[sample]), f64(q[sample]))
+        shadow.decode()
+        e = slice_rel_err(o_s, o_ref, 1)
+        worst_o = max(worst_o, e)
+        assert e <= REL_TOL, f"step {t}: rel err {e:.3g}"
+        if flushed.any():
+            ck = model.ckpt[torch.as_tensor(sample, device="cuda")].cpu()
+            es = slice_rel_err(ck, orc.ckpt, 2)
+            worst_s = max(worst_s, es)
+            assert es <= REL_TOL, f"step {t}: checkpoint rel err {es:.3g}"
+        if t % 16 == 15 or t < 3:
+            start, count, err = model.read_pointers()
+            assert err == 0
+            assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count)
+    print(f"decode b256: worst output rel err {worst_o:.2e}, checkpoint {worst_s:.2e}")
+
+
+def test_mamba2_verify_b512_t4_64_rounds():
+    require_gpu()
+    shape = synth.PRESETS["mamba2_verify_b512_t4"]
+    T = shape.T_max
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    model = ReplaySSM(layer_shape(shape), dev(S0))
+    sample = _sample(shape.B)
+    sidx = torch.as_tensor(sample, device="cuda")
+    orc = oracle.ReplayOracle(f64(S0[sample]), L=shape.L, R=shape.R, G=shape.G)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    del S0
+    worst = 0.0
+    flushes = 0
+    for r in range(64):
+        a, v, k, q = synth.verify_round_inputs(shape, T, gen)
+        O = model.verify(dev(a), dev(v), dev(k), dev(q))
+        O_ref = orc.verify(f64(a[sample]), f64(v[sample]), f64(k[sample]), f64(q[sample]))
+        shadow.verify(T)
+        e = slice_rel_err(O[sidx].cpu(), O_ref, 1)
+        worst = max(worst, e)
+        assert e <= REL_TOL, f"round {r}: verify rel err {e:.3g}"
+        acc = synth.accepted_lengths(shape.B, T, gen)
+        model.commit(dev(acc))
+        orc.commit(acc.numpy()[sample])
+        shadow.commit(acc.numpy())
+        model.flush(shape.L)
+        fl = orc.flush(shape.L)
+        shadow.flush(shape.L)
+        start, count, err = model.read_pointers()
+        assert err == 0
+        assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count), f"round {r}"
+        if fl.any():
+            flushes += int(fl.sum())
+            ck = model.ckpt[sidx].cpu()
+            for i in np.nonzero(fl)[0]:
+                assert slice_rel_err(ck[i], orc.ckpt[i], 2) <= REL_TOL, f"round {r}"
+    assert flushes > 0
+    print(f"verify b512: worst output rel err {worst:.2e}, sampled flushes {flushes}")
