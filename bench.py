@@ -426,6 +426,122 @@ def run_reference(args, world, rank):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+VERIFY_WORKLOAD = synth.PRESETS["mamba2_verify_b512_t4"]
+VERIFY_METRIC = "speculative verify draft-tokens/s at B=512, T=4, L=16 (verify + commit + flush per round)"
+
+
+def verify_round_bytes(s, T: int, counts: np.ndarray, accepted: np.ndarray):
+    """Algorithmic HBM bytes of one speculative round for the whole batch.
+
+    verify: per sequence |S| + c|r| + T(|in| + |r| + |o|): the checkpoint once, the
+    c committed records, the T drafts' records and queries, T outputs and the T
+    appended records. commit: 12 B per sequence. flush: every sequence that
+    reaches L records reads |S| and its c records and writes |S| once.
+    Returns (verify_bytes, flush_bytes, counts_after).
+    """
+    es = 2 if s.in_dtype == "bf16" else 4
+    S = 4 * s.H * s.P * s.N
+    r = record_bytes(s)
+    inp = r + es * s.G * s.N
+    out = 4 * s.H * s.P
+    vb = int(np.sum(S + counts * r + T * (inp + r + out)))
+    c2 = counts + accepted
+    fl = c2 >= s.L
+    fb = int(np.sum(np.where(fl, 2 * S + c2 * r, 0))) + 12 * len(counts)
+    return vb, fb, np.where(fl, 0, c2)
+
+
+def run_verify(args, world, rank, local):
+    from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM
+
+    torch.cuda.set_device(local)
+    s = VERIFY_WORKLOAD if args.batch is None else VERIFY_WORKLOAD.with_(B=args.batch)
+    T = s.T_max
+    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=T, in_dtype=s.in_dtype)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(s.seed + 1000 * rank)
+    model = ReplaySSM(ls, torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev) * 0.1)
+    sc = 1.0 / math.sqrt(s.N)
+    pool = []
+    for _ in range(8):
+        u = torch.randn((s.B, T, s.H), generator=gen, device=dev)
+        pool.append((torch.exp(-torch.nn.functional.softplus(u)).float(),
+                     (torch.randn((s.B, T, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
+                     (torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
+                     (torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)))
+    cgen = synth.make_generator(s.seed + 7)
+    rounds = args.warmup + args.steps
+    acc_host = [synth.accepted_lengths(s.B, T, cgen) for _ in range(rounds)]
+    acc_dev = [a.to(dev) for a in acc_host]
+    out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=dev)
+
+    def one_round(i, ev=None):
+        a, v, k, q = pool[i % len(pool)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if ev is not None else None
+        if e: e[0].record(stream)
+        model.verify(a, v, k, q, out=out)
+        if e: e[1].record(stream)
+        model.commit(acc_dev[i])
+        if e: e[2].record(stream)
+        model.flush(s.L)
+        if e: e[3].record(stream); ev.append(e)
+
+    counts = np.zeros(s.B, np.int64)
+    for i in range(args.warmup):
+        one_round(i)
+        _, _, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64))
+    torch.cuda.synchronize()
+    model.read_pointers()
+    ev = []
+    vbytes = fbytes = 0
+    for i in range(args.warmup, rounds):
+        vb, fb, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64))
+        vbytes += vb
+        fbytes += fb
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.warmup, rounds):
+            one_round(i, ev)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    _, count_dev, err = model.read_pointers()
+    assert np.array_equal(count_dev.numpy(), counts), "host pointer replay diverged from the device"
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, world)
+    tv = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    tc = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    tf = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    peak, peak_kind = measured_peak_gbs()
+    achieved = vbytes / tv / 1e9
+    if rank != 0:
+        return None
+    return {
+        "metric": VERIFY_METRIC, "value": world * s.B * T * args.steps / elapsed, "unit": "draft-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"ReplaySSM speculative round: B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
+                               f"T={T}, bf16 inputs; one step = verify + commit (seeded accepted lengths "
+                               f"0..{T}) + flush of sequences at {s.L} records",
+                   "global_batch": s.B * world, "l2": "no flush needed: 2 GiB checkpoint per replica"},
+        "seq_rounds_per_s": world * s.B * args.steps / elapsed,
+        "roofline": {"bound": "hbm", "kernel": "verify", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": vbytes / args.steps,
+                     "mean_launch_ms": tv / args.steps * 1e3},
+        "breakdown_ms_per_round": {"verify": tv / args.steps * 1e3, "commit": tc / args.steps * 1e3,
+                                   "flush": tf / args.steps * 1e3,
+                                   "flush_hbm_gbs": fbytes / tf / 1e9 if tf > 0 else None},
+        "clocks": clk.summary(), "gpu_launches": 3 * args.steps, "device_error_word": err,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,6 +553,8 @@ def main(argv=None):
     ap.add_argument("--no-conventional", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller cases for ncu captures; not a bench line)")
+    ap.add_argument("--workload", choices=["decode", "verify"], default="decode",
+                    help="decode: the headline metric; verify: speculative rounds (B=512, T=4)")
     ap.add_argument("--read-fmt", choices=["e4m3", "e2m1"], default=None,
                     help="non-flush steps read a low-precision copy of the checkpoint")
     args = ap.parse_args(argv)
@@ -448,7 +566,7 @@ def main(argv=None):
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
-        line = run_ours(args, world, rank, local)
+        line = run_verify(args, world, rank, local) if args.workload == "verify" else run_ours(args, world, rank, local)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -117,22 +117,38 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
   const size_t budget = kSmemMax - fixed;
   const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, budget / (tile + 3 * slot)));
   const int slots = (int)std::max<size_t>(2, std::min<size_t>(kMaxSlots, (budget - stages * tile) / slot));
+  // Dot groups: as many heads in flight as keeps two tile stages per group.
+  int dgroups = 1;
+  while (dgroups < 8 && stages >= 4 * dgroups && slots >= 4 * dgroups) dgroups *= 2;
+#ifdef RSSM_DGROUPS  // build-time override for tuning
+  dgroups = RSSM_DGROUPS;
+#endif
+  while (dgroups > 1 && (stages < dgroups || slots < dgroups)) dgroups /= 2;
+  // Every ring's length must be a multiple of the number of consumers that take
+  // its entries in turn. Then the previous use of an entry belongs to the same
+  // consumer and has completed, and an mbarrier parity wait cannot be satisfied
+  // by the previous phase.
+  const int stages_used = stages - stages % dgroups;
+  const int slot_mult = std::max(kNCoef, dgroups);  // both are powers of two
+  const int slots_used = slots - slots % slot_mult;
+  if (stages_used < 2 || slots_used < slot_mult) return fail(RSSM_EUNSUPPORTED, "shared memory too small for the rings");
   rssm::Params& p = pl->p;
-  p.stages = stages;
+  p.dgroups = dgroups;
+  p.stages = stages_used;
   p.stage_bytes = (int)tile;
-  p.slots = slots;
+  p.slots = slots_used;
   p.slot_bytes = (int)slot;
   p.sv_off = (int)sv_off;
   p.sc_off = (int)sc_off;
-  size_t off = (size_t)stages * tile;
-  p.slot_off = (int)off; off += (size_t)slots * slot;
+  size_t off = (size_t)stages_used * tile;
+  p.slot_off = (int)off; off += (size_t)slots_used * slot;
   p.gb_off = (int)off; off += 2 * gb;
   p.gb_bytes = (int)gb;
   p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
   p.bar_off = (int)off; off += bars;
   if (off > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
-  pl->stages = stages;
+  pl->stages = stages_used;
   pl->smem = off;
   return RSSM_OK;
 }
@@ -355,6 +371,7 @@ rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* coun
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "read pointers");
   if (err_host) *err_host = err;
+  if (err & rssm::kErrPlan) return fail(RSSM_EUNSUPPORTED, "a kernel refused its launch plan (error word 0x%x)", err);
   if (err & rssm::kErrTimeout) return fail(RSSM_ETIMEOUT, "a bounded wait inside a kernel expired (error word 0x%x)", err);
   if (err & (rssm::kErrCapacity | rssm::kErrAccept))
     return fail(RSSM_ECAPACITY, "ring overflow or bad accepted length (error word 0x%x)", err);

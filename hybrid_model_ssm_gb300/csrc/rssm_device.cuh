@@ -36,10 +36,17 @@ namespace rssm {
 #define RSSM_ROWS_PER_WARP 8
 #endif
 constexpr int kNDW = RSSM_DOT_WARPS;       // dot warps per CTA (stream the checkpoint tile)
+#ifndef RSSM_GATHER_BULK
+#define RSSM_GATHER_BULK 0  // value-row gathers: 16-byte cp.async chunks (0) or one bulk copy per row (1)
+#endif
+#ifndef RSSM_APPEND_BULK
+#define RSSM_APPEND_BULK 0  // ring appends: 16-byte stores (0) or one bulk store per row (1)
+#endif
 #ifndef RSSM_COEF_WARPS
 #define RSSM_COEF_WARPS 2
 #endif
 constexpr int kNCoef = RSSM_COEF_WARPS;    // warps computing the per-head decay terms (alternate heads)
+static_assert((kNCoef & (kNCoef - 1)) == 0, "coefficient warps: a power of two");
 constexpr int kTileWarp = kNDW;            // warp that issues the bulk tile copies
 constexpr int kCoef0 = kNDW + 1;           // first coefficient warp
 constexpr int kGatherWarp = kNDW + 1 + kNCoef;  // warp that gathers the records, keys and queries
@@ -56,7 +63,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4 };
 enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2 };
-enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u };
+enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u, kErrPlan = 8u };
 
 struct Params {
   int B, H, P, N, G, L, R, Rp, HPG, T, min_count;
@@ -82,6 +89,7 @@ struct Params {
   //   values [R][P] of a fold, or the verify weights [kTMax][kRMax];
   //   two group areas of [k_j rows (R x N) | queries (kTMax x N)].
   int stages, stage_bytes, slots, slot_bytes, slot_off, sv_off, sc_off;
+  int dgroups;  // dot-warp groups (1, 2, 4 or 8): group d takes every dgroups-th head, so that many are in flight
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
 };
@@ -153,6 +161,17 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+
+// Bulk store shared -> global (the ring appends), tracked by the thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The shared-memory sources of this thread's bulk stores have been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Small asynchronous copies global -> shared (the record gathers).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -300,13 +319,32 @@ template <int K>
 struct TRed<K, 0> {
   static __device__ __forceinline__ void run(float*, int, int&) {}
 };
-
-template <int LPR>
-__device__ __forceinline__ float seg_max(float x) {
+// The same transposed scheme for a maximum.
+template <int K, int M>
+struct TMax {
+  static __device__ __forceinline__ void run(float* v, int lane, int& off) {
+    if constexpr (K > 1) {
+      constexpr int H2 = K / 2;
+      const bool up = (lane & M) != 0;
 #pragma unroll
-  for (int m = LPR / 2; m >= 1; m >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, m));
-  return x;
-}
+      for (int i = 0; i < H2; ++i) {
+        const float send = up ? v[i] : v[i + H2];
+        const float keep = up ? v[i + H2] : v[i];
+        v[i] = fmaxf(keep, __shfl_xor_sync(kFull, send, M));
+      }
+      if (up) off += H2;
+      TMax<H2, M / 2>::run(v, lane, off);
+    } else {
+      v[0] = fmaxf(v[0], __shfl_xor_sync(kFull, v[0], M));
+      TMax<1, M / 2>::run(v, lane, off);
+    }
+  }
+};
+template <int K>
+struct TMax<K, 0> {
+  static __device__ __forceinline__ void run(float*, int, int&) {}
+};
+
 template <int D>
 __device__ __forceinline__ float low_sum(float x) {
 #pragma unroll
@@ -355,43 +393,79 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
   return d;
 }
 
-// ------------------------------------------------------------ quantize a row slice
-// Lane holds 4 consecutive elements (x) of a row covered by LPR lanes.
-// Writes its codes, and the scales when it owns them, into the head's read copy.
-template <int RF, int LPR>
-__device__ __forceinline__ void quantize_store(const float4 x, bool live_row, int row, int col4, int N,
-                                               uint8_t* head_copy, int bsc_off, int rsc_off) {
-  float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-  a = seg_max<LPR>(a);  // row amax (all lanes of the row)
-  const bool live = a > 7.888609052210118e-31f;  // 2^-100
+// ------------------------------------------------------------ quantize a warp's rows
+// The warp holds KR rows; row kk is covered by LPR lanes with 4 consecutive
+// elements (x[kk]) each. Writes the rows' codes and scales into the head's read
+// copy. The row and block maxima use transposed reductions, so each scale is
+// computed once, by the lane that ends up holding its maximum, and broadcast.
+__device__ __forceinline__ float absmax4(const float4 x) {
+  return fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+}
+template <int RF, int LPR, int KR>
+__device__ __forceinline__ void quantize_rows(const float4 (&x)[KR], int lane, int row0, int row_step, int P, int N,
+                                              uint8_t* head_copy, int bsc_off, int rsc_off) {
+  static_assert(KR <= LPR && (LPR % KR) == 0 && KR >= 4, "row maxima need KR <= LPR");
+  constexpr int LPK = LPR / KR;  // lanes that end up holding one row's maximum
+  const int col4 = lane % LPR;
+  const int seg = lane - col4;   // first lane of this lane's row segment
+  // row k of the warp is row0 + k * row_step (rows at or beyond P hold zeros)
+  float a[KR];
+#pragma unroll
+  for (int kk = 0; kk < KR; ++kk) a[kk] = absmax4(x[kk]);
+  int off = 0;
+  TMax<KR, LPR / 2>::run(a, lane, off);  // lane: the maximum of row `off`
+  const float am = a[0];
+  const bool live = am > 7.888609052210118e-31f;  // 2^-100
+  const bool owner = (lane & (LPK - 1)) == 0;
+  const int orow = row0 + off * row_step;
   if constexpr (RF == kRfE4m3) {
-    const float inv = live ? __fdiv_rn(448.f, a) : 0.f;
-    const float s = live ? __fdiv_rn(a, 448.f) : 0.f;
-    const uint32_t c = enc_e4m3x4(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv), __fmul_rn(x.z, inv), __fmul_rn(x.w, inv));
-    if (live_row) {
-      *reinterpret_cast<uint32_t*>(head_copy + (size_t)row * N + col4 * 4) = c;
-      if (col4 == 0) *reinterpret_cast<float*>(head_copy + rsc_off + row * 4) = s;
+    const float inv_own = live ? __fdiv_rn(448.f, am) : 0.f;
+    if (owner && orow < P) *reinterpret_cast<float*>(head_copy + rsc_off + orow * 4) = live ? __fdiv_rn(am, 448.f) : 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KR; ++kk) {
+      const float inv = __shfl_sync(kFull, inv_own, seg + kk * LPK);
+      const uint32_t c = enc_e4m3x4(__fmul_rn(x[kk].x, inv), __fmul_rn(x[kk].y, inv), __fmul_rn(x[kk].z, inv),
+                                    __fmul_rn(x[kk].w, inv));
+      const int row = row0 + kk * row_step;
+      if (row < P) *reinterpret_cast<uint32_t*>(head_copy + (size_t)row * N + col4 * 4) = c;
     }
   } else {
-    const float s_r = live ? __fdiv_rn(a, 2688.f) : 0.f;
-    const float d6 = __fmul_rn(6.f, s_r);
-    float ab = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-    ab = fmaxf(ab, __shfl_xor_sync(kFull, ab, 1));
-    ab = fmaxf(ab, __shfl_xor_sync(kFull, ab, 2));  // 16-element block = 4 lanes
-    const float ratio = d6 > 0.f ? __fdiv_rn(ab, d6) : 0.f;
-    const uint32_t sb = enc_e4m3(ratio);
-    const float d = __fmul_rn(dec_e4m3(sb), s_r);
-    const float r = d > 0.f ? __fdiv_rn(1.f, d) : 0.f;
-    const uint32_t c = enc_e2m1x4(__fmul_rn(x.x, r), __fmul_rn(x.y, r), __fmul_rn(x.z, r), __fmul_rn(x.w, r));
-    if (live_row) {
-      *reinterpret_cast<uint16_t*>(head_copy + (size_t)row * (N / 2) + col4 * 2) = (uint16_t)c;
-      if ((col4 & 3) == 0) head_copy[bsc_off + row * (N / 16) + (col4 >> 2)] = (uint8_t)sb;
-      if (col4 == 0) *reinterpret_cast<float*>(head_copy + rsc_off + row * 4) = s_r;
+    const float sr_own = live ? __fdiv_rn(am, 2688.f) : 0.f;
+    if (owner && orow < P) *reinterpret_cast<float*>(head_copy + rsc_off + orow * 4) = sr_own;
+    float sr[KR];
+#pragma unroll
+    for (int kk = 0; kk < KR; ++kk) sr[kk] = __shfl_sync(kFull, sr_own, seg + kk * LPK);
+    // 16-element blocks are 4 lanes: transposed maximum over them
+    constexpr int VB = KR / 4;  // rows per lane after it
+    float bm[KR];
+#pragma unroll
+    for (int kk = 0; kk < KR; ++kk) bm[kk] = absmax4(x[kk]);
+    int boff = 0;
+    TMax<KR, 2>::run(bm, lane, boff);  // lane: block maxima of rows boff .. boff + VB - 1
+    float r[VB];
+#pragma unroll
+    for (int i = 0; i < VB; ++i) {
+      float s_r = sr[0];
+#pragma unroll
+      for (int kk = 1; kk < KR; ++kk) s_r = (kk == boff + i) ? sr[kk] : s_r;
+      const float d6 = __fmul_rn(6.f, s_r);
+      const float ratio = d6 > 0.f ? __fdiv_rn(bm[i], d6) : 0.f;
+      const uint32_t sb = enc_e4m3(ratio);
+      const float d = __fmul_rn(dec_e4m3(sb), s_r);
+      r[i] = d > 0.f ? __fdiv_rn(1.f, d) : 0.f;
+      const int row = row0 + (boff + i) * row_step;
+      if (row < P) head_copy[bsc_off + row * (N / 16) + (col4 >> 2)] = (uint8_t)sb;
+    }
+#pragma unroll
+    for (int kk = 0; kk < KR; ++kk) {
+      const float rk = __shfl_sync(kFull, r[kk % VB], (lane & ~3) + kk / VB);
+      const uint32_t c = enc_e2m1x4(__fmul_rn(x[kk].x, rk), __fmul_rn(x[kk].y, rk), __fmul_rn(x[kk].z, rk),
+                                    __fmul_rn(x[kk].w, rk));
+      const int row = row0 + kk * row_step;
+      if (row < P) *reinterpret_cast<uint16_t*>(head_copy + (size_t)row * (N / 2) + col4 * 2) = (uint16_t)c;
     }
   }
 }
-
-
 
 // ============================================================================
 // The head kernel.
@@ -439,18 +513,26 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   const long long h1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
   const int nq = (MODE == kVerify) ? p.T : 1;
 
+  // The parity waits need every ring to be a multiple of the consumers that take
+  // its entries in turn (see the host plan). Refuse any other plan.
+  if (p.dgroups < 1 || p.stages < p.dgroups || p.stages > kMaxStages || p.slots > kMaxSlots ||
+      p.stages % p.dgroups != 0 || p.slots % kNCoef != 0 || p.slots % p.dgroups != 0 || kNDW % p.dgroups != 0) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
+    return;
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(tfull0 + 8 * s, 1);
-      mbar_init(tempty0 + 8 * s, kNDW);
+      mbar_init(tempty0 + 8 * s, kNDW / p.dgroups);  // the warps of the head's dot group
     }
     for (int s = 0; s < p.slots; ++s) {
-      mbar_init(sfull0 + 8 * s, 32);
+      mbar_init(sfull0 + 8 * s, 1 + 32);  // lane 0's value-row bytes + 32 decay gathers
       mbar_init(scoef0 + 8 * s, 1);
-      mbar_init(sempty0 + 8 * s, kNDW + 1);
+      mbar_init(sempty0 + 8 * s, kNDW / p.dgroups + 1);  // the head's dot group + its coefficient warp
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(gfull0 + 8 * s, 32);
+      mbar_init(gfull0 + 8 * s, 1);  // lane 0's key and query bytes
       mbar_init(gempty0 + 8 * s, kNDW + kNCoef);
     }
     mbar_init(end_bar, kThreads);
@@ -545,7 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     long long cur_gg = -1;
     bool load = false, flush = false, bad = false;
     const int chp = p.P * ES / 16;  // 16-byte chunks per value row
-    const int vj0 = lane / chp, vch0 = lane % chp, vdj = 32 / chp, vdch = 32 % chp;
+    const int vcp = chp < 32 ? chp : 32;         // lanes per record in the value-row gather
+    const int vdj = 32 / vcp, vj0 = lane / vcp;  // records per pass, this lane's record offset
+    const int vch = lane - vj0 * vcp;            // this lane's first chunk
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
@@ -568,8 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if (!__all_sync(kFull, w)) { ok = false; break; }
           const uint32_t gdst = smem_u32(smem + p.gb_off + gs * p.gb_bytes);
           const size_t grow = (size_t)b * p.G + g;
-          for (int idx = lane; idx < J * CHN; idx += 32) {
-            const int j = idx / CHN, ch = idx % CHN;  // CHN is a power of two
+          if (lane == 0) mbar_arrive_tx(gfull0 + 8 * gs, (uint32_t)(J + (kQuery ? nq : 0)) * N * ES);
+          __syncwarp();
+          if (lane < J) {  // one bulk copy per key row (J <= 32)
+            const int j = lane;
             const uint8_t* src;
             if (MODE == kConv || (MODE == kDecode && j >= c))
               src = reinterpret_cast<const uint8_t*>(p.k) + grow * N * ES;
@@ -577,23 +663,25 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               src = reinterpret_cast<const uint8_t*>(p.ring_k) + (grow * p.R + ring_slot(st, j, p.R)) * N * ES;
             else  // verify draft j - c
               src = reinterpret_cast<const uint8_t*>(p.k) + (((size_t)b * p.T + (j - c)) * p.G + g) * N * ES;
-            cp_async16(gdst + j * N * ES + ch * 16, src + ch * 16);
+            tma_load_1d(gdst + j * N * ES, src, N * ES, gfull0 + 8 * gs);
           }
           if constexpr (kQuery) {
-            for (int idx = lane; idx < nq * CHN; idx += 32) {
-              const int t = idx / CHN, ch = idx % CHN;
+            if (lane < nq) {
+              const int t = lane;
               const size_t row = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
-              cp_async16(gdst + p.gq_off + t * N * ES + ch * 16,
-                         reinterpret_cast<const uint8_t*>(p.q) + row * N * ES + ch * 16);
+              tma_load_1d(gdst + p.gq_off + t * N * ES, reinterpret_cast<const uint8_t*>(p.q) + row * N * ES, N * ES,
+                          gfull0 + 8 * gs);
             }
           }
-          cp_async_arrive(gfull0 + 8 * gs);
           ++gi;
         }
       }
       const bool w = li < p.slots || mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err);
       if (!__all_sync(kFull, w)) { ok = false; break; }
       const uint32_t sdst = smem_u32(smem + p.slot_off + (size_t)rs * p.slot_bytes);
+      // lane j: the decay of record j; the value rows as 16-byte cp.async chunks spread
+      // over the lanes (RSSM_GATHER_BULK=1: one bulk copy per value row instead)
+      const uint8_t* vsrc = nullptr;
       if (lane < J) {
         const int j = lane;
         const float* asrc;
@@ -602,13 +690,24 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         else if (MODE == kVerify) asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
         else asrc = p.alpha + hrow;
         cp_async4(sdst + 4 * j, asrc);
+        vsrc = vrow_src(j, c, st, b, hh, hrow);
       }
-      for (int j = vj0, ch = vch0; j < J;) {
-        cp_async16(sdst + p.sv_off + j * p.P * ES + ch * 16, vrow_src(j, c, st, b, hh, hrow) + ch * 16);
-        j += vdj;
-        ch += vdch;
-        if (ch >= chp) { ch -= chp; ++j; }
+#if RSSM_GATHER_BULK
+      if (lane == 0) mbar_arrive_tx(sfull0 + 8 * rs, (uint32_t)J * p.P * ES);
+      __syncwarp();
+      if (lane < J) tma_load_1d(sdst + p.sv_off + lane * p.P * ES, vsrc, p.P * ES, sfull0 + 8 * rs);
+#else
+      if (lane == 0) mbar_arrive(sfull0 + 8 * rs);
+      for (int j = 0; j < J; j += vdj) {  // vdj records per pass, vcp lanes per record
+        const int jr = j + vj0;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, reinterpret_cast<uintptr_t>(vsrc),
+                                                                          min(jr, 31)));
+        if (jr < J) {
+          for (int ch = vch; ch < chp; ch += vcp)
+            cp_async16(sdst + p.sv_off + jr * p.P * ES + ch * 16, src + ch * 16);
+        }
       }
+#endif
       cp_async_arrive(sfull0 + 8 * rs);
       slot_next();
       ++li;
@@ -639,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         if (gg != cur_gg) {
           cur_gg = gg;
           if (gi > 0) {
+            bulk_wait_read();  // key appends from the previous group area have read it
             __syncwarp();
             if (lane == 0) mbar_arrive(gempty0 + 8 * ((gi - 1) & 1));
           }
@@ -671,14 +771,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if constexpr (kAppendMode) {  // the group's first head (if this CTA owns it) appends the new keys
             const long long gfirst = (long long)b * p.H + (long long)g * p.HPG;
             const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
-            if (cwi == 0 && gfirst >= h0 && na > 0) {
+            if (cwi == 0 && gfirst >= h0 && lane < na) {  // lane t: one bulk store per new key row
               const size_t grow = (size_t)b * p.G + g;
-              for (int idx = lane; idx < na * CHN; idx += 32) {
-                const int t = idx / CHN, ch = idx % CHN;
-                const uint4 val = *reinterpret_cast<const uint4*>(gK + (c + t) * N * ES + ch * 16);
-                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.ring_k) +
-                                          (grow * p.R + ring_slot(st, c + t, p.R)) * N * ES + ch * 16) = val;
-              }
+              const int t = lane;
+              bulk_store(reinterpret_cast<uint8_t*>(p.ring_k) + (grow * p.R + ring_slot(st, c + t, p.R)) * N * ES,
+                         smem_u32(gK + (c + t) * N * ES), N * ES);
+              bulk_commit();
             }
           }
           ++gi;
@@ -745,20 +843,32 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(scoef0 + 8 * rs);  // coefficients published
-      if constexpr (kAppendMode) {                   // the new decays and value rows go to the ring
+      if constexpr (kAppendMode) {  // the new decays and value rows go to the ring
         const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
+#if RSSM_APPEND_BULK
+        if (lane < na) {  // lane t: one bulk store per value row
+          const int slot_t = ring_slot(st, c + lane, p.R);
+          p.ring_a[hrow * p.Rp + slot_t] = sa[c + lane];
+          bulk_store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + slot_t) * p.P * ES,
+                     smem_u32(sv + (c + lane) * p.P * ES), p.P * ES);
+          bulk_commit();
+          bulk_wait_read();  // the slot may be refilled once its rows have been read
+        }
+#else
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[c + lane];
         const int chp = p.P * ES / 16;
-        for (int t = 0; t < na; ++t) {
+        for (int t = 0; t < na; ++t) {  // 16-byte stores spread over the lanes
           uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
           for (int ch = lane; ch < chp; ch += 32)
             *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
         }
+#endif
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty0 + 8 * rs);  // this warp is done with the slot
       slot_next();
     }
+    bulk_wait_all();  // every append has reached global memory before the warp leaves
   } else {
     // ====================================================================== dot warps
     const int col4 = lane % LPR, rsub = lane / LPR;
@@ -773,8 +883,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     constexpr int RPIc = 32 / LPRc;
     constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
     float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
-    const int rows_pass = kNDW * kKR * RPI;
+    const int wpg = kNDW / p.dgroups;                 // warps per dot group
+    const int dgrp = warp / wpg, wr = warp - dgrp * wpg;  // this warp's group and rank in it
+    const int rows_pass = wpg * kKR * RPI;
     const int npass = (p.P + rows_pass - 1) / rows_pass;
+    int lh = 0;  // loaded heads seen
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
@@ -807,6 +920,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
+      if ((lh++ % p.dgroups) != dgrp) {  // another dot group takes this head
+        tile_next();
+        slot_next();
+        continue;
+      }
       // the coefficient warp arrives only after the record gathers landed, so
       // its barrier also covers alpha_j and v_j
       const bool got = mbar_wait(tfull0 + 8 * ts, tph, abort_flag, p.err) &&
@@ -822,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       if constexpr (MODE == kVerify) {
         // ================================================ verify (T queries)
         for (int pass = 0; pass < npass; ++pass) {
-          const int rbase = (pass * kNDW + warp) * kKR;
+          const int rbase = (pass * wpg + wr) * kKR;
           for (int t0 = 0; t0 < p.T; t0 += kTQ) {
             float4 qv[kTQ];
 #pragma unroll
@@ -862,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const float gam = sc[0];
         const float* su = sc + kCoefOff;  // [J][P]
         for (int pass = 0; pass < npass; ++pass) {
-          const int rbase = (pass * kNDW + warp) * kKR;
+          const int rbase = (pass * wpg + wr) * kKR;
           if (rbase * RPI >= p.P) break;  // warp-uniform: no rows left for this warp
           float4 acc[kKR];
           if constexpr (RPI == 1) {
@@ -930,18 +1048,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               }
             }
           }
+          if constexpr (MODE != kQuant) {
 #pragma unroll
-          for (int kk = 0; kk < kKR; ++kk) {
-            const int row = (rbase + kk) * RPI + rsub;
-            const bool live_row = row < p.P;
-            if constexpr (MODE != kQuant) {
-              if (live_row) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
+            for (int kk = 0; kk < kKR; ++kk) {
+              const int row = (rbase + kk) * RPI + rsub;
+              if (row < p.P) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
             }
-            if constexpr (RF != kRfNone && MODE != kConv) {
-              // rows beyond P still join the shuffles, with zeros
-              quantize_store<RF, LPR>(acc[kk], live_row, row, col4, N, p.copy + hrow * p.head_stride, p.bsc_off,
-                                      p.rsc_off);
-            }
+          }
+          if constexpr (RF != kRfNone && MODE != kConv) {
+            quantize_rows<RF, LPR, kKR>(acc, lane, rbase * RPI + rsub, RPI, p.P, N, p.copy + hrow * p.head_stride,
+                                        p.bsc_off, p.rsc_off);
           }
           if constexpr (MODE == kDecode || MODE == kConv) {
             float part[kKR];
@@ -964,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const float* sov = sc + kCoefOff;  // [P]
         for (int pass = 0; pass < npass; ++pass) {
           if constexpr (RF == kRfNone) {
-            const int rbase = (pass * kNDW + warp) * kKR;
+            const int rbase = (pass * wpg + wr) * kKR;
             float part[kKR];
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
@@ -982,7 +1098,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             }
           } else {
             // read copy: lanes own CPL consecutive codes of a row
-            const int rows0 = (pass * kNDW + warp) * kKR * RPI;  // first row of this warp
+            const int rows0 = (pass * wpg + wr) * kKR * RPI;  // first row of this warp
             const int colc = lane % LPRc, rsc = lane / LPRc;
             const float* rscale = reinterpret_cast<const float*>(tile + p.rsc_off);
             float part[KRc];

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "RSSM_OK", 1: "RSSM_EINVAL", 2: "RSSM_ECAPACITY", 3: "RSSM_EC
                 5: "RSSM_ETIMEOUT"}
 DTYPES = {"f32": 0, "bf16": 1}
 READ_FMTS = {None: 0, "none": 0, "e4m3": 1, "e2m1": 2}
-ERR_CAPACITY, ERR_ACCEPT, ERR_TIMEOUT = 1, 2, 4
+ERR_CAPACITY, ERR_ACCEPT, ERR_TIMEOUT, ERR_PLAN = 1, 2, 4, 8
 
 # The C ABI functions, with their argument types.
 _c_size_p = ctypes.POINTER(ctypes.c_size_t)

@@ -162,8 +162,10 @@ rssm_status rssm_commit(rssm_handle h, const int32_t* accepted, void* stream);
 rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream);
 
 /* Copy start[B], count[B] (int32) and the error word to host memory,
- * synchronizing the stream first. Any output may be NULL. Returns RSSM_OK,
- * RSSM_ECAPACITY (bits 1|2 set) or RSSM_ETIMEOUT (bit 4 set). */
+ * synchronizing the stream first. Any output may be NULL. Error word bits:
+ * 1 ring overflow, 2 bad accepted length, 4 a bounded wait expired, 8 a kernel
+ * refused its launch plan. Returns RSSM_OK, RSSM_EUNSUPPORTED (bit 8),
+ * RSSM_ETIMEOUT (bit 4) or RSSM_ECAPACITY (bits 1|2). */
 rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* count_host,
                                uint32_t* err_host, void* stream);
 
