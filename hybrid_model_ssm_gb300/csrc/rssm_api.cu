@@ -99,22 +99,23 @@ struct Plan {
 };
 
 // Tile stages, record slots and shared-memory carve for one launch (see Params in rssm_device.cuh).
-rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
+// Shared-memory plan of a head-kernel launch: the group areas, scratch and
+// barriers at the top of the CTA's shared memory, and below them two layouts of
+// tile stages and record slots (see rssm::Params). lay[0] fits every head.
+// lay[1], offered to decode steps, holds only non-flush heads: its stages hold
+// the tile that non-flush steps read (the read copy when there is one) and its
+// slots at most L - 1 records and no fold coefficients, so more heads fit.
+rssm_status plan_layout(const rssm_config* c, const Geom& g, bool nf, size_t budget, rssm::Layout* L) {
   using namespace rssm;
   auto a128 = [](size_t x) { return align_up(x, 128); };
   const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
-  const size_t tile = a128(P * N * 4);  // a read copy (head_stride bytes) is smaller
-  const size_t sv_off = (size_t)kRMax * 4;
-  const size_t sc_off = align_up(sv_off + R * P * es, 16);
-  const size_t sc_floats = 16 + std::max({P, R * P, (size_t)kTMax * kRMax});
+  const size_t tile = a128(nf && g.head_stride ? g.head_stride : P * N * 4);
+  const size_t vrows = nf ? (size_t)c->L : R;
+  const size_t sv_off = (size_t)(kRMax + kTMax) * 4;  // decays: kRMax ring slots, then kTMax new records
+  const size_t sc_off = align_up(sv_off + vrows * P * es, 16);
+  const size_t sc_floats = nf ? 16 + P : 16 + std::max({P, R * P, (size_t)kTMax * kRMax});
   const size_t slot = a128(sc_off + sc_floats * 4);
-  const size_t gq_off = R * N * es;
-  const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
-  const size_t wsc = a128((size_t)kNCoef * kTMax * kRMax * 4);
-  const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6) * 8);
-  const size_t fixed = 2 * gb + wsc + bars;
-  if (fixed + 2 * tile + 2 * slot > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
-  const size_t budget = kSmemMax - fixed;
+  if (2 * tile + 2 * slot > budget) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
   const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, budget / (tile + 3 * slot)));
   const int slots = (int)std::max<size_t>(2, std::min<size_t>(kMaxSlots, (budget - stages * tile) / slot));
   // Dot groups: as many heads in flight as keeps two tile stages per group.
@@ -132,23 +133,43 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl) {
   const int slot_mult = std::max(kNCoef, dgroups);  // both are powers of two
   const int slots_used = slots - slots % slot_mult;
   if (stages_used < 2 || slots_used < slot_mult) return fail(RSSM_EUNSUPPORTED, "shared memory too small for the rings");
+  L->dgroups = dgroups;
+  L->stages = stages_used;
+  L->stage_bytes = (int)tile;
+  L->slots = slots_used;
+  L->slot_bytes = (int)slot;
+  L->slot_off = (int)((size_t)stages_used * tile);
+  L->sv_off = (int)sv_off;
+  L->sc_off = (int)sc_off;
+  if ((size_t)L->slot_off + (size_t)slots_used * slot > budget) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
+  return RSSM_OK;
+}
+
+rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, bool decode = false) {
+  using namespace rssm;
+  auto a128 = [](size_t x) { return align_up(x, 128); };
+  const size_t N = c->N, es = (size_t)g.esize, R = g.R;
+  const size_t gq_off = R * N * es;
+  const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
+  const size_t wsc = a128((size_t)kNCoef * kTMax * kRMax * 4);
+  const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6) * 8);
+  const size_t fixed = 2 * gb + wsc + bars;
+  if (fixed >= (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "group areas too large for shared memory");
+  const size_t budget = ((size_t)kSmemMax - fixed) / 128 * 128;
   rssm::Params& p = pl->p;
-  p.dgroups = dgroups;
-  p.stages = stages_used;
-  p.stage_bytes = (int)tile;
-  p.slots = slots_used;
-  p.slot_bytes = (int)slot;
-  p.sv_off = (int)sv_off;
-  p.sc_off = (int)sc_off;
-  size_t off = (size_t)stages_used * tile;
-  p.slot_off = (int)off; off += (size_t)slots_used * slot;
+  rssm_status s = plan_layout(c, g, false, budget, &p.lay[0]);
+  if (s != RSSM_OK) return s;
+  p.lay[1] = p.lay[0];
+  p.nf_ok = 0;
+  if (decode && c->L >= 2 && plan_layout(c, g, true, budget, &p.lay[1]) == RSSM_OK) p.nf_ok = 1;
+  size_t off = budget;
   p.gb_off = (int)off; off += 2 * gb;
   p.gb_bytes = (int)gb;
   p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
   p.bar_off = (int)off; off += bars;
   if (off > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
-  pl->stages = stages_used;
+  pl->stages = p.lay[0].stages;
   pl->smem = off;
   return RSSM_OK;
 }
@@ -294,7 +315,7 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
   Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, true);
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
@@ -467,7 +488,7 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
     tickets = g_static_ticket_addr[dev];
   }
   Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, true);
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.ticket = tickets;

@@ -37,7 +37,9 @@ namespace rssm {
 #endif
 constexpr int kNDW = RSSM_DOT_WARPS;       // dot warps per CTA (stream the checkpoint tile)
 #ifndef RSSM_GATHER_BULK
-#define RSSM_GATHER_BULK 0  // value-row gathers: 16-byte cp.async chunks (0) or one bulk copy per row (1)
+// record gathers: 16-byte cp.async chunks (0), one bulk copy per value row (1),
+// or bulk copies of the ring's contiguous runs (2)
+#define RSSM_GATHER_BULK 2
 #endif
 #ifndef RSSM_APPEND_BULK
 #define RSSM_APPEND_BULK 0  // ring appends: 16-byte stores (0) or one bulk store per row (1)
@@ -51,19 +53,25 @@ constexpr int kTileWarp = kNDW;            // warp that issues the bulk tile cop
 constexpr int kCoef0 = kNDW + 1;           // first coefficient warp
 constexpr int kGatherWarp = kNDW + 1 + kNCoef;  // warp that gathers the records, keys and queries
 constexpr int kThreads = (kNDW + 2 + kNCoef) * 32;
-constexpr int kMaxSlots = 16;              // largest record-slot ring
+constexpr int kMaxSlots = 32;              // largest record-slot ring
 constexpr int kKR = RSSM_ROWS_PER_WARP;    // FP32-tile row-instructions per warp per pass (multiple of 4)
 static_assert(kKR % 4 == 0, "rows per warp must be a multiple of 4");
 constexpr int kTQ = 4;                     // verify queries per pass over the tile
 constexpr int kTMax = 8;                   // largest draft count
 constexpr int kRMax = 32;                  // largest ring (records per head)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr unsigned kFull = 0xffffffffu;
 
 enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4 };
 enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2 };
 enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u, kErrPlan = 8u };
+
+// One partition of a CTA's shared memory into tile stages and record slots.
+struct Layout {
+  int stages, stage_bytes, slots, slot_bytes, slot_off, sv_off, sc_off;
+  int dgroups;  // dot-warp groups (1, 2, 4 or 8): group d takes every dgroups-th head, so that many are in flight
+};
 
 struct Params {
   int B, H, P, N, G, L, R, Rp, HPG, T, min_count;
@@ -82,14 +90,18 @@ struct Params {
   const void* k;       // decode/conv [B,G,N]; verify [B,T,G,N]
   const void* q;       // decode/conv [B,G,N]; verify [B,T,G,N]
   float* o;            // decode/conv [B,H,P]; verify [B,T,H,P]
-  // Shared memory (bytes).
+  // Shared memory (bytes). From offset 0, one of two layouts:
   //   `stages` tile stages: the head tile (P x N fp32, or the read copy);
-  //   `slots` record slots: [alpha_j (kRMax fp32) | v_j rows (R x P) | coefficients],
+  //   `slots` record slots: [alpha_j (kRMax fp32) | v_j rows | coefficients],
   //   coefficients: g (or g_t) at 0..15, then the value term [P], the scaled
-  //   values [R][P] of a fold, or the verify weights [kTMax][kRMax];
-  //   two group areas of [k_j rows (R x N) | queries (kTMax x N)].
-  int stages, stage_bytes, slots, slot_bytes, slot_off, sv_off, sc_off;
-  int dgroups;  // dot-warp groups (1, 2, 4 or 8): group d takes every dgroups-th head, so that many are in flight
+  //   values [R][P] of a fold, or the verify weights [kTMax][kRMax].
+  // lay[0] fits every head; lay[1] (decode) only non-flush heads: tiles of the
+  // read copy, at most L - 1 records and no fold, so more heads are in flight.
+  // A CTA takes lay[1] when none of its sequences flushes in this launch.
+  // Behind both: two group areas of [k_j rows (R x N) | queries (kTMax x N)],
+  // the coefficient-warp scratch and the barriers.
+  Layout lay[2];
+  int nf_ok;  // lay[1] is valid
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
 };
@@ -513,23 +525,49 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   const long long h1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
   const int nq = (MODE == kVerify) ? p.T : 1;
 
+  // Layout: the non-flush one unless one of this CTA's sequences flushes now.
+  // Every thread decides alike from the same counts, which no CTA changes
+  // before all CTAs of the sequence are done with them.
+  bool lean = false;
+  if constexpr (MODE == kDecode) {
+    if (p.nf_ok && h1 > h0) {
+      bool need = false;
+      const int b_last = (int)((h1 - 1) / p.H);
+      for (int b = (int)(h0 / p.H) + lane; b <= b_last; b += 32) {
+        const int c = p.count[b];
+        need |= (c >= 0 && c + 1 <= p.R && c + 1 >= p.L);
+      }
+      lean = !__any_sync(kFull, need);
+    }
+  }
+  Layout lay;  // field by field, so that no copy goes through local memory
+  lay.stages = lean ? p.lay[1].stages : p.lay[0].stages;
+  lay.stage_bytes = lean ? p.lay[1].stage_bytes : p.lay[0].stage_bytes;
+  lay.slots = lean ? p.lay[1].slots : p.lay[0].slots;
+  lay.slot_bytes = lean ? p.lay[1].slot_bytes : p.lay[0].slot_bytes;
+  lay.slot_off = lean ? p.lay[1].slot_off : p.lay[0].slot_off;
+  lay.sv_off = lean ? p.lay[1].sv_off : p.lay[0].sv_off;
+  lay.sc_off = lean ? p.lay[1].sc_off : p.lay[0].sc_off;
+  lay.dgroups = lean ? p.lay[1].dgroups : p.lay[0].dgroups;
+
   // The parity waits need every ring to be a multiple of the consumers that take
   // its entries in turn (see the host plan). Refuse any other plan.
-  if (p.dgroups < 1 || p.stages < p.dgroups || p.stages > kMaxStages || p.slots > kMaxSlots ||
-      p.stages % p.dgroups != 0 || p.slots % kNCoef != 0 || p.slots % p.dgroups != 0 || kNDW % p.dgroups != 0) {
+  if (lay.dgroups < 1 || lay.stages < lay.dgroups || lay.stages > kMaxStages || lay.slots > kMaxSlots ||
+      lay.stages % lay.dgroups != 0 || lay.slots % kNCoef != 0 || lay.slots % lay.dgroups != 0 ||
+      kNDW % lay.dgroups != 0) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
     return;
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
+    for (int s = 0; s < lay.stages; ++s) {
       mbar_init(tfull0 + 8 * s, 1);
-      mbar_init(tempty0 + 8 * s, kNDW / p.dgroups);  // the warps of the head's dot group
+      mbar_init(tempty0 + 8 * s, kNDW / lay.dgroups);  // the warps of the head's dot group
     }
-    for (int s = 0; s < p.slots; ++s) {
+    for (int s = 0; s < lay.slots; ++s) {
       mbar_init(sfull0 + 8 * s, 1 + 32);  // lane 0's value-row bytes + 32 decay gathers
       mbar_init(scoef0 + 8 * s, 1);
-      mbar_init(sempty0 + 8 * s, kNDW / p.dgroups + 1);  // the head's dot group + its coefficient warp
+      mbar_init(sempty0 + 8 * s, kNDW / lay.dgroups + 1);  // the head's dot group + its coefficient warp
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(gfull0 + 8 * s, 1);  // lane 0's key and query bytes
@@ -582,10 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   // Ring positions (index, phase parity) of the tile stages and record slots.
   int ts = 0, tph = 0, rs = 0, rph = 0;
   auto tile_next = [&]() {
-    if (++ts == p.stages) { ts = 0; tph ^= 1; }
+    if (++ts == lay.stages) { ts = 0; tph ^= 1; }
   };
   auto slot_next = [&]() {
-    if (++rs == p.slots) { rs = 0; rph ^= 1; }
+    if (++rs == lay.slots) { rs = 0; rph ^= 1; }
   };
 
   bool ok = true;
@@ -603,21 +641,21 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           seq_plan(b, c, st, load, flush, bad);
         }
         if (!load) continue;
-        if (li >= p.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        if (li >= lay.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
         const void* src = from_copy ? (const void*)(p.copy + (size_t)gh * p.head_stride)
                                     : (const void*)(p.ckpt + (size_t)gh * p.P * N);
         const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)p.P * N * 4;
         mbar_arrive_tx(tfull0 + 8 * ts, bytes);
-        tma_load_1d(smem_u32(smem + (size_t)ts * p.stage_bytes), src, bytes, tfull0 + 8 * ts);
+        tma_load_1d(smem_u32(smem + (size_t)ts * lay.stage_bytes), src, bytes, tfull0 + 8 * ts);
         tile_next();
         ++li;
       }
       if (!ok) {  // drain the bulk copies still in flight (bounded), then leave
         volatile int dummy = 0;
-        for (int k = 0; k < p.stages && k < li; ++k) {
+        for (int k = 0; k < lay.stages && k < li; ++k) {
           const int i = li - 1 - k;
-          mbar_wait(tfull0 + 8 * (i % p.stages), (i / p.stages) & 1, &dummy, p.err);
+          mbar_wait(tfull0 + 8 * (i % lay.stages), (i / lay.stages) & 1, &dummy, p.err);
         }
       }
     }
@@ -676,9 +714,36 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      const bool w = li < p.slots || mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err);
+      const bool w = li < lay.slots || mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err);
       if (!__all_sync(kFull, w)) { ok = false; break; }
-      const uint32_t sdst = smem_u32(smem + p.slot_off + (size_t)rs * p.slot_bytes);
+      const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
+      // Slot: decays at [ring slot] for committed records and at kRMax + (j - c)
+      // for new ones; value rows in record order from sv_off.
+      const int nnew = J - c;  // records that come from the call's inputs
+#if RSSM_GATHER_BULK == 2
+      // Committed records sit in the ring at slots st .. st + c - 1 (mod R): their
+      // value rows are at most two contiguous runs and their decays one row of Rp.
+      // Lane 0 issues those bulk copies; lane t < nnew one for new record t.
+      if (lane == 0) {
+        const uint32_t rbytes = (uint32_t)p.P * ES;
+        mbar_arrive_tx(sfull0 + 8 * rs, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
+        if (c > 0) {
+          tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sfull0 + 8 * rs);
+          const int n1 = min(c, p.R - st);
+          const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * rbytes;
+          tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * rbytes, (uint32_t)n1 * rbytes, sfull0 + 8 * rs);
+          if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * rbytes, rv, (uint32_t)(c - n1) * rbytes, sfull0 + 8 * rs);
+        }
+      }
+      __syncwarp();
+      if (lane < nnew) {
+        const int t = lane;
+        const size_t nrow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.H + hh : hrow;
+        cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
+        tma_load_1d(sdst + lay.sv_off + (c + t) * p.P * ES, reinterpret_cast<const uint8_t*>(p.v) + nrow * p.P * ES,
+                    (uint32_t)p.P * ES, sfull0 + 8 * rs);
+      }
+#else
       // lane j: the decay of record j; the value rows as 16-byte cp.async chunks spread
       // over the lanes (RSSM_GATHER_BULK=1: one bulk copy per value row instead)
       const uint8_t* vsrc = nullptr;
@@ -689,13 +754,13 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         else if (j < c) asrc = p.ring_a + hrow * p.Rp + ring_slot(st, j, p.R);
         else if (MODE == kVerify) asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
         else asrc = p.alpha + hrow;
-        cp_async4(sdst + 4 * j, asrc);
+        cp_async4(sdst + 4 * (j < c ? ring_slot(st, j, p.R) : kRMax + j - c), asrc);
         vsrc = vrow_src(j, c, st, b, hh, hrow);
       }
 #if RSSM_GATHER_BULK
       if (lane == 0) mbar_arrive_tx(sfull0 + 8 * rs, (uint32_t)J * p.P * ES);
       __syncwarp();
-      if (lane < J) tma_load_1d(sdst + p.sv_off + lane * p.P * ES, vsrc, p.P * ES, sfull0 + 8 * rs);
+      if (lane < J) tma_load_1d(sdst + lay.sv_off + lane * p.P * ES, vsrc, p.P * ES, sfull0 + 8 * rs);
 #else
       if (lane == 0) mbar_arrive(sfull0 + 8 * rs);
       for (int j = 0; j < J; j += vdj) {  // vdj records per pass, vcp lanes per record
@@ -704,9 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                                                                           min(jr, 31)));
         if (jr < J) {
           for (int ch = vch; ch < chp; ch += vcp)
-            cp_async16(sdst + p.sv_off + jr * p.P * ES + ch * 16, src + ch * 16);
+            cp_async16(sdst + lay.sv_off + jr * p.P * ES + ch * 16, src + ch * 16);
         }
       }
+#endif
 #endif
       cp_async_arrive(sfull0 + 8 * rs);
       slot_next();
@@ -787,11 +853,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         continue;
       }
       if (!__all_sync(kFull, mbar_wait(sfull0 + 8 * rs, rph, abort_flag, p.err))) { ok = false; break; }
-      uint8_t* slot = smem + p.slot_off + (size_t)rs * p.slot_bytes;
-      const float* sa = reinterpret_cast<const float*>(slot);  // alpha_j, record order
-      const uint8_t* sv = slot + p.sv_off;                      // v_j rows, record order
-      float* sc = reinterpret_cast<float*>(slot + p.sc_off);    // coefficients
-      const float aj = (lane < J) ? sa[lane] : 1.f;             // lane j holds alpha of record j
+      uint8_t* slot = smem + lay.slot_off + (size_t)rs * lay.slot_bytes;
+      const float* sa = reinterpret_cast<const float*>(slot);  // decays: [ring slot] committed, [kRMax + t] new
+      const uint8_t* sv = slot + lay.sv_off;                      // v_j rows, record order
+      float* sc = reinterpret_cast<float*>(slot + lay.sc_off);    // coefficients
+      // lane j holds alpha of record j
+      const float aj = (lane < c) ? sa[ring_slot(st, lane, p.R)] : (lane < J) ? sa[kRMax + lane - c] : 1.f;
       if constexpr (MODE == kVerify) {
         for (int t = 0; t < p.T; ++t) {
           const int ht = c + t + 1;
@@ -848,14 +915,14 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #if RSSM_APPEND_BULK
         if (lane < na) {  // lane t: one bulk store per value row
           const int slot_t = ring_slot(st, c + lane, p.R);
-          p.ring_a[hrow * p.Rp + slot_t] = sa[c + lane];
+          p.ring_a[hrow * p.Rp + slot_t] = sa[kRMax + lane];
           bulk_store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + slot_t) * p.P * ES,
                      smem_u32(sv + (c + lane) * p.P * ES), p.P * ES);
           bulk_commit();
           bulk_wait_read();  // the slot may be refilled once its rows have been read
         }
 #else
-        if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[c + lane];
+        if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[kRMax + lane];
         const int chp = p.P * ES / 16;
         for (int t = 0; t < na; ++t) {  // 16-byte stores spread over the lanes
           uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
@@ -883,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     constexpr int RPIc = 32 / LPRc;
     constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
     float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
-    const int wpg = kNDW / p.dgroups;                 // warps per dot group
+    const int wpg = kNDW / lay.dgroups;                 // warps per dot group
     const int dgrp = warp / wpg, wr = warp - dgrp * wpg;  // this warp's group and rank in it
     const int rows_pass = wpg * kKR * RPI;
     const int npass = (p.P + rows_pass - 1) / rows_pass;
@@ -920,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      if ((lh++ % p.dgroups) != dgrp) {  // another dot group takes this head
+      if ((lh++ % lay.dgroups) != dgrp) {  // another dot group takes this head
         tile_next();
         slot_next();
         continue;
@@ -931,11 +998,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                        mbar_wait(scoef0 + 8 * rs, rph, abort_flag, p.err) &&
                        (MODE != kVerify || mbar_wait(sfull0 + 8 * rs, rph, abort_flag, p.err));
       if (!__all_sync(kFull, got)) { ok = false; break; }
-      const uint8_t* tile = smem + (size_t)ts * p.stage_bytes;
+      const uint8_t* tile = smem + (size_t)ts * lay.stage_bytes;
       const float* tf = reinterpret_cast<const float*>(tile);
-      const uint8_t* slot = smem + p.slot_off + (size_t)rs * p.slot_bytes;
-      const uint8_t* sv = slot + p.sv_off;
-      const float* sc = reinterpret_cast<const float*>(slot + p.sc_off);
+      const uint8_t* slot = smem + lay.slot_off + (size_t)rs * lay.slot_bytes;
+      const uint8_t* sv = slot + lay.sv_off;
+      const float* sc = reinterpret_cast<const float*>(slot + lay.sc_off);
 
       if constexpr (MODE == kVerify) {
         // ================================================ verify (T queries)

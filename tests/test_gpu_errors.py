@@ -127,3 +127,4 @@ def test_bounded_wait_expires_and_reports():
     a, v, k, q = (dev(x) for x in synth.decode_step_inputs(shape, gen))
     model.decode_step(a, v, k, q)
     assert model.read_pointers()[2] == 0
+

@@ -118,3 +118,37 @@ def test_save_and_resume_gives_identical_outputs():
     second = [model.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu() for a, v, k, q in steps[7:]]
     for x, y in zip(first, second):
         assert torch.equal(x, y)
+
+
+def test_mixed_calls_without_pointer_reads():
+    """Decode steps, verify rounds, commits and flushes in a seeded random order,
+    with no pointer read in between, so the launch plans rest on the host's
+    count bounds alone. Outputs follow the oracle at every call; the pointers
+    and the error word are checked once at the end."""
+    require_gpu()
+    shape = S(B=6, H=4, P=32, N=64, G=2, L=5, T_max=3, seed=34)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    orc = oracle.ReplayOracle(f64(S0), L=shape.L, R=shape.R, G=shape.G)
+    model = ReplaySSM(layer_shape(shape), dev(S0))
+    ops = np.random.default_rng(7).integers(0, 3, size=60)
+    for i, op in enumerate(ops):
+        if op < 2:  # decode
+            a, v, k, q = synth.decode_step_inputs(shape, gen)
+            o = model.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu()
+            o_ref, _ = orc.decode(f64(a), f64(v), f64(k), f64(q))
+            assert slice_rel_err(o, o_ref, 1) <= REL_TOL, f"call {i}: decode"
+        else:  # verify, commit, flush at L
+            T = 1 + i % shape.T_max
+            a, v, k, q = synth.verify_round_inputs(shape, T, gen)
+            O = model.verify(dev(a), dev(v), dev(k), dev(q)).cpu()
+            assert slice_rel_err(O, orc.verify(f64(a), f64(v), f64(k), f64(q)), 1) <= REL_TOL, f"call {i}: verify"
+            acc = synth.accepted_lengths(shape.B, T, gen)
+            model.commit(dev(acc))
+            orc.commit(acc.numpy())
+            model.flush(shape.L)
+            orc.flush(shape.L)
+    start, count, err = model.read_pointers()
+    assert err == 0
+    assert np.array_equal(start.numpy(), orc.start) and np.array_equal(count.numpy(), orc.count)
+    assert slice_rel_err(model.ckpt.cpu(), orc.ckpt, 2) <= REL_TOL
