@@ -542,6 +542,119 @@ def run_verify(args, world, rank, local):
     }
 
 
+MULTI_SHAPES = {"mamba2": synth.PRESETS["mamba2_layer_b256_l16"], "alt": synth.PRESETS["alt_h32_p128_n128_g16"]}
+
+
+def run_multilayer(args, world, rank, local):
+    """A stack of SSM layers: every decode step runs all layers in turn.
+
+    Sweeps batch and window. Per point: the time of one decode step over all
+    layers (CUDA events; launched one by one, and replayed from a CUDA graph
+    captured over one step of all layers), the algorithmic HBM bytes of that
+    step (window average) and the bandwidth they imply. The per-CTA layout
+    choice is made on the device, so a captured step stays valid at every
+    window position and the graph is captured once.
+    """
+    from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM, workspace_size
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    base = MULTI_SHAPES[args.shape]
+    batches = [int(x) for x in args.batches.split(",")]
+    windows = [int(x) for x in args.windows.split(",")]
+    n_layers = args.layers
+    peak, peak_kind = measured_peak_gbs()
+    points = []
+    total_launches = 0
+    with ClockSampler(local) as clk:
+        for L in windows:
+            for B in batches:
+                s = base.with_(B=B, L=L)
+                ls = LayerShape(B=B, H=s.H, P=s.P, N=s.N, G=s.G, L=L, T_max=1, in_dtype=s.in_dtype)
+                ring_b, ptr_b, _ = workspace_size(ls)
+                state_b = B * s.H * s.P * s.N * 4
+                need = n_layers * (state_b + ring_b + ptr_b + 4 * B * s.H * s.P)
+                free, _ = torch.cuda.mem_get_info()
+                if need > 0.85 * free:
+                    points.append({"B": B, "L": L, "skipped": f"needs {need / 2**30:.1f} GiB, {free / 2**30:.1f} free"})
+                    continue
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(s.seed + 1000 * rank + 17 * L + B)
+                models = [ReplaySSM(ls, torch.randn((B, s.H, s.P, s.N), generator=gen, device=dev) * 0.1)
+                          for _ in range(n_layers)]
+                sc = 1.0 / math.sqrt(s.N)
+                pool = []
+                for _ in range(4):
+                    u = torch.randn((B, s.H), generator=gen, device=dev)
+                    pool.append((torch.exp(-torch.nn.functional.softplus(u)).float(),
+                                 (torch.randn((B, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
+                                 (torch.randn((B, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
+                                 (torch.randn((B, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)))
+                outs = [torch.empty((B, s.H, s.P), dtype=torch.float32, device=dev) for _ in range(n_layers)]
+
+                def step(i):
+                    a, v, k, q = pool[i % len(pool)]
+                    for m, o in zip(models, outs):
+                        m.decode_step(a, v, k, q, out=o)
+
+                for i in range(max(L, args.warmup)):  # every layer has flushed once
+                    step(i)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for i in range(args.steps):
+                    step(i)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                t_eager = e0.elapsed_time(e1) / 1e3 / args.steps
+                # one step of all layers as a CUDA graph, replayed
+                graph = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(graph, stream=side):
+                        step(0)
+                stream.wait_stream(side)
+                for _ in range(L):
+                    graph.replay()
+                torch.cuda.synchronize()
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+                for _ in range(args.steps):
+                    graph.replay()
+                g1.record(stream)
+                torch.cuda.synchronize()
+                t_graph = g0.elapsed_time(g1) / 1e3 / args.steps
+                errs = [m.read_pointers()[2] for m in models]
+                total_launches += n_layers * (2 * args.steps + max(L, args.warmup) + 1 + L)
+                step_bytes = n_layers * B * window_bytes(s)["replay_per_seq_step"]
+                points.append({
+                    "B": B, "L": L, "ms_per_step": t_eager * 1e3, "ms_per_step_graph": t_graph * 1e3,
+                    "seq_steps_per_s_graph": B / t_graph, "algorithmic_bytes_per_step": step_bytes,
+                    "hbm_gbs": step_bytes / t_eager / 1e9, "hbm_gbs_graph": step_bytes / t_graph / 1e9,
+                    "frac_graph": step_bytes / t_graph / 1e9 / peak,
+                    "state_bytes_all_layers": n_layers * state_b,
+                    "l2_may_hold_state": n_layers * state_b < 129e6,
+                    "device_error_words": sorted(set(errs))})
+                del graph, models, pool, outs
+                torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    return {
+        "metric": f"multi-layer decode step time ({n_layers} layers), batch x window sweep", "unit": "ms/step",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{n_layers} SSM layers of H={base.H} P={base.P} N={base.N} G={base.G}, bf16 v/k/q, "
+                               f"fp32 checkpoints; one step = one decode step through every layer; inputs: 4 "
+                               f"resident steps shared by the layers",
+                   "batches": batches, "windows": windows,
+                   "l2": "state of all layers vs the 129 MB L2 is given per point (l2_may_hold_state)"},
+        "peak_gbs": peak, "peak_kind": peak_kind, "points": points, "clocks": clk.summary(),
+        "gpu_launches": total_launches,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,8 +666,14 @@ def main(argv=None):
     ap.add_argument("--no-conventional", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller cases for ncu captures; not a bench line)")
-    ap.add_argument("--workload", choices=["decode", "verify"], default="decode",
-                    help="decode: the headline metric; verify: speculative rounds (B=512, T=4)")
+    ap.add_argument("--workload", choices=["decode", "verify", "multilayer"], default="decode",
+                    help="decode: the headline metric; verify: speculative rounds (B=512, T=4); "
+                         "multilayer: a stack of layers, batch x window sweep (--steps = decode steps per point)")
+    ap.add_argument("--layers", type=int, default=40, help="multilayer: layers in the stack")
+    ap.add_argument("--shape", choices=sorted(MULTI_SHAPES), default="mamba2",
+                    help="multilayer: mamba2 (H=128 P=64 N=128 G=8) or alt (H=32 P=128 N=128 G=16)")
+    ap.add_argument("--batches", default="1,32,128,256,512", help="multilayer: batch sizes")
+    ap.add_argument("--windows", default="4,8,16,32", help="multilayer: windows L")
     ap.add_argument("--read-fmt", choices=["e4m3", "e2m1"], default=None,
                     help="non-flush steps read a low-precision copy of the checkpoint")
     args = ap.parse_args(argv)
@@ -566,7 +685,8 @@ def main(argv=None):
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
-        line = run_verify(args, world, rank, local) if args.workload == "verify" else run_ours(args, world, rank, local)
+        run = {"decode": run_ours, "verify": run_verify, "multilayer": run_multilayer}[args.workload]
+        line = run(args, world, rank, local)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:
