@@ -36,11 +36,6 @@ namespace rssm {
 #define RSSM_ROWS_PER_WARP 8
 #endif
 constexpr int kNDW = RSSM_DOT_WARPS;       // dot warps per CTA (stream the checkpoint tile)
-#ifndef RSSM_GATHER_BULK
-// record gathers: 16-byte cp.async chunks (0), one bulk copy per value row (1),
-// or bulk copies of the ring's contiguous runs (2)
-#define RSSM_GATHER_BULK 2
-#endif
 #ifndef RSSM_APPEND_BULK
 #define RSSM_APPEND_BULK 0  // ring appends: 16-byte stores (0) or one bulk store per row (1)
 #endif
@@ -186,9 +181,6 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Small asynchronous copies global -> shared (the record gathers).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -552,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 
   // The parity waits need every ring to be a multiple of the consumers that take
   // its entries in turn (see the host plan). Refuse any other plan.
-  if (lay.dgroups < 1 || lay.stages < lay.dgroups || lay.stages > kMaxStages || lay.slots > kMaxSlots ||
+  if (lay.dgroups < 1 || (lay.dgroups & (lay.dgroups - 1)) != 0 || lay.stages < lay.dgroups ||
+      lay.stages > kMaxStages || lay.slots > kMaxSlots ||
       lay.stages % lay.dgroups != 0 || lay.slots % kNCoef != 0 || lay.slots % lay.dgroups != 0 ||
       kNDW % lay.dgroups != 0) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrPlan);
@@ -565,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       mbar_init(tempty0 + 8 * s, kNDW / lay.dgroups);  // the warps of the head's dot group
     }
     for (int s = 0; s < lay.slots; ++s) {
-      mbar_init(sfull0 + 8 * s, 1 + 32);  // lane 0's value-row bytes + 32 decay gathers
+      mbar_init(sfull0 + 8 * s, 2);  // the gather lane's expected bytes + its cp.async decays
       mbar_init(scoef0 + 8 * s, 1);
       mbar_init(sempty0 + 8 * s, kNDW / lay.dgroups + 1);  // the head's dot group + its coefficient warp
     }
@@ -607,14 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     else if constexpr (MODE == kFlush) return c;
     else if constexpr (MODE == kConv) return 1;
     else return 0;
-  };
-  // Source of record j's value row 0 for head (b, hh).
-  auto vrow_src = [&](int j, int c, int st, int b, int hh, size_t hrow) -> const uint8_t* {
-    if (MODE == kConv) return reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
-    if (j < c) return reinterpret_cast<const uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, j, p.R)) * p.P * ES;
-    if (MODE == kVerify)
-      return reinterpret_cast<const uint8_t*>(p.v) + (((size_t)b * p.T + (j - c)) * p.H + hh) * p.P * ES;
-    return reinterpret_cast<const uint8_t*>(p.v) + hrow * p.P * ES;
   };
 
   // Ring positions (index, phase parity) of the tile stages and record slots.
@@ -660,125 +645,96 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       }
     }
   } else if (warp == kGatherWarp) {
-    // ====================================================================== gather warp
-    int li = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
-    long long cur_gg = -1;
-    bool load = false, flush = false, bad = false;
-    const int chp = p.P * ES / 16;  // 16-byte chunks per value row
-    const int vcp = chp < 32 ? chp : 32;         // lanes per record in the value-row gather
-    const int vdj = 32 / vcp, vj0 = lane / vcp;  // records per pass, this lane's record offset
-    const int vch = lane - vj0 * vcp;            // this lane's first chunk
-    HeadIter it;
-    it.init(h0, p.H, p.HPG);
-    for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
-      const int b = it.b, hh = it.hh, g = it.g;
-      const long long gg = (long long)b * p.G + g;
-      const size_t hrow = (size_t)gh;
-      if (b != cur_b) {
-        cur_b = b;
-        seq_plan(b, c, st, load, flush, bad);
-        if (bad && lane == 0) atomicOr(p.err, kErrCapacity);
-        J = records(c);
-        cur_gg = -1;
-      }
-      if (!load) continue;
-      if constexpr (kGroupData) {
-        if (gg != cur_gg) {
-          cur_gg = gg;
-          const int gs = gi & 1, guse = gi >> 1;
-          const bool w = guse == 0 || mbar_wait(gempty0 + 8 * gs, (guse - 1) & 1, abort_flag, p.err);
-          if (!__all_sync(kFull, w)) { ok = false; break; }
-          const uint32_t gdst = smem_u32(smem + p.gb_off + gs * p.gb_bytes);
-          const size_t grow = (size_t)b * p.G + g;
-          if (lane == 0) mbar_arrive_tx(gfull0 + 8 * gs, (uint32_t)(J + (kQuery ? nq : 0)) * N * ES);
-          __syncwarp();
-          if (lane < J) {  // one bulk copy per key row (J <= 32)
-            const int j = lane;
-            const uint8_t* src;
-            if (MODE == kConv || (MODE == kDecode && j >= c))
-              src = reinterpret_cast<const uint8_t*>(p.k) + grow * N * ES;
-            else if (j < c)
-              src = reinterpret_cast<const uint8_t*>(p.ring_k) + (grow * p.R + ring_slot(st, j, p.R)) * N * ES;
-            else  // verify draft j - c
-              src = reinterpret_cast<const uint8_t*>(p.k) + (((size_t)b * p.T + (j - c)) * p.G + g) * N * ES;
-            tma_load_1d(gdst + j * N * ES, src, N * ES, gfull0 + 8 * gs);
-          }
-          if constexpr (kQuery) {
-            if (lane < nq) {
-              const int t = lane;
-              const size_t row = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
-              tma_load_1d(gdst + p.gq_off + t * N * ES, reinterpret_cast<const uint8_t*>(p.q) + row * N * ES, N * ES,
-                          gfull0 + 8 * gs);
-            }
-          }
-          ++gi;
+    // ====================================================================== gather (one lane)
+    // Per group: the keys and queries into a group area; per head: the records
+    // into a slot. Committed records sit in the ring at slots st .. st + c - 1
+    // (mod R), so their key rows, value rows and decays are at most two
+    // contiguous runs each; every run is one bulk copy. New records come from
+    // the call's inputs: one bulk copy per row and a 4-byte cp.async per decay.
+    if (lane == 0) {
+      int li = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
+      long long cur_gg = -1;
+      bool load = false, flush = false, bad = false;
+      const uint32_t rbytes = (uint32_t)p.P * ES, kbytes = (uint32_t)N * ES;
+      HeadIter it;
+      it.init(h0, p.H, p.HPG);
+      for (long long gh = h0; gh < h1; ++gh, it.next(p.H, p.HPG)) {
+        const int b = it.b, hh = it.hh, g = it.g;
+        const long long gg = (long long)b * p.G + g;
+        const size_t hrow = (size_t)gh;
+        if (b != cur_b) {
+          cur_b = b;
+          seq_plan(b, c, st, load, flush, bad);
+          if (bad) atomicOr(p.err, kErrCapacity);
+          J = records(c);
+          cur_gg = -1;
         }
-      }
-      const bool w = li < lay.slots || mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err);
-      if (!__all_sync(kFull, w)) { ok = false; break; }
-      const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
-      // Slot: decays at [ring slot] for committed records and at kRMax + (j - c)
-      // for new ones; value rows in record order from sv_off.
-      const int nnew = J - c;  // records that come from the call's inputs
-#if RSSM_GATHER_BULK == 2
-      // Committed records sit in the ring at slots st .. st + c - 1 (mod R): their
-      // value rows are at most two contiguous runs and their decays one row of Rp.
-      // Lane 0 issues those bulk copies; lane t < nnew one for new record t.
-      if (lane == 0) {
-        const uint32_t rbytes = (uint32_t)p.P * ES;
-        mbar_arrive_tx(sfull0 + 8 * rs, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
+        if (!load) continue;
+        const int nnew = J - c;  // records that come from the call's inputs
+        if constexpr (kGroupData) {
+          if (gg != cur_gg) {
+            cur_gg = gg;
+            const int gs = gi & 1, guse = gi >> 1;
+            if (guse > 0 && !mbar_wait(gempty0 + 8 * gs, (guse - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+            const uint32_t gbar = gfull0 + 8 * gs;
+            const uint32_t gdst = smem_u32(smem + p.gb_off + gs * p.gb_bytes);
+            const size_t grow = (size_t)b * p.G + g;
+            mbar_arrive_tx(gbar, (uint32_t)(J + (kQuery ? nq : 0)) * kbytes);
+            if (c > 0) {
+              const int n1 = min(c, p.R - st);
+              const uint8_t* rk = reinterpret_cast<const uint8_t*>(p.ring_k) + grow * p.R * kbytes;
+              tma_load_1d(gdst, rk + (size_t)st * kbytes, (uint32_t)n1 * kbytes, gbar);
+              if (c > n1) tma_load_1d(gdst + n1 * kbytes, rk, (uint32_t)(c - n1) * kbytes, gbar);
+            }
+            for (int t = 0; t < nnew; ++t) {
+              const size_t krow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
+              tma_load_1d(gdst + (c + t) * kbytes, reinterpret_cast<const uint8_t*>(p.k) + krow * kbytes, kbytes, gbar);
+            }
+            if constexpr (kQuery) {
+              for (int t = 0; t < nq; ++t) {
+                const size_t qrow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
+                tma_load_1d(gdst + p.gq_off + t * kbytes, reinterpret_cast<const uint8_t*>(p.q) + qrow * kbytes,
+                            kbytes, gbar);
+              }
+            }
+            ++gi;
+          }
+        }
+        if (li >= lay.slots && !mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        const uint32_t sbar = sfull0 + 8 * rs;
+        const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
+        // slot: decays at [ring slot] (committed) and kRMax + t (new); value rows in record order
+        mbar_arrive_tx(sbar, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
         if (c > 0) {
-          tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sfull0 + 8 * rs);
+          tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
           const int n1 = min(c, p.R - st);
           const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * rbytes;
-          tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * rbytes, (uint32_t)n1 * rbytes, sfull0 + 8 * rs);
-          if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * rbytes, rv, (uint32_t)(c - n1) * rbytes, sfull0 + 8 * rs);
+          tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * rbytes, (uint32_t)n1 * rbytes, sbar);
+          if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * rbytes, rv, (uint32_t)(c - n1) * rbytes, sbar);
+        }
+        for (int t = 0; t < nnew; ++t) {
+          const size_t nrow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.H + hh : hrow;
+          cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
+          tma_load_1d(sdst + lay.sv_off + (c + t) * rbytes, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes,
+                      rbytes, sbar);
+        }
+        cp_async_arrive(sbar);  // completes with this lane's decay copies
+        slot_next();
+        ++li;
+      }
+      cp_async_wait_all();
+      if (!ok) {  // wait (bounded) for the copies still in flight, then leave
+        volatile int dummy = 0;
+        for (int k = 0; k < lay.slots && k < li; ++k) {
+          const int i = li - 1 - k;
+          mbar_wait(sfull0 + 8 * (i % lay.slots), (i / lay.slots) & 1, &dummy, p.err);
+        }
+        for (int k = 0; k < 2 && k < gi; ++k) {
+          const int i = gi - 1 - k;
+          mbar_wait(gfull0 + 8 * (i & 1), (i >> 1) & 1, &dummy, p.err);
         }
       }
-      __syncwarp();
-      if (lane < nnew) {
-        const int t = lane;
-        const size_t nrow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.H + hh : hrow;
-        cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
-        tma_load_1d(sdst + lay.sv_off + (c + t) * p.P * ES, reinterpret_cast<const uint8_t*>(p.v) + nrow * p.P * ES,
-                    (uint32_t)p.P * ES, sfull0 + 8 * rs);
-      }
-#else
-      // lane j: the decay of record j; the value rows as 16-byte cp.async chunks spread
-      // over the lanes (RSSM_GATHER_BULK=1: one bulk copy per value row instead)
-      const uint8_t* vsrc = nullptr;
-      if (lane < J) {
-        const int j = lane;
-        const float* asrc;
-        if (MODE == kConv) asrc = p.alpha + hrow;
-        else if (j < c) asrc = p.ring_a + hrow * p.Rp + ring_slot(st, j, p.R);
-        else if (MODE == kVerify) asrc = p.alpha + ((size_t)b * p.T + (j - c)) * p.H + hh;
-        else asrc = p.alpha + hrow;
-        cp_async4(sdst + 4 * (j < c ? ring_slot(st, j, p.R) : kRMax + j - c), asrc);
-        vsrc = vrow_src(j, c, st, b, hh, hrow);
-      }
-#if RSSM_GATHER_BULK
-      if (lane == 0) mbar_arrive_tx(sfull0 + 8 * rs, (uint32_t)J * p.P * ES);
-      __syncwarp();
-      if (lane < J) tma_load_1d(sdst + lay.sv_off + lane * p.P * ES, vsrc, p.P * ES, sfull0 + 8 * rs);
-#else
-      if (lane == 0) mbar_arrive(sfull0 + 8 * rs);
-      for (int j = 0; j < J; j += vdj) {  // vdj records per pass, vcp lanes per record
-        const int jr = j + vj0;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, reinterpret_cast<uintptr_t>(vsrc),
-                                                                          min(jr, 31)));
-        if (jr < J) {
-          for (int ch = vch; ch < chp; ch += vcp)
-            cp_async16(sdst + lay.sv_off + jr * p.P * ES + ch * 16, src + ch * 16);
-        }
-      }
-#endif
-#endif
-      cp_async_arrive(sfull0 + 8 * rs);
-      slot_next();
-      ++li;
     }
-    cp_async_wait_all();
   } else if (warp >= kCoef0 && warp < kCoef0 + kNCoef) {
     // ====================================================================== coefficients
     const int cwi = warp - kCoef0;  // this warp takes the loaded heads with index = cwi (mod kNCoef)
@@ -987,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           ++gi;
         }
       }
-      if ((lh++ % lay.dgroups) != dgrp) {  // another dot group takes this head
+      if ((lh++ & (lay.dgroups - 1)) != dgrp) {  // another dot group takes this head (dgroups: power of two)
         tile_next();
         slot_next();
         continue;
