@@ -105,15 +105,22 @@ struct Plan {
 // lay[1], offered to decode steps, holds only non-flush heads: its stages hold
 // the tile that non-flush steps read (the read copy when there is one) and its
 // slots at most L - 1 records and no fold coefficients, so more heads fit.
-rssm_status plan_layout(const rssm_config* c, const Geom& g, bool nf, size_t budget, rssm::Layout* L) {
+enum class LayoutKind { kGeneral, kNonFlush, kVerify };
+
+rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, size_t budget, rssm::Layout* L) {
   using namespace rssm;
   auto a128 = [](size_t x) { return align_up(x, 128); };
+  const bool nf = kind == LayoutKind::kNonFlush;
   const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
   const size_t tile = a128(nf && g.head_stride ? g.head_stride : P * N * 4);
   const size_t vrows = nf ? (size_t)c->L : R;
   const size_t sv_off = (size_t)(kRMax + kTMax) * 4;  // decays: kRMax ring slots, then kTMax new records
   const size_t sc_off = align_up(sv_off + vrows * P * es, 16);
-  const size_t sc_floats = nf ? 16 + P : 16 + std::max({P, R * P, (size_t)kTMax * kRMax});
+  // coefficients: 16 scalars, then the value term [P] (non-flush), the record
+  // weights [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general)
+  const size_t sc_floats = nf ? 16 + P
+                              : kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax
+                                                            : 16 + std::max({P, R * P, (size_t)c->T_max * P});
   const size_t slot = a128(sc_off + sc_floats * 4);
   if (2 * tile + 2 * slot > budget) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
   const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, budget / (tile + 3 * slot)));
@@ -145,7 +152,9 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, bool nf, size_t bud
   return RSSM_OK;
 }
 
-rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, bool decode = false) {
+// kind: kGeneral (flush, quantize, conventional), kNonFlush (decode: the general
+// layout plus the non-flush one), kVerify (verify: no fold area).
+rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind kind = LayoutKind::kGeneral) {
   using namespace rssm;
   auto a128 = [](size_t x) { return align_up(x, 128); };
   const size_t N = c->N, es = (size_t)g.esize, R = g.R;
@@ -157,11 +166,14 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, bool decode
   if (fixed >= (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "group areas too large for shared memory");
   const size_t budget = ((size_t)kSmemMax - fixed) / 128 * 128;
   rssm::Params& p = pl->p;
-  rssm_status s = plan_layout(c, g, false, budget, &p.lay[0]);
+  rssm_status s = plan_layout(c, g, kind == LayoutKind::kVerify ? LayoutKind::kVerify : LayoutKind::kGeneral, budget,
+                              &p.lay[0]);
   if (s != RSSM_OK) return s;
   p.lay[1] = p.lay[0];
   p.nf_ok = 0;
-  if (decode && c->L >= 2 && plan_layout(c, g, true, budget, &p.lay[1]) == RSSM_OK) p.nf_ok = 1;
+  if (kind == LayoutKind::kNonFlush && c->L >= 2 &&
+      plan_layout(c, g, LayoutKind::kNonFlush, budget, &p.lay[1]) == RSSM_OK)
+    p.nf_ok = 1;
   size_t off = budget;
   p.gb_off = (int)off; off += 2 * gb;
   p.gb_bytes = (int)gb;
@@ -315,7 +327,7 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
   Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, true);
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kNonFlush);
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
@@ -335,7 +347,7 @@ rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
   Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl);
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kVerify);
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.T = T;
@@ -488,7 +500,7 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
     tickets = g_static_ticket_addr[dev];
   }
   Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, true);
+  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kNonFlush);
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.ticket = tickets;

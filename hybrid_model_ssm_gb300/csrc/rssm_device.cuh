@@ -349,12 +349,6 @@ struct TMax<K, 0> {
   static __device__ __forceinline__ void run(float*, int, int&) {}
 };
 
-template <int D>
-__device__ __forceinline__ float low_sum(float x) {
-#pragma unroll
-  for (int m = 1; m < D; m <<= 1) x += __shfl_xor_sync(kFull, x, m);
-  return x;
-}
 // incl[lane] = prod_{i >= lane} x_i over the warp.
 __device__ __forceinline__ float suffix_prod(float x, int lane) {
 #pragma unroll
@@ -816,6 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       // lane j holds alpha of record j
       const float aj = (lane < c) ? sa[ring_slot(st, lane, p.R)] : (lane < J) ? sa[kRMax + lane - c] : 1.f;
       if constexpr (MODE == kVerify) {
+        // Per query t (records 0 .. c + t): g_{1:c+t+1} into sc[t] and the record
+        // weights g_{j+2:c+t+1} (k_j^T q_t) into sc[kCoefOff + t kRMax + j].
         for (int t = 0; t < p.T; ++t) {
           const int ht = c + t + 1;
           const float x = (lane < ht) ? aj : 1.f;
@@ -906,6 +902,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     constexpr int RPIc = 32 / LPRc;
     constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
     float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
+    // FP32 non-flush rows (N >= 64): LP16 lanes per row, 16 columns per lane as
+    // 4 chunks of 4 interleaved over the row's lanes (each quarter warp reads
+    // 128 contiguous bytes: no bank conflicts); q16 holds the matching q values.
+    constexpr bool kWideRows = (RF == kRfNone && MODE == kDecode && N >= 64);
+    constexpr int LP16 = kWideRows ? N / 16 : 1;
+    float q16[kWideRows ? 16 : 1];
     const int wpg = kNDW / lay.dgroups;                 // warps per dot group
     const int dgrp = warp / wpg, wr = warp - dgrp * wpg;  // this warp's group and rank in it
     const int rows_pass = wpg * kKR * RPI;
@@ -936,6 +938,13 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           gK = smem + p.gb_off + gs * p.gb_bytes;
           gQ = gK + p.gq_off;
           if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
+          if constexpr (kWideRows) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float4 qq = In<TIn>::lds4(gQ, (c * LP16 + lane % LP16) * 4);
+              q16[4 * c] = qq.x; q16[4 * c + 1] = qq.y; q16[4 * c + 2] = qq.z; q16[4 * c + 3] = qq.w;
+            }
+          }
           if constexpr (RF != kRfNone && MODE == kDecode) {
 #pragma unroll
             for (int i = 0; i < CPL; ++i) qc[i] = In<TIn>::lds(gQ, (lane % LPRc) * CPL + i);
@@ -951,8 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       // the coefficient warp arrives only after the record gathers landed, so
       // its barrier also covers alpha_j and v_j
       const bool got = mbar_wait(tfull0 + 8 * ts, tph, abort_flag, p.err) &&
-                       mbar_wait(scoef0 + 8 * rs, rph, abort_flag, p.err) &&
-                       (MODE != kVerify || mbar_wait(sfull0 + 8 * rs, rph, abort_flag, p.err));
+                       mbar_wait(scoef0 + 8 * rs, rph, abort_flag, p.err);
       if (!__all_sync(kFull, got)) { ok = false; break; }
       const uint8_t* tile = smem + (size_t)ts * lay.stage_bytes;
       const float* tf = reinterpret_cast<const float*>(tile);
@@ -962,38 +970,124 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 
       if constexpr (MODE == kVerify) {
         // ================================================ verify (T queries)
-        for (int pass = 0; pass < npass; ++pass) {
-          const int rbase = (pass * wpg + wr) * kKR;
+        // o[t][row] = g_{1:c+t+1} (S q_t)[row] + sum_j w_tj v_j[row]. The lanes of a
+        // row split the records (lane k of the row takes j = k, k + lanes, ...) and
+        // add their share to the scaled dot before the row reduction, so the value
+        // term costs no shuffles. w_tj = 0 for records that query t does not see.
+        const float* cw = sc + kCoefOff;  // [kTMax][kRMax]
+        if constexpr (N >= 64) {
+          // LPV lanes per row, 16 columns per lane in 4 interleaved chunks (as the
+          // wide non-flush rows); KWV row instructions x kTQ queries per pass.
+          constexpr int LPV = N / 16, RPW = 32 / LPV, KWV = 2, JI = kRMax / LPV;
+          const int cl = lane % LPV, rw = lane / LPV;
           for (int t0 = 0; t0 < p.T; t0 += kTQ) {
-            float4 qv[kTQ];
+            float qv[kTQ][16];
+            float g[kTQ];
+            float wv[JI][kTQ];  // this lane's record weights
 #pragma unroll
-            for (int t = 0; t < kTQ; ++t)
-              qv[t] = (t0 + t < p.T) ? In<TIn>::lds4(gQ, (t0 + t) * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float part[kKR * kTQ];
+            for (int tt = 0; tt < kTQ; ++tt) {
+              const bool tv = t0 + tt < p.T;
+              g[tt] = tv ? sc[t0 + tt] : 0.f;
 #pragma unroll
-            for (int kk = 0; kk < kKR; ++kk) {
-              const int row = (rbase + kk) * RPI + rsub;
-              const float4 x4 = (row < p.P) ? lds4(tf + ((size_t)row * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int t = 0; t < kTQ; ++t) part[kk * kTQ + t] = dot4(x4, qv[t]);
-            }
-            int off = 0;
-            TRed<kKR * kTQ, LPR / 2>::run(part, lane, off);
-            constexpr int KF = (kKR * kTQ / LPR) > 0 ? (kKR * kTQ / LPR) : 1;
-            constexpr int D = (LPR / (kKR * kTQ)) > 0 ? (LPR / (kKR * kTQ)) : 1;
-            const int dup = lane & (D - 1);
-#pragma unroll
-            for (int i = 0; i < KF; ++i) {
-              const int kk = (off + i) / kTQ, t = t0 + (off + i) % kTQ;
-              const int row = (rbase + kk) * RPI + rsub;
-              const bool valid = row < p.P && t < p.T;
-              float ov = 0.f;
-              if (valid) {
-                const float* cwt = sc + kCoefOff + t * kRMax;
-                for (int j = dup; j < J; j += D) ov = fmaf(cwt[j], In<TIn>::lds(sv, j * p.P + row), ov);
+              for (int cc = 0; cc < 4; ++cc) {
+                const float4 qq = tv ? In<TIn>::lds4(gQ, (t0 + tt) * N + (cc * LPV + cl) * 4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                qv[tt][4 * cc] = qq.x; qv[tt][4 * cc + 1] = qq.y; qv[tt][4 * cc + 2] = qq.z; qv[tt][4 * cc + 3] = qq.w;
               }
-              ov = low_sum<D>(ov);
-              if (dup == 0 && valid) p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = fmaf(sc[t], part[i], ov);
+#pragma unroll
+              for (int i = 0; i < JI; ++i) {
+                const int j = cl + LPV * i;
+                wv[i][tt] = (tv && j < J) ? cw[(t0 + tt) * kRMax + j] : 0.f;
+              }
+            }
+            for (int r0 = wr * KWV * RPW; r0 < p.P; r0 += wpg * KWV * RPW) {
+              float part[KWV * kTQ];
+#pragma unroll
+              for (int kk = 0; kk < KWV; ++kk) {
+                const int row = r0 + kk * RPW + rw;
+                float a[kTQ];
+#pragma unroll
+                for (int tt = 0; tt < kTQ; ++tt) a[tt] = 0.f;
+                if (row < p.P) {
+                  const float* rp = tf + (size_t)row * N;
+#pragma unroll
+                  for (int cc = 0; cc < 4; ++cc) {
+                    const float4 x = lds4(rp + (cc * LPV + cl) * 4);
+#pragma unroll
+                    for (int tt = 0; tt < kTQ; ++tt) {
+                      a[tt] = fmaf(x.x, qv[tt][4 * cc], a[tt]);
+                      a[tt] = fmaf(x.y, qv[tt][4 * cc + 1], a[tt]);
+                      a[tt] = fmaf(x.z, qv[tt][4 * cc + 2], a[tt]);
+                      a[tt] = fmaf(x.w, qv[tt][4 * cc + 3], a[tt]);
+                    }
+                  }
+#pragma unroll
+                  for (int tt = 0; tt < kTQ; ++tt) a[tt] *= g[tt];
+#pragma unroll
+                  for (int i = 0; i < JI; ++i) {
+                    const int j = cl + LPV * i;
+                    if (j < J) {
+                      const float vj = In<TIn>::lds(sv, j * p.P + row);
+#pragma unroll
+                      for (int tt = 0; tt < kTQ; ++tt) a[tt] = fmaf(wv[i][tt], vj, a[tt]);
+                    }
+                  }
+                }
+#pragma unroll
+                for (int tt = 0; tt < kTQ; ++tt) part[kk * kTQ + tt] = a[tt];
+              }
+              int off = 0;
+              TRed<KWV * kTQ, LPV / 2>::run(part, lane, off);
+              constexpr int KF = (KWV * kTQ / LPV) > 0 ? (KWV * kTQ / LPV) : 1;
+              constexpr int D = (LPV / (KWV * kTQ)) > 0 ? (LPV / (KWV * kTQ)) : 1;
+#pragma unroll
+              for (int i = 0; i < KF; ++i) {
+                const int kk = (off + i) / kTQ, t = t0 + (off + i) % kTQ;
+                const int row = r0 + kk * RPW + rw;
+                if ((cl & (D - 1)) == 0 && row < p.P && t < p.T)
+                  p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = part[i];
+              }
+            }
+          }
+        } else {
+          for (int pass = 0; pass < npass; ++pass) {
+            const int rbase = (pass * wpg + wr) * kKR;
+            for (int t0 = 0; t0 < p.T; t0 += kTQ) {
+              float4 qv[kTQ];
+              float g[kTQ];
+#pragma unroll
+              for (int t = 0; t < kTQ; ++t) {
+                qv[t] = (t0 + t < p.T) ? In<TIn>::lds4(gQ, (t0 + t) * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                g[t] = (t0 + t < p.T) ? sc[t0 + t] : 0.f;
+              }
+              float part[kKR * kTQ];
+#pragma unroll
+              for (int kk = 0; kk < kKR; ++kk) {
+                const int row = (rbase + kk) * RPI + rsub;
+                const float4 x4 =
+                    (row < p.P) ? lds4(tf + ((size_t)row * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < kTQ; ++t) part[kk * kTQ + t] = g[t] * dot4(x4, qv[t]);
+                if (row < p.P) {
+                  for (int j = col4; j < J; j += LPR) {  // this lane's share of the records
+                    const float vj = In<TIn>::lds(sv, j * p.P + row);
+#pragma unroll
+                    for (int t = 0; t < kTQ; ++t)
+                      if (t0 + t < p.T) part[kk * kTQ + t] = fmaf(cw[(t0 + t) * kRMax + j], vj, part[kk * kTQ + t]);
+                  }
+                }
+              }
+              int off = 0;
+              TRed<kKR * kTQ, LPR / 2>::run(part, lane, off);
+              constexpr int KF = (kKR * kTQ / LPR) > 0 ? (kKR * kTQ / LPR) : 1;
+              constexpr int D = (LPR / (kKR * kTQ)) > 0 ? (LPR / (kKR * kTQ)) : 1;
+#pragma unroll
+              for (int i = 0; i < KF; ++i) {
+                const int kk = (off + i) / kTQ, t = t0 + (off + i) % kTQ;
+                const int row = (rbase + kk) * RPI + rsub;
+                if ((lane & (D - 1)) == 0 && row < p.P && t < p.T)
+                  p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = part[i];
+              }
             }
           }
         }
@@ -1101,6 +1195,35 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         // ================================================ non-flush decode: o = g (S q) + value term
         const float gam = sc[0];
         const float* sov = sc + kCoefOff;  // [P]
+        if constexpr (kWideRows) {
+          constexpr int RPW = 32 / LP16, KW = 4;  // rows per warp instruction, row instructions per pass
+          const int cl = lane % LP16, rw = lane / LP16;
+          for (int r0 = wr * KW * RPW; r0 < p.P; r0 += wpg * KW * RPW) {
+            float part[KW];
+#pragma unroll
+            for (int kk = 0; kk < KW; ++kk) {
+              const int row = r0 + kk * RPW + rw;
+              float a0 = 0.f, a1 = 0.f;
+              if (row < p.P) {
+                const float* rp = tf + (size_t)row * N;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const float4 x = lds4(rp + (c * LP16 + cl) * 4);
+                  a0 = fmaf(x.x, q16[4 * c], a0);
+                  a1 = fmaf(x.y, q16[4 * c + 1], a1);
+                  a0 = fmaf(x.z, q16[4 * c + 2], a0);
+                  a1 = fmaf(x.w, q16[4 * c + 3], a1);
+                }
+              }
+              part[kk] = a0 + a1;
+            }
+            int off = 0;
+            TRed<KW, LP16 / 2>::run(part, lane, off);  // lane: row r0 + off * RPW + rw
+            constexpr int D = (LP16 / KW) > 0 ? (LP16 / KW) : 1;  // lanes holding the same row
+            const int row = r0 + off * RPW + rw;
+            if ((cl & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[0], sov[row]);
+          }
+        } else
         for (int pass = 0; pass < npass; ++pass) {
           if constexpr (RF == kRfNone) {
             const int rbase = (pass * wpg + wr) * kKR;
