@@ -116,11 +116,12 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   const size_t vrows = nf ? (size_t)c->L : R;
   const size_t sv_off = (size_t)(kRMax + kTMax) * 4;  // decays: kRMax ring slots, then kTMax new records
   const size_t sc_off = align_up(sv_off + vrows * P * es, 16);
-  // coefficients: 16 scalars, then the value term [P] (non-flush), the record
-  // weights [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general)
-  const size_t sc_floats = nf ? 16 + P
+  // coefficients: 16 scalars, then the record weights [kRMax] (non-flush),
+  // [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general, which
+  // also serves non-flush heads)
+  const size_t sc_floats = nf ? 16 + std::max(P, (size_t)kRMax)
                               : kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax
-                                                            : 16 + std::max({P, R * P, (size_t)c->T_max * P});
+                                                            : 16 + std::max({(size_t)kRMax, R * P, (size_t)c->T_max * P});
   const size_t slot = a128(sc_off + sc_floats * 4);
   if (2 * tile + 2 * slot > budget) return fail(RSSM_EUNSUPPORTED, "tile too large for shared memory");
   const int stages = (int)std::max<size_t>(2, std::min<size_t>(kMaxStages, budget / (tile + 3 * slot)));

@@ -837,27 +837,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             }
           }
         } else if constexpr (MODE == kDecode) {
-          // non-flush: value term sum_j g_{j+2:J} (k_j^T q) v_j[p] for row pairs 2*lane + 64 m (P <= 128)
-          const float cj = (lane < J) ? wj * sj : 0.f;
-          float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 4
-          for (int j = 0; j < J; ++j) {
-            const float cjj = __shfl_sync(kFull, cj, j);
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              const int r = 2 * lane + 64 * m;
-              if (r < p.P) {
-                const float2 v2 = In<TIn>::lds2(sv, j * p.P + r);
-                acc[m].x = fmaf(cjj, v2.x, acc[m].x);
-                acc[m].y = fmaf(cjj, v2.y, acc[m].y);
-              }
-            }
-          }
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const int r = 2 * lane + 64 * m;
-            if (r < p.P) *reinterpret_cast<float2*>(sc + kCoefOff + r) = acc[m];
-          }
+          // non-flush: the record weights c_j = g_{j+2:J} (k_j^T q); the dot warps
+          // add sum_j c_j v_j[p] inside their row reductions
+          sc[kCoefOff + lane] = (lane < J) ? wj * sj : 0.f;
         }
       }
       __syncwarp();
@@ -1193,11 +1175,18 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         }
       } else if constexpr (MODE == kDecode) {
         // ================================================ non-flush decode: o = g (S q) + value term
+        // o[row] = g (S q)[row] + sum_j c_j v_j[row]: the lanes of a row split the
+        // records (lane k of the row takes j = k, k + lanes, ...) and add their
+        // share to the scaled dot before the row reduction.
         const float gam = sc[0];
-        const float* sov = sc + kCoefOff;  // [P]
+        const float* scj = sc + kCoefOff;  // [kRMax] record weights, 0 past J
         if constexpr (kWideRows) {
           constexpr int RPW = 32 / LP16, KW = 4;  // rows per warp instruction, row instructions per pass
+          constexpr int JI = kRMax / LP16;
           const int cl = lane % LP16, rw = lane / LP16;
+          float cwv[JI];
+#pragma unroll
+          for (int i = 0; i < JI; ++i) cwv[i] = scj[cl + LP16 * i];
           for (int r0 = wr * KW * RPW; r0 < p.P; r0 += wpg * KW * RPW) {
             float part[KW];
 #pragma unroll
@@ -1214,14 +1203,20 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                   a0 = fmaf(x.z, q16[4 * c + 2], a0);
                   a1 = fmaf(x.w, q16[4 * c + 3], a1);
                 }
+                a0 = gam * (a0 + a1);
+#pragma unroll
+                for (int i = 0; i < JI; ++i) {
+                  const int j = cl + LP16 * i;
+                  if (j < J) a0 = fmaf(cwv[i], In<TIn>::lds(sv, j * p.P + row), a0);
+                }
               }
-              part[kk] = a0 + a1;
+              part[kk] = a0;
             }
             int off = 0;
             TRed<KW, LP16 / 2>::run(part, lane, off);  // lane: row r0 + off * RPW + rw
             constexpr int D = (LP16 / KW) > 0 ? (LP16 / KW) : 1;  // lanes holding the same row
             const int row = r0 + off * RPW + rw;
-            if ((cl & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[0], sov[row]);
+            if ((cl & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = part[0];
           }
         } else
         for (int pass = 0; pass < npass; ++pass) {
@@ -1231,7 +1226,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
               const int row = (rbase + kk) * RPI + rsub;
-              part[kk] = (row < p.P) ? dot4(lds4(tf + ((size_t)row * LPR + col4) * 4), q4) : 0.f;
+              float a = 0.f;
+              if (row < p.P) {
+                a = gam * dot4(lds4(tf + ((size_t)row * LPR + col4) * 4), q4);
+                for (int j = col4; j < J; j += LPR) a = fmaf(scj[j], In<TIn>::lds(sv, j * p.P + row), a);
+              }
+              part[kk] = a;
             }
             int off = 0;
             TRed<kKR, LPR / 2>::run(part, lane, off);
@@ -1240,19 +1240,26 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
               const int row = (rbase + off + i) * RPI + rsub;
-              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[i], sov[row]);
+              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = part[i];
             }
           } else {
             // read copy: lanes own CPL consecutive codes of a row
             const int rows0 = (pass * wpg + wr) * kKR * RPI;  // first row of this warp
             const int colc = lane % LPRc, rsc = lane / LPRc;
             const float* rscale = reinterpret_cast<const float*>(tile + p.rsc_off);
+            constexpr int JIc = kRMax / LPRc;  // this lane's records: j = colc + LPRc i
             float part[KRc];
 #pragma unroll
             for (int kk = 0; kk < KRc; ++kk) {
               const int row = rows0 + kk * RPIc + rsc;
               float acc = 0.f;
               if (row < p.P) {
+                float val = 0.f;  // this lane's share of sum_j c_j v_j[row], loads issued first
+#pragma unroll
+                for (int i = 0; i < JIc; ++i) {
+                  const int j = colc + LPRc * i;
+                  if (j < J) val = fmaf(scj[j], In<TIn>::lds(sv, j * p.P + row), val);
+                }
                 if constexpr (RF == kRfE4m3) {
                   const uint4 cwd = *reinterpret_cast<const uint4*>(tile + (size_t)row * N + colc * 16);
                   const uint32_t ws[4] = {cwd.x, cwd.y, cwd.z, cwd.w};
@@ -1277,7 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                   }
                   acc = fmaf(dec_e4m3(bsp[0]), blk[0], dec_e4m3(bsp[1]) * blk[1]);
                 }
-                acc *= rscale[row];
+                acc = fmaf(acc, gam * rscale[row], val);
               }
               part[kk] = acc;
             }
@@ -1288,7 +1295,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
             for (int i = 0; i < KF; ++i) {
               const int row = rows0 + (off + i) * RPIc + rsc;
-              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = fmaf(gam, part[i], sov[row]);
+              if ((lane & (D - 1)) == 0 && row < p.P) p.o[hrow * p.P + row] = part[i];
             }
           }
         }
