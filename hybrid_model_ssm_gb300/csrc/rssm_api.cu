@@ -129,6 +129,9 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   // Dot groups: as many heads in flight as keeps two tile stages per group.
   int dgroups = 1;
   while (dgroups < 8 && stages >= 4 * dgroups && slots >= 4 * dgroups) dgroups *= 2;
+  // verify heads are compute-heavier (T queries): one stage per dot group measured best
+  if (kind == LayoutKind::kVerify)
+    while (dgroups < 8 && stages >= 2 * dgroups && slots >= 4 * dgroups) dgroups *= 2;
 #ifdef RSSM_DGROUPS  // build-time override for tuning
   dgroups = RSSM_DGROUPS;
 #endif
