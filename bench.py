@@ -452,7 +452,7 @@ def verify_round_bytes(s, T: int, counts: np.ndarray, accepted: np.ndarray):
 
 
 def run_verify(args, world, rank, local):
-    from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM
+    from hybrid_model_ssm_gb300 import ConventionalVerifier, LayerShape, ReplaySSM
 
     torch.cuda.set_device(local)
     s = VERIFY_WORKLOAD if args.batch is None else VERIFY_WORKLOAD.with_(B=args.batch)
@@ -519,6 +519,41 @@ def run_verify(args, world, rank, local):
     tf = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
     peak, peak_kind = measured_peak_gbs()
     achieved = vbytes / tv / 1e9
+
+    # in-run comparison: conventional verify with per-draft snapshots (one state
+    # read and T writes per round, commit by slot index), same inputs and accepts
+    comp = None
+    if not args.no_conventional:
+        del model
+        torch.cuda.empty_cache()
+        conv = ConventionalVerifier(ls, torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev) * 0.1)
+        for i in range(args.warmup):
+            a, v, k, q = pool[i % len(pool)]
+            conv.verify(a, v, k, q, out=out)
+            conv.commit(acc_dev[i])
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(args.warmup, rounds):
+            a, v, k, q = pool[i % len(pool)]
+            conv.verify(a, v, k, q, out=out)
+            conv.commit(acc_dev[i])
+        c1.record(stream)
+        torch.cuda.synchronize()
+        assert int(conv.err.item()) == 0
+        ct = c0.elapsed_time(c1) / 1e3
+        es = 2 if s.in_dtype == "bf16" else 4
+        Sb = 4 * s.H * s.P * s.N
+        inp = record_bytes(s) + es * s.G * s.N
+        conv_round = s.B * ((1 + T) * Sb + T * (inp + 4 * s.H * s.P)) + 8 * s.B
+        comp = {"conventional_draft_tokens_per_s": s.B * T * args.steps / ct,
+                "conventional_ms_per_round": ct / args.steps * 1e3,
+                "conventional_hbm_gbs": conv_round * args.steps / ct / 1e9,
+                "replay_speedup": (world * s.B * T * args.steps / elapsed) / (s.B * T * args.steps / ct),
+                "algorithmic_bytes_replay_over_conventional": (vbytes + fbytes) / (conv_round * args.steps),
+                "method": "every draft advances the full fp32 state and writes a snapshot; commit selects the "
+                          "accepted snapshot by a per-sequence slot index"}
+        del conv
     if rank != 0:
         return None
     return {
@@ -538,6 +573,7 @@ def run_verify(args, world, rank, local):
         "breakdown_ms_per_round": {"verify": tv / args.steps * 1e3, "commit": tc / args.steps * 1e3,
                                    "flush": tf / args.steps * 1e3,
                                    "flush_hbm_gbs": fbytes / tf / 1e9 if tf > 0 else None},
+        "comparison": comp,
         "clocks": clk.summary(), "gpu_launches": 3 * args.steps, "device_error_word": err,
     }
 

@@ -5,6 +5,7 @@ The kernels live in ``csrc/`` and are built into ``librssm.so`` by
 This package only marshals arguments. It has no CPU implementation of the path.
 """
 from .rssm import (  # noqa: F401
+    ConventionalVerifier,
     LayerShape,
     ReplaySSM,
     RssmError,

@@ -457,6 +457,47 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
   return RSSM_OK;
 }
 
+rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, const int32_t* cur, int32_t T,
+                                     const float* alpha, const void* v, const void* k, const void* q, float* o,
+                                     uint32_t* err_word, void* stream) {
+  Geom g;
+  rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (T < 1 || T > cfg->T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, cfg->T_max);
+  if (!states || !cur || !alpha || !v || !k || !q || !o || !err_word) return fail(RSSM_EINVAL, "NULL pointer");
+  if (!aligned16(states) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
+    return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
+  Plan pl;
+  s = plan_smem(cfg, g, &pl, LayoutKind::kVerify);
+  if (s != RSSM_OK) return s;
+  rssm::Params& p = pl.p;
+  p.B = cfg->B; p.H = cfg->H; p.P = cfg->P; p.N = cfg->N; p.G = cfg->G; p.L = cfg->L;
+  p.R = g.R; p.Rp = g.Rp; p.HPG = cfg->H / cfg->G; p.T = T; p.min_count = 1;
+  p.ckpt = states;
+  p.cur = cur;
+  p.nslot = cfg->T_max + 1;
+  p.err = err_word;
+  p.alpha = alpha; p.v = v; p.k = k; p.q = q; p.o = o;
+  const long long heads = (long long)cfg->B * cfg->H;
+  const cudaError_t e = rssm::launch_snap(p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
+                                          cfg->N, cfg->in_dtype);
+  if (e != cudaSuccess) return cuda_fail(e, "conventional verify launch");
+  return RSSM_OK;
+}
+
+rssm_status rssm_conventional_commit(const rssm_config* cfg, int32_t* cur, const int32_t* accepted, int32_t T,
+                                     uint32_t* err_word, void* stream) {
+  Geom g;
+  const rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (T < 1 || T > cfg->T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, cfg->T_max);
+  if (!cur || !accepted || !err_word) return fail(RSSM_EINVAL, "NULL pointer");
+  const cudaError_t e = rssm::launch_snap_commit(cfg->B, T, cfg->T_max + 1, accepted, cur, err_word,
+                                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "conventional commit launch");
+  return RSSM_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Decode step with library-owned scratch.
 //

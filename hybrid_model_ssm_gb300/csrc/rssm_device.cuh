@@ -58,7 +58,7 @@ constexpr int kMaxStages = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr unsigned kFull = 0xffffffffu;
 
-enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4 };
+enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4, kSnap = 5 };
 enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2 };
 enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u, kErrPlan = 8u };
 
@@ -70,7 +70,7 @@ struct Layout {
 
 struct Params {
   int B, H, P, N, G, L, R, Rp, HPG, T, min_count;
-  float* ckpt;         // [B,H,P,N] checkpoint, or the full state for kConv
+  float* ckpt;         // [B,H,P,N] checkpoint; the full state for kConv; kSnap: [nslot][B,H,P,N] state slots
   uint8_t* copy;       // read copy: head_stride bytes per (b,h), or null
   int head_stride, bsc_off, rsc_off;
   float* ring_a;       // [B,H,Rp] decays
@@ -79,6 +79,8 @@ struct Params {
   int32_t* start;      // [B]
   int32_t* count;      // [B]
   int32_t* ticket;     // [B], zero between launches
+  const int32_t* cur;  // kSnap: [B] slot holding each sequence's state
+  int nslot;           // kSnap: state slots (T_max + 1)
   uint32_t* err;       // error word
   const float* alpha;  // decode/conv [B,H]; verify [B,T,H]
   const void* v;       // decode/conv [B,H,P]; verify [B,T,H,P]
@@ -491,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr int CHN = N * ES / 16;  // 16-byte chunks per k or q row
   constexpr bool kAppendMode = (MODE == kDecode || MODE == kVerify);
   constexpr bool kGroupData = (MODE != kQuant);
-  constexpr bool kQuery = (MODE == kDecode || MODE == kVerify || MODE == kConv);
+  constexpr bool kQuery = (MODE == kDecode || MODE == kVerify || MODE == kConv || MODE == kSnap);
+  constexpr bool kDrafts = (MODE == kVerify || MODE == kSnap);  // inputs carry a draft axis [B,T,...]
   constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -509,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   const long long total = (long long)p.B * p.H;
   const long long h0 = (long long)blockIdx.x * total / gridDim.x;
   const long long h1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
-  const int nq = (MODE == kVerify) ? p.T : 1;
+  const int nq = kDrafts ? p.T : 1;
 
   // Layout: the non-flush one unless one of this CTA's sequences flushes now.
   // Every thread decides alike from the same counts, which no CTA changes
@@ -574,6 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       flush = true;
       return;
     }
+    if constexpr (MODE == kSnap) {  // no ring: the T drafts are all new records; st = state slot
+      st = p.cur[b];
+      bad = st < 0 || st >= p.nslot;
+      load = !bad;
+      return;
+    }
     c = p.count[b];
     st = p.start[b];
     if constexpr (MODE == kDecode) {
@@ -593,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     else if constexpr (MODE == kVerify) return c + p.T;
     else if constexpr (MODE == kFlush) return c;
     else if constexpr (MODE == kConv) return 1;
+    else if constexpr (MODE == kSnap) return p.T;
     else return 0;
   };
 
@@ -622,8 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         if (!load) continue;
         if (li >= lay.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
+        size_t srow = (size_t)gh;  // kSnap: the head's row in the sequence's current state slot
+        if constexpr (MODE == kSnap) srow += (size_t)st * ((size_t)p.B * p.H);
         const void* src = from_copy ? (const void*)(p.copy + (size_t)gh * p.head_stride)
-                                    : (const void*)(p.ckpt + (size_t)gh * p.P * N);
+                                    : (const void*)(p.ckpt + srow * p.P * N);
         const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)p.P * N * 4;
         mbar_arrive_tx(tfull0 + 8 * ts, bytes);
         tma_load_1d(smem_u32(smem + (size_t)ts * lay.stage_bytes), src, bytes, tfull0 + 8 * ts);
@@ -681,12 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               if (c > n1) tma_load_1d(gdst + n1 * kbytes, rk, (uint32_t)(c - n1) * kbytes, gbar);
             }
             for (int t = 0; t < nnew; ++t) {
-              const size_t krow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
+              const size_t krow = kDrafts ? ((size_t)b * p.T + t) * p.G + g : grow;
               tma_load_1d(gdst + (c + t) * kbytes, reinterpret_cast<const uint8_t*>(p.k) + krow * kbytes, kbytes, gbar);
             }
             if constexpr (kQuery) {
               for (int t = 0; t < nq; ++t) {
-                const size_t qrow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.G + g : grow;
+                const size_t qrow = kDrafts ? ((size_t)b * p.T + t) * p.G + g : grow;
                 tma_load_1d(gdst + p.gq_off + t * kbytes, reinterpret_cast<const uint8_t*>(p.q) + qrow * kbytes,
                             kbytes, gbar);
               }
@@ -707,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * rbytes, rv, (uint32_t)(c - n1) * rbytes, sbar);
         }
         for (int t = 0; t < nnew; ++t) {
-          const size_t nrow = (MODE == kVerify) ? ((size_t)b * p.T + t) * p.H + hh : hrow;
+          const size_t nrow = kDrafts ? ((size_t)b * p.T + t) * p.H + hh : hrow;
           cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
           tma_load_1d(sdst + lay.sv_off + (c + t) * rbytes, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes,
                       rbytes, sbar);
@@ -821,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           sc[kCoefOff + t * kRMax + lane] = (lane < ht) ? w * skq_w[t * kRMax + lane] : 0.f;
           if (lane == 0) sc[t] = incl;
         }
-      } else {
+      } else if constexpr (MODE != kSnap) {
         const float incl = suffix_prod(aj, lane);
         const float nxt = __shfl_down_sync(kFull, incl, 1);
         const float wj = (lane < 31) ? nxt : 1.f;  // lane j: weight g_{j+2:J} of record j
@@ -1070,6 +1082,49 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                 if ((lane & (D - 1)) == 0 && row < p.P && t < p.T)
                   p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = part[i];
               }
+            }
+          }
+        }
+      } else if constexpr (MODE == kSnap) {
+        // ================================================ conventional verify with snapshots
+        // x <- a_t x + v_t[row] k_t ; o_t = x q_t ; x -> state slot (st + 1 + t) mod nslot,
+        // for t = 0 .. T-1: one read of the state, T writes.
+        const float* sa = reinterpret_cast<const float*>(slot);  // new records' decays at kRMax + t
+        for (int pass = 0; pass < npass; ++pass) {
+          const int rbase = (pass * wpg + wr) * kKR;
+          if (rbase * RPI >= p.P) break;  // warp-uniform: no rows left for this warp
+          float4 x[kKR];
+#pragma unroll
+          for (int kk = 0; kk < kKR; ++kk) {
+            const int row = (rbase + kk) * RPI + rsub;
+            x[kk] = (row < p.P) ? lds4(tf + ((size_t)row * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int t = 0; t < p.T; ++t) {
+            const float at = sa[kRMax + t];
+            const float4 kt = In<TIn>::lds4(gK, t * N + col4 * 4);
+            const float4 qt = In<TIn>::lds4(gQ, t * N + col4 * 4);
+            const int slot_t = (st + 1 + t) % p.nslot;
+            float* dst = p.ckpt + ((size_t)slot_t * p.B * p.H + hrow) * p.P * N;
+            float part[kKR];
+#pragma unroll
+            for (int kk = 0; kk < kKR; ++kk) {
+              const int row = (rbase + kk) * RPI + rsub;
+              const float vt = (row < p.P) ? In<TIn>::lds(sv, t * p.P + row) : 0.f;
+              x[kk].x = fmaf(vt, kt.x, at * x[kk].x);
+              x[kk].y = fmaf(vt, kt.y, at * x[kk].y);
+              x[kk].z = fmaf(vt, kt.z, at * x[kk].z);
+              x[kk].w = fmaf(vt, kt.w, at * x[kk].w);
+              if (row < p.P) *reinterpret_cast<float4*>(dst + (size_t)row * N + col4 * 4) = x[kk];
+              part[kk] = dot4(x[kk], qt);
+            }
+            int off = 0;
+            TRed<kKR, LPR / 2>::run(part, lane, off);
+            constexpr int KF = (kKR / LPR) > 0 ? (kKR / LPR) : 1;
+            constexpr int D = (LPR / kKR) > 0 ? (LPR / kKR) : 1;
+#pragma unroll
+            for (int i = 0; i < KF; ++i) {
+              const int row = (rbase + off + i) * RPI + rsub;
+              if ((lane & (D - 1)) == 0 && row < p.P) p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = part[i];
             }
           }
         }

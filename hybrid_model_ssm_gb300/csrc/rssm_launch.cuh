@@ -54,5 +54,8 @@ cudaError_t launch_conv(const Params& p, int grid, size_t smem, cudaStream_t st,
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t st);
 cudaError_t launch_commit(int B, int T, int R, const int32_t* accepted, int32_t* count, uint32_t* err,
                           cudaStream_t st);
+cudaError_t launch_snap(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
+cudaError_t launch_snap_commit(int B, int T, int nslot, const int32_t* accepted, int32_t* cur, uint32_t* err,
+                               cudaStream_t st);
 
 }  // namespace rssm

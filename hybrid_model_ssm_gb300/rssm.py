@@ -54,6 +54,8 @@ SIGNATURES = {
     "rssm_destroy": [_vp],
     "rssm_last_error": [],
     "rssm_conventional_step": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_conventional_verify": [_Cfg_p, _vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_conventional_commit": [_Cfg_p, _vp, _vp, ctypes.c_int32, _vp, _vp],
 }
 
 
@@ -263,3 +265,55 @@ def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream
     _check(lib().rssm_conventional_step(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(v), _ptr(k), _ptr(q),
                                         _ptr(out), _stream_ptr(stream)))
     return out
+
+
+class ConventionalVerifier:
+    """Comparison path: conventional speculative verify with per-draft state snapshots.
+
+    The state of every sequence sits in one of T_max + 1 slots of ``states``
+    ([T_max + 1, B, H, P, N] fp32, allocated here; slot 0 starts as ``state0``).
+    ``verify`` advances the full state through the T drafts and writes a snapshot
+    after each (one state read, T writes); ``commit`` points each sequence at the
+    snapshot after its accepted drafts. ``err`` is the device error word.
+    """
+
+    def __init__(self, shape: LayerShape, state0: torch.Tensor):
+        s = shape
+        _expect(state0, (s.B, s.H, s.P, s.N), torch.float32, "state0")
+        self.shape = shape
+        self.nslot = s.T_max + 1
+        self.states = torch.empty((self.nslot, s.B, s.H, s.P, s.N), dtype=torch.float32, device=state0.device)
+        self.states[0].copy_(state0)
+        self.cur = torch.zeros(s.B, dtype=torch.int32, device=state0.device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=state0.device)
+        self._cfg = s.config()
+        self._last_T = 0
+
+    def verify(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+        s = self.shape
+        T = alpha.shape[1]
+        _expect(alpha, (s.B, T, s.H), torch.float32, "alpha")
+        _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v")
+        _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k")
+        _expect(q, (s.B, T, s.G, s.N), s.torch_in_dtype, "q")
+        if out is None:
+            out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=alpha.device)
+        _expect(out, (s.B, T, s.H, s.P), torch.float32, "out")
+        _check(lib().rssm_conventional_verify(ctypes.byref(self._cfg), _ptr(self.states), _ptr(self.cur), T,
+                                              _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out), _ptr(self.err),
+                                              _stream_ptr(stream)))
+        self._last_T = T
+        return out
+
+    def commit(self, accepted: torch.Tensor, stream=None):
+        _expect(accepted, (self.shape.B,), torch.int32, "accepted")
+        if self._last_T < 1:
+            raise ValueError("commit without a pending verify")
+        _check(lib().rssm_conventional_commit(ctypes.byref(self._cfg), _ptr(self.cur), _ptr(accepted), self._last_T,
+                                              _ptr(self.err), _stream_ptr(stream)))
+        self._last_T = 0
+
+    def state(self) -> torch.Tensor:
+        """The committed state [B,H,P,N] (gathered from each sequence's slot; a copy)."""
+        idx = self.cur.long()
+        return self.states[idx, torch.arange(self.shape.B, device=idx.device)]

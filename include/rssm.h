@@ -212,6 +212,33 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
                                    const void* v, const void* k, const void* q, float* o,
                                    void* stream);
 
+/* Comparison kernels (not part of the replay path): conventional speculative
+ * verify with per-draft state snapshots, the rollback scheme the replay design
+ * replaces (aikraft.ru page §02 and §05; sitech.ge page, traffic and rollback
+ * section). Each sequence's state lives in one of nslot = T_max + 1 slots.
+ *
+ * rssm_conventional_verify: for t = 0 .. T-1, S <- alpha_t S + v_t k_t^T,
+ * o[b,t] = S q_t, and S is written to slot (cur[b] + 1 + t) mod nslot. The state
+ * is read once and written T times; slot cur[b] is left as it was.
+ *  - states: [nslot][B,H,P,N] fp32, device, caller-owned, 16-byte aligned.
+ *  - cur: [B] int32 device, the slot of each sequence's state (caller
+ *    initialises it, e.g. to 0). A value outside 0..nslot-1 skips the sequence
+ *    and sets bit 1 in *err_word.
+ *  - alpha [B,T,H] fp32; v [B,T,H,P], k and q [B,T,G,N] in cfg->in_dtype;
+ *    o [B,T,H,P] fp32 (the layouts of rssm_verify).
+ *  - err_word: one uint32 in device memory (bit 1 as above).
+ *  - 1 <= T <= cfg->T_max, else RSSM_EINVAL. cfg->L and read_fmt are ignored.
+ * rssm_conventional_commit: cur[b] <- (cur[b] + accepted[b]) mod nslot, which
+ * selects the snapshot after the accepted drafts (accepted[b] = 0 keeps the
+ * state). accepted[b] outside 0..T, or cur[b] outside 0..nslot-1, leaves the
+ * sequence alone and sets bit 2 in *err_word. Both calls are asynchronous on
+ * `stream`. */
+rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, const int32_t* cur, int32_t T,
+                                     const float* alpha, const void* v, const void* k, const void* q,
+                                     float* o, uint32_t* err_word, void* stream);
+rssm_status rssm_conventional_commit(const rssm_config* cfg, int32_t* cur, const int32_t* accepted, int32_t T,
+                                     uint32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
