@@ -18,10 +18,12 @@ Sources. Citations give the page and its section:
        section "方法/产品要点" (core representation, two step kinds,
        output-only evaluation formula).
 Format definitions for the quantizers come from the OCP 8-bit floating point
-specification (E4M3) and the OCP Microscaling specification (E2M1).
+specification (E4M3) and the OCP Microscaling specification (E2M1). The
+stochastic rounding of the FP16 checkpoint draws from Philox4x32-10 (Salmon et
+al., SC'11), written from its published definition.
 
-Each function here is pinned by ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_quant.py`` to something other than itself: closed forms,
+Each function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_oracle_quant.py`` and ``tests/test_oracle_sround.py`` to something other than itself: closed forms,
 hand-computed golden cases, brute force, library conversions and
 invariants. No function is left with unpinned parity.
 """
@@ -47,4 +49,12 @@ from .quant import (  # noqa: F401
     dequantize_rows_e2m1,
     element_error_bound,
     FullyQuantizedState,
+)
+from .sround import (  # noqa: F401
+    philox4x32_10,
+    sr_words,
+    stochastic_round_f16,
+    nearest_f16,
+    f16_toward_zero,
+    ReplayOracleF16,
 )
