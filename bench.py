@@ -65,17 +65,18 @@ def copy_bytes_per_head(s, read_fmt) -> int:
     return -(-(rsc + 4 * P) // 16) * 16
 
 
-def window_bytes(s, read_fmt=None) -> dict:
+def window_bytes(s, read_fmt=None, ckpt_bytes: int = 4) -> dict:
     """Algorithmic HBM bytes of one sequence over one window of L decode steps.
 
     Every step reads its inputs (record + q) and writes its output. Step t of
     the window (t = 0..L-1) also reads the t buffered records, and every
     non-flush step appends its record. The L-1 non-flush steps each read the
     checkpoint |S|, or its read copy |C| when there is one. The flush step
-    reads |S| and writes it once, plus the refreshed copy.
+    reads |S| and writes it once, plus the refreshed copy. ckpt_bytes is the
+    checkpoint's element size (2 for an FP16 checkpoint).
     """
     es = 2 if s.in_dtype == "bf16" else 4
-    S = 4 * s.H * s.P * s.N
+    S = ckpt_bytes * s.H * s.P * s.N
     C = s.H * copy_bytes_per_head(s, read_fmt)
     r = record_bytes(s)
     inp = r + es * s.G * s.N
@@ -83,7 +84,7 @@ def window_bytes(s, read_fmt=None) -> dict:
     L = s.L
     reads = (L - 1) * (C if read_fmt else S) + S
     total = reads + S + C + r * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * r
-    conv = L * (2 * S + inp + out)
+    conv = L * (2 * 4 * s.H * s.P * s.N + inp + out)
     return {"replay_window": total, "replay_per_seq_step": total / L, "conventional_per_seq_step": conv / L,
             "state": S}
 
@@ -239,13 +240,14 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     s = WORKLOAD if args.batch is None else WORKLOAD.with_(B=args.batch)
-    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype, read_fmt=args.read_fmt)
+    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype, read_fmt=args.read_fmt,
+                    ckpt=args.ckpt, seed=s.seed)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev)
     gen.manual_seed(s.seed + 1000 * rank)
     ckpt = (torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev, dtype=torch.float32) * 0.1)
-    model = ReplaySSM(ls, ckpt)
+    model = ReplaySSM(ls, ckpt.to(ls.torch_ckpt_dtype))
     pool = []
     sc = 1.0 / math.sqrt(s.N)
     for _ in range(16):  # 16 resident steps of inputs, cycled
@@ -297,7 +299,8 @@ def run_ours(args, world, rank, local):
     seq_steps = world * s.B * L * args.steps
     value = seq_steps / elapsed_max
     mean_launch = sum(launch_s) / len(launch_s)
-    wb = window_bytes(s, args.read_fmt)
+    ckpt_es = 4 if args.ckpt == "f32" else 2
+    wb = window_bytes(s, args.read_fmt, ckpt_es)
     alg_bytes_launch = wb["replay_per_seq_step"] * s.B
     achieved = alg_bytes_launch / mean_launch / 1e9
     peak, peak_kind = measured_peak_gbs()
@@ -329,7 +332,7 @@ def run_ours(args, world, rank, local):
         comp = {"conventional_seq_steps_per_s": conv_value,
                 "conventional_hbm_gbs": conv_bytes / conv_t / 1e9,
                 "replay_speedup": value / world / conv_value,
-                "replay_state_bytes_per_window_over_conventional": (L + 1) / (2 * L),
+                "replay_state_bytes_per_window_over_conventional": (L + 1) / (2 * L) * ckpt_es / 4,
                 "windows_timed": n_conv}
         del state
 
@@ -368,7 +371,8 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.ckpt == "f32" else "f32 (fp16 checkpoint)",
+        "data": "synthetic",
         "config": {"workload": f"ReplaySSM decode, one Mamba-2-shaped layer: B={s.B} H={s.H} P={s.P} N={s.N} "
                                f"G={s.G} L={L}, bf16 v/k/q, fp32 checkpoint and outputs; one step = one window "
                                f"of {L} decode launches ({L - 1} non-flush + 1 flush)",
@@ -712,6 +716,8 @@ def main(argv=None):
     ap.add_argument("--windows", default="4,8,16,32", help="multilayer: windows L")
     ap.add_argument("--read-fmt", choices=["e4m3", "e2m1"], default=None,
                     help="non-flush steps read a low-precision copy of the checkpoint")
+    ap.add_argument("--ckpt", choices=["f32", "f16_sr", "f16_rn"], default="f32",
+                    help="checkpoint storage: FP32, or FP16 stored with stochastic / nearest rounding")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -11,6 +11,7 @@ from .rssm import (  # noqa: F401
     RssmError,
     conventional_step,
     read_copy_layout,
+    round_f16,
     ring_offsets,
     workspace_size,
     lib,

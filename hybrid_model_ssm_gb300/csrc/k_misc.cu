@@ -33,4 +33,35 @@ cudaError_t launch_conv(const Params& p, int grid, size_t smem, cudaStream_t st,
   return dtype == 0 ? dispatch_n<kConv, float>(p, grid, smem, st, N, kRfNone)
                     : dispatch_n<kConv, __nv_bfloat16>(p, grid, smem, st, N, kRfNone);
 }
+// Test support: the checkpoint store's binary32 -> binary16 rounding applied to
+// x[0..n), element i taking word (i % 4) of the generator call for element
+// group (base + i) / 4 at the given epoch (base a multiple of 4).
+__global__ void sround_test_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, long long n, long long base,
+                                   uint32_t epoch, unsigned long long seed, int sr) {
+  const long long g4 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (g4 >= n) return;
+  const unsigned long long grp = (unsigned long long)(base + g4) >> 2;
+  const uint4 w = philox4x32_10(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), epoch, 0u),
+                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  float xv[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) xv[e] = (g4 + e < n) ? x[g4 + e] : 0.f;
+  // the same two paths as the fold's store
+  const uint32_t h01 = sr ? ((uint32_t)to_f16_bits(xv[0], ww[0], true) | ((uint32_t)to_f16_bits(xv[1], ww[1], true) << 16))
+                          : rn_f16x2_sat(xv[0], xv[1]);
+  const uint32_t h23 = sr ? ((uint32_t)to_f16_bits(xv[2], ww[2], true) | ((uint32_t)to_f16_bits(xv[3], ww[3], true) << 16))
+                          : rn_f16x2_sat(xv[2], xv[3]);
+  const uint16_t hv[4] = {(uint16_t)h01, (uint16_t)(h01 >> 16), (uint16_t)h23, (uint16_t)(h23 >> 16)};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (g4 + e < n) y[g4 + e] = hv[e];
+}
+cudaError_t launch_sround_test(const float* x, uint16_t* y, long long n, long long base, uint32_t epoch,
+                               unsigned long long seed, int sr, cudaStream_t st) {
+  const long long groups = (n + 3) / 4;
+  const int threads = 256;
+  sround_test_kernel<<<(unsigned)((groups + threads - 1) / threads), threads, 0, st>>>(x, y, n, base, epoch, seed, sr);
+  return cudaGetLastError();
+}
 }  // namespace rssm

@@ -16,9 +16,9 @@ __global__ void commit_kernel(int B, int T, int R, const int32_t* __restrict__ a
   count[b] = c + a;
 }
 
-cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype) {
-  return dtype == 0 ? dispatch_n<kVerify, float>(p, grid, smem, st, N, kRfNone)
-                    : dispatch_n<kVerify, __nv_bfloat16>(p, grid, smem, st, N, kRfNone);
+cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf) {
+  return dtype == 0 ? dispatch_n<kVerify, float>(p, grid, smem, st, N, rf)
+                    : dispatch_n<kVerify, __nv_bfloat16>(p, grid, smem, st, N, rf);
 }
 cudaError_t launch_commit(int B, int T, int R, const int32_t* accepted, int32_t* count, uint32_t* err,
                           cudaStream_t st) {

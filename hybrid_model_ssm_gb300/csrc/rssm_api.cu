@@ -39,9 +39,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Geom {
-  int R = 0, Rp = 0, esize = 0;
+  int R = 0, Rp = 0, esize = 0, ck_es = 4, rf = 0;  // ck_es: checkpoint bytes per element; rf: tile format
   size_t v_off = 0, k_off = 0, ring_bytes = 0;
-  size_t off_count = 0, off_ticket = 0, off_err = 0, ptr_bytes = 0;
+  size_t off_count = 0, off_ticket = 0, off_err = 0, off_epoch = 0, ptr_bytes = 0;
   size_t head_stride = 0, bsc_off = 0, rsc_off = 0, copy_bytes = 0;
 };
 
@@ -65,10 +65,15 @@ rssm_status derive(const rssm_config* c, Geom* g) {
   if (R > rssm::kRMax) return fail(RSSM_EUNSUPPORTED, "R = L + T_max - 1 = %d > %d", R, rssm::kRMax);
   if (c->read_fmt != RSSM_READ_NONE && c->N < 64)
     return fail(RSSM_EUNSUPPORTED, "read copies need N in {64, 128}");
+  if (c->ckpt_fmt < RSSM_CKPT_F32 || c->ckpt_fmt > RSSM_CKPT_F16_RN) return fail(RSSM_EINVAL, "ckpt_fmt %d", c->ckpt_fmt);
+  if (c->ckpt_fmt != RSSM_CKPT_F32 && (c->N < 64 || c->read_fmt != RSSM_READ_NONE))
+    return fail(RSSM_EUNSUPPORTED, "an FP16 checkpoint needs N in {64, 128} and no read copy");
   if ((long long)c->B * c->H > (1ll << 30)) return fail(RSSM_EUNSUPPORTED, "B*H too large");
   g->R = R;
   g->Rp = (R + 3) / 4 * 4;
   g->esize = c->in_dtype == RSSM_F32 ? 4 : 2;
+  g->ck_es = c->ckpt_fmt == RSSM_CKPT_F32 ? 4 : 2;
+  g->rf = c->ckpt_fmt != RSSM_CKPT_F32 ? (int)rssm::kCkF16 : c->read_fmt;
   const size_t B = c->B, H = c->H, P = c->P, N = c->N, G = c->G;
   const size_t a_bytes = B * H * g->Rp * 4;
   g->v_off = align_up(a_bytes, 256);
@@ -78,7 +83,8 @@ rssm_status derive(const rssm_config* c, Geom* g) {
   g->off_count = pb;
   g->off_ticket = 2 * pb;
   g->off_err = 3 * pb;
-  g->ptr_bytes = 3 * pb + 256;
+  g->off_epoch = 3 * pb + 256;
+  g->ptr_bytes = 4 * pb + 256;
   if (c->read_fmt == RSSM_READ_E4M3_ROW) {
     g->bsc_off = P * N;
     g->rsc_off = P * N;
@@ -112,7 +118,7 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   auto a128 = [](size_t x) { return align_up(x, 128); };
   const bool nf = kind == LayoutKind::kNonFlush;
   const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
-  const size_t tile = a128(nf && g.head_stride ? g.head_stride : P * N * 4);
+  const size_t tile = a128(nf && g.head_stride ? g.head_stride : P * N * (size_t)g.ck_es);
   const size_t vrows = nf ? (size_t)c->L : R;
   const size_t sv_off = (size_t)(kRMax + kTMax) * 4;  // decays: kRMax ring slots, then kTMax new records
   const size_t sc_off = align_up(sv_off + vrows * P * es, 16);
@@ -208,7 +214,7 @@ int sm_count() {
 struct rssm_ctx {
   rssm_config cfg;
   Geom g;
-  float* ckpt;
+  void* ckpt;  // fp32 or fp16 [B,H,P,N]
   uint8_t* ring;
   uint8_t* ptrs;
   uint8_t* copy;
@@ -221,7 +227,7 @@ void fill_common(const rssm_ctx* h, rssm::Params* p) {
   const rssm_config& c = h->cfg;
   p->B = c.B; p->H = c.H; p->P = c.P; p->N = c.N; p->G = c.G; p->L = c.L;
   p->R = h->g.R; p->Rp = h->g.Rp; p->HPG = c.H / c.G; p->T = 1; p->min_count = 1;
-  p->ckpt = h->ckpt;
+  p->ckpt = static_cast<float*>(h->ckpt);  // the kernels read fp16 checkpoints through byte offsets
   p->copy = h->copy;
   p->head_stride = (int)h->g.head_stride;
   p->bsc_off = (int)h->g.bsc_off;
@@ -233,6 +239,9 @@ void fill_common(const rssm_ctx* h, rssm::Params* p) {
   p->count = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_count);
   p->ticket = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_ticket);
   p->err = reinterpret_cast<uint32_t*>(h->ptrs + h->g.off_err);
+  p->epoch = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_epoch);
+  p->seed = c.seed;
+  p->sr = c.ckpt_fmt == RSSM_CKPT_F16_SR ? 1 : 0;
 }
 
 int persistent_grid(long long heads) {
@@ -278,7 +287,7 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
   return RSSM_OK;
 }
 
-rssm_status rssm_create(const rssm_config* cfg, float* ckpt, void* ring, void* ptrs, void* read_copy,
+rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* ptrs, void* read_copy,
                         void* stream, rssm_handle* out) {
   if (!out) return fail(RSSM_EINVAL, "out is NULL");
   *out = nullptr;
@@ -294,7 +303,7 @@ rssm_status rssm_create(const rssm_config* cfg, float* ckpt, void* ring, void* p
   if (!h) return fail(RSSM_EINVAL, "out of host memory");
   h->cfg = *cfg;
   h->g = g;
-  h->ckpt = ckpt;
+  h->ckpt = ckpt;  // fp32 or fp16
   h->ring = static_cast<uint8_t*>(ring);
   h->ptrs = static_cast<uint8_t*>(ptrs);
   h->copy = cfg->read_fmt != RSSM_READ_NONE ? static_cast<uint8_t*>(read_copy) : nullptr;
@@ -337,7 +346,7 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
   pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
   const long long heads = (long long)h->cfg.B * h->cfg.H;
   const cudaError_t e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
-                                            h->cfg.N, h->cfg.in_dtype, h->cfg.read_fmt);
+                                            h->cfg.N, h->cfg.in_dtype, h->g.rf);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   h->last_T = 0;
   return RSSM_OK;
@@ -357,8 +366,10 @@ rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void
   pl.p.T = T;
   pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
   const long long heads = (long long)h->cfg.B * h->cfg.H;
+  // verify reads the checkpoint itself, never a read copy
+  const int vrf = h->g.rf == rssm::kCkF16 ? (int)rssm::kCkF16 : (int)rssm::kRfNone;
   const cudaError_t e = rssm::launch_verify(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
-                                            h->cfg.N, h->cfg.in_dtype);
+                                            h->cfg.N, h->cfg.in_dtype, vrf);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   h->last_T = T;
   return RSSM_OK;
@@ -388,7 +399,7 @@ rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream) {
   // one CTA per (sequence, group): CTAs of sequences that do not flush exit at once
   const int grid = h->cfg.B * h->cfg.G;
   const cudaError_t e = rssm::launch_flush(pl.p, grid, pl.smem, static_cast<cudaStream_t>(stream), h->cfg.N,
-                                           h->cfg.in_dtype, h->cfg.read_fmt);
+                                           h->cfg.in_dtype, h->g.rf);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   h->last_T = 0;
   return RSSM_OK;
@@ -439,6 +450,8 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
   Geom g;
   rssm_status s = derive(cfg, &g);
   if (s != RSSM_OK) return s;
+  g.ck_es = 4;  // the comparison keeps an fp32 state
+  g.rf = rssm::kRfNone;
   if (!state || !alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(state) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
@@ -463,6 +476,8 @@ rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, cons
   Geom g;
   rssm_status s = derive(cfg, &g);
   if (s != RSSM_OK) return s;
+  g.ck_es = 4;  // the comparison keeps fp32 states
+  g.rf = rssm::kRfNone;
   if (T < 1 || T > cfg->T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, cfg->T_max);
   if (!states || !cur || !alpha || !v || !k || !q || !o || !err_word) return fail(RSSM_EINVAL, "NULL pointer");
   if (!aligned16(states) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
@@ -495,6 +510,16 @@ rssm_status rssm_conventional_commit(const rssm_config* cfg, int32_t* cur, const
   const cudaError_t e = rssm::launch_snap_commit(cfg->B, T, cfg->T_max + 1, accepted, cur, err_word,
                                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "conventional commit launch");
+  return RSSM_OK;
+}
+
+rssm_status rssm_round_f16(const float* x, uint16_t* y, int64_t n, int64_t base, uint32_t epoch, uint64_t seed,
+                           int32_t sr, void* stream) {
+  if (n < 0 || base < 0 || (base & 3) != 0) return fail(RSSM_EINVAL, "n=%lld base=%lld", (long long)n, (long long)base);
+  if (n == 0) return RSSM_OK;
+  if (!x || !y) return fail(RSSM_EINVAL, "NULL pointer");
+  const cudaError_t e = rssm::launch_sround_test(x, y, n, base, epoch, seed, sr, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "round launch");
   return RSSM_OK;
 }
 
@@ -555,7 +580,7 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
   e = cudaMemsetAsync(tickets, 0, (size_t)h->cfg.B * sizeof(int32_t), st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static tickets)");
   const long long heads = (long long)h->cfg.B * h->cfg.H;
-  e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, st, h->cfg.N, h->cfg.in_dtype, h->cfg.read_fmt);
+  e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, st, h->cfg.N, h->cfg.in_dtype, h->g.rf);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");
   h->last_T = 0;
   return RSSM_OK;

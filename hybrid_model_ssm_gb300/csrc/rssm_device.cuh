@@ -59,7 +59,9 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr unsigned kFull = 0xffffffffu;
 
 enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4, kSnap = 5 };
-enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2 };
+// Storage formats of the head tile: the FP32 checkpoint (kRfNone), an E4M3 or
+// E2M1 read copy next to it, or an FP16 checkpoint (kCkF16: no read copy).
+enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2, kCkF16 = 3 };
 enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u, kErrPlan = 8u };
 
 // One partition of a CTA's shared memory into tile stages and record slots.
@@ -79,6 +81,9 @@ struct Params {
   int32_t* start;      // [B]
   int32_t* count;      // [B]
   int32_t* ticket;     // [B], zero between launches
+  int32_t* epoch;      // [B] flushes so far (FP16 checkpoint: part of the rounding counter)
+  unsigned long long seed;  // FP16 checkpoint: generator key
+  int sr;              // FP16 checkpoint: 1 stochastic rounding, 0 round to nearest
   const int32_t* cur;  // kSnap: [B] slot holding each sequence's state
   int nslot;           // kSnap: state slots (T_max + 1)
   uint32_t* err;       // error word
@@ -467,6 +472,67 @@ __device__ __forceinline__ void quantize_rows(const float4 (&x)[KR], int lane, i
   }
 }
 
+// ------------------------------------------------------------ FP16 checkpoint
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC'11): per round the 64-bit products of c0 and
+// c2 with the two multipliers are split into halves and mixed with c1, c3 and
+// the key; the key advances by the Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+// binary32 -> binary16 bits. Stochastic (sr): with lo = x rounded toward zero
+// and hi the next binary16 away from zero, hi is taken when r < floor(frac 2^32),
+// frac = (|x| - |lo|) / (|hi| - |lo|) (exact in binary32); otherwise round to
+// nearest even. Both saturate to +-65504 and keep the sign; NaN gives 0x7E00.
+__device__ __forceinline__ uint16_t to_f16_bits(float x, uint32_t r, bool sr) {
+  const float ax = fabsf(x);
+  const uint16_t sign = (uint16_t)((__float_as_uint(x) >> 16) & 0x8000u);
+  if (!(ax == ax)) return 0x7E00u;
+  if (ax >= 65504.f) return sign | 0x7BFFu;
+  uint16_t mag;
+  if (sr) {
+    const uint16_t lo = __half_as_ushort(__float2half_rz(ax));
+    const float lo_f = __half2float(__ushort_as_half(lo));
+    // the binary16 spacing above lo is 2^(max(E, 1) - 25), E = lo's exponent field, so
+    // frac 2^32 = (|x| - lo) 2^(57 - max(E, 1)): an exact power-of-two scaling
+    const uint32_t e16 = max((uint32_t)(lo >> 10), 1u);
+    const float scale = __uint_as_float((57u - e16 + 127u) << 23);
+    const uint32_t t = __float2uint_rz((ax - lo_f) * scale);  // floor(frac 2^32), exact
+    mag = (r < t) ? (uint16_t)(lo + 1) : lo;
+  } else {
+    mag = __half_as_ushort(__float2half_rn(ax));
+    if (mag > 0x7BFFu) mag = 0x7BFFu;
+  }
+  return sign | mag;
+}
+// Two binary32 values -> binary16x2 (lo in the low half), round to nearest even,
+// saturating to +-65504 (the round-to-nearest store, two elements per instruction).
+__device__ __forceinline__ uint32_t rn_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Four consecutive checkpoint elements as float4, from an FP32 or FP16 tile.
+template <bool F16>
+__device__ __forceinline__ float4 ld_tile4(const uint8_t* tile, size_t e) {
+  if constexpr (F16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(tile + e * 2);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return *reinterpret_cast<const float4*>(tile + e * 4);
+  }
+}
+
 // ============================================================================
 // The head kernel.
 // ============================================================================
@@ -495,6 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr bool kGroupData = (MODE != kQuant);
   constexpr bool kQuery = (MODE == kDecode || MODE == kVerify || MODE == kConv || MODE == kSnap);
   constexpr bool kDrafts = (MODE == kVerify || MODE == kSnap);  // inputs carry a draft axis [B,T,...]
+  constexpr bool kCopyRF = (RF == kRfE4m3 || RF == kRfE2m1);    // a low-precision read copy exists
+  constexpr bool kF16 = (RF == kCkF16);                          // the checkpoint itself is FP16
+  constexpr int CKES = kF16 ? 2 : 4;                             // checkpoint bytes per element
   constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -631,12 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         }
         if (!load) continue;
         if (li >= lay.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
-        const bool from_copy = (RF != kRfNone) && (MODE == kDecode) && !flush;
+        const bool from_copy = kCopyRF && (MODE == kDecode) && !flush;
         size_t srow = (size_t)gh;  // kSnap: the head's row in the sequence's current state slot
         if constexpr (MODE == kSnap) srow += (size_t)st * ((size_t)p.B * p.H);
         const void* src = from_copy ? (const void*)(p.copy + (size_t)gh * p.head_stride)
-                                    : (const void*)(p.ckpt + srow * p.P * N);
-        const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)p.P * N * 4;
+                                    : (const void*)(reinterpret_cast<const uint8_t*>(p.ckpt) + srow * p.P * N * CKES);
+        const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)(p.P * N * CKES);
         mbar_arrive_tx(tfull0 + 8 * ts, bytes);
         tma_load_1d(smem_u32(smem + (size_t)ts * lay.stage_bytes), src, bytes, tfull0 + 8 * ts);
         tile_next();
@@ -888,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     int gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
     long long cur_gg = -1;
     bool load = false, flush = false, bad = false;
+    int ep = 0;  // FP16 checkpoint: the sequence's flush epoch (rounding counter)
     const uint8_t* gK = smem + p.gb_off;
     const uint8_t* gQ = gK + p.gq_off;
     float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -895,11 +965,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     constexpr int LPRc = (N / CPL) > 0 ? (N / CPL) : 1;
     constexpr int RPIc = 32 / LPRc;
     constexpr int KRc = (kKR * 4 / CPL) > 0 ? (kKR * 4 / CPL) : 1;
-    float qc[(RF != kRfNone && MODE == kDecode) ? CPL : 1];
+    float qc[(kCopyRF && MODE == kDecode) ? CPL : 1];
     // FP32 non-flush rows (N >= 64): LP16 lanes per row, 16 columns per lane as
     // 4 chunks of 4 interleaved over the row's lanes (each quarter warp reads
     // 128 contiguous bytes: no bank conflicts); q16 holds the matching q values.
-    constexpr bool kWideRows = (RF == kRfNone && MODE == kDecode && N >= 64);
+    constexpr bool kWideRows = ((RF == kRfNone || kF16) && MODE == kDecode && N >= 64);
     constexpr int LP16 = kWideRows ? N / 16 : 1;
     float q16[kWideRows ? 16 : 1];
     const int wpg = kNDW / lay.dgroups;                 // warps per dot group
@@ -918,6 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         seq_plan(b, c, st, load, flush, bad);
         J = records(c);
         cur_gg = -1;
+        if constexpr (kF16) ep = p.epoch[b];
       }
       if (!load) continue;
       if constexpr (kGroupData) {
@@ -932,14 +1003,25 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           gK = smem + p.gb_off + gs * p.gb_bytes;
           gQ = gK + p.gq_off;
           if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
-          if constexpr (kWideRows) {
+          if constexpr (kWideRows && !kF16) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const float4 qq = In<TIn>::lds4(gQ, (c * LP16 + lane % LP16) * 4);
               q16[4 * c] = qq.x; q16[4 * c + 1] = qq.y; q16[4 * c + 2] = qq.z; q16[4 * c + 3] = qq.w;
             }
           }
-          if constexpr (RF != kRfNone && MODE == kDecode) {
+          if constexpr (kWideRows && kF16) {  // two chunks of 8 halves per lane
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+              for (int hq = 0; hq < 2; ++hq) {
+                const float4 qq = In<TIn>::lds4(gQ, (c * LP16 + lane % LP16) * 8 + 4 * hq);
+                q16[8 * c + 4 * hq] = qq.x; q16[8 * c + 4 * hq + 1] = qq.y;
+                q16[8 * c + 4 * hq + 2] = qq.z; q16[8 * c + 4 * hq + 3] = qq.w;
+              }
+            }
+          }
+          if constexpr (kCopyRF && MODE == kDecode) {
 #pragma unroll
             for (int i = 0; i < CPL; ++i) qc[i] = In<TIn>::lds(gQ, (lane % LPRc) * CPL + i);
           }
@@ -969,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         // add their share to the scaled dot before the row reduction, so the value
         // term costs no shuffles. w_tj = 0 for records that query t does not see.
         const float* cw = sc + kCoefOff;  // [kTMax][kRMax]
-        if constexpr (N >= 64) {
+        if constexpr (N >= 64 && !kF16) {
           // LPV lanes per row, 16 columns per lane in 4 interleaved chunks (as the
           // wide non-flush rows); KWV row instructions x kTQ queries per pass.
           constexpr int LPV = N / 16, RPW = 32 / LPV, KWV = 2, JI = kRMax / LPV;
@@ -1059,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               for (int kk = 0; kk < kKR; ++kk) {
                 const int row = (rbase + kk) * RPI + rsub;
                 const float4 x4 =
-                    (row < p.P) ? lds4(tf + ((size_t)row * LPR + col4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    (row < p.P) ? ld_tile4<kF16>(tile, (size_t)row * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int t = 0; t < kTQ; ++t) part[kk * kTQ + t] = g[t] * dot4(x4, qv[t]);
                 if (row < p.P) {
@@ -1143,8 +1225,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             f32x2 A[kKR / 2][4];
 #pragma unroll
             for (int kp = 0; kp < kKR / 2; ++kp) {
-              const float4 x0 = lds4(tf + ((size_t)(rbase + 2 * kp) * LPR + col4) * 4);
-              const float4 x1 = lds4(tf + ((size_t)(rbase + 2 * kp + 1) * LPR + col4) * 4);
+              const float4 x0 = ld_tile4<kF16>(tile, (size_t)(rbase + 2 * kp) * N + col4 * 4);
+              const float4 x1 = ld_tile4<kF16>(tile, (size_t)(rbase + 2 * kp + 1) * N + col4 * 4);
               A[kp][0] = pk2(gam * x0.x, gam * x1.x);
               A[kp][1] = pk2(gam * x0.y, gam * x1.y);
               A[kp][2] = pk2(gam * x0.z, gam * x1.z);
@@ -1179,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             for (int kk = 0; kk < kKR; ++kk) {
               const int row = (rbase + kk) * RPI + rsub;
               if (row < p.P) {
-                const float4 x = lds4(tf + ((size_t)row * LPR + col4) * 4);
+                const float4 x = ld_tile4<kF16>(tile, (size_t)row * N + col4 * 4);
                 acc[kk] = make_float4(gam * x.x, gam * x.y, gam * x.z, gam * x.w);
               } else {
                 acc[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1206,10 +1288,29 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
               const int row = (rbase + kk) * RPI + rsub;
-              if (row < p.P) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
+              if constexpr (kF16) {
+                if (row < p.P) {
+                  // counter: (element group e / 4, epoch of this flush, 0); key: the seed
+                  const size_t e = (hrow * p.P + row) * N + col4 * 4;  // first of the four elements
+                  const size_t grp = e >> 2;
+                  uint32_t h01, h23;
+                  if (p.sr) {
+                    const uint4 w = philox4x32_10(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)ep, 0u),
+                                                  make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+                    h01 = (uint32_t)to_f16_bits(acc[kk].x, w.x, true) | ((uint32_t)to_f16_bits(acc[kk].y, w.y, true) << 16);
+                    h23 = (uint32_t)to_f16_bits(acc[kk].z, w.z, true) | ((uint32_t)to_f16_bits(acc[kk].w, w.w, true) << 16);
+                  } else {
+                    h01 = rn_f16x2_sat(acc[kk].x, acc[kk].y);
+                    h23 = rn_f16x2_sat(acc[kk].z, acc[kk].w);
+                  }
+                  *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.ckpt) + e * 2) = make_uint2(h01, h23);
+                }
+              } else {
+                if (row < p.P) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
+              }
             }
           }
-          if constexpr (RF != kRfNone && MODE != kConv) {
+          if constexpr (kCopyRF && MODE != kConv) {
             quantize_rows<RF, LPR, kKR>(acc, lane, rbase * RPI + rsub, RPI, p.P, N, p.copy + hrow * p.head_stride,
                                         p.bsc_off, p.rsc_off);
           }
@@ -1249,14 +1350,28 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               const int row = r0 + kk * RPW + rw;
               float a0 = 0.f, a1 = 0.f;
               if (row < p.P) {
-                const float* rp = tf + (size_t)row * N;
+                if constexpr (kF16) {  // two 16-byte chunks of 8 halves
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  const float4 x = lds4(rp + (c * LP16 + cl) * 4);
-                  a0 = fmaf(x.x, q16[4 * c], a0);
-                  a1 = fmaf(x.y, q16[4 * c + 1], a1);
-                  a0 = fmaf(x.z, q16[4 * c + 2], a0);
-                  a1 = fmaf(x.w, q16[4 * c + 3], a1);
+                  for (int c = 0; c < 2; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(tile + ((size_t)row * N + (c * LP16 + cl) * 8) * 2);
+                    const uint32_t hw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+                      a0 = fmaf(f.x, q16[8 * c + 2 * e], a0);
+                      a1 = fmaf(f.y, q16[8 * c + 2 * e + 1], a1);
+                    }
+                  }
+                } else {
+                  const float* rp = tf + (size_t)row * N;
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) {
+                    const float4 x = lds4(rp + (c * LP16 + cl) * 4);
+                    a0 = fmaf(x.x, q16[4 * c], a0);
+                    a1 = fmaf(x.y, q16[4 * c + 1], a1);
+                    a0 = fmaf(x.z, q16[4 * c + 2], a0);
+                    a1 = fmaf(x.w, q16[4 * c + 3], a1);
+                  }
                 }
                 a0 = gam * (a0 + a1);
 #pragma unroll
@@ -1275,7 +1390,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           }
         } else
         for (int pass = 0; pass < npass; ++pass) {
-          if constexpr (RF == kRfNone) {
+          if constexpr (!kCopyRF) {
             const int rbase = (pass * wpg + wr) * kKR;
             float part[kKR];
 #pragma unroll
@@ -1283,7 +1398,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               const int row = (rbase + kk) * RPI + rsub;
               float a = 0.f;
               if (row < p.P) {
-                a = gam * dot4(lds4(tf + ((size_t)row * LPR + col4) * 4), q4);
+                a = gam * dot4(ld_tile4<kF16>(tile, (size_t)row * N + col4 * 4), q4);
                 for (int j = col4; j < J; j += LPR) a = fmaf(scj[j], In<TIn>::lds(sv, j * p.P + row), a);
               }
               part[kk] = a;
@@ -1397,6 +1512,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           } else {
             p.start[b] = (st + c) % p.R;
             p.count[b] = 0;
+          }
+          if constexpr (kF16) {
+            if (MODE == kFlush || flush) p.epoch[b] += 1;
           }
           p.ticket[b] = 0;
         }

@@ -22,7 +22,8 @@ cudaError_t launch_one(const Params& p, int grid, size_t smem, cudaStream_t st) 
   return cudaGetLastError();
 }
 
-// N in {16,32,64,128}; dtype 0 = f32, 1 = bf16; rf 0/1/2 (1,2 only for N >= 64).
+// N in {16,32,64,128}; dtype 0 = f32, 1 = bf16; rf 0/1/2/3 (1, 2 and 3 only for N >= 64;
+// 3, the FP16 checkpoint, for decode, verify and flush).
 template <int MODE, typename TIn>
 cudaError_t dispatch_n(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf) {
   if (rf == kRfNone) {
@@ -43,11 +44,19 @@ cudaError_t dispatch_n(const Params& p, int grid, size_t smem, cudaStream_t st, 
       if (N == 128) return launch_one<MODE, 128, TIn, kRfE2m1>(p, grid, smem, st);
     }
   }
+  if constexpr (MODE == kDecode || MODE == kVerify || MODE == kFlush) {
+    if (rf == kCkF16) {
+      if (N == 64) return launch_one<MODE, 64, TIn, kCkF16>(p, grid, smem, st);
+      if (N == 128) return launch_one<MODE, 128, TIn, kCkF16>(p, grid, smem, st);
+    }
+  }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
-cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
+cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
+cudaError_t launch_sround_test(const float* x, uint16_t* y, long long n, long long base, uint32_t epoch,
+                               unsigned long long seed, int sr, cudaStream_t st);
 cudaError_t launch_flush(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
 cudaError_t launch_quant(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf);
 cudaError_t launch_conv(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);

@@ -24,6 +24,7 @@ STATUS_NAMES = {0: "RSSM_OK", 1: "RSSM_EINVAL", 2: "RSSM_ECAPACITY", 3: "RSSM_EC
                 5: "RSSM_ETIMEOUT"}
 DTYPES = {"f32": 0, "bf16": 1}
 READ_FMTS = {None: 0, "none": 0, "e4m3": 1, "e2m1": 2}
+CKPT_FMTS = {"f32": 0, "f16_sr": 1, "f16_rn": 2}
 ERR_CAPACITY, ERR_ACCEPT, ERR_TIMEOUT, ERR_PLAN = 1, 2, 4, 8
 
 # The C ABI functions, with their argument types.
@@ -34,7 +35,8 @@ _vp = ctypes.c_void_p
 
 
 class Config(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("B", "H", "P", "N", "G", "L", "T_max", "in_dtype", "read_fmt")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "H", "P", "N", "G", "L", "T_max", "in_dtype", "read_fmt",
+                                              "ckpt_fmt")] + [("seed", ctypes.c_uint64)]
 
 
 _Cfg_p = ctypes.POINTER(Config)
@@ -56,6 +58,7 @@ SIGNATURES = {
     "rssm_conventional_step": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_conventional_verify": [_Cfg_p, _vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_conventional_commit": [_Cfg_p, _vp, _vp, ctypes.c_int32, _vp, _vp],
+    "rssm_round_f16": [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int32, _vp],
 }
 
 
@@ -105,6 +108,8 @@ class LayerShape:
     T_max: int = 1
     in_dtype: str = "bf16"
     read_fmt: str | None = None
+    ckpt: str = "f32"  # checkpoint storage: "f32", "f16_sr" (stochastic rounding) or "f16_rn"
+    seed: int = 0      # key of the stochastic rounding
 
     @property
     def R(self) -> int:
@@ -114,9 +119,13 @@ class LayerShape:
     def torch_in_dtype(self) -> torch.dtype:
         return {"bf16": torch.bfloat16, "f32": torch.float32}[self.in_dtype]
 
+    @property
+    def torch_ckpt_dtype(self) -> torch.dtype:
+        return torch.float32 if self.ckpt == "f32" else torch.float16
+
     def config(self) -> Config:
         return Config(self.B, self.H, self.P, self.N, self.G, self.L, self.T_max, DTYPES[self.in_dtype],
-                      READ_FMTS[self.read_fmt])
+                      READ_FMTS[self.read_fmt], CKPT_FMTS[self.ckpt], self.seed)
 
 
 def workspace_size(shape: LayerShape) -> tuple[int, int, int]:
@@ -168,7 +177,7 @@ class ReplaySSM:
     """
 
     def __init__(self, shape: LayerShape, ckpt: torch.Tensor, stream=None):
-        _expect(ckpt, (shape.B, shape.H, shape.P, shape.N), torch.float32, "ckpt")
+        _expect(ckpt, (shape.B, shape.H, shape.P, shape.N), shape.torch_ckpt_dtype, "ckpt")
         self.shape = shape
         self.ckpt = ckpt
         ring_b, ptr_b, copy_b = workspace_size(shape)
@@ -317,3 +326,14 @@ class ConventionalVerifier:
         """The committed state [B,H,P,N] (gathered from each sequence's slot; a copy)."""
         idx = self.cur.long()
         return self.states[idx, torch.arange(self.shape.B, device=idx.device)]
+
+
+def round_f16(x: torch.Tensor, base: int = 0, epoch: int = 0, seed: int = 0, stochastic: bool = True,
+              stream=None) -> torch.Tensor:
+    """The FP16 checkpoint store's rounding applied to x (fp32, on the GPU); returns fp16 (test support)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 CUDA tensor")
+    y = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    _check(lib().rssm_round_f16(_ptr(x), _ptr(y), x.numel(), base, epoch, seed, 1 if stochastic else 0,
+                                _stream_ptr(stream)))
+    return y

@@ -71,10 +71,18 @@ typedef enum {
  * (1 for plain decoding). The ring has R = L + T_max - 1 slots per head.
  * in_dtype is the storage type of v, k and q (rssm_dtype); alpha, the
  * checkpoint and all outputs are fp32. read_fmt is an rssm_read_fmt. */
+typedef enum {
+  RSSM_CKPT_F32 = 0,    /* FP32 checkpoint (default) */
+  RSSM_CKPT_F16_SR = 1, /* FP16 checkpoint, each fold stored with stochastic rounding */
+  RSSM_CKPT_F16_RN = 2  /* FP16 checkpoint, stored rounded to nearest (comparison) */
+} rssm_ckpt_fmt;
+
 typedef struct {
   int32_t B, H, P, N, G, L, T_max;
   int32_t in_dtype;
   int32_t read_fmt;
+  int32_t ckpt_fmt;   /* rssm_ckpt_fmt; FP16 needs N in {64, 128} and read_fmt NONE */
+  uint64_t seed;      /* FP16 stochastic rounding: generator key */
 } rssm_config;
 
 typedef struct rssm_ctx* rssm_handle;
@@ -84,8 +92,9 @@ typedef struct rssm_ctx* rssm_handle;
  *      alpha [B,H,Rp] fp32 (Rp = R rounded up to 4) at offset 0,
  *      V     [B,H,R,P] in_dtype at offset v_off,
  *      K     [B,G,R,N] in_dtype at offset k_off (see rssm_ring_offsets).
- *  ptr_bytes: pointer block of int32 start[B], count[B], ticket[B] and one
- *      uint32 error word, padded to 256 bytes.
+ *  ptr_bytes: pointer block of int32 start[B], count[B], ticket[B], one
+ *      uint32 error word (256 bytes) and int32 epoch[B] (flushes per sequence),
+ *      each array 256-byte aligned.
  *  read_copy_bytes: B*H*head_stride for a read copy, else 0.
  * Any output pointer may be NULL. Returns RSSM_EINVAL or RSSM_EUNSUPPORTED for
  * a bad configuration. */
@@ -112,15 +121,24 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
                                   size_t* rscale_off);
 
 /* Bind a decoding context to caller memory.
- *  ckpt      [B,H,P,N] fp32 device: the initial state. It becomes the checkpoint
- *            and is updated in place at every flush.
+ *  ckpt      [B,H,P,N] device: the initial state, fp32, or fp16 (binary16) when
+ *            ckpt_fmt is an FP16 format. It becomes the checkpoint and is
+ *            updated in place at every flush. An FP16 checkpoint is folded in
+ *            FP32 and stored back rounded (aikraft.ru page §06: an FP16
+ *            recurrent checkpoint with stochastic rounding stays close to FP32):
+ *            stochastically with RSSM_CKPT_F16_SR, using Philox4x32-10 keyed by
+ *            cfg->seed, counter (element index / 4, the sequence's epoch, 0);
+ *            the value x rounds up to the next binary16 away from zero iff the
+ *            word is below floor(frac * 2^32), frac being x's position between
+ *            its binary16 neighbours; saturates to +-65504. The flush step's
+ *            own output uses the unrounded FP32 state.
  *  ring      device buffer of ring_bytes; contents need not be initialised.
  *  ptrs      device buffer of ptr_bytes; zeroed here (start = count = 0).
  *  read_copy device buffer of read_copy_bytes, or NULL when read_fmt is NONE;
  *            filled here by quantizing ckpt.
  * The buffers must stay valid until rssm_destroy. Enqueues a memset and,
  * with a read copy, one kernel on the stream. *out receives the handle. */
-rssm_status rssm_create(const rssm_config* cfg, float* ckpt, void* ring, void* ptrs, void* read_copy,
+rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* ptrs, void* read_copy,
                         void* stream, rssm_handle* out);
 
 /* One decode step for all B sequences (aikraft.ru page §03, "non-flush" and
@@ -238,6 +256,14 @@ rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, cons
                                      float* o, uint32_t* err_word, void* stream);
 rssm_status rssm_conventional_commit(const rssm_config* cfg, int32_t* cur, const int32_t* accepted, int32_t T,
                                      uint32_t* err_word, void* stream);
+
+/* Test support (no counterpart in the pages): the FP16 checkpoint store's
+ * rounding applied to x[0..n) fp32 device -> y[0..n) binary16 bits device,
+ * element i rounding with word (i mod 4) of the generator call for element
+ * group (base + i) / 4 at `epoch` with key `seed`; sr = 1 stochastic, 0 nearest.
+ * base must be a multiple of 4 and n >= 0, else RSSM_EINVAL. Asynchronous. */
+rssm_status rssm_round_f16(const float* x, uint16_t* y, int64_t n, int64_t base, uint32_t epoch, uint64_t seed,
+                           int32_t sr, void* stream);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rssm_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(rssm_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_function_is_exported(lib):
@@ -50,7 +50,7 @@ def test_workspace_layout_of_the_layer_workload(lib):
     assert k_off == v_off + 256 * 128 * R * 64 * 2
     assert ring == k_off + 256 * 8 * R * 128 * 2
     assert v_off % 256 == 0 and k_off % 256 == 0
-    assert ptrs == 3 * 1024 + 256
+    assert ptrs == 4 * 1024 + 256  # start, count, ticket, error word (256 B), epoch
     assert copy == 0
 
 
