@@ -1232,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               A[kp][2] = pk2(gam * x0.z, gam * x1.z);
               A[kp][3] = pk2(gam * x0.w, gam * x1.w);
             }
-#pragma unroll 2
+#pragma unroll 4
             for (int j = 0; j < J; ++j) {
               const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
               const f32x2 kx = pk2(kv.x, kv.x), ky = pk2(kv.y, kv.y), kz = pk2(kv.z, kv.z), kw = pk2(kv.w, kv.w);
