@@ -23,7 +23,7 @@ stochastic rounding of the FP16 checkpoint draws from Philox4x32-10 (Salmon et
 al., SC'11), written from its published definition.
 
 Each function here is pinned by ``tests/test_oracle_pins.py``,
-``tests/test_oracle_quant.py`` and ``tests/test_oracle_sround.py`` to something other than itself: closed forms,
+``tests/test_oracle_quant.py``, ``tests/test_oracle_sround.py`` and ``tests/test_oracle_delta.py`` to something other than itself: closed forms,
 hand-computed golden cases, brute force, library conversions and
 invariants. No function is left with unpinned parity.
 """
@@ -57,4 +57,10 @@ from .sround import (  # noqa: F401
     nearest_f16,
     f16_toward_zero,
     ReplayOracleF16,
+)
+from .delta import (  # noqa: F401
+    delta_step,
+    delta_replay_output,
+    delta_fold,
+    DeltaReplayOracle,
 )

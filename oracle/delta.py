@@ -1,0 +1,120 @@
+"""Gated delta-rule layers (Gated DeltaNet) under replay decoding: float64 oracle.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring for who may use it).
+
+The pages name Gated DeltaNet among the SSM layers of hybrid models and say
+that the same replay form applies to it ([ZH] 方法/产品要点 and the open
+questions list; [RU] introduction), but give no formula. Readings:
+
+Recurrence (the gated delta rule), per (sequence, value head), with the key and
+query of the head's group:
+    S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t
+S is P x N, alpha_t in (0, 1] the decay, beta_t the write strength.
+
+Replay form derived here. With A_t = alpha_t (I - beta_t k_t k_t^T), h records
+after a checkpoint S_0 give
+    S_h = S_0 A_1 ... A_h + sum_j beta_j v_j k_j^T A_{j+1} ... A_h,
+so the output needs the query carried backwards through the records:
+    u_h = q,   c_j = beta_j (k_j^T u_j),   u_{j-1} = alpha_j (u_j - c_j k_j),
+    o = S_0 u_0 + sum_j c_j v_j.
+The checkpoint is read once per step, as for the outer-product recurrence;
+the extra work is O(h N) per head. A fold applies the records in order:
+    S <- alpha_j S + beta_j (v_j - alpha_j S k_j) k_j^T.
+Flush policy and pointers are those of ``replay.ReplayOracle``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .recurrence import head_groups
+
+
+def delta_step(S, alpha, beta, v, k, q):
+    """One step of the definition for every (sequence, head).
+
+    S [B,H,P,N], alpha and beta [B,H], v [B,H,P], k and q [B,G,N] (float64).
+    Returns (S_t, o_t [B,H,P]).
+    """
+    S = np.asarray(S, np.float64)
+    B, H, P, N = S.shape
+    g = head_groups(H, k.shape[1])
+    kh, qh = k[:, g, :], q[:, g, :]  # [B,H,N]
+    Sk = np.einsum("bhpn,bhn->bhp", S, kh)
+    a = alpha[:, :, None, None]
+    bt = beta[:, :, None, None]
+    # alpha S (I - beta k k^T) + beta v k^T
+    S_new = a * (S - bt * Sk[..., None] * kh[:, :, None, :]) + bt * v[..., None] * kh[:, :, None, :]
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, qh)
+
+
+def delta_replay_output(S_ckpt, alphas, betas, vs, ks, q):
+    """Output-only evaluation for one sequence after h records (form above).
+
+    S_ckpt [H,P,N]; alphas, betas [h,H]; vs [h,H,P]; ks [h,G,N]; q [G,N].
+    Returns o [H,P].
+    """
+    S_ckpt = np.asarray(S_ckpt, np.float64)
+    H, P, N = S_ckpt.shape
+    g = head_groups(H, q.shape[0])
+    h = len(alphas)
+    o = np.empty((H, P))
+    for head in range(H):
+        u = np.array(q[g[head]], np.float64)
+        val = np.zeros(P)
+        for j in range(h - 1, -1, -1):
+            kj = ks[j, g[head]]
+            c = betas[j, head] * float(kj @ u)
+            val += c * vs[j, head]
+            u = alphas[j, head] * (u - c * kj)
+        o[head] = S_ckpt[head] @ u + val
+    return o
+
+
+def delta_fold(S_ckpt, alphas, betas, vs, ks):
+    """The state after h records, applied in order (one sequence)."""
+    S = np.array(S_ckpt, np.float64)
+    H = S.shape[0]
+    g = head_groups(H, ks.shape[1])
+    for j in range(len(alphas)):
+        for head in range(H):
+            kj = ks[j, g[head]]
+            y = S[head] @ kj
+            S[head] = alphas[j, head] * S[head] + np.outer(betas[j, head] * (vs[j, head] - alphas[j, head] * y), kj)
+    return S
+
+
+class DeltaReplayOracle:
+    """Replay decoding of a gated delta-rule layer with an FP32 checkpoint.
+
+    The exact target is the definition, so ``S`` advances by ``delta_step``
+    and the outputs are its outputs; ``ckpt`` is the exact state at each
+    sequence's last flush. The integers (start, count, flush events) follow the
+    eager policy of ``ReplayOracle``: the step whose append brings the count to
+    L folds all records.
+    """
+
+    def __init__(self, S0, L: int, R: int, G: int):
+        self.S = np.array(S0, np.float64)
+        self.ckpt = self.S.copy()
+        self.B = self.S.shape[0]
+        self.L, self.R, self.G = L, R, G
+        self.start = np.zeros(self.B, np.int64)
+        self.count = np.zeros(self.B, np.int64)
+
+    def decode(self, alpha, beta, v, k, q):
+        h = self.count + 1
+        if np.any(h > self.R):
+            raise ValueError("decode would exceed the ring capacity")
+        self.S, o = delta_step(self.S, alpha, beta, v, k, q)
+        flush = h >= self.L
+        self.ckpt[flush] = self.S[flush]
+        self.start = np.where(flush, (self.start + h) % self.R, self.start)
+        self.count = np.where(flush, 0, h)
+        return o, flush
+
+    def flush(self, min_count: int):
+        mask = (self.count >= min_count) & (self.count > 0)
+        self.ckpt[mask] = self.S[mask]
+        self.start = np.where(mask, (self.start + self.count) % self.R, self.start)
+        self.count = np.where(mask, 0, self.count)
+        return mask

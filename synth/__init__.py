@@ -10,6 +10,7 @@ from .inputs import (  # noqa: F401
     make_generator,
     initial_state,
     decode_step_inputs,
+    delta_step_inputs,
     verify_round_inputs,
     accepted_lengths,
 )

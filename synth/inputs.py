@@ -115,3 +115,24 @@ def verify_round_inputs(shape: Shape, T: int, gen: torch.Generator, mu: float = 
 def accepted_lengths(B: int, T: int, gen: torch.Generator) -> torch.Tensor:
     """Accepted draft count per sequence, uniform on 0..T, int32 [B]."""
     return torch.randint(0, T + 1, (B,), generator=gen, dtype=torch.int32)
+
+
+def delta_step_inputs(shape: Shape, gen: torch.Generator, mu: float = 0.0):
+    """One decode step's inputs for a gated delta-rule layer.
+
+    Draw order: u ~ N(mu, 1) [B,H] -> alpha = exp(-softplus(u)); z ~ N(0, 1)
+    [B,H] -> beta = sigmoid(z) (write strength in (0, 1)); v ~ N(0,1)/sqrt(N)
+    [B,H,P]; k and q ~ N(0, 1) [B,G,N], each scaled to unit L2 norm per
+    (sequence, group) as delta-rule layers normalize their keys and queries.
+    v, k and q are then cast to the storage dtype. Returns (alpha, beta, v, k, q).
+    """
+    B, H, P, N, G = shape.B, shape.H, shape.P, shape.N, shape.G
+    u = torch.randn((B, H), generator=gen, dtype=torch.float32) + mu
+    alpha = _decay_from_normal(u)
+    beta = torch.sigmoid(torch.randn((B, H), generator=gen, dtype=torch.float32))
+    v = (torch.randn((B, H, P), generator=gen, dtype=torch.float32) / math.sqrt(N)).to(shape.torch_dtype)
+    k = torch.randn((B, G, N), generator=gen, dtype=torch.float32)
+    q = torch.randn((B, G, N), generator=gen, dtype=torch.float32)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(shape.torch_dtype)
+    q = (q / q.norm(dim=-1, keepdim=True)).to(shape.torch_dtype)
+    return alpha, beta, v, k, q
