@@ -48,10 +48,10 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_step_b256_l16.md")
 
 
 # ----------------------------------------------------------------- analytic bytes
-def record_bytes(s) -> int:
-    """Bytes of one input record (alpha, v, k) of one sequence."""
+def record_bytes(s, delta: bool = False) -> int:
+    """Bytes of one input record (alpha, v, k; and beta for a delta-rule layer) of one sequence."""
     es = 2 if s.in_dtype == "bf16" else 4
-    return 4 * s.H + es * s.H * s.P + es * s.G * s.N
+    return 4 * s.H * (2 if delta else 1) + es * s.H * s.P + es * s.G * s.N
 
 
 def copy_bytes_per_head(s, read_fmt) -> int:
@@ -65,7 +65,7 @@ def copy_bytes_per_head(s, read_fmt) -> int:
     return -(-(rsc + 4 * P) // 16) * 16
 
 
-def window_bytes(s, read_fmt=None, ckpt_bytes: int = 4) -> dict:
+def window_bytes(s, read_fmt=None, ckpt_bytes: int = 4, delta: bool = False) -> dict:
     """Algorithmic HBM bytes of one sequence over one window of L decode steps.
 
     Every step reads its inputs (record + q) and writes its output. Step t of
@@ -73,12 +73,13 @@ def window_bytes(s, read_fmt=None, ckpt_bytes: int = 4) -> dict:
     non-flush step appends its record. The L-1 non-flush steps each read the
     checkpoint |S|, or its read copy |C| when there is one. The flush step
     reads |S| and writes it once, plus the refreshed copy. ckpt_bytes is the
-    checkpoint's element size (2 for an FP16 checkpoint).
+    checkpoint's element size (2 for an FP16 checkpoint). A delta-rule layer's
+    records carry beta too; its state bytes are the same.
     """
     es = 2 if s.in_dtype == "bf16" else 4
     S = ckpt_bytes * s.H * s.P * s.N
     C = s.H * copy_bytes_per_head(s, read_fmt)
-    r = record_bytes(s)
+    r = record_bytes(s, delta)
     inp = r + es * s.G * s.N
     out = 4 * s.H * s.P
     L = s.L
@@ -210,27 +211,30 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------- CPU oracle timing
-def time_oracle(shape, n_seq: int, n_steps: int, seed: int = 0) -> tuple[float, int]:
-    """Seconds for n_steps conventional float64 steps of the oracle on n_seq sequences."""
+def time_oracle(shape, n_seq: int, n_steps: int, seed: int = 0, delta: bool = False) -> tuple[float, int]:
+    """Seconds for n_steps float64 steps of the oracle's recurrence (its definition) on n_seq sequences."""
     import oracle
     s = shape.with_(B=n_seq)
     gen = synth.make_generator(seed)
     S = oracle.to_f64(synth.initial_state(s, gen))
-    steps = [tuple(oracle.to_f64(x) for x in synth.decode_step_inputs(s, gen)) for _ in range(min(n_steps, 4))]
+    draw = synth.delta_step_inputs if delta else synth.decode_step_inputs
+    step = oracle.delta_step if delta else oracle.conventional_step
+    steps = [tuple(oracle.to_f64(x) for x in draw(s, gen)) for _ in range(min(n_steps, 4))]
     t0 = time.perf_counter()
     for i in range(n_steps):
-        S, o = oracle.conventional_step(S, *steps[i % len(steps)])
+        S, o = step(S, *steps[i % len(steps)])
     return time.perf_counter() - t0, n_seq * n_steps
 
 
-def cpu_baseline_line(shape, budget_s: float = 12.0) -> dict:
+def cpu_baseline_line(shape, budget_s: float = 12.0, delta: bool = False) -> dict:
     n_seq = 4
-    t, units = time_oracle(shape, n_seq, 2)  # calibrate
+    t, units = time_oracle(shape, n_seq, 2, delta=delta)  # calibrate
     per_step = t / 2
     steps = max(4, int(budget_s / max(per_step, 1e-6)))
-    t, units = time_oracle(shape, n_seq, steps)
+    t, units = time_oracle(shape, n_seq, steps, delta=delta)
+    what = "gated delta rule" if delta else "conventional recurrence"
     return {"value": units / t, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"float64 conventional recurrence, {n_seq} of {shape.B} sequences x all {shape.H} heads, "
+            "sample": f"float64 {what}, {n_seq} of {shape.B} sequences x all {shape.H} heads, "
                       f"{steps} steps ({t:.1f} s); numpy elementwise, one thread"}
 
 
@@ -240,8 +244,9 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     s = WORKLOAD if args.batch is None else WORKLOAD.with_(B=args.batch)
+    delta = args.recurrence == "delta"
     ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype, read_fmt=args.read_fmt,
-                    ckpt=args.ckpt, seed=s.seed)
+                    ckpt=args.ckpt, seed=s.seed, recurrence=args.recurrence)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev)
@@ -256,22 +261,34 @@ def run_ours(args, world, rank, local):
         v = (torch.randn((s.B, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
         k = (torch.randn((s.B, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
         q = (torch.randn((s.B, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
-        pool.append((alpha, v, k, q))
+        if delta:  # write strengths in (0, 1); unit-norm keys and queries
+            beta = torch.sigmoid(torch.randn((s.B, s.H), generator=gen, device=dev)).float()
+            k = (k.float() / k.float().norm(dim=-1, keepdim=True)).to(ls.torch_in_dtype)
+            q = (q.float() / q.float().norm(dim=-1, keepdim=True)).to(ls.torch_in_dtype)
+            pool.append((alpha, v, k, q, beta))
+        else:
+            pool.append((alpha, v, k, q))
     out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=dev)
     L = s.L
 
+    def step(x, o):
+        if delta:
+            model.decode_step(*x[:4], out=o, beta=x[4])
+        else:
+            model.decode_step(*x, out=o)
+
     def window(i0: int, ev: list | None = None):
         for j in range(L):
-            a, v, k, q = pool[(i0 + j) % len(pool)]
+            x = pool[(i0 + j) % len(pool)]
             if ev is not None:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                model.decode_step(a, v, k, q, out=out)
+                step(x, out)
                 e1.record(stream)
                 ev.append((e0, e1))
             else:
-                model.decode_step(a, v, k, q, out=out)
+                step(x, out)
 
     # warm-up (whole windows keep every sequence aligned on the window)
     for w in range(args.warmup):
@@ -300,7 +317,7 @@ def run_ours(args, world, rank, local):
     value = seq_steps / elapsed_max
     mean_launch = sum(launch_s) / len(launch_s)
     ckpt_es = 4 if args.ckpt == "f32" else 2
-    wb = window_bytes(s, args.read_fmt, ckpt_es)
+    wb = window_bytes(s, args.read_fmt, ckpt_es, delta)
     alg_bytes_launch = wb["replay_per_seq_step"] * s.B
     achieved = alg_bytes_launch / mean_launch / 1e9
     peak, peak_kind = measured_peak_gbs()
@@ -314,16 +331,17 @@ def run_ours(args, world, rank, local):
     if not args.no_conventional:
         state = ckpt.clone()
         n_conv = max(1, min(args.steps, 50))
+        def conv(x):
+            conventional_step(ls, state, *x[:4], out=out, beta=x[4] if delta else None)
+
         for i in range(L):
-            a, v, k, q = pool[i % len(pool)]
-            conventional_step(ls, state, a, v, k, q, out=out)
+            conv(pool[i % len(pool)])
         torch.cuda.synchronize()
         c0 = torch.cuda.Event(enable_timing=True)
         c1 = torch.cuda.Event(enable_timing=True)
         c0.record(stream)
         for i in range(n_conv * L):
-            a, v, k, q = pool[i % len(pool)]
-            conventional_step(ls, state, a, v, k, q, out=out)
+            conv(pool[i % len(pool)])
         c1.record(stream)
         torch.cuda.synchronize()
         conv_t = c0.elapsed_time(c1) / 1e3
@@ -353,7 +371,7 @@ def run_ours(args, world, rank, local):
             ds = dpool[i % 2]
             for d, h in zip(ds, hs):
                 d.copy_(h, non_blocking=True)
-            model.decode_step(*ds, out=out)
+            step(ds, out)
             host_out.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         tw = max_over_ranks(time.perf_counter() - tw0, world)
@@ -363,7 +381,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_line(s)
+        cpu = cpu_baseline_line(s, delta=delta)
 
     if rank != 0:
         return None
@@ -373,7 +391,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.ckpt == "f32" else "f32 (fp16 checkpoint)",
         "data": "synthetic",
-        "config": {"workload": f"ReplaySSM decode, one Mamba-2-shaped layer: B={s.B} H={s.H} P={s.P} N={s.N} "
+        "config": {"workload": f"ReplaySSM decode, one {'gated delta-rule' if delta else 'Mamba-2-shaped'} layer: "
+                               f"B={s.B} H={s.H} P={s.P} N={s.N} "
                                f"G={s.G} L={L}, bf16 v/k/q, fp32 checkpoint and outputs; one step = one window "
                                f"of {L} decode launches ({L - 1} non-flush + 1 flush)",
                    "global_batch": s.B * world, "parallelism": "replicas" if world > 1 else "single",
@@ -381,7 +400,8 @@ def run_ours(args, world, rank, local):
                    "inputs": "16 resident steps of seeded inputs, cycled"},
         "hbm_gbs_achieved": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(),
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic() if (not delta and args.read_fmt is None and args.ckpt == "f32"
+                                                      and args.batch is None) else None,
                      "algorithmic_bytes_per_launch": alg_bytes_launch,
                      "mean_launch_ms": mean_launch * 1e3,
                      "mean_nonflush_launch_ms": 1e3 * sum(nonflush_s) / max(1, len(nonflush_s)),
@@ -718,7 +738,11 @@ def main(argv=None):
                     help="non-flush steps read a low-precision copy of the checkpoint")
     ap.add_argument("--ckpt", choices=["f32", "f16_sr", "f16_rn"], default="f32",
                     help="checkpoint storage: FP32, or FP16 stored with stochastic / nearest rounding")
+    ap.add_argument("--recurrence", choices=["outer", "delta"], default="outer",
+                    help="decode: the gated outer-product recurrence or the gated delta rule (beta inputs)")
     args = ap.parse_args(argv)
+    if args.recurrence == "delta" and (args.workload != "decode" or args.read_fmt or args.ckpt != "f32"):
+        ap.error("--recurrence delta: decode workload, FP32 checkpoint, no read copy")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

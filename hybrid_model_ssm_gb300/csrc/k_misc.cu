@@ -4,6 +4,7 @@
 
 namespace rssm {
 cudaError_t launch_flush(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf) {
+  if (rf == kDelta) return launch_delta(kFlush, p, grid, smem, st, N, dtype);
   return dtype == 0 ? dispatch_n<kFlush, float>(p, grid, smem, st, N, rf)
                     : dispatch_n<kFlush, __nv_bfloat16>(p, grid, smem, st, N, rf);
 }

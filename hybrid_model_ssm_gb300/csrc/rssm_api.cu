@@ -40,7 +40,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Geom {
   int R = 0, Rp = 0, esize = 0, ck_es = 4, rf = 0;  // ck_es: checkpoint bytes per element; rf: tile format
-  size_t v_off = 0, k_off = 0, ring_bytes = 0;
+  size_t b_off = 0, v_off = 0, k_off = 0, ring_bytes = 0;  // b_off: beta rows (delta layers)
   size_t off_count = 0, off_ticket = 0, off_err = 0, off_epoch = 0, ptr_bytes = 0;
   size_t head_stride = 0, bsc_off = 0, rsc_off = 0, copy_bytes = 0;
 };
@@ -68,15 +68,23 @@ rssm_status derive(const rssm_config* c, Geom* g) {
   if (c->ckpt_fmt < RSSM_CKPT_F32 || c->ckpt_fmt > RSSM_CKPT_F16_RN) return fail(RSSM_EINVAL, "ckpt_fmt %d", c->ckpt_fmt);
   if (c->ckpt_fmt != RSSM_CKPT_F32 && (c->N < 64 || c->read_fmt != RSSM_READ_NONE))
     return fail(RSSM_EUNSUPPORTED, "an FP16 checkpoint needs N in {64, 128} and no read copy");
+  if (c->recurrence != RSSM_GATED_OUTER && c->recurrence != RSSM_GATED_DELTA)
+    return fail(RSSM_EINVAL, "recurrence %d", c->recurrence);
+  if (c->recurrence == RSSM_GATED_DELTA &&
+      (c->N < 64 || c->read_fmt != RSSM_READ_NONE || c->ckpt_fmt != RSSM_CKPT_F32 || c->T_max != 1))
+    return fail(RSSM_EUNSUPPORTED, "a delta-rule layer needs N in {64, 128}, an FP32 checkpoint, no read copy and T_max = 1");
   if ((long long)c->B * c->H > (1ll << 30)) return fail(RSSM_EUNSUPPORTED, "B*H too large");
   g->R = R;
   g->Rp = (R + 3) / 4 * 4;
   g->esize = c->in_dtype == RSSM_F32 ? 4 : 2;
   g->ck_es = c->ckpt_fmt == RSSM_CKPT_F32 ? 4 : 2;
-  g->rf = c->ckpt_fmt != RSSM_CKPT_F32 ? (int)rssm::kCkF16 : c->read_fmt;
+  g->rf = c->recurrence == RSSM_GATED_DELTA ? (int)rssm::kDelta
+         : c->ckpt_fmt != RSSM_CKPT_F32    ? (int)rssm::kCkF16
+                                           : c->read_fmt;
   const size_t B = c->B, H = c->H, P = c->P, N = c->N, G = c->G;
   const size_t a_bytes = B * H * g->Rp * 4;
-  g->v_off = align_up(a_bytes, 256);
+  g->b_off = c->recurrence == RSSM_GATED_DELTA ? align_up(a_bytes, 256) : 0;
+  g->v_off = align_up((g->b_off ? g->b_off + a_bytes : a_bytes), 256);
   g->k_off = align_up(g->v_off + B * H * R * P * g->esize, 256);
   g->ring_bytes = align_up(g->k_off + B * G * R * N * g->esize, 256);
   const size_t pb = align_up(B * 4, 256);
@@ -120,12 +128,17 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
   const size_t tile = a128(nf && g.head_stride ? g.head_stride : P * N * (size_t)g.ck_es);
   const size_t vrows = nf ? (size_t)c->L : R;
-  const size_t sv_off = (size_t)(kRMax + kTMax) * 4;  // decays: kRMax ring slots, then kTMax new records
+  // decays: kRMax ring slots, then kTMax new records; delta layers keep the
+  // write strengths the same way right after them
+  const bool delta = g.rf == rssm::kDelta;
+  const size_t sv_off = (size_t)(kRMax + kTMax) * 4 * (delta ? 2 : 1);
   const size_t sc_off = align_up(sv_off + vrows * P * es, 16);
   // coefficients: 16 scalars, then the record weights [kRMax] (non-flush),
   // [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general, which
   // also serves non-flush heads)
-  const size_t sc_floats = nf ? 16 + std::max(P, (size_t)kRMax)
+  // delta layers: 16 scalars, the record weights [kRMax] and the carried query u_0 [N]
+  const size_t sc_floats = delta ? 16 + (size_t)kRMax + N
+                         : nf    ? 16 + std::max(P, (size_t)kRMax)
                               : kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax
                                                             : 16 + std::max({(size_t)kRMax, R * P, (size_t)c->T_max * P});
   const size_t slot = a128(sc_off + sc_floats * 4);
@@ -233,6 +246,7 @@ void fill_common(const rssm_ctx* h, rssm::Params* p) {
   p->bsc_off = (int)h->g.bsc_off;
   p->rsc_off = (int)h->g.rsc_off;
   p->ring_a = reinterpret_cast<float*>(h->ring);
+  p->ring_b = h->g.b_off ? reinterpret_cast<float*>(h->ring + h->g.b_off) : nullptr;
   p->ring_v = h->ring + h->g.v_off;
   p->ring_k = h->ring + h->g.k_off;
   p->start = reinterpret_cast<int32_t*>(h->ptrs);
@@ -333,8 +347,29 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
   return RSSM_OK;
 }
 
+namespace {
+rssm_status decode_impl(rssm_handle h, const float* alpha, const float* beta, const void* v, const void* k,
+                        const void* q, float* o, void* stream);
+}
+
 rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, const void* k, const void* q,
                              float* o, void* stream) {
+  if (h && h->cfg.recurrence == RSSM_GATED_DELTA)
+    return fail(RSSM_EINVAL, "a delta-rule layer decodes with rssm_decode_step_delta");
+  return decode_impl(h, alpha, nullptr, v, k, q, o, stream);
+}
+
+rssm_status rssm_decode_step_delta(rssm_handle h, const float* alpha, const float* beta, const void* v,
+                                   const void* k, const void* q, float* o, void* stream) {
+  if (h && h->cfg.recurrence != RSSM_GATED_DELTA)
+    return fail(RSSM_EINVAL, "rssm_decode_step_delta needs a delta-rule layer");
+  if (!beta || !aligned16(beta)) return fail(RSSM_EINVAL, "beta must be a 16-byte aligned device pointer");
+  return decode_impl(h, alpha, beta, v, k, q, o, stream);
+}
+
+namespace {
+rssm_status decode_impl(rssm_handle h, const float* alpha, const float* beta, const void* v, const void* k,
+                        const void* q, float* o, void* stream) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");
   if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
@@ -343,7 +378,7 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
   const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kNonFlush);
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
-  pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
+  pl.p.alpha = alpha; pl.p.beta = beta; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
   const long long heads = (long long)h->cfg.B * h->cfg.H;
   const cudaError_t e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
                                             h->cfg.N, h->cfg.in_dtype, h->g.rf);
@@ -351,10 +386,12 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
   h->last_T = 0;
   return RSSM_OK;
 }
+}  // namespace
 
 rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k, const void* q,
                         float* o, void* stream) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (h->cfg.recurrence == RSSM_GATED_DELTA) return fail(RSSM_EUNSUPPORTED, "verify is not offered for delta-rule layers");
   if (T < 1 || T > h->cfg.T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, h->cfg.T_max);
   if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
@@ -445,15 +482,21 @@ rssm_status rssm_destroy(rssm_handle h) {
   return RSSM_OK;
 }
 
-rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const float* alpha, const void* v,
-                                   const void* k, const void* q, float* o, void* stream) {
+namespace {
+rssm_status conventional_impl(const rssm_config* cfg, float* state, const float* alpha, const float* beta,
+                              const void* v, const void* k, const void* q, float* o, void* stream) {
   Geom g;
   rssm_status s = derive(cfg, &g);
   if (s != RSSM_OK) return s;
+  const bool delta = cfg->recurrence == RSSM_GATED_DELTA;
+  if (delta != (beta != nullptr))
+    return fail(RSSM_EINVAL, delta ? "a delta-rule layer steps with rssm_conventional_step_delta"
+                                   : "rssm_conventional_step_delta needs a delta-rule configuration");
   g.ck_es = 4;  // the comparison keeps an fp32 state
-  g.rf = rssm::kRfNone;
+  g.rf = delta ? rssm::kDelta : rssm::kRfNone;
   if (!state || !alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
-  if (!aligned16(state) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
+  if (!aligned16(state) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o) ||
+      (beta && !aligned16(beta)))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
   Plan pl;
   s = plan_smem(cfg, g, &pl);
@@ -462,12 +505,27 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
   p.B = cfg->B; p.H = cfg->H; p.P = cfg->P; p.N = cfg->N; p.G = cfg->G; p.L = cfg->L;
   p.R = g.R; p.Rp = g.Rp; p.HPG = cfg->H / cfg->G; p.T = 1; p.min_count = 1;
   p.ckpt = state;
-  p.alpha = alpha; p.v = v; p.k = k; p.q = q; p.o = o;
+  p.alpha = alpha; p.beta = beta; p.v = v; p.k = k; p.q = q; p.o = o;
   const long long heads = (long long)cfg->B * cfg->H;
-  const cudaError_t e = rssm::launch_conv(p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
-                                          cfg->N, cfg->in_dtype);
+  const cudaError_t e =
+      delta ? rssm::launch_delta(rssm::kConv, p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
+                                 cfg->N, cfg->in_dtype)
+            : rssm::launch_conv(p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream), cfg->N,
+                                cfg->in_dtype);
   if (e != cudaSuccess) return cuda_fail(e, "conventional launch");
   return RSSM_OK;
+}
+}  // namespace
+
+rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const float* alpha, const void* v,
+                                   const void* k, const void* q, float* o, void* stream) {
+  return conventional_impl(cfg, state, alpha, nullptr, v, k, q, o, stream);
+}
+
+rssm_status rssm_conventional_step_delta(const rssm_config* cfg, float* state, const float* alpha, const float* beta,
+                                         const void* v, const void* k, const void* q, float* o, void* stream) {
+  if (!beta) return fail(RSSM_EINVAL, "NULL beta");
+  return conventional_impl(cfg, state, alpha, beta, v, k, q, o, stream);
 }
 
 rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, const int32_t* cur, int32_t T,
@@ -478,6 +536,7 @@ rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, cons
   if (s != RSSM_OK) return s;
   g.ck_es = 4;  // the comparison keeps fp32 states
   g.rf = rssm::kRfNone;
+  if (cfg->recurrence != RSSM_GATED_OUTER) return fail(RSSM_EUNSUPPORTED, "the snapshot comparator is outer-product only");
   if (T < 1 || T > cfg->T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, cfg->T_max);
   if (!states || !cur || !alpha || !v || !k || !q || !o || !err_word) return fail(RSSM_EINVAL, "NULL pointer");
   if (!aligned16(states) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
@@ -546,6 +605,8 @@ std::mutex g_static_ticket_mu;
 rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, const void* v, const void* k,
                                             const void* q, float* o, void* stream) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (h->cfg.recurrence == RSSM_GATED_DELTA)
+    return fail(RSSM_EUNSUPPORTED, "the static-scratch step serves the outer-product recurrence");
   if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");

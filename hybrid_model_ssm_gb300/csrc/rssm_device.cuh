@@ -61,7 +61,9 @@ constexpr unsigned kFull = 0xffffffffu;
 enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4, kSnap = 5 };
 // Storage formats of the head tile: the FP32 checkpoint (kRfNone), an E4M3 or
 // E2M1 read copy next to it, or an FP16 checkpoint (kCkF16: no read copy).
-enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2, kCkF16 = 3 };
+// kDelta: an FP32 checkpoint of a gated delta-rule layer (the same tiles, the
+// delta rule's replay form and fold).
+enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2, kCkF16 = 3, kDelta = 4 };
 enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u, kErrPlan = 8u };
 
 // One partition of a CTA's shared memory into tile stages and record slots.
@@ -76,6 +78,7 @@ struct Params {
   uint8_t* copy;       // read copy: head_stride bytes per (b,h), or null
   int head_stride, bsc_off, rsc_off;
   float* ring_a;       // [B,H,Rp] decays
+  float* ring_b;       // [B,H,Rp] write strengths (delta-rule layers)
   void* ring_v;        // [B,H,R,P] values (input dtype)
   void* ring_k;        // [B,G,R,N] keys (input dtype)
   int32_t* start;      // [B]
@@ -88,6 +91,7 @@ struct Params {
   int nslot;           // kSnap: state slots (T_max + 1)
   uint32_t* err;       // error word
   const float* alpha;  // decode/conv [B,H]; verify [B,T,H]
+  const float* beta;   // delta-rule decode [B,H]
   const void* v;       // decode/conv [B,H,P]; verify [B,T,H,P]
   const void* k;       // decode/conv [B,G,N]; verify [B,T,G,N]
   const void* q;       // decode/conv [B,G,N]; verify [B,T,G,N]
@@ -356,6 +360,13 @@ struct TMax<K, 0> {
   static __device__ __forceinline__ void run(float*, int, int&) {}
 };
 
+// Sum over the warp, returned to every lane.
+__device__ __forceinline__ float warp_allsum(float x) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(kFull, x, m);
+  return x;
+}
+
 // incl[lane] = prod_{i >= lane} x_i over the warp.
 __device__ __forceinline__ float suffix_prod(float x, int lane) {
 #pragma unroll
@@ -564,6 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr bool kCopyRF = (RF == kRfE4m3 || RF == kRfE2m1);    // a low-precision read copy exists
   constexpr bool kF16 = (RF == kCkF16);                          // the checkpoint itself is FP16
   constexpr int CKES = kF16 ? 2 : 4;                             // checkpoint bytes per element
+  constexpr bool kDel = (RF == kDelta);                          // gated delta-rule layer
+  constexpr int kSbOff = (kRMax + kTMax) * 4;                    // delta: slot offset of the write strengths
   constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -779,9 +792,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const uint32_t sbar = sfull0 + 8 * rs;
         const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
         // slot: decays at [ring slot] (committed) and kRMax + t (new); value rows in record order
-        mbar_arrive_tx(sbar, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
+        mbar_arrive_tx(sbar, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 * (kDel ? 2 : 1) : 0u));
         if (c > 0) {
           tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
+          if constexpr (kDel) tma_load_1d(sdst + kSbOff, p.ring_b + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
           const int n1 = min(c, p.R - st);
           const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * rbytes;
           tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * rbytes, (uint32_t)n1 * rbytes, sbar);
@@ -790,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         for (int t = 0; t < nnew; ++t) {
           const size_t nrow = kDrafts ? ((size_t)b * p.T + t) * p.H + hh : hrow;
           cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
+          if constexpr (kDel) cp_async4(sdst + kSbOff + 4 * (kRMax + t), p.beta + nrow);
           tma_load_1d(sdst + lay.sv_off + (c + t) * rbytes, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes,
                       rbytes, sbar);
         }
@@ -818,6 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     long long cur_gg = -1;
     bool load = false, flush = false, bad = false;
     float sj = 0.f;  // decode: lane j holds k_j^T q
+    const uint8_t* cK = smem + p.gb_off;  // the current group area: keys, then queries
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
@@ -843,7 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if (!__all_sync(kFull, mbar_wait(gfull0 + 8 * gs, (gi >> 1) & 1, abort_flag, p.err))) { ok = false; break; }
           const uint8_t* gK = smem + p.gb_off + gs * p.gb_bytes;
           const uint8_t* gQ = gK + p.gq_off;
-          if constexpr (MODE == kDecode || MODE == kVerify) {
+          cK = gK;
+          if constexpr ((MODE == kDecode || MODE == kVerify) && !kDel) {
             // k_j^T q_t: one pair per lane, N/4 chunks visited from a lane-dependent start
             const int npair = J * nq;
             for (int pr = lane; pr < ((npair + 31) & ~31); pr += 32) {
@@ -902,6 +919,56 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           sc[kCoefOff + t * kRMax + lane] = (lane < ht) ? w * skq_w[t * kRMax + lane] : 0.f;
           if (lane == 0) sc[t] = incl;
         }
+      } else if constexpr (kDel) {
+        // Gated delta rule, output without a fold: the query is carried back
+        // through the records, u_J = q, c_j = beta_j k_j^T u_j,
+        // u_{j-1} = alpha_j (u_j - c_j k_j); then o = S u_0 + sum_j c_j v_j, which
+        // the dot warps form with sc[0] = 1, the weights c_j and u_0. A folding
+        // head needs nothing here: the dot warps apply its records in order.
+        if constexpr (MODE == kDecode) {
+          if (!flush) {
+            constexpr int NPL = N / 32;  // query elements per lane: N/32 consecutive
+            static_assert(NPL == 2 || NPL == 4, "delta-rule layers: N in {64, 128}");
+            const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
+            const uint8_t* cQ = cK + p.gq_off;
+            float u[NPL];
+            if constexpr (NPL == 4) {
+              const float4 x = In<TIn>::lds4(cQ, lane * 4);
+              u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
+            } else {
+              const float2 x = In<TIn>::lds2(cQ, lane * 2);
+              u[0] = x.x; u[1] = x.y;
+            }
+            float cj = 0.f;  // lane j: c_j
+            for (int j = J - 1; j >= 0; --j) {
+              const int sl = (j < c) ? ring_slot(st, j, p.R) : kRMax + j - c;
+              const float al = sa[sl], be = sbeta[sl];
+              float kx[NPL];
+              if constexpr (NPL == 4) {
+                const float4 x = In<TIn>::lds4(cK, j * N + lane * 4);
+                kx[0] = x.x; kx[1] = x.y; kx[2] = x.z; kx[3] = x.w;
+              } else {
+                const float2 x = In<TIn>::lds2(cK, j * N + lane * 2);
+                kx[0] = x.x; kx[1] = x.y;
+              }
+              float d = 0.f;
+#pragma unroll
+              for (int e = 0; e < NPL; ++e) d = fmaf(kx[e], u[e], d);
+              const float cc = be * warp_allsum(d);
+              if (lane == j) cj = cc;
+#pragma unroll
+              for (int e = 0; e < NPL; ++e) u[e] = al * fmaf(-cc, kx[e], u[e]);
+            }
+            if (lane == 0) sc[0] = 1.f;
+            sc[kCoefOff + lane] = (lane < J) ? cj : 0.f;
+            float* su0 = sc + kCoefOff + kRMax;  // u_0, natural order
+            if constexpr (NPL == 4) {
+              *reinterpret_cast<float4*>(su0 + lane * 4) = make_float4(u[0], u[1], u[2], u[3]);
+            } else {
+              *reinterpret_cast<float2*>(su0 + lane * 2) = make_float2(u[0], u[1]);
+            }
+          }
+        }
       } else if constexpr (MODE != kSnap) {
         const float incl = suffix_prod(aj, lane);
         const float nxt = __shfl_down_sync(kFull, incl, 1);
@@ -931,6 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         if (lane < na) {  // lane t: one bulk store per value row
           const int slot_t = ring_slot(st, c + lane, p.R);
           p.ring_a[hrow * p.Rp + slot_t] = sa[kRMax + lane];
+          if constexpr (kDel) p.ring_b[hrow * p.Rp + slot_t] = reinterpret_cast<const float*>(slot + kSbOff)[kRMax + lane];
           bulk_store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + slot_t) * p.P * ES,
                      smem_u32(sv + (c + lane) * p.P * ES), p.P * ES);
           bulk_commit();
@@ -938,6 +1006,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         }
 #else
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[kRMax + lane];
+        if constexpr (kDel) {
+          if (lane < na)
+            p.ring_b[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = reinterpret_cast<const float*>(slot + kSbOff)[kRMax + lane];
+        }
         const int chp = p.P * ES / 16;
         for (int t = 0; t < na; ++t) {  // 16-byte stores spread over the lanes
           uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
@@ -969,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     // FP32 non-flush rows (N >= 64): LP16 lanes per row, 16 columns per lane as
     // 4 chunks of 4 interleaved over the row's lanes (each quarter warp reads
     // 128 contiguous bytes: no bank conflicts); q16 holds the matching q values.
-    constexpr bool kWideRows = ((RF == kRfNone || kF16) && MODE == kDecode && N >= 64);
+    constexpr bool kWideRows = ((RF == kRfNone || kF16 || kDel) && MODE == kDecode && N >= 64);
     constexpr int LP16 = kWideRows ? N / 16 : 1;
     float q16[kWideRows ? 16 : 1];
     const int wpg = kNDW / lay.dgroups;                 // warps per dot group
@@ -1003,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           gK = smem + p.gb_off + gs * p.gb_bytes;
           gQ = gK + p.gq_off;
           if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
-          if constexpr (kWideRows && !kF16) {
+          if constexpr (kWideRows && !kF16 && !kDel) {  // delta-rule heads take u_0 per head instead
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const float4 qq = In<TIn>::lds4(gQ, (c * LP16 + lane % LP16) * 4);
@@ -1219,7 +1291,43 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           const int rbase = (pass * wpg + wr) * kKR;
           if (rbase * RPI >= p.P) break;  // warp-uniform: no rows left for this warp
           float4 acc[kKR];
-          if constexpr (RPI == 1) {
+          if constexpr (kDel) {
+            // Gated delta rule, records in order: y = S k_j (the current S),
+            // S <- alpha_j S + beta_j (v_j - alpha_j y) k_j^T. The row sums of the
+            // warp's kKR row instructions are reduced transposed (lane seg + kk D
+            // ends with row kk's sum) and handed back to every lane of the row.
+            static_assert(LPR >= kKR, "delta-rule fold: a row spans at least kKR lanes");
+            constexpr int D = LPR / kKR;
+            const float* salpha = reinterpret_cast<const float*>(slot);
+            const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
+            const int seg = lane & ~(LPR - 1);
+#pragma unroll
+            for (int kk = 0; kk < kKR; ++kk) {
+              const int row = (rbase + kk) * RPI + rsub;
+              acc[kk] = (row < p.P) ? ld_tile4<false>(tile, (size_t)row * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int j = 0; j < J; ++j) {
+              const int sl = (j < c) ? ring_slot(st, j, p.R) : kRMax + j - c;
+              const float al = salpha[sl], be = sbeta[sl];
+              const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
+              float part[kKR];
+#pragma unroll
+              for (int kk = 0; kk < kKR; ++kk) part[kk] = dot4(acc[kk], kv);
+              int off = 0;
+              TRed<kKR, LPR / 2>::run(part, lane, off);
+#pragma unroll
+              for (int kk = 0; kk < kKR; ++kk) {
+                const float y = __shfl_sync(kFull, part[0], seg + kk * D);
+                const int row = (rbase + kk) * RPI + rsub;
+                const float vv = (row < p.P) ? In<TIn>::lds(sv, j * p.P + row) : 0.f;
+                const float w = be * fmaf(-al, y, vv);
+                acc[kk].x = fmaf(al, acc[kk].x, w * kv.x);
+                acc[kk].y = fmaf(al, acc[kk].y, w * kv.y);
+                acc[kk].z = fmaf(al, acc[kk].z, w * kv.z);
+                acc[kk].w = fmaf(al, acc[kk].w, w * kv.w);
+              }
+            }
+          } else if constexpr (RPI == 1) {
             // The warp's 8 rows are consecutive and all valid (P is a multiple of 8).
             // Accumulate row pairs with packed fp32x2 fmas: A[kp][col] = {row 2kp, row 2kp+1}.
             f32x2 A[kKR / 2][4];
@@ -1343,6 +1451,14 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           float cwv[JI];
 #pragma unroll
           for (int i = 0; i < JI; ++i) cwv[i] = scj[cl + LP16 * i];
+          if constexpr (kDel) {  // the head's carried query u_0 replaces q
+            const float* su0 = sc + kCoefOff + kRMax;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float4 qq = lds4(su0 + (c * LP16 + cl) * 4);
+              q16[4 * c] = qq.x; q16[4 * c + 1] = qq.y; q16[4 * c + 2] = qq.z; q16[4 * c + 3] = qq.w;
+            }
+          }
           for (int r0 = wr * KW * RPW; r0 < p.P; r0 += wpg * KW * RPW) {
             float part[KW];
 #pragma unroll

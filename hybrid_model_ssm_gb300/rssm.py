@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "RSSM_OK", 1: "RSSM_EINVAL", 2: "RSSM_ECAPACITY", 3: "RSSM_EC
 DTYPES = {"f32": 0, "bf16": 1}
 READ_FMTS = {None: 0, "none": 0, "e4m3": 1, "e2m1": 2}
 CKPT_FMTS = {"f32": 0, "f16_sr": 1, "f16_rn": 2}
+RECURRENCES = {"outer": 0, "delta": 1}
 ERR_CAPACITY, ERR_ACCEPT, ERR_TIMEOUT, ERR_PLAN = 1, 2, 4, 8
 
 # The C ABI functions, with their argument types.
@@ -36,7 +37,7 @@ _vp = ctypes.c_void_p
 
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "H", "P", "N", "G", "L", "T_max", "in_dtype", "read_fmt",
-                                              "ckpt_fmt")] + [("seed", ctypes.c_uint64)]
+                                              "ckpt_fmt")] + [("seed", ctypes.c_uint64), ("recurrence", ctypes.c_int32)]
 
 
 _Cfg_p = ctypes.POINTER(Config)
@@ -47,6 +48,7 @@ SIGNATURES = {
     "rssm_create": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)],
     "rssm_decode_step": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_decode_step_static_scratch": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_decode_step_delta": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_verify": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_commit": [_vp, _vp, _vp],
     "rssm_flush": [_vp, ctypes.c_int32, _vp],
@@ -56,6 +58,7 @@ SIGNATURES = {
     "rssm_destroy": [_vp],
     "rssm_last_error": [],
     "rssm_conventional_step": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_conventional_step_delta": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_conventional_verify": [_Cfg_p, _vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_conventional_commit": [_Cfg_p, _vp, _vp, ctypes.c_int32, _vp, _vp],
     "rssm_round_f16": [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int32, _vp],
@@ -110,6 +113,7 @@ class LayerShape:
     read_fmt: str | None = None
     ckpt: str = "f32"  # checkpoint storage: "f32", "f16_sr" (stochastic rounding) or "f16_rn"
     seed: int = 0      # key of the stochastic rounding
+    recurrence: str = "outer"  # "outer" (gated outer product) or "delta" (gated delta rule)
 
     @property
     def R(self) -> int:
@@ -125,7 +129,7 @@ class LayerShape:
 
     def config(self) -> Config:
         return Config(self.B, self.H, self.P, self.N, self.G, self.L, self.T_max, DTYPES[self.in_dtype],
-                      READ_FMTS[self.read_fmt], CKPT_FMTS[self.ckpt], self.seed)
+                      READ_FMTS[self.read_fmt], CKPT_FMTS[self.ckpt], self.seed, RECURRENCES[self.recurrence])
 
 
 def workspace_size(shape: LayerShape) -> tuple[int, int, int]:
@@ -198,17 +202,25 @@ class ReplaySSM:
             self._h = None
 
     # ------------------------------------------------------------ decode path
-    def decode_step(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+    def decode_step(self, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:
+        """One decode step; a delta-rule layer also takes beta [B,H] fp32."""
         s = self.shape
         _expect(alpha, (s.B, s.H), torch.float32, "alpha")
+        if (beta is None) != (s.recurrence == "outer"):
+            raise ValueError("beta is required for (and only for) a delta-rule layer")
         _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v")
         _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k")
         _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q")
         if out is None:
             out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=alpha.device)
         _expect(out, (s.B, s.H, s.P), torch.float32, "out")
-        _check(lib().rssm_decode_step(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
-                                      _stream_ptr(stream)))
+        if beta is None:
+            _check(lib().rssm_decode_step(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
+                                          _stream_ptr(stream)))
+        else:
+            _expect(beta, (s.B, s.H), torch.float32, "beta")
+            _check(lib().rssm_decode_step_delta(self._h, _ptr(alpha), _ptr(beta), _ptr(v), _ptr(k), _ptr(q),
+                                                _ptr(out), _stream_ptr(stream)))
         return out
 
     def verify(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
@@ -259,9 +271,21 @@ class ReplaySSM:
         K = self.ring[k_off: k_off + s.B * s.G * R * s.N * es].view(s.torch_in_dtype).view(s.B, s.G, R, s.N)
         return a, V, K
 
+    def ring_betas(self):
+        """Write strengths [B,H,Rp] f32 of a delta-rule layer's ring (next 256-byte boundary after the decays)."""
+        s = self.shape
+        if s.recurrence != "delta":
+            raise ValueError("only delta-rule layers keep write strengths")
+        Rp = (s.R + 3) // 4 * 4
+        off = (s.B * s.H * Rp * 4 + 255) // 256 * 256
+        return self.ring[off: off + s.B * s.H * Rp * 4].view(torch.float32).view(s.B, s.H, Rp)
 
-def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
-    """The comparison kernel: S <- alpha S + v k^T, o = S q, state read and written in full."""
+
+def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:
+    """The comparison kernel: S <- alpha S + v k^T, o = S q, state read and written in full.
+
+    For a delta-rule shape (beta [B,H] given): S <- alpha S (I - beta k k^T) + beta v k^T.
+    """
     s = shape
     _expect(state, (s.B, s.H, s.P, s.N), torch.float32, "state")
     _expect(alpha, (s.B, s.H), torch.float32, "alpha")
@@ -271,8 +295,13 @@ def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream
     if out is None:
         out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=state.device)
     cfg = s.config()
-    _check(lib().rssm_conventional_step(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(v), _ptr(k), _ptr(q),
-                                        _ptr(out), _stream_ptr(stream)))
+    if beta is None:
+        _check(lib().rssm_conventional_step(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(v), _ptr(k), _ptr(q),
+                                            _ptr(out), _stream_ptr(stream)))
+    else:
+        _expect(beta, (s.B, s.H), torch.float32, "beta")
+        _check(lib().rssm_conventional_step_delta(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(beta), _ptr(v),
+                                                  _ptr(k), _ptr(q), _ptr(out), _stream_ptr(stream)))
     return out
 
 

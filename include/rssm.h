@@ -77,12 +77,25 @@ typedef enum {
   RSSM_CKPT_F16_RN = 2  /* FP16 checkpoint, stored rounded to nearest (comparison) */
 } rssm_ckpt_fmt;
 
+/* The layer's recurrence. RSSM_GATED_OUTER (default): S_t = alpha_t S_{t-1} +
+ * v_t k_t^T (Mamba-2-style heads, aikraft.ru page §01). RSSM_GATED_DELTA: the
+ * gated delta rule S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ * of Gated DeltaNet layers, which the pages name as using the same replay form
+ * (ai.cheesepanini.fun page, 方法/产品要点). Its replay output carries the query
+ * back through the buffered records: u_h = q, c_j = beta_j k_j^T u_j,
+ * u_{j-1} = alpha_j (u_j - c_j k_j), o = S_ckpt u_0 + sum_j c_j v_j; a fold
+ * applies S <- alpha_j S + beta_j (v_j - alpha_j S k_j) k_j^T in order. Delta
+ * layers decode with rssm_decode_step_delta; they need ckpt_fmt F32, read_fmt
+ * NONE, T_max = 1 and N in {64, 128} (verify is not offered for them). */
+typedef enum { RSSM_GATED_OUTER = 0, RSSM_GATED_DELTA = 1 } rssm_recurrence;
+
 typedef struct {
   int32_t B, H, P, N, G, L, T_max;
   int32_t in_dtype;
   int32_t read_fmt;
   int32_t ckpt_fmt;   /* rssm_ckpt_fmt; FP16 needs N in {64, 128} and read_fmt NONE */
   uint64_t seed;      /* FP16 stochastic rounding: generator key */
+  int32_t recurrence; /* rssm_recurrence */
 } rssm_config;
 
 typedef struct rssm_ctx* rssm_handle;
@@ -90,6 +103,7 @@ typedef struct rssm_ctx* rssm_handle;
 /* Byte sizes of the three caller-allocated buffers that rssm_create binds.
  *  ring_bytes: the record ring, made of
  *      alpha [B,H,Rp] fp32 (Rp = R rounded up to 4) at offset 0,
+ *      (delta layers) beta [B,H,Rp] fp32 right after it, 256-aligned,
  *      V     [B,H,R,P] in_dtype at offset v_off,
  *      K     [B,G,R,N] in_dtype at offset k_off (see rssm_ring_offsets).
  *  ptr_bytes: pointer block of int32 start[B], count[B], ticket[B], one
@@ -222,13 +236,31 @@ const char* rssm_last_error(void);
 rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, const void* v, const void* k,
                                             const void* q, float* o, void* stream);
 
+/* One decode step of a gated delta-rule layer (recurrence RSSM_GATED_DELTA):
+ * rssm_decode_step plus beta [B,H] fp32, the write strength of each head's
+ * record, kept in the ring beside alpha. Non-flush steps compute only the
+ * output (the replay form above); the step whose append brings the count to L
+ * folds the records in order and writes the checkpoint once. RSSM_EINVAL on a
+ * handle of the other recurrence (and rssm_decode_step refuses delta handles). */
+rssm_status rssm_decode_step_delta(rssm_handle h, const float* alpha, const float* beta, const void* v,
+                                   const void* k, const void* q, float* o, void* stream);
+
 /* Comparison kernel (not part of the replay path): the conventional fused
  * read-update-write step S <- alpha S + v k^T, o = S q on a full state
  * [B,H,P,N] fp32, read and written every step (aikraft.ru page §01). cfg's
- * L, T_max and read_fmt are ignored. */
+ * L, T_max and read_fmt are ignored; a delta-rule cfg is RSSM_EINVAL. */
 rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const float* alpha,
                                    const void* v, const void* k, const void* q, float* o,
                                    void* stream);
+
+/* Comparison kernel for gated delta-rule layers: the conventional step of that
+ * recurrence, S <- alpha S (I - beta k k^T) + beta v k^T, o = S q, reading and
+ * writing the full fp32 state every step. cfg->recurrence must be
+ * RSSM_GATED_DELTA (and rssm_conventional_step refuses such a cfg); beta [B,H]
+ * fp32, 16-byte aligned; the other arguments as for rssm_conventional_step. */
+rssm_status rssm_conventional_step_delta(const rssm_config* cfg, float* state, const float* alpha,
+                                         const float* beta, const void* v, const void* k, const void* q,
+                                         float* o, void* stream);
 
 /* Comparison kernels (not part of the replay path): conventional speculative
  * verify with per-draft state snapshots, the rollback scheme the replay design
@@ -245,7 +277,8 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
  *  - alpha [B,T,H] fp32; v [B,T,H,P], k and q [B,T,G,N] in cfg->in_dtype;
  *    o [B,T,H,P] fp32 (the layouts of rssm_verify).
  *  - err_word: one uint32 in device memory (bit 1 as above).
- *  - 1 <= T <= cfg->T_max, else RSSM_EINVAL. cfg->L and read_fmt are ignored.
+ *  - 1 <= T <= cfg->T_max, else RSSM_EINVAL. cfg->L and read_fmt are ignored;
+ *    a delta-rule cfg is RSSM_EUNSUPPORTED.
  * rssm_conventional_commit: cur[b] <- (cur[b] + accepted[b]) mod nslot, which
  * selects the snapshot after the accepted drafts (accepted[b] = 0 keeps the
  * state). accepted[b] outside 0..T, or cur[b] outside 0..nslot-1, leaves the

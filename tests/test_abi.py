@@ -93,3 +93,56 @@ def test_null_config_and_handle(lib):
     lib.rssm_last_error.restype = ctypes.c_char_p
     assert b"NULL" in lib.rssm_last_error()
     assert lib.rssm_destroy(None) == 0
+
+
+def test_config_struct_matches_the_header(tmp_path):
+    """ctypes' Config against the C compiler's layout of rssm_config."""
+    from hybrid_model_ssm_gb300.rssm import Config
+    src = tmp_path / "layout.c"
+    fields = [f for f, _ in Config._fields_]
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "rssm.h"\nint main(void) {\n'
+                   '  printf("%zu", sizeof(rssm_config));\n'
+                   + "".join(f'  printf(" %zu", offsetof(rssm_config, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(Config)
+    assert got[1:] == [getattr(Config, f).offset for f in fields]
+
+
+def test_delta_rule_ring_layout(lib):
+    """Delta-rule layers keep the write strengths [B,H,Rp] between the decays and V."""
+    s = LayerShape(B=3, H=4, P=64, N=128, G=2, L=5, recurrence="delta")
+    Rp, R = 8, 5
+    a_bytes = 3 * 4 * Rp * 4
+    b_off = (a_bytes + 255) // 256 * 256
+    v_off, k_off = ring_offsets(s)
+    assert v_off == (b_off + a_bytes + 255) // 256 * 256
+    assert k_off == (v_off + 3 * 4 * R * 64 * 2 + 255) // 256 * 256
+    assert workspace_size(s)[0] == (k_off + 3 * 2 * R * 128 * 2 + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=32), RSSM_EUNSUPPORTED),
+    (dict(T_max=2), RSSM_EUNSUPPORTED),
+    (dict(read_fmt="e4m3"), RSSM_EUNSUPPORTED),
+    (dict(ckpt="f16_sr"), RSSM_EUNSUPPORTED),
+])
+def test_delta_rule_configurations_are_limited(lib, kw, status):
+    base = dict(B=2, H=4, P=16, N=64, G=2, L=4, T_max=1, recurrence="delta")
+    base.update(kw)
+    with pytest.raises(RssmError) as ei:
+        workspace_size(LayerShape(**base))
+    assert ei.value.status == status
+
+
+def test_unknown_recurrence_is_rejected(lib):
+    from hybrid_model_ssm_gb300.rssm import Config
+    cfg = LayerShape(B=2, H=4, P=16, N=64, G=2, L=4).config()
+    cfg.recurrence = 7
+    r, p, q = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    lib.rssm_workspace_size.restype = ctypes.c_int
+    assert lib.rssm_workspace_size(ctypes.byref(cfg), ctypes.byref(r), ctypes.byref(p), ctypes.byref(q)) == RSSM_EINVAL
+    assert isinstance(cfg, Config)
