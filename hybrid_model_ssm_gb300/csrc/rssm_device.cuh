@@ -79,6 +79,7 @@ struct Params {
   int head_stride, bsc_off, rsc_off;
   float* ring_a;       // [B,H,Rp] decays
   float* ring_b;       // [B,H,Rp] write strengths (delta-rule layers)
+  float* ring_x;       // [B,H,R,Rp] rows of the inverse coupling matrix X (delta-rule layers)
   void* ring_v;        // [B,H,R,P] values (input dtype)
   void* ring_k;        // [B,G,R,N] keys (input dtype)
   int32_t* start;      // [B]
@@ -110,6 +111,7 @@ struct Params {
   int nf_ok;  // lay[1] is valid
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
+  int dsc_off;           // delta-rule layers: dot-warp scratch, [R][16] fp32 per dot warp
 };
 
 // ----------------------------------------------------------------- input types
@@ -577,18 +579,21 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr int CKES = kF16 ? 2 : 4;                             // checkpoint bytes per element
   constexpr bool kDel = (RF == kDelta);                          // gated delta-rule layer
   constexpr int kSbOff = (kRMax + kTMax) * 4;                    // delta: slot offset of the write strengths
+  constexpr int kXOff = 2 * (kRMax + kTMax) * 4;                 // delta: slot offset of the rows of X [R][Rp]
   constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   // bars: tfull[kMaxStages], tempty[kMaxStages], sfull[kMaxSlots], scoef[kMaxSlots],
-  //       sempty[kMaxSlots], gfull[2], gempty[2], end; then the abort flag
+  //       sempty[kMaxSlots], gfull[2], gempty[2], end; then the abort flag; then one
+  //       barrier per dot group (delta-rule heads: the group's shared coefficients)
   const uint32_t tfull0 = smem_u32(bars), tempty0 = smem_u32(bars + kMaxStages);
   const uint32_t sfull0 = smem_u32(bars + 2 * kMaxStages), scoef0 = sfull0 + 8 * kMaxSlots;
   const uint32_t sempty0 = scoef0 + 8 * kMaxSlots;
   const uint32_t gfull0 = sempty0 + 8 * kMaxSlots, gempty0 = gfull0 + 16;
   const uint32_t end_bar = gempty0 + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 3 * kMaxSlots + 5);
+  const uint32_t dgbar0 = smem_u32(bars + 2 * kMaxStages + 3 * kMaxSlots + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = (long long)p.B * p.H;
@@ -646,6 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       mbar_init(gempty0 + 8 * s, kNDW + kNCoef);
     }
     mbar_init(end_bar, kThreads);
+    if constexpr (kDel)
+      for (int g = 0; g < lay.dgroups; ++g) mbar_init(dgbar0 + 8 * g, kNDW / lay.dgroups);  // one arrival per warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -792,10 +799,13 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const uint32_t sbar = sfull0 + 8 * rs;
         const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
         // slot: decays at [ring slot] (committed) and kRMax + t (new); value rows in record order
-        mbar_arrive_tx(sbar, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 * (kDel ? 2 : 1) : 0u));
+        mbar_arrive_tx(sbar, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 * (kDel ? 2 + c : 1) : 0u));
         if (c > 0) {
           tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
-          if constexpr (kDel) tma_load_1d(sdst + kSbOff, p.ring_b + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
+          if constexpr (kDel) {  // the write strengths and the committed records' rows of X
+            tma_load_1d(sdst + kSbOff, p.ring_b + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
+            tma_load_1d(sdst + kXOff, p.ring_x + hrow * p.R * p.Rp, (uint32_t)(c * p.Rp) * 4, sbar);
+          }
           const int n1 = min(c, p.R - st);
           const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * rbytes;
           tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * rbytes, (uint32_t)n1 * rbytes, sbar);
@@ -828,11 +838,13 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   } else if (warp >= kCoef0 && warp < kCoef0 + kNCoef) {
     // ====================================================================== coefficients
     const int cwi = warp - kCoef0;  // this warp takes the loaded heads with index = cwi (mod kNCoef)
-    float* skq_w = reinterpret_cast<float*>(smem + p.wsc_off) + cwi * kTMax * kRMax;  // [kTMax][kRMax] (verify)
+    // scratch: [kTMax][kRMax] verify weights; delta: a row of couplings [kRMax]
+    float* skq_w = reinterpret_cast<float*>(smem + p.wsc_off) + cwi * kTMax * kRMax;
     int lh = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
     long long cur_gg = -1;
     bool load = false, flush = false, bad = false;
     float sj = 0.f;  // decode: lane j holds k_j^T q
+    float mj = 0.f;  // delta: lane j < c holds k_j^T k_c (the new record's key)
     const uint8_t* cK = smem + p.gb_off;  // the current group area: keys, then queries
     HeadIter it;
     it.init(h0, p.H, p.HPG);
@@ -860,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           const uint8_t* gK = smem + p.gb_off + gs * p.gb_bytes;
           const uint8_t* gQ = gK + p.gq_off;
           cK = gK;
-          if constexpr ((MODE == kDecode || MODE == kVerify) && !kDel) {
+          if constexpr (MODE == kDecode || MODE == kVerify) {
             // k_j^T q_t: one pair per lane, N/4 chunks visited from a lane-dependent start
             const int npair = J * nq;
             for (int pr = lane; pr < ((npair + 31) & ~31); pr += 32) {
@@ -881,6 +893,17 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               }
             }
             __syncwarp();
+          }
+          if constexpr (kDel && MODE != kFlush) {  // lane j < c: k_j^T k_c, the new key against the buffered ones
+            float acc = 0.f;
+            if (lane < c) {
+#pragma unroll 8
+              for (int t = 0; t < N / 4; ++t) {
+                const int c4 = (t + lane) & (N / 4 - 1);
+                acc += dot4(In<TIn>::lds4(gK, lane * N + 4 * c4), In<TIn>::lds4(gK, c * N + 4 * c4));
+              }
+            }
+            mj = acc;
           }
           if constexpr (kAppendMode) {  // the group's first head (if this CTA owns it) appends the new keys
             const long long gfirst = (long long)b * p.H + (long long)g * p.HPG;
@@ -920,52 +943,77 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if (lane == 0) sc[t] = incl;
         }
       } else if constexpr (kDel) {
-        // Gated delta rule, output without a fold: the query is carried back
-        // through the records, u_J = q, c_j = beta_j k_j^T u_j,
-        // u_{j-1} = alpha_j (u_j - c_j k_j); then o = S u_0 + sum_j c_j v_j, which
-        // the dot warps form with sc[0] = 1, the weights c_j and u_0. A folding
-        // head needs nothing here: the dot warps apply its records in order.
-        if constexpr (MODE == kDecode) {
-          if (!flush) {
-            constexpr int NPL = N / 32;  // query elements per lane: N/32 consecutive
-            static_assert(NPL == 2 || NPL == 4, "delta-rule layers: N in {64, 128}");
-            const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
-            const uint8_t* cQ = cK + p.gq_off;
-            float u[NPL];
-            if constexpr (NPL == 4) {
-              const float4 x = In<TIn>::lds4(cQ, lane * 4);
-              u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
-            } else {
-              const float2 x = In<TIn>::lds2(cQ, lane * 2);
-              u[0] = x.x; u[1] = x.y;
-            }
-            float cj = 0.f;  // lane j: c_j
-            for (int j = J - 1; j >= 0; --j) {
-              const int sl = (j < c) ? ring_slot(st, j, p.R) : kRMax + j - c;
-              const float al = sa[sl], be = sbeta[sl];
-              float kx[NPL];
-              if constexpr (NPL == 4) {
-                const float4 x = In<TIn>::lds4(cK, j * N + lane * 4);
-                kx[0] = x.x; kx[1] = x.y; kx[2] = x.z; kx[3] = x.w;
-              } else {
-                const float2 x = In<TIn>::lds2(cK, j * N + lane * 2);
-                kx[0] = x.x; kx[1] = x.y;
-              }
-              float d = 0.f;
+        // Gated delta rule. Per row of the state, the records' values w_j solve
+        // T w = r with r_j = beta_j (v_j - alpha_j P_j S k_j), P_j = alpha_0 .. alpha_{j-1},
+        // and T = I + diag(beta alpha) A, A_ji = alpha_{i+1} .. alpha_{j-1} k_i^T k_j (i < j):
+        // the state after the J records is (prod alpha) S + sum_i W_i w_i k_i^T with
+        // W_i = alpha_{i+1} .. alpha_{J-1}. X = T^-1 is unit lower triangular and
+        // grows by one row per record (row c from rows < c), so the ring keeps its
+        // rows and every coefficient below is a parallel sum.
+        const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
+        float* sX = reinterpret_cast<float*>(slot + kXOff);  // [R][Rp], row j = record j
+        const int Rp = p.Rp;
+        const float bj = (lane < J) ? sbeta[(lane < c) ? ring_slot(st, lane, p.R) : kRMax + lane - c] : 0.f;
+        // scratch: [0, 32) a row of couplings, [32, 64) and [64, 96) broadcast weights
+        float* sw = skq_w;
+        float incl;  // alpha_lane .. alpha_{J-1}
+        if constexpr (MODE != kFlush) {
+          // row c of X for the new record: X_ci = -beta_c alpha_c sum_{l=i}^{c-1} A_cl X_li
+          const float sfx = suffix_prod((lane < c) ? aj : 1.f, lane);  // alpha_lane .. alpha_{c-1}
+          const float dn = __shfl_down_sync(kFull, sfx, 1);
+          const float ac = __shfl_sync(kFull, aj, c), bc = __shfl_sync(kFull, bj, c);
+          incl = (lane <= c) ? sfx * ac : 1.f;
+          sw[lane] = (lane < c) ? ((lane < 31) ? dn : 1.f) * mj : 0.f;  // A_c,lane
+          __syncwarp();
+          float xs = 0.f;
+#pragma unroll 4
+          for (int l = lane; l < c; ++l) xs = fmaf(sw[l], sX[l * Rp + lane], xs);
+          xs = (lane < c) ? -(ac * bc) * xs : (lane == c ? 1.f : 0.f);
+          if (lane < Rp) sX[c * Rp + lane] = xs;
+        } else {
+          incl = suffix_prod(aj, lane);
+        }
+        const float nxt = __shfl_down_sync(kFull, incl, 1);
+        const float wsuf = (lane < 31) ? nxt : 1.f;   // W_lane
+        const float gall = __shfl_sync(kFull, incl, 0);
+        float pin = aj;                               // alpha_0 .. alpha_lane
 #pragma unroll
-              for (int e = 0; e < NPL; ++e) d = fmaf(kx[e], u[e], d);
-              const float cc = be * warp_allsum(d);
-              if (lane == j) cj = cc;
-#pragma unroll
-              for (int e = 0; e < NPL; ++e) u[e] = al * fmaf(-cc, kx[e], u[e]);
-            }
-            if (lane == 0) sc[0] = 1.f;
-            sc[kCoefOff + lane] = (lane < J) ? cj : 0.f;
-            float* su0 = sc + kCoefOff + kRMax;  // u_0, natural order
-            if constexpr (NPL == 4) {
-              *reinterpret_cast<float4*>(su0 + lane * 4) = make_float4(u[0], u[1], u[2], u[3]);
-            } else {
-              *reinterpret_cast<float2*>(su0 + lane * 2) = make_float2(u[0], u[1]);
+        for (int d = 1; d < 32; d <<= 1) {
+          const float y = __shfl_up_sync(kFull, pin, d);
+          if (lane >= d) pin *= y;
+        }
+        const float pup = __shfl_up_sync(kFull, pin, 1);
+        const float pex = (lane == 0) ? 1.f : pup;    // P_lane
+        __syncwarp();
+        if (MODE == kDecode && !flush) {
+          // o = (prod alpha) S q + sum_j z_j r_j with z_j = sum_{i>=j} W_i s_i X_ij:
+          // record weights c_j = z_j beta_j and the carried query
+          // u_0 = (prod alpha) q - sum_j z_j beta_j alpha_j P_j k_j, so o = S u_0 + sum_j c_j v_j
+          static_assert(N == 64 || N == 128, "delta-rule layers: N in {64, 128}");
+          sw[32 + lane] = wsuf * sj;  // W_i s_i
+          __syncwarp();
+          float z = 0.f;
+#pragma unroll 4
+          for (int i = lane; i < J; ++i) z = fmaf(sw[32 + i], sX[i * Rp + lane], z);
+          const float cme = (lane < J) ? z * bj : 0.f;
+          // the dot group forms u_0 from q, the keys and e_j (all its threads at once)
+          if (lane == 0) { sc[0] = 1.f; sc[1] = gall; }
+          sc[kCoefOff + lane] = cme;                  // c_j, 0 past J
+          sc[kCoefOff + kRMax + lane] = cme * aj * pex;  // e_j, 0 past J
+        } else {
+          // fold: per row u_i = sum_{j<=i} Bv_ij v_j + Bw_ij (S k_j) = Vp_i + S kappa_i with
+          // Bv_ij = W_i X_ij beta_j and Bw_ij = -W_i X_ij beta_j alpha_j P_j; the dot
+          // group forms kappa_i = sum_{j<=i} Bw_ij k_j and Vp_i = sum_{j<=i} Bv_ij v_j
+          if (lane == 0) sc[0] = gall;
+          float* Bv = sc + kCoefOff;
+          float* Bw = Bv + p.R * p.R;
+          const float fw = -bj * aj * pex;
+          for (int i = 0; i < J; ++i) {
+            const float wi = __shfl_sync(kFull, wsuf, i);
+            if (lane <= i) {
+              const float xw = wi * sX[i * Rp + lane];
+              Bv[i * p.R + lane] = xw * bj;
+              Bw[i * p.R + lane] = xw * fw;
             }
           }
         }
@@ -1017,6 +1065,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
         }
 #endif
+        if constexpr (kDel) {  // the new record's row of X, by record index
+          if (na > 0 && lane < p.Rp)
+            p.ring_x[(hrow * p.R + c) * p.Rp + lane] = reinterpret_cast<const float*>(slot + kXOff)[c * p.Rp + lane];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty0 + 8 * rs);  // this warp is done with the slot
@@ -1048,6 +1100,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     const int dgrp = warp / wpg, wr = warp - dgrp * wpg;  // this warp's group and rank in it
     const int rows_pass = wpg * kKR * RPI;
     const int npass = (p.P + rows_pass - 1) / rows_pass;
+    // delta-rule heads: the group's warps share per-head work through the group's
+    // barrier (bounded wait; one arrival per warp, phase dph)
+    int dph = 0;
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dgbar0 + 8 * dgrp);
+      const bool w = mbar_wait(dgbar0 + 8 * dgrp, dph, abort_flag, p.err);
+      dph ^= 1;
+      return __all_sync(kFull, w);
+    };
     int lh = 0;  // loaded heads seen
     HeadIter it;
     it.init(h0, p.H, p.HPG);
@@ -1285,49 +1347,100 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       } else if (flush) {
         // ================================================ fold path
         // S_new = g_{1:J} S + sum_j u_j k_j^T with u_j = g_{j+2:J} v_j ; store ; o = S_new q
+        // Delta rule: the same update, with the values u_i of each row formed here
+        // from the head's kappa_i and Vp_i (rows of this warp only, into its scratch).
         const float gam = sc[0];
-        const float* su = sc + kCoefOff;  // [J][P]
+        const float* su = sc + kCoefOff;  // [J][P] scaled values (outer-product rule)
+        float* dU = kDel ? reinterpret_cast<float*>(smem + p.dsc_off) + warp * p.R * 16 : nullptr;  // [R][16]
+        if constexpr (kDel) {  // kappa_i [N] and Vp_i [P] of the head, formed by the group's threads
+          float* kapw = const_cast<float*>(sc) + ((kCoefOff + 2 * p.R * p.R + 3) & ~3);
+          float* vptw = kapw + p.R * N;
+          const float* Bv = sc + kCoefOff;
+          const float* Bw = Bv + p.R * p.R;
+          const int nk = J * (N / 4), nv = J * (p.P / 2);
+          for (int it = wr * 32 + lane; it < nk + nv; it += wpg * 32) {
+            if (it < nk) {
+              const int i = it / (N / 4), ch = it - i * (N / 4);
+              float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+              for (int j = 0; j <= i; ++j) {
+                const float bw = Bw[i * p.R + j];
+                const float4 kv = In<TIn>::lds4(gK, j * N + ch * 4);
+                a.x = fmaf(bw, kv.x, a.x); a.y = fmaf(bw, kv.y, a.y);
+                a.z = fmaf(bw, kv.z, a.z); a.w = fmaf(bw, kv.w, a.w);
+              }
+              *reinterpret_cast<float4*>(kapw + i * N + ch * 4) = a;
+            } else {
+              const int t = it - nk, i = t / (p.P / 2), pr = t - i * (p.P / 2);
+              float2 a = make_float2(0.f, 0.f);
+#pragma unroll 4
+              for (int j = 0; j <= i; ++j) {
+                const float bv = Bv[i * p.R + j];
+                const float2 v2 = In<TIn>::lds2(sv, j * p.P + 2 * pr);
+                a.x = fmaf(bv, v2.x, a.x); a.y = fmaf(bv, v2.y, a.y);
+              }
+              *reinterpret_cast<float2*>(vptw + i * p.P + 2 * pr) = a;
+            }
+          }
+          if (!group_sync()) { ok = false; break; }
+        }
         for (int pass = 0; pass < npass; ++pass) {
           const int rbase = (pass * wpg + wr) * kKR;
           if (rbase * RPI >= p.P) break;  // warp-uniform: no rows left for this warp
-          float4 acc[kKR];
+          // values of the warp's rows: ub[j * us + local row], local row = row - rbase * RPI
+          const float* ub = kDel ? dU : su + rbase * RPI;
+          const int us = kDel ? 16 : p.P;
           if constexpr (kDel) {
-            // Gated delta rule, records in order: y = S k_j (the current S),
-            // S <- alpha_j S + beta_j (v_j - alpha_j y) k_j^T. The row sums of the
-            // warp's kKR row instructions are reduced transposed (lane seg + kk D
-            // ends with row kk's sum) and handed back to every lane of the row.
-            static_assert(LPR >= kKR, "delta-rule fold: a row spans at least kKR lanes");
-            constexpr int D = LPR / kKR;
-            const float* salpha = reinterpret_cast<const float*>(slot);
-            const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
-            const int seg = lane & ~(LPR - 1);
+            // u_i[row] = Vp_i[row] + S_row . kappa_i for the warp's rows. Here a row
+            // spans LPW = N/16 lanes of 16 columns (4 interleaved chunks of 4, as in the
+            // non-flush rows) and each lane holds two rows; RB records per transposed
+            // reduction leave one (record, row) sum per lane.
+            constexpr int LPW = N / 16, RPW = 32 / LPW, RB = LPW / 2;
+            static_assert(2 * RPW == kKR * RPI && kKR * RPI <= 16, "delta-rule fold: two row instructions per pass");
+            const int cl = lane % LPW, rw = lane / LPW;
+            const float* kap = sc + ((kCoefOff + 2 * p.R * p.R + 3) & ~3);
+            const float* vpt = kap + p.R * N;
+            f32x2 xr[2][8];  // column pairs of the lane's two rows
 #pragma unroll
-            for (int kk = 0; kk < kKR; ++kk) {
-              const int row = (rbase + kk) * RPI + rsub;
-              acc[kk] = (row < p.P) ? ld_tile4<false>(tile, (size_t)row * N + col4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            for (int j = 0; j < J; ++j) {
-              const int sl = (j < c) ? ring_slot(st, j, p.R) : kRMax + j - c;
-              const float al = salpha[sl], be = sbeta[sl];
-              const float4 kv = In<TIn>::lds4(gK, j * N + col4 * 4);
-              float part[kKR];
+            for (int ri = 0; ri < 2; ++ri) {
+              const int row = rbase * RPI + ri * RPW + rw;
 #pragma unroll
-              for (int kk = 0; kk < kKR; ++kk) part[kk] = dot4(acc[kk], kv);
-              int off = 0;
-              TRed<kKR, LPR / 2>::run(part, lane, off);
-#pragma unroll
-              for (int kk = 0; kk < kKR; ++kk) {
-                const float y = __shfl_sync(kFull, part[0], seg + kk * D);
-                const int row = (rbase + kk) * RPI + rsub;
-                const float vv = (row < p.P) ? In<TIn>::lds(sv, j * p.P + row) : 0.f;
-                const float w = be * fmaf(-al, y, vv);
-                acc[kk].x = fmaf(al, acc[kk].x, w * kv.x);
-                acc[kk].y = fmaf(al, acc[kk].y, w * kv.y);
-                acc[kk].z = fmaf(al, acc[kk].z, w * kv.z);
-                acc[kk].w = fmaf(al, acc[kk].w, w * kv.w);
+              for (int cc = 0; cc < 4; ++cc) {
+                ulonglong2 t = make_ulonglong2(0ull, 0ull);
+                if (row < p.P) t = *reinterpret_cast<const ulonglong2*>(tf + (size_t)row * N + (cc * LPW + cl) * 4);
+                xr[ri][2 * cc] = t.x;
+                xr[ri][2 * cc + 1] = t.y;
               }
             }
-          } else if constexpr (RPI == 1) {
+            for (int i0 = 0; i0 < J; i0 += RB) {
+              float part[2 * RB];
+#pragma unroll
+              for (int jj = 0; jj < RB; ++jj) {
+                f32x2 a0 = 0ull, a1 = 0ull;
+                if (i0 + jj < J) {
+                  const float* kr = kap + (i0 + jj) * N;
+#pragma unroll
+                  for (int cc = 0; cc < 4; ++cc) {
+                    const ulonglong2 kq = *reinterpret_cast<const ulonglong2*>(kr + (cc * LPW + cl) * 4);
+                    a0 = fma2(xr[0][2 * cc], kq.x, a0);
+                    a0 = fma2(xr[0][2 * cc + 1], kq.y, a0);
+                    a1 = fma2(xr[1][2 * cc], kq.x, a1);
+                    a1 = fma2(xr[1][2 * cc + 1], kq.y, a1);
+                  }
+                }
+                part[2 * jj] = lo2(a0) + hi2(a0);
+                part[2 * jj + 1] = lo2(a1) + hi2(a1);
+              }
+              int off = 0;
+              TRed<2 * RB, LPW / 2>::run(part, lane, off);
+              const int i = i0 + (off >> 1), lr = (off & 1) * RPW + rw;
+              const int row = rbase * RPI + lr;
+              if (i < J && row < p.P) dU[i * 16 + lr] = part[0] + vpt[i * p.P + row];
+            }
+            __syncwarp();
+          }
+          float4 acc[kKR];
+          if constexpr (RPI == 1) {
             // The warp's 8 rows are consecutive and all valid (P is a multiple of 8).
             // Accumulate row pairs with packed fp32x2 fmas: A[kp][col] = {row 2kp, row 2kp+1}.
             f32x2 A[kKR / 2][4];
@@ -1347,7 +1460,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               f32x2 U[kKR / 2];
 #pragma unroll
               for (int qd = 0; qd < kKR / 4; ++qd) {
-                const ulonglong2 uq = *reinterpret_cast<const ulonglong2*>(su + j * p.P + rbase + 4 * qd);
+                const ulonglong2 uq = *reinterpret_cast<const ulonglong2*>(ub + j * us + 4 * qd);
                 U[2 * qd] = uq.x;
                 U[2 * qd + 1] = uq.y;
               }
@@ -1381,7 +1494,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
               for (int kk = 0; kk < kKR; ++kk) {
                 const int row = (rbase + kk) * RPI + rsub;
-                uu[kk] = (row < p.P) ? su[j * p.P + row] : 0.f;
+                uu[kk] = (row < p.P) ? ub[j * us + kk * RPI + rsub] : 0.f;
               }
 #pragma unroll
               for (int kk = 0; kk < kKR; ++kk) {
@@ -1451,8 +1564,23 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           float cwv[JI];
 #pragma unroll
           for (int i = 0; i < JI; ++i) cwv[i] = scj[cl + LP16 * i];
-          if constexpr (kDel) {  // the head's carried query u_0 replaces q
-            const float* su0 = sc + kCoefOff + kRMax;
+          if constexpr (kDel) {  // u_0 = (prod alpha) q - sum_j e_j k_j, formed by the group, replaces q
+            float* su0 = const_cast<float*>(sc) + kCoefOff + 2 * kRMax;
+            const float gall = sc[1];
+            const float* ej = sc + kCoefOff + kRMax;
+            for (int ch = wr * 32 + lane; ch < N / 4; ch += wpg * 32) {
+              const float4 qv = In<TIn>::lds4(gQ, ch * 4);
+              float4 u = make_float4(gall * qv.x, gall * qv.y, gall * qv.z, gall * qv.w);
+#pragma unroll 4
+              for (int j = 0; j < J; ++j) {
+                const float e = ej[j];
+                const float4 kv = In<TIn>::lds4(gK, j * N + ch * 4);
+                u.x = fmaf(-e, kv.x, u.x); u.y = fmaf(-e, kv.y, u.y);
+                u.z = fmaf(-e, kv.z, u.z); u.w = fmaf(-e, kv.w, u.w);
+              }
+              *reinterpret_cast<float4*>(su0 + ch * 4) = u;
+            }
+            if (!group_sync()) { ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const float4 qq = lds4(su0 + (c * LP16 + cl) * 4);
