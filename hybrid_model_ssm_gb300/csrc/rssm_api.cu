@@ -40,7 +40,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Geom {
   int R = 0, Rp = 0, esize = 0, ck_es = 4, rf = 0;  // ck_es: checkpoint bytes per element; rf: tile format
-  size_t b_off = 0, x_off = 0, v_off = 0, k_off = 0, ring_bytes = 0;  // b_off, x_off: delta layers only
+  size_t v_off = 0, k_off = 0, ring_bytes = 0;
   size_t off_count = 0, off_ticket = 0, off_err = 0, off_epoch = 0, ptr_bytes = 0;
   size_t head_stride = 0, bsc_off = 0, rsc_off = 0, copy_bytes = 0;
 };
@@ -83,12 +83,10 @@ rssm_status derive(const rssm_config* c, Geom* g) {
                                            : c->read_fmt;
   const size_t B = c->B, H = c->H, P = c->P, N = c->N, G = c->G;
   const size_t a_bytes = B * H * g->Rp * 4;
-  // delta layers: the write strengths [B,H,Rp] and the inverse coupling rows [B,H,R,Rp]
-  const bool delta = c->recurrence == RSSM_GATED_DELTA;
-  g->b_off = delta ? align_up(a_bytes, 256) : 0;
-  g->x_off = delta ? align_up(g->b_off + a_bytes, 256) : 0;
-  g->v_off = delta ? align_up(g->x_off + B * H * R * g->Rp * 4, 256) : align_up(a_bytes, 256);
-  g->k_off = align_up(g->v_off + B * H * R * P * g->esize, 256);
+  // delta layers keep each record's pseudo-value w (fp32) where the others keep v
+  const size_t w_es = c->recurrence == RSSM_GATED_DELTA ? 4 : (size_t)g->esize;
+  g->v_off = align_up(a_bytes, 256);
+  g->k_off = align_up(g->v_off + B * H * R * P * w_es, 256);
   g->ring_bytes = align_up(g->k_off + B * G * R * N * g->esize, 256);
   const size_t pb = align_up(B * 4, 256);
   g->off_count = pb;
@@ -131,20 +129,19 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   const size_t P = c->P, N = c->N, es = (size_t)g.esize, R = g.R;
   const size_t tile = a128(nf && g.head_stride ? g.head_stride : P * N * (size_t)g.ck_es);
   const size_t vrows = nf ? (size_t)c->L : R;
-  // decays: kRMax ring slots, then kTMax new records; delta layers keep the
-  // write strengths the same way right after them, then the rows of X [R][Rp]
+  // decays: kRMax ring slots, then kTMax new records; delta layers keep the new
+  // records' write strengths the same way right after them, their buffered
+  // pseudo-values (fp32) as the value rows and the new record's v row after those
   const bool delta = g.rf == rssm::kDelta;
-  const size_t sv_off = delta ? align_up((size_t)(kRMax + kTMax) * 8 + R * g.Rp * 4, 16) : (size_t)(kRMax + kTMax) * 4;
-  const size_t sc_off = align_up(sv_off + vrows * P * es, 16);
+  const size_t sv_off = (size_t)(kRMax + kTMax) * 4 * (delta ? 2 : 1);
+  const size_t nv_off = sv_off + vrows * P * (delta ? 4 : es);
+  const size_t sc_off = align_up(nv_off + (delta ? P * es : 0), 16);
   // coefficients: 16 scalars, then the record weights [kRMax] (non-flush),
   // [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general, which
   // also serves non-flush heads)
-  // delta layers: non-flush heads 16 scalars, the record weights c_j and e_j
-  // [kRMax] each and the carried query u_0 [N]; folding heads 16 scalars, the two
-  // value maps [R][R], then kappa [R][N] and the value parts [R][P]
-  const size_t delta_nf = 16 + 2 * (size_t)kRMax + N;
-  const size_t delta_fold = align_up(16 + 2 * R * R, 4) + R * N + R * P;
-  const size_t sc_floats = delta ? (nf ? delta_nf : std::max(delta_nf, delta_fold))
+  // delta layers: 16 scalars, the output weights and the new record's couplings
+  // [kRMax] each, then (general) the fold's scaled values [R][P]
+  const size_t sc_floats = delta ? 16 + 2 * (size_t)kRMax + (nf ? 0 : R * P)
                          : nf    ? 16 + std::max(P, (size_t)kRMax)
                               : kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax
                                                             : 16 + std::max({(size_t)kRMax, R * P, (size_t)c->T_max * P});
@@ -177,6 +174,7 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   L->slot_bytes = (int)slot;
   L->slot_off = (int)((size_t)stages_used * tile);
   L->sv_off = (int)sv_off;
+  L->nv_off = (int)nv_off;
   L->sc_off = (int)sc_off;
   if ((size_t)L->slot_off + (size_t)slots_used * slot > budget) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
   return RSSM_OK;
@@ -191,10 +189,8 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   const size_t gq_off = R * N * es;
   const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
   const size_t wsc = a128((size_t)kNCoef * kTMax * kRMax * 4);
-  // delta layers: per dot warp, the fold's values of its rows [R][16]
-  const size_t dsc = g.rf == rssm::kDelta ? (size_t)kNDW * R * 16 * 4 : 0;
-  const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6 + 8) * 8);  // + one barrier per dot group
-  const size_t fixed = 2 * gb + wsc + dsc + bars;
+  const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6) * 8);
+  const size_t fixed = 2 * gb + wsc + bars;
   if (fixed >= (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "group areas too large for shared memory");
   const size_t budget = ((size_t)kSmemMax - fixed) / 128 * 128;
   rssm::Params& p = pl->p;
@@ -211,7 +207,6 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   p.gb_bytes = (int)gb;
   p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
-  p.dsc_off = (int)off; off += dsc;
   p.bar_off = (int)off; off += bars;
   if (off > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
   pl->stages = p.lay[0].stages;
@@ -256,8 +251,6 @@ void fill_common(const rssm_ctx* h, rssm::Params* p) {
   p->bsc_off = (int)h->g.bsc_off;
   p->rsc_off = (int)h->g.rsc_off;
   p->ring_a = reinterpret_cast<float*>(h->ring);
-  p->ring_b = h->g.b_off ? reinterpret_cast<float*>(h->ring + h->g.b_off) : nullptr;
-  p->ring_x = h->g.x_off ? reinterpret_cast<float*>(h->ring + h->g.x_off) : nullptr;
   p->ring_v = h->ring + h->g.v_off;
   p->ring_k = h->ring + h->g.k_off;
   p->start = reinterpret_cast<int32_t*>(h->ptrs);

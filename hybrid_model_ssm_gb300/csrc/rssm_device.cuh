@@ -61,14 +61,15 @@ constexpr unsigned kFull = 0xffffffffu;
 enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4, kSnap = 5 };
 // Storage formats of the head tile: the FP32 checkpoint (kRfNone), an E4M3 or
 // E2M1 read copy next to it, or an FP16 checkpoint (kCkF16: no read copy).
-// kDelta: an FP32 checkpoint of a gated delta-rule layer (the same tiles, the
-// delta rule's replay form and fold).
+// kDelta: an FP32 checkpoint of a gated delta-rule layer (the same tiles; the
+// ring keeps each record's pseudo-value w instead of v).
 enum Rf : int { kRfNone = 0, kRfE4m3 = 1, kRfE2m1 = 2, kCkF16 = 3, kDelta = 4 };
 enum Err : uint32_t { kErrCapacity = 1u, kErrAccept = 2u, kErrTimeout = 4u, kErrPlan = 8u };
 
 // One partition of a CTA's shared memory into tile stages and record slots.
 struct Layout {
   int stages, stage_bytes, slots, slot_bytes, slot_off, sv_off, sc_off;
+  int nv_off;   // delta-rule layers: the new record's v row
   int dgroups;  // dot-warp groups (1, 2, 4 or 8): group d takes every dgroups-th head, so that many are in flight
 };
 
@@ -78,9 +79,7 @@ struct Params {
   uint8_t* copy;       // read copy: head_stride bytes per (b,h), or null
   int head_stride, bsc_off, rsc_off;
   float* ring_a;       // [B,H,Rp] decays
-  float* ring_b;       // [B,H,Rp] write strengths (delta-rule layers)
-  float* ring_x;       // [B,H,R,Rp] rows of the inverse coupling matrix X (delta-rule layers)
-  void* ring_v;        // [B,H,R,P] values (input dtype)
+  void* ring_v;        // [B,H,R,P] values (input dtype); delta-rule layers: pseudo-values w (fp32)
   void* ring_k;        // [B,G,R,N] keys (input dtype)
   int32_t* start;      // [B]
   int32_t* count;      // [B]
@@ -111,7 +110,6 @@ struct Params {
   int nf_ok;  // lay[1] is valid
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
-  int dsc_off;           // delta-rule layers: dot-warp scratch, [R][16] fp32 per dot warp
 };
 
 // ----------------------------------------------------------------- input types
@@ -579,21 +577,18 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr int CKES = kF16 ? 2 : 4;                             // checkpoint bytes per element
   constexpr bool kDel = (RF == kDelta);                          // gated delta-rule layer
   constexpr int kSbOff = (kRMax + kTMax) * 4;                    // delta: slot offset of the write strengths
-  constexpr int kXOff = 2 * (kRMax + kTMax) * 4;                 // delta: slot offset of the rows of X [R][Rp]
   constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   // bars: tfull[kMaxStages], tempty[kMaxStages], sfull[kMaxSlots], scoef[kMaxSlots],
-  //       sempty[kMaxSlots], gfull[2], gempty[2], end; then the abort flag; then one
-  //       barrier per dot group (delta-rule heads: the group's shared coefficients)
+  //       sempty[kMaxSlots], gfull[2], gempty[2], end; then the abort flag
   const uint32_t tfull0 = smem_u32(bars), tempty0 = smem_u32(bars + kMaxStages);
   const uint32_t sfull0 = smem_u32(bars + 2 * kMaxStages), scoef0 = sfull0 + 8 * kMaxSlots;
   const uint32_t sempty0 = scoef0 + 8 * kMaxSlots;
   const uint32_t gfull0 = sempty0 + 8 * kMaxSlots, gempty0 = gfull0 + 16;
   const uint32_t end_bar = gempty0 + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 3 * kMaxSlots + 5);
-  const uint32_t dgbar0 = smem_u32(bars + 2 * kMaxStages + 3 * kMaxSlots + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total = (long long)p.B * p.H;
@@ -624,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   lay.slot_off = lean ? p.lay[1].slot_off : p.lay[0].slot_off;
   lay.sv_off = lean ? p.lay[1].sv_off : p.lay[0].sv_off;
   lay.sc_off = lean ? p.lay[1].sc_off : p.lay[0].sc_off;
+  lay.nv_off = lean ? p.lay[1].nv_off : p.lay[0].nv_off;
   lay.dgroups = lean ? p.lay[1].dgroups : p.lay[0].dgroups;
 
   // The parity waits need every ring to be a multiple of the consumers that take
@@ -651,8 +647,6 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       mbar_init(gempty0 + 8 * s, kNDW + kNCoef);
     }
     mbar_init(end_bar, kThreads);
-    if constexpr (kDel)
-      for (int g = 0; g < lay.dgroups; ++g) mbar_init(dgbar0 + 8 * g, kNDW / lay.dgroups);  // one arrival per warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -799,24 +793,23 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         const uint32_t sbar = sfull0 + 8 * rs;
         const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
         // slot: decays at [ring slot] (committed) and kRMax + t (new); value rows in record order
-        mbar_arrive_tx(sbar, (uint32_t)J * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 * (kDel ? 2 + c : 1) : 0u));
+        // delta-rule layers: buffered records bring their pseudo-values (fp32) and
+        // the new record its v row, to nv_off
+        const uint32_t vb = kDel ? (uint32_t)p.P * 4 : rbytes;  // bytes of a buffered value row
+        mbar_arrive_tx(sbar, (uint32_t)c * vb + (uint32_t)nnew * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
         if (c > 0) {
           tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
-          if constexpr (kDel) {  // the write strengths and the committed records' rows of X
-            tma_load_1d(sdst + kSbOff, p.ring_b + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
-            tma_load_1d(sdst + kXOff, p.ring_x + hrow * p.R * p.Rp, (uint32_t)(c * p.Rp) * 4, sbar);
-          }
           const int n1 = min(c, p.R - st);
-          const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * rbytes;
-          tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * rbytes, (uint32_t)n1 * rbytes, sbar);
-          if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * rbytes, rv, (uint32_t)(c - n1) * rbytes, sbar);
+          const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * vb;
+          tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * vb, (uint32_t)n1 * vb, sbar);
+          if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * vb, rv, (uint32_t)(c - n1) * vb, sbar);
         }
         for (int t = 0; t < nnew; ++t) {
           const size_t nrow = kDrafts ? ((size_t)b * p.T + t) * p.H + hh : hrow;
           cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
           if constexpr (kDel) cp_async4(sdst + kSbOff + 4 * (kRMax + t), p.beta + nrow);
-          tma_load_1d(sdst + lay.sv_off + (c + t) * rbytes, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes,
-                      rbytes, sbar);
+          const uint32_t vdst = kDel ? sdst + lay.nv_off + t * rbytes : sdst + lay.sv_off + (c + t) * rbytes;
+          tma_load_1d(vdst, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes, rbytes, sbar);
         }
         cp_async_arrive(sbar);  // completes with this lane's decay copies
         slot_next();
@@ -943,77 +936,40 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           if (lane == 0) sc[t] = incl;
         }
       } else if constexpr (kDel) {
-        // Gated delta rule. Per row of the state, the records' values w_j solve
-        // T w = r with r_j = beta_j (v_j - alpha_j P_j S k_j), P_j = alpha_0 .. alpha_{j-1},
-        // and T = I + diag(beta alpha) A, A_ji = alpha_{i+1} .. alpha_{j-1} k_i^T k_j (i < j):
-        // the state after the J records is (prod alpha) S + sum_i W_i w_i k_i^T with
-        // W_i = alpha_{i+1} .. alpha_{J-1}. X = T^-1 is unit lower triangular and
-        // grows by one row per record (row c from rows < c), so the ring keeps its
-        // rows and every coefficient below is a parallel sum.
-        const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
-        float* sX = reinterpret_cast<float*>(slot + kXOff);  // [R][Rp], row j = record j
-        const int Rp = p.Rp;
-        const float bj = (lane < J) ? sbeta[(lane < c) ? ring_slot(st, lane, p.R) : kRMax + lane - c] : 0.f;
-        // scratch: [0, 32) a row of couplings, [32, 64) and [64, 96) broadcast weights
-        float* sw = skq_w;
-        float incl;  // alpha_lane .. alpha_{J-1}
-        if constexpr (MODE != kFlush) {
-          // row c of X for the new record: X_ci = -beta_c alpha_c sum_{l=i}^{c-1} A_cl X_li
-          const float sfx = suffix_prod((lane < c) ? aj : 1.f, lane);  // alpha_lane .. alpha_{c-1}
-          const float dn = __shfl_down_sync(kFull, sfx, 1);
-          const float ac = __shfl_sync(kFull, aj, c), bc = __shfl_sync(kFull, bj, c);
-          incl = (lane <= c) ? sfx * ac : 1.f;
-          sw[lane] = (lane < c) ? ((lane < 31) ? dn : 1.f) * mj : 0.f;  // A_c,lane
-          __syncwarp();
-          float xs = 0.f;
-#pragma unroll 4
-          for (int l = lane; l < c; ++l) xs = fmaf(sw[l], sX[l * Rp + lane], xs);
-          xs = (lane < c) ? -(ac * bc) * xs : (lane == c ? 1.f : 0.f);
-          if (lane < Rp) sX[c * Rp + lane] = xs;
-        } else {
-          incl = suffix_prod(aj, lane);
+        // Gated delta rule through pseudo-values. After records 0..J-1 the state is
+        //   gamma S + sum_i W_i w_i k_i^T,  gamma = alpha_0 .. alpha_{J-1}, W_i = alpha_{i+1} .. alpha_{J-1},
+        // where the ring keeps w_i = beta_i (v_i - alpha_i y_i), y_i = (state before record i) k_i.
+        // The new record c gets y_c = P_c (S k_c) + sum_{i<c} D_ic (k_i^T k_c) w_i with
+        // P_c = alpha_0 .. alpha_{c-1} and D_ic = alpha_{i+1} .. alpha_{c-1} (the dot warps
+        // hold S), and the output is o = gamma S q + sum_i W_i (k_i^T q) w_i.
+        // sc: [0] gamma, [2] P_c, [3] alpha_c, [4] beta_c, [5] k_c^T q,
+        //     [16 + i] W_i k_i^T q and [16 + kRMax + i] D_ic k_i^T k_c (i < c), and for a
+        //     fold [16 + 2 kRMax + i P + p] W_i w_i[p] (buffered records; the dot warps add record c)
+        const int cn = (MODE == kFlush) ? J : c;  // records from the ring
+        const float sfx = suffix_prod((lane < cn) ? aj : 1.f, lane);  // alpha_lane .. alpha_{cn-1}
+        const float dn = __shfl_down_sync(kFull, sfx, 1);
+        const float dex = (lane < 31) ? dn : 1.f;  // alpha_{lane+1} .. alpha_{cn-1}
+        const float anew = (MODE == kFlush) ? 1.f : __shfl_sync(kFull, aj, cn);
+        const float wsuf = dex * anew;             // W_lane for lane < cn
+        const float pc = __shfl_sync(kFull, sfx, 0);
+        const float sqc = __shfl_sync(kFull, sj, cn);
+        if (lane == 0) {
+          sc[0] = pc * anew;
+          sc[2] = pc;
+          sc[3] = anew;
+          sc[4] = (MODE == kFlush) ? 0.f : reinterpret_cast<const float*>(slot + kSbOff)[kRMax];
+          sc[5] = sqc;
         }
-        const float nxt = __shfl_down_sync(kFull, incl, 1);
-        const float wsuf = (lane < 31) ? nxt : 1.f;   // W_lane
-        const float gall = __shfl_sync(kFull, incl, 0);
-        float pin = aj;                               // alpha_0 .. alpha_lane
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const float y = __shfl_up_sync(kFull, pin, d);
-          if (lane >= d) pin *= y;
-        }
-        const float pup = __shfl_up_sync(kFull, pin, 1);
-        const float pex = (lane == 0) ? 1.f : pup;    // P_lane
-        __syncwarp();
-        if (MODE == kDecode && !flush) {
-          // o = (prod alpha) S q + sum_j z_j r_j with z_j = sum_{i>=j} W_i s_i X_ij:
-          // record weights c_j = z_j beta_j and the carried query
-          // u_0 = (prod alpha) q - sum_j z_j beta_j alpha_j P_j k_j, so o = S u_0 + sum_j c_j v_j
-          static_assert(N == 64 || N == 128, "delta-rule layers: N in {64, 128}");
-          sw[32 + lane] = wsuf * sj;  // W_i s_i
-          __syncwarp();
-          float z = 0.f;
-#pragma unroll 4
-          for (int i = lane; i < J; ++i) z = fmaf(sw[32 + i], sX[i * Rp + lane], z);
-          const float cme = (lane < J) ? z * bj : 0.f;
-          // the dot group forms u_0 from q, the keys and e_j (all its threads at once)
-          if (lane == 0) { sc[0] = 1.f; sc[1] = gall; }
-          sc[kCoefOff + lane] = cme;                  // c_j, 0 past J
-          sc[kCoefOff + kRMax + lane] = cme * aj * pex;  // e_j, 0 past J
-        } else {
-          // fold: per row u_i = sum_{j<=i} Bv_ij v_j + Bw_ij (S k_j) = Vp_i + S kappa_i with
-          // Bv_ij = W_i X_ij beta_j and Bw_ij = -W_i X_ij beta_j alpha_j P_j; the dot
-          // group forms kappa_i = sum_{j<=i} Bw_ij k_j and Vp_i = sum_{j<=i} Bv_ij v_j
-          if (lane == 0) sc[0] = gall;
-          float* Bv = sc + kCoefOff;
-          float* Bw = Bv + p.R * p.R;
-          const float fw = -bj * aj * pex;
-          for (int i = 0; i < J; ++i) {
-            const float wi = __shfl_sync(kFull, wsuf, i);
-            if (lane <= i) {
-              const float xw = wi * sX[i * Rp + lane];
-              Bv[i * p.R + lane] = xw * bj;
-              Bw[i * p.R + lane] = xw * fw;
+        sc[kCoefOff + lane] = (lane < cn) ? wsuf * sj : 0.f;
+        sc[kCoefOff + kRMax + lane] = (lane < cn) ? dex * mj : 0.f;
+        if (flush) {  // the fold's scaled pseudo-values of the buffered records
+          const float* sw = reinterpret_cast<const float*>(sv);
+          float* su = sc + kCoefOff + 2 * kRMax;
+          for (int j = 0; j < cn; ++j) {
+            const float wj = __shfl_sync(kFull, wsuf, j);
+            for (int r = 2 * lane; r < p.P; r += 64) {
+              const float2 w2 = *reinterpret_cast<const float2*>(sw + j * p.P + r);
+              *reinterpret_cast<float2*>(su + j * p.P + r) = make_float2(wj * w2.x, wj * w2.y);
             }
           }
         }
@@ -1041,34 +997,30 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(scoef0 + 8 * rs);  // coefficients published
       if constexpr (kAppendMode) {  // the new decays and value rows go to the ring
+        // (delta-rule layers: the dot warps append the pseudo-value row instead)
         const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
 #if RSSM_APPEND_BULK
         if (lane < na) {  // lane t: one bulk store per value row
           const int slot_t = ring_slot(st, c + lane, p.R);
           p.ring_a[hrow * p.Rp + slot_t] = sa[kRMax + lane];
-          if constexpr (kDel) p.ring_b[hrow * p.Rp + slot_t] = reinterpret_cast<const float*>(slot + kSbOff)[kRMax + lane];
-          bulk_store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + slot_t) * p.P * ES,
-                     smem_u32(sv + (c + lane) * p.P * ES), p.P * ES);
-          bulk_commit();
-          bulk_wait_read();  // the slot may be refilled once its rows have been read
+          if constexpr (!kDel) {
+            bulk_store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + slot_t) * p.P * ES,
+                       smem_u32(sv + (c + lane) * p.P * ES), p.P * ES);
+            bulk_commit();
+            bulk_wait_read();  // the slot may be refilled once its rows have been read
+          }
         }
 #else
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[kRMax + lane];
-        if constexpr (kDel) {
-          if (lane < na)
-            p.ring_b[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = reinterpret_cast<const float*>(slot + kSbOff)[kRMax + lane];
-        }
-        const int chp = p.P * ES / 16;
-        for (int t = 0; t < na; ++t) {  // 16-byte stores spread over the lanes
-          uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
-          for (int ch = lane; ch < chp; ch += 32)
-            *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
+        if constexpr (!kDel) {
+          const int chp = p.P * ES / 16;
+          for (int t = 0; t < na; ++t) {  // 16-byte stores spread over the lanes
+            uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
+            for (int ch = lane; ch < chp; ch += 32)
+              *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
+          }
         }
 #endif
-        if constexpr (kDel) {  // the new record's row of X, by record index
-          if (na > 0 && lane < p.Rp)
-            p.ring_x[(hrow * p.R + c) * p.Rp + lane] = reinterpret_cast<const float*>(slot + kXOff)[c * p.Rp + lane];
-        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty0 + 8 * rs);  // this warp is done with the slot
@@ -1096,20 +1048,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     constexpr bool kWideRows = ((RF == kRfNone || kF16 || kDel) && MODE == kDecode && N >= 64);
     constexpr int LP16 = kWideRows ? N / 16 : 1;
     float q16[kWideRows ? 16 : 1];
+    float k16[kDel ? 16 : 1];  // delta-rule layers: the new record's key, same columns as q16
     const int wpg = kNDW / lay.dgroups;                 // warps per dot group
     const int dgrp = warp / wpg, wr = warp - dgrp * wpg;  // this warp's group and rank in it
     const int rows_pass = wpg * kKR * RPI;
     const int npass = (p.P + rows_pass - 1) / rows_pass;
-    // delta-rule heads: the group's warps share per-head work through the group's
-    // barrier (bounded wait; one arrival per warp, phase dph)
-    int dph = 0;
-    auto group_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dgbar0 + 8 * dgrp);
-      const bool w = mbar_wait(dgbar0 + 8 * dgrp, dph, abort_flag, p.err);
-      dph ^= 1;
-      return __all_sync(kFull, w);
-    };
     int lh = 0;  // loaded heads seen
     HeadIter it;
     it.init(h0, p.H, p.HPG);
@@ -1137,11 +1080,15 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           gK = smem + p.gb_off + gs * p.gb_bytes;
           gQ = gK + p.gq_off;
           if constexpr (MODE == kDecode || MODE == kConv) q4 = In<TIn>::lds4(gQ, col4 * 4);
-          if constexpr (kWideRows && !kF16 && !kDel) {  // delta-rule heads take u_0 per head instead
+          if constexpr (kWideRows && !kF16) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const float4 qq = In<TIn>::lds4(gQ, (c * LP16 + lane % LP16) * 4);
-              q16[4 * c] = qq.x; q16[4 * c + 1] = qq.y; q16[4 * c + 2] = qq.z; q16[4 * c + 3] = qq.w;
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float4 qq = In<TIn>::lds4(gQ, (c4 * LP16 + lane % LP16) * 4);
+              q16[4 * c4] = qq.x; q16[4 * c4 + 1] = qq.y; q16[4 * c4 + 2] = qq.z; q16[4 * c4 + 3] = qq.w;
+              if constexpr (kDel) {
+                const float4 kq = In<TIn>::lds4(gK, c * N + (c4 * LP16 + lane % LP16) * 4);
+                k16[4 * c4] = kq.x; k16[4 * c4 + 1] = kq.y; k16[4 * c4 + 2] = kq.z; k16[4 * c4 + 3] = kq.w;
+              }
             }
           }
           if constexpr (kWideRows && kF16) {  // two chunks of 8 halves per lane
@@ -1347,95 +1294,37 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       } else if (flush) {
         // ================================================ fold path
         // S_new = g_{1:J} S + sum_j u_j k_j^T with u_j = g_{j+2:J} v_j ; store ; o = S_new q
-        // Delta rule: the same update, with the values u_i of each row formed here
-        // from the head's kappa_i and Vp_i (rows of this warp only, into its scratch).
+        // Delta rule: the same update with the scaled pseudo-values W_i w_i; the new
+        // record's w_c (decode, conventional step) is formed first for this warp's rows.
         const float gam = sc[0];
-        const float* su = sc + kCoefOff;  // [J][P] scaled values (outer-product rule)
-        float* dU = kDel ? reinterpret_cast<float*>(smem + p.dsc_off) + warp * p.R * 16 : nullptr;  // [R][16]
-        if constexpr (kDel) {  // kappa_i [N] and Vp_i [P] of the head, formed by the group's threads
-          float* kapw = const_cast<float*>(sc) + ((kCoefOff + 2 * p.R * p.R + 3) & ~3);
-          float* vptw = kapw + p.R * N;
-          const float* Bv = sc + kCoefOff;
-          const float* Bw = Bv + p.R * p.R;
-          const int nk = J * (N / 4), nv = J * (p.P / 2);
-          for (int it = wr * 32 + lane; it < nk + nv; it += wpg * 32) {
-            if (it < nk) {
-              const int i = it / (N / 4), ch = it - i * (N / 4);
-              float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-              for (int j = 0; j <= i; ++j) {
-                const float bw = Bw[i * p.R + j];
-                const float4 kv = In<TIn>::lds4(gK, j * N + ch * 4);
-                a.x = fmaf(bw, kv.x, a.x); a.y = fmaf(bw, kv.y, a.y);
-                a.z = fmaf(bw, kv.z, a.z); a.w = fmaf(bw, kv.w, a.w);
-              }
-              *reinterpret_cast<float4*>(kapw + i * N + ch * 4) = a;
-            } else {
-              const int t = it - nk, i = t / (p.P / 2), pr = t - i * (p.P / 2);
-              float2 a = make_float2(0.f, 0.f);
-#pragma unroll 4
-              for (int j = 0; j <= i; ++j) {
-                const float bv = Bv[i * p.R + j];
-                const float2 v2 = In<TIn>::lds2(sv, j * p.P + 2 * pr);
-                a.x = fmaf(bv, v2.x, a.x); a.y = fmaf(bv, v2.y, a.y);
-              }
-              *reinterpret_cast<float2*>(vptw + i * p.P + 2 * pr) = a;
-            }
-          }
-          if (!group_sync()) { ok = false; break; }
-        }
+        float* su = const_cast<float*>(sc) + (kDel ? kCoefOff + 2 * kRMax : kCoefOff);  // [J][P]
         for (int pass = 0; pass < npass; ++pass) {
           const int rbase = (pass * wpg + wr) * kKR;
           if (rbase * RPI >= p.P) break;  // warp-uniform: no rows left for this warp
-          // values of the warp's rows: ub[j * us + local row], local row = row - rbase * RPI
-          const float* ub = kDel ? dU : su + rbase * RPI;
-          const int us = kDel ? 16 : p.P;
-          if constexpr (kDel) {
-            // u_i[row] = Vp_i[row] + S_row . kappa_i for the warp's rows. Here a row
-            // spans LPW = N/16 lanes of 16 columns (4 interleaved chunks of 4, as in the
-            // non-flush rows) and each lane holds two rows; RB records per transposed
-            // reduction leave one (record, row) sum per lane.
-            constexpr int LPW = N / 16, RPW = 32 / LPW, RB = LPW / 2;
-            static_assert(2 * RPW == kKR * RPI && kKR * RPI <= 16, "delta-rule fold: two row instructions per pass");
-            const int cl = lane % LPW, rw = lane / LPW;
-            const float* kap = sc + ((kCoefOff + 2 * p.R * p.R + 3) & ~3);
-            const float* vpt = kap + p.R * N;
-            f32x2 xr[2][8];  // column pairs of the lane's two rows
+          const float* ub = su + rbase * RPI;  // values of the warp's rows: ub[j * P + local row]
+          if constexpr (kDel && MODE != kFlush) {
+            // w_c = beta_c (v_c - alpha_c (P_c S k_c + sum_{i<c} D_ic k_i^T k_c w_i)) per row;
+            // the row sums S k_c are reduced transposed (lane seg + kk D ends with row kk's)
+            static_assert(LPR >= kKR, "delta-rule fold: a row spans at least kKR lanes");
+            constexpr int D = LPR / kKR;
+            const float4 kc4 = In<TIn>::lds4(gK, c * N + col4 * 4);
+            float part[kKR];
 #pragma unroll
-            for (int ri = 0; ri < 2; ++ri) {
-              const int row = rbase * RPI + ri * RPW + rw;
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                ulonglong2 t = make_ulonglong2(0ull, 0ull);
-                if (row < p.P) t = *reinterpret_cast<const ulonglong2*>(tf + (size_t)row * N + (cc * LPW + cl) * 4);
-                xr[ri][2 * cc] = t.x;
-                xr[ri][2 * cc + 1] = t.y;
-              }
+            for (int kk = 0; kk < kKR; ++kk) {
+              const int row = (rbase + kk) * RPI + rsub;
+              part[kk] = (row < p.P) ? dot4(ld_tile4<false>(tile, (size_t)row * N + col4 * 4), kc4) : 0.f;
             }
-            for (int i0 = 0; i0 < J; i0 += RB) {
-              float part[2 * RB];
-#pragma unroll
-              for (int jj = 0; jj < RB; ++jj) {
-                f32x2 a0 = 0ull, a1 = 0ull;
-                if (i0 + jj < J) {
-                  const float* kr = kap + (i0 + jj) * N;
-#pragma unroll
-                  for (int cc = 0; cc < 4; ++cc) {
-                    const ulonglong2 kq = *reinterpret_cast<const ulonglong2*>(kr + (cc * LPW + cl) * 4);
-                    a0 = fma2(xr[0][2 * cc], kq.x, a0);
-                    a0 = fma2(xr[0][2 * cc + 1], kq.y, a0);
-                    a1 = fma2(xr[1][2 * cc], kq.x, a1);
-                    a1 = fma2(xr[1][2 * cc + 1], kq.y, a1);
-                  }
-                }
-                part[2 * jj] = lo2(a0) + hi2(a0);
-                part[2 * jj + 1] = lo2(a1) + hi2(a1);
-              }
-              int off = 0;
-              TRed<2 * RB, LPW / 2>::run(part, lane, off);
-              const int i = i0 + (off >> 1), lr = (off & 1) * RPW + rw;
-              const int row = rbase * RPI + lr;
-              if (i < J && row < p.P) dU[i * 16 + lr] = part[0] + vpt[i * p.P + row];
+            int off = 0;
+            TRed<kKR, LPR / 2>::run(part, lane, off);
+            const int row = (rbase + off) * RPI + rsub;
+            if ((lane & (D - 1)) == 0 && row < p.P) {
+              const float* sw = reinterpret_cast<const float*>(sv);
+              const float* dk = sc + kCoefOff + kRMax;
+              float y = sc[2] * part[0];
+#pragma unroll 4
+              for (int i = 0; i < c; ++i) y = fmaf(dk[i], sw[i * p.P + row], y);
+              const float vn = In<TIn>::lds(slot + lay.nv_off, row);
+              su[c * p.P + row] = sc[4] * fmaf(-sc[3], y, vn);  // W_c = 1
             }
             __syncwarp();
           }
@@ -1460,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               f32x2 U[kKR / 2];
 #pragma unroll
               for (int qd = 0; qd < kKR / 4; ++qd) {
-                const ulonglong2 uq = *reinterpret_cast<const ulonglong2*>(ub + j * us + 4 * qd);
+                const ulonglong2 uq = *reinterpret_cast<const ulonglong2*>(ub + j * p.P + 4 * qd);
                 U[2 * qd] = uq.x;
                 U[2 * qd + 1] = uq.y;
               }
@@ -1494,7 +1383,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
               for (int kk = 0; kk < kKR; ++kk) {
                 const int row = (rbase + kk) * RPI + rsub;
-                uu[kk] = (row < p.P) ? ub[j * us + kk * RPI + rsub] : 0.f;
+                uu[kk] = (row < p.P) ? ub[j * p.P + kk * RPI + rsub] : 0.f;
               }
 #pragma unroll
               for (int kk = 0; kk < kKR; ++kk) {
@@ -1557,36 +1446,84 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         // share to the scaled dot before the row reduction.
         const float gam = sc[0];
         const float* scj = sc + kCoefOff;  // [kRMax] record weights, 0 past J
-        if constexpr (kWideRows) {
+        if constexpr (kDel) {
+          // Delta rule: per row, A = gamma (S q) + sum_{i<c} W_i s_i w_i and
+          // B = P_c (S k_c) + sum_{i<c} D_ic M_ic w_i; then the new record's pseudo-value
+          // w_c = beta_c (v_c - alpha_c B) goes to the ring and o = A + s_c w_c.
+          // Rows as in the FP32 non-flush path; lane k of a row takes records k, k + LP16, ...
+          constexpr int RPW = 32 / LP16, KW = 4;
+          constexpr int JI = kRMax / LP16;
+          const int cl = lane % LP16, rw = lane / LP16;
+          float cwv[JI], dwv[JI];
+#pragma unroll
+          for (int i = 0; i < JI; ++i) {
+            cwv[i] = scj[cl + LP16 * i];
+            dwv[i] = sc[kCoefOff + kRMax + cl + LP16 * i];
+          }
+          const float pcv = sc[2], acv = sc[3], bcv = sc[4], sqc = sc[5];
+          const float* sw = reinterpret_cast<const float*>(sv);
+          const uint8_t* nv = slot + lay.nv_off;
+          float* wring = reinterpret_cast<float*>(p.ring_v) + (hrow * p.R + ring_slot(st, c, p.R)) * p.P;
+          for (int r0 = wr * KW * RPW; r0 < p.P; r0 += wpg * KW * RPW) {
+            float part[2 * KW];
+#pragma unroll
+            for (int kk = 0; kk < KW; ++kk) {
+              const int row = r0 + kk * RPW + rw;
+              float ra = 0.f, rb = 0.f;
+              if (row < p.P) {
+                const float* rp = tf + (size_t)row * N;
+                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                  const float4 x = lds4(rp + (c4 * LP16 + cl) * 4);
+                  a0 = fmaf(x.x, q16[4 * c4], a0); a1 = fmaf(x.y, q16[4 * c4 + 1], a1);
+                  a0 = fmaf(x.z, q16[4 * c4 + 2], a0); a1 = fmaf(x.w, q16[4 * c4 + 3], a1);
+                  b0 = fmaf(x.x, k16[4 * c4], b0); b1 = fmaf(x.y, k16[4 * c4 + 1], b1);
+                  b0 = fmaf(x.z, k16[4 * c4 + 2], b0); b1 = fmaf(x.w, k16[4 * c4 + 3], b1);
+                }
+                ra = gam * (a0 + a1);
+                rb = pcv * (b0 + b1);
+#pragma unroll
+                for (int i = 0; i < JI; ++i) {
+                  const int j = cl + LP16 * i;
+                  if (j < c) {
+                    const float wv = sw[j * p.P + row];
+                    ra = fmaf(cwv[i], wv, ra);
+                    rb = fmaf(dwv[i], wv, rb);
+                  }
+                }
+              }
+              part[2 * kk] = ra;
+              part[2 * kk + 1] = rb;
+            }
+            int off = 0;
+            TRed<2 * KW, LP16 / 2>::run(part, lane, off);  // lane: value off (and off + 1 if LP16 < 2 KW)
+            float va, vb;
+            bool wo, ww;  // this lane writes the output / the pseudo-value
+            if constexpr (LP16 < 2 * KW) {  // both values of row off / 2 in this lane
+              va = part[0]; vb = part[1];
+              wo = ww = true;
+            } else {  // one value per lane: lanes off and off ^ 1 hold a row's pair
+              const float other = __shfl_xor_sync(kFull, part[0], 1);
+              const bool isa = (off & 1) == 0;
+              va = isa ? part[0] : other;
+              vb = isa ? other : part[0];
+              wo = isa; ww = !isa;
+            }
+            const int row = r0 + (off >> 1) * RPW + rw;
+            if (row < p.P) {
+              const float w = bcv * fmaf(-acv, vb, In<TIn>::lds(nv, row));
+              if (wo) p.o[hrow * p.P + row] = fmaf(sqc, w, va);
+              if (ww) wring[row] = w;
+            }
+          }
+        } else if constexpr (kWideRows) {
           constexpr int RPW = 32 / LP16, KW = 4;  // rows per warp instruction, row instructions per pass
           constexpr int JI = kRMax / LP16;
           const int cl = lane % LP16, rw = lane / LP16;
           float cwv[JI];
 #pragma unroll
           for (int i = 0; i < JI; ++i) cwv[i] = scj[cl + LP16 * i];
-          if constexpr (kDel) {  // u_0 = (prod alpha) q - sum_j e_j k_j, formed by the group, replaces q
-            float* su0 = const_cast<float*>(sc) + kCoefOff + 2 * kRMax;
-            const float gall = sc[1];
-            const float* ej = sc + kCoefOff + kRMax;
-            for (int ch = wr * 32 + lane; ch < N / 4; ch += wpg * 32) {
-              const float4 qv = In<TIn>::lds4(gQ, ch * 4);
-              float4 u = make_float4(gall * qv.x, gall * qv.y, gall * qv.z, gall * qv.w);
-#pragma unroll 4
-              for (int j = 0; j < J; ++j) {
-                const float e = ej[j];
-                const float4 kv = In<TIn>::lds4(gK, j * N + ch * 4);
-                u.x = fmaf(-e, kv.x, u.x); u.y = fmaf(-e, kv.y, u.y);
-                u.z = fmaf(-e, kv.z, u.z); u.w = fmaf(-e, kv.w, u.w);
-              }
-              *reinterpret_cast<float4*>(su0 + ch * 4) = u;
-            }
-            if (!group_sync()) { ok = false; break; }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const float4 qq = lds4(su0 + (c * LP16 + cl) * 4);
-              q16[4 * c] = qq.x; q16[4 * c + 1] = qq.y; q16[4 * c + 2] = qq.z; q16[4 * c + 3] = qq.w;
-            }
-          }
           for (int r0 = wr * KW * RPW; r0 < p.P; r0 += wpg * KW * RPW) {
             float part[KW];
 #pragma unroll

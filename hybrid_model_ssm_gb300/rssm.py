@@ -271,14 +271,13 @@ class ReplaySSM:
         K = self.ring[k_off: k_off + s.B * s.G * R * s.N * es].view(s.torch_in_dtype).view(s.B, s.G, R, s.N)
         return a, V, K
 
-    def ring_betas(self):
-        """Write strengths [B,H,Rp] f32 of a delta-rule layer's ring (next 256-byte boundary after the decays)."""
+    def ring_pseudo_values(self):
+        """Pseudo-values w [B,H,R,P] f32 of a delta-rule layer's ring (where V sits for the other recurrence)."""
         s = self.shape
         if s.recurrence != "delta":
-            raise ValueError("only delta-rule layers keep write strengths")
-        Rp = (s.R + 3) // 4 * 4
-        off = (s.B * s.H * Rp * 4 + 255) // 256 * 256
-        return self.ring[off: off + s.B * s.H * Rp * 4].view(torch.float32).view(s.B, s.H, Rp)
+            raise ValueError("only delta-rule layers keep pseudo-values")
+        v_off, _ = ring_offsets(s)
+        return self.ring[v_off: v_off + s.B * s.H * s.R * s.P * 4].view(torch.float32).view(s.B, s.H, s.R, s.P)
 
 
 def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:

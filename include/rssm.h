@@ -81,12 +81,16 @@ typedef enum {
  * v_t k_t^T (Mamba-2-style heads, aikraft.ru page §01). RSSM_GATED_DELTA: the
  * gated delta rule S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
  * of Gated DeltaNet layers, which the pages name as using the same replay form
- * (ai.cheesepanini.fun page, 方法/产品要点). Its replay output carries the query
- * back through the buffered records: u_h = q, c_j = beta_j k_j^T u_j,
- * u_{j-1} = alpha_j (u_j - c_j k_j), o = S_ckpt u_0 + sum_j c_j v_j; a fold
- * applies S <- alpha_j S + beta_j (v_j - alpha_j S k_j) k_j^T in order. Delta
- * layers decode with rssm_decode_step_delta; they need ckpt_fmt F32, read_fmt
- * NONE, T_max = 1 and N in {64, 128} (verify is not offered for them). */
+ * (ai.cheesepanini.fun page, 方法/产品要点). Its ring keeps, in place of v_j,
+ * each record's pseudo-value w_j = beta_j (v_j - alpha_j y_j), y_j the state
+ * just before record j applied to k_j. After records 0..J-1 the state is then
+ * g S_ckpt + sum_j W_j w_j k_j^T (g the product of all J decays, W_j that of
+ * the decays after j): the outer-product replay form with v replaced by w. The
+ * step that appends record c forms y_c = P_c S_ckpt k_c + sum_{i<c} D_ic
+ * (k_i^T k_c) w_i (P_c the decays before c, D_ic those strictly between i and
+ * c) while it reads the checkpoint anyway. Delta layers decode with
+ * rssm_decode_step_delta; they need ckpt_fmt F32, read_fmt NONE, T_max = 1 and
+ * N in {64, 128} (verify is not offered for them). */
 typedef enum { RSSM_GATED_OUTER = 0, RSSM_GATED_DELTA = 1 } rssm_recurrence;
 
 typedef struct {
@@ -103,8 +107,8 @@ typedef struct rssm_ctx* rssm_handle;
 /* Byte sizes of the three caller-allocated buffers that rssm_create binds.
  *  ring_bytes: the record ring, made of
  *      alpha [B,H,Rp] fp32 (Rp = R rounded up to 4) at offset 0,
- *      (delta layers) beta [B,H,Rp] fp32 right after it, 256-aligned,
- *      V     [B,H,R,P] in_dtype at offset v_off,
+ *      V     [B,H,R,P] in_dtype at offset v_off (delta layers: the
+ *            pseudo-values w [B,H,R,P] fp32),
  *      K     [B,G,R,N] in_dtype at offset k_off (see rssm_ring_offsets).
  *  ptr_bytes: pointer block of int32 start[B], count[B], ticket[B], one
  *      uint32 error word (256 bytes) and int32 epoch[B] (flushes per sequence),
@@ -237,11 +241,12 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
                                             const void* q, float* o, void* stream);
 
 /* One decode step of a gated delta-rule layer (recurrence RSSM_GATED_DELTA):
- * rssm_decode_step plus beta [B,H] fp32, the write strength of each head's
- * record, kept in the ring beside alpha. Non-flush steps compute only the
- * output (the replay form above); the step whose append brings the count to L
- * folds the records in order and writes the checkpoint once. RSSM_EINVAL on a
- * handle of the other recurrence (and rssm_decode_step refuses delta handles). */
+ * rssm_decode_step plus beta [B,H] fp32 (16-byte aligned), the write strength
+ * of each head's record. Non-flush steps read the checkpoint once, append the
+ * record's pseudo-value and compute the output (the form above); the step
+ * whose append brings the count to L folds all records and writes the
+ * checkpoint once. RSSM_EINVAL on a handle of the other recurrence (and
+ * rssm_decode_step refuses delta handles). */
 rssm_status rssm_decode_step_delta(rssm_handle h, const float* alpha, const float* beta, const void* v,
                                    const void* k, const void* q, float* o, void* stream);
 

@@ -60,6 +60,7 @@ from .sround import (  # noqa: F401
 )
 from .delta import (  # noqa: F401
     delta_step,
+    delta_pseudo_value,
     delta_replay_output,
     delta_fold,
     DeltaReplayOracle,

@@ -47,6 +47,16 @@ def delta_step(S, alpha, beta, v, k, q):
     return S_new, np.einsum("bhpn,bhn->bhp", S_new, qh)
 
 
+def delta_pseudo_value(S, alpha, beta, v, k):
+    """The write term of one step: w = beta (v - alpha S k), so that
+    S_t = alpha S + w k^T. S [B,H,P,N] is the state before the step, alpha and
+    beta [B,H], v [B,H,P], k [B,G,N]. Returns w [B,H,P]."""
+    S = np.asarray(S, np.float64)
+    g = head_groups(S.shape[1], k.shape[1])
+    Sk = np.einsum("bhpn,bhn->bhp", S, k[:, g, :])
+    return beta[:, :, None] * (v - alpha[:, :, None] * Sk)
+
+
 def delta_replay_output(S_ckpt, alphas, betas, vs, ks, q):
     """Output-only evaluation for one sequence after h records (form above).
 

@@ -113,18 +113,14 @@ def test_config_struct_matches_the_header(tmp_path):
 
 
 def test_delta_rule_ring_layout(lib):
-    """Delta-rule layers keep the write strengths [B,H,Rp] and the rows of the
-    inverse coupling matrix [B,H,R,Rp] between the decays and V."""
+    """Delta-rule layers keep fp32 pseudo-values [B,H,R,P] where V sits."""
     s = LayerShape(B=3, H=4, P=64, N=128, G=2, L=5, recurrence="delta")
     Rp, R = 8, 5
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    a_bytes = 3 * 4 * Rp * 4
-    b_off = up(a_bytes)
-    x_off = up(b_off + a_bytes)
     v_off, k_off = ring_offsets(s)
-    assert v_off == up(x_off + 3 * 4 * R * Rp * 4)
-    assert k_off == (v_off + 3 * 4 * R * 64 * 2 + 255) // 256 * 256
-    assert workspace_size(s)[0] == (k_off + 3 * 2 * R * 128 * 2 + 255) // 256 * 256
+    assert v_off == up(3 * 4 * Rp * 4)
+    assert k_off == up(v_off + 3 * 4 * R * 64 * 4)
+    assert workspace_size(s)[0] == up(k_off + 3 * 2 * R * 128 * 2)
 
 
 @pytest.mark.parametrize("kw,status", [

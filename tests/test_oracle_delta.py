@@ -9,7 +9,8 @@ Each check rests on something other than the function it checks:
 - a scalar case (P = N = 1) worked by hand;
 - the replay formula and the fold, two different computations, against the
   step-by-step definition;
-- the pointer bookkeeping against the outer-product oracle's, bit for bit.
+- the pointer bookkeeping against the outer-product oracle's, bit for bit;
+- the pseudo-value w of a step against the step itself: S_t - alpha S = w k^T.
 """
 import numpy as np
 
@@ -108,3 +109,15 @@ def test_pointers_follow_the_outer_product_oracle():
         assert np.array_equal(f1, f2) and np.array_equal(d.start, r.start) and np.array_equal(d.count, r.count)
     assert np.array_equal(d.flush(1), r.flush(1))
     assert np.array_equal(d.start, r.start) and np.array_equal(d.count, r.count)
+
+
+def test_pseudo_value_is_the_steps_write_term():
+    rng = np.random.default_rng(5)
+    B, H, G, P, N = 2, 4, 2, 5, 7
+    S = rng.standard_normal((B, H, P, N))
+    a, b = rng.uniform(0.2, 1.0, (B, H)), rng.uniform(0.0, 1.0, (B, H))
+    v, k, q = rng.standard_normal((B, H, P)), rng.standard_normal((B, G, N)), rng.standard_normal((B, G, N))
+    S1, _ = delta.delta_step(S, a, b, v, k, q)
+    w = delta.delta_pseudo_value(S, a, b, v, k)
+    g = oracle.head_groups(H, G)
+    assert np.allclose(S1 - a[:, :, None, None] * S, w[..., None] * k[:, g, None, :], atol=1e-12)
