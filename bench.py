@@ -45,6 +45,8 @@ WORKLOAD = synth.PRESETS["mamba2_layer_b256_l16"]
 FALLBACK_HBM_GBS = 6800.0
 DECODE_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_decode.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_step_b256_l16.md")
+DELTA_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_delta.cu"]
+DELTA_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "delta_decode_step_b256_l16.md")
 
 
 # ----------------------------------------------------------------- analytic bytes
@@ -74,17 +76,18 @@ def window_bytes(s, read_fmt=None, ckpt_bytes: int = 4, delta: bool = False) -> 
     checkpoint |S|, or its read copy |C| when there is one. The flush step
     reads |S| and writes it once, plus the refreshed copy. ckpt_bytes is the
     checkpoint's element size (2 for an FP16 checkpoint). A delta-rule layer's
-    records carry beta too; its state bytes are the same.
+    inputs carry beta too, and its buffered records hold the fp32 pseudo-value
+    w in place of v.
     """
     es = 2 if s.in_dtype == "bf16" else 4
     S = ckpt_bytes * s.H * s.P * s.N
     C = s.H * copy_bytes_per_head(s, read_fmt)
-    r = record_bytes(s, delta)
-    inp = r + es * s.G * s.N
+    ring_rec = 4 * s.H + (4 if delta else es) * s.H * s.P + es * s.G * s.N  # a buffered record
+    inp = record_bytes(s, delta) + es * s.G * s.N                            # a step's inputs
     out = 4 * s.H * s.P
     L = s.L
     reads = (L - 1) * (C if read_fmt else S) + S
-    total = reads + S + C + r * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * r
+    total = reads + S + C + ring_rec * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * ring_rec
     conv = L * (2 * 4 * s.H * s.P * s.N + inp + out)
     return {"replay_window": total, "replay_per_seq_step": total / L, "conventional_per_seq_step": conv / L,
             "state": S}
@@ -100,24 +103,24 @@ def measured_peak_gbs() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in DECODE_KERNEL_SOURCES:
+    for rel in sources or DECODE_KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic() -> float | None:
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on this kernel source."""
+def profiled_traffic(path: str = TRAFFIC_FILE, sources=None) -> float | None:
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken on this kernel source."""
     try:
         kv = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             for line in f:
                 if ":" in line and line.strip().startswith("- "):
                     k, v = line.strip()[2:].split(":", 1)
                     kv[k.strip()] = v.strip().strip("`")
-        if kv.get("kernel_source_sha256") != kernel_source_hash():
+        if kv.get("kernel_source_sha256") != kernel_source_hash(sources):
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -400,8 +403,9 @@ def run_ours(args, world, rank, local):
                    "inputs": "16 resident steps of seeded inputs, cycled"},
         "hbm_gbs_achieved": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic() if (not delta and args.read_fmt is None and args.ckpt == "f32"
-                                                      and args.batch is None) else None,
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": (None if (args.read_fmt or args.ckpt != "f32" or args.batch is not None)
+                                 else profiled_traffic(DELTA_TRAFFIC_FILE, DELTA_KERNEL_SOURCES) if delta
+                                 else profiled_traffic()),
                      "algorithmic_bytes_per_launch": alg_bytes_launch,
                      "mean_launch_ms": mean_launch * 1e3,
                      "mean_nonflush_launch_ms": 1e3 * sum(nonflush_s) / max(1, len(nonflush_s)),

@@ -1317,12 +1317,17 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             int off = 0;
             TRed<kKR, LPR / 2>::run(part, lane, off);
             const int row = (rbase + off) * RPI + rsub;
-            if ((lane & (D - 1)) == 0 && row < p.P) {
+            // the D lanes holding a row split the buffered records (lane d: i = d, d + D, ...)
+            const int d = lane & (D - 1);
+            float y = (d == 0) ? sc[2] * part[0] : 0.f;
+            if (row < p.P) {
               const float* sw = reinterpret_cast<const float*>(sv);
               const float* dk = sc + kCoefOff + kRMax;
-              float y = sc[2] * part[0];
-#pragma unroll 4
-              for (int i = 0; i < c; ++i) y = fmaf(dk[i], sw[i * p.P + row], y);
+              for (int i = d; i < c; i += D) y = fmaf(dk[i], sw[i * p.P + row], y);
+            }
+#pragma unroll
+            for (int m = 1; m < D; m <<= 1) y += __shfl_xor_sync(kFull, y, m);
+            if (d == 0 && row < p.P) {
               const float vn = In<TIn>::lds(slot + lay.nv_off, row);
               su[c * p.P + row] = sc[4] * fmaf(-sc[3], y, vn);  // W_c = 1
             }
