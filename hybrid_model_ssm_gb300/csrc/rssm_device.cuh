@@ -925,15 +925,23 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       const float aj = (lane < c) ? sa[ring_slot(st, lane, p.R)] : (lane < J) ? sa[kRMax + lane - c] : 1.f;
       if constexpr (MODE == kVerify) {
         // Per query t (records 0 .. c + t): g_{1:c+t+1} into sc[t] and the record
-        // weights g_{j+2:c+t+1} (k_j^T q_t) into sc[kCoefOff + t kRMax + j].
+        // weights g_{j+2:c+t+1} (k_j^T q_t) into sc[kCoefOff + t kRMax + j]. One scan
+        // covers the committed records; the drafts' decays enter as per-lane running
+        // products: record l's weight for query t is
+        // (alpha_{l+1} .. alpha_{c-1}) (alpha_{max(l+1,c)} .. alpha_{c+t}).
+        const float sfx = suffix_prod((lane < c) ? aj : 1.f, lane);  // alpha_lane .. alpha_{c-1}
+        const float dn = __shfl_down_sync(kFull, sfx, 1);
+        const float dpart = (lane < 31) ? dn : 1.f;                  // alpha_{lane+1} .. alpha_{c-1}
+        const float call = __shfl_sync(kFull, sfx, 0);                // alpha_0 .. alpha_{c-1}
+        const int s0 = max(lane + 1 - c, 0);                           // first draft after record lane
+        float np = 1.f, nall = 1.f;                                    // drafts s0 .. t; drafts 0 .. t
         for (int t = 0; t < p.T; ++t) {
+          const float at = sa[kRMax + t];
+          nall *= at;
+          if (t >= s0) np *= at;
           const int ht = c + t + 1;
-          const float x = (lane < ht) ? aj : 1.f;
-          const float incl = suffix_prod(x, lane);
-          const float nxt = __shfl_down_sync(kFull, incl, 1);
-          const float w = (lane < 31) ? nxt : 1.f;
-          sc[kCoefOff + t * kRMax + lane] = (lane < ht) ? w * skq_w[t * kRMax + lane] : 0.f;
-          if (lane == 0) sc[t] = incl;
+          sc[kCoefOff + t * kRMax + lane] = (lane < ht) ? dpart * np * skq_w[t * kRMax + lane] : 0.f;
+          if (lane == 0) sc[t] = call * nall;
         }
       } else if constexpr (kDel) {
         // Gated delta rule through pseudo-values. After records 0..J-1 the state is
@@ -1012,7 +1020,19 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         }
 #else
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[kRMax + lane];
-        if constexpr (!kDel) {
+        if constexpr (MODE == kVerify) {
+          // the T value rows: one bulk store per contiguous ring run (at most two),
+          // issued by one lane; the slot is released once the copies have read it
+          if (lane == 0 && na > 0) {
+            const int s1 = ring_slot(st, c, p.R);
+            const int n1 = min(na, p.R - s1);
+            uint8_t* rv = reinterpret_cast<uint8_t*>(p.ring_v) + hrow * p.R * p.P * ES;
+            bulk_store(rv + (size_t)s1 * p.P * ES, smem_u32(sv + c * p.P * ES), n1 * p.P * ES);
+            if (na > n1) bulk_store(rv, smem_u32(sv + (c + n1) * p.P * ES), (na - n1) * p.P * ES);
+            bulk_commit();
+            bulk_wait_read();
+          }
+        } else if constexpr (!kDel) {
           const int chp = p.P * ES / 16;
           for (int t = 0; t < na; ++t) {  // 16-byte stores spread over the lanes
             uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + ring_slot(st, c + t, p.R)) * p.P * ES;
