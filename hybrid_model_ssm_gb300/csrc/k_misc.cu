@@ -8,6 +8,44 @@ cudaError_t launch_flush(const Params& p, int grid, size_t smem, cudaStream_t st
   return dtype == 0 ? dispatch_n<kFlush, float>(p, grid, smem, st, N, rf)
                     : dispatch_n<kFlush, __nv_bfloat16>(p, grid, smem, st, N, rf);
 }
+// The sequences a standalone flush folds (count >= min_count, 0 < count <= R),
+// in increasing order, into flist[0 .. *fcount). One block.
+__global__ void flush_list_kernel(const int32_t* count, int B, int R, int min_count, int32_t* flist,
+                                  int32_t* fcount) {
+  __shared__ int warp_n[32];
+  __shared__ int base;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    bool f = false;
+    if (b < B) {
+      const int c = count[b];
+      f = c >= min_count && c > 0 && c <= R;
+    }
+    const unsigned m = __ballot_sync(kFull, f);
+    if (lane == 0) warp_n[w] = __popc(m);
+    __syncthreads();
+    int off = base;
+    for (int i = 0; i < w; ++i) off += warp_n[i];
+    if (f) flist[off + __popc(m & ((1u << lane) - 1u))] = b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int t = 0;
+      for (int i = 0; i < nw; ++i) t += warp_n[i];
+      base += t;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *fcount = base;
+}
+
+cudaError_t launch_flush_list(const int32_t* count, int B, int R, int min_count, int32_t* flist, int32_t* fcount,
+                              cudaStream_t st) {
+  flush_list_kernel<<<1, 1024, 0, st>>>(count, B, R, min_count, flist, fcount);
+  return cudaGetLastError();
+}
 cudaError_t launch_quant(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf) {
   if (rf == kRfNone) return cudaErrorInvalidValue;
   return dispatch_n<kQuant, float>(p, grid, smem, st, N, rf);

@@ -41,7 +41,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Geom {
   int R = 0, Rp = 0, esize = 0, ck_es = 4, rf = 0;  // ck_es: checkpoint bytes per element; rf: tile format
   size_t v_off = 0, k_off = 0, ring_bytes = 0;
-  size_t off_count = 0, off_ticket = 0, off_err = 0, off_epoch = 0, ptr_bytes = 0;
+  size_t off_count = 0, off_ticket = 0, off_err = 0, off_epoch = 0, off_flist = 0, off_fcount = 0, ptr_bytes = 0;
   size_t head_stride = 0, bsc_off = 0, rsc_off = 0, copy_bytes = 0;
 };
 
@@ -93,7 +93,9 @@ rssm_status derive(const rssm_config* c, Geom* g) {
   g->off_ticket = 2 * pb;
   g->off_err = 3 * pb;
   g->off_epoch = 3 * pb + 256;
-  g->ptr_bytes = 4 * pb + 256;
+  g->off_flist = 4 * pb + 256;   // the standalone flush's list of folding sequences
+  g->off_fcount = 5 * pb + 256;  // and their number
+  g->ptr_bytes = 5 * pb + 512;
   if (c->read_fmt == RSSM_READ_E4M3_ROW) {
     g->bsc_off = P * N;
     g->rsc_off = P * N;
@@ -437,10 +439,17 @@ rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream) {
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.min_count = min_count;
-  // one CTA per (sequence, group): CTAs of sequences that do not flush exit at once
-  const int grid = h->cfg.B * h->cfg.G;
-  const cudaError_t e = rssm::launch_flush(pl.p, grid, pl.smem, static_cast<cudaStream_t>(stream), h->cfg.N,
-                                           h->cfg.in_dtype, h->g.rf);
+  // A one-block kernel lists the folding sequences; the persistent kernel then
+  // spreads exactly their heads over the SMs.
+  int32_t* flist = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_flist);
+  int32_t* fcount = reinterpret_cast<int32_t*>(h->ptrs + h->g.off_fcount);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = rssm::launch_flush_list(pl.p.count, h->cfg.B, h->g.R, min_count, flist, fcount, st);
+  if (e != cudaSuccess) return cuda_fail(e, "flush list launch");
+  pl.p.flist = flist;
+  pl.p.fcount = fcount;
+  e = rssm::launch_flush(pl.p, persistent_grid((long long)h->cfg.B * h->cfg.H), pl.smem, st, h->cfg.N,
+                         h->cfg.in_dtype, h->g.rf);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   h->last_T = 0;
   return RSSM_OK;

@@ -85,6 +85,8 @@ struct Params {
   int32_t* count;      // [B]
   int32_t* ticket;     // [B], zero between launches
   int32_t* epoch;      // [B] flushes so far (FP16 checkpoint: part of the rounding counter)
+  const int32_t* flist;   // kFlush: the flushing sequences in order, or null (every sequence)
+  const int32_t* fcount;  // kFlush: their number
   unsigned long long seed;  // FP16 checkpoint: generator key
   int sr;              // FP16 checkpoint: 1 stochastic rounding, 0 round to nearest
   const int32_t* cur;  // kSnap: [B] slot holding each sequence's state
@@ -591,7 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 3 * kMaxSlots + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long total = (long long)p.B * p.H;
+  // kFlush with a list: heads are numbered over the listed sequences only
+  const bool listed = (MODE == kFlush) && p.flist != nullptr;
+  const long long total = listed ? (long long)min(max(*p.fcount, 0), p.B) * p.H : (long long)p.B * p.H;
+  auto seq_of = [&](int vb) -> int { return listed ? p.flist[vb] : vb; };
   const long long h0 = (long long)blockIdx.x * total / gridDim.x;
   const long long h1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
   const int nq = kDrafts ? p.T : 1;
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       HeadIter it;
       it.init(h0, p.H, p.HPG);
       for (long long gh = h0; gh < h1; ++gh, it.next(p.H, p.HPG)) {
-        const int b = it.b;
+        const int b = seq_of(it.b);
         if (b != cur_b) {
           cur_b = b;
           seq_plan(b, c, st, load, flush, bad);
@@ -715,9 +720,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         if (!load) continue;
         if (li >= lay.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const bool from_copy = kCopyRF && (MODE == kDecode) && !flush;
-        size_t srow = (size_t)gh;  // kSnap: the head's row in the sequence's current state slot
+        const size_t hrow = (size_t)b * p.H + it.hh;
+        size_t srow = hrow;  // kSnap: the head's row in the sequence's current state slot
         if constexpr (MODE == kSnap) srow += (size_t)st * ((size_t)p.B * p.H);
-        const void* src = from_copy ? (const void*)(p.copy + (size_t)gh * p.head_stride)
+        const void* src = from_copy ? (const void*)(p.copy + hrow * p.head_stride)
                                     : (const void*)(reinterpret_cast<const uint8_t*>(p.ckpt) + srow * p.P * N * CKES);
         const uint32_t bytes = from_copy ? (uint32_t)p.head_stride : (uint32_t)(p.P * N * CKES);
         mbar_arrive_tx(tfull0 + 8 * ts, bytes);
@@ -748,9 +754,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       HeadIter it;
       it.init(h0, p.H, p.HPG);
       for (long long gh = h0; gh < h1; ++gh, it.next(p.H, p.HPG)) {
-        const int b = it.b, hh = it.hh, g = it.g;
+        const int b = seq_of(it.b), hh = it.hh, g = it.g;
         const long long gg = (long long)b * p.G + g;
-        const size_t hrow = (size_t)gh;
+        const size_t hrow = (size_t)b * p.H + hh;
         if (b != cur_b) {
           cur_b = b;
           seq_plan(b, c, st, load, flush, bad);
@@ -842,9 +848,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
-      const int b = it.b, g = it.g;
+      const int b = seq_of(it.b), g = it.g;
       const long long gg = (long long)b * p.G + g;
-      const size_t hrow = (size_t)gh;
+      const size_t hrow = (size_t)b * p.H + it.hh;
       if (b != cur_b) {
         cur_b = b;
         seq_plan(b, c, st, load, flush, bad);
@@ -1077,9 +1083,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     HeadIter it;
     it.init(h0, p.H, p.HPG);
     for (long long gh = h0; gh < h1 && ok; ++gh, it.next(p.H, p.HPG)) {
-      const int b = it.b, hh = it.hh, g = it.g;
+      const int b = seq_of(it.b), hh = it.hh, g = it.g;
       const long long gg = (long long)b * p.G + g;
-      const size_t hrow = (size_t)gh;
+      const size_t hrow = (size_t)b * p.H + hh;
       if (b != cur_b) {
         cur_b = b;
         seq_plan(b, c, st, load, flush, bad);
@@ -1696,9 +1702,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     const bool done = mbar_wait(end_bar, 0, abort_flag, p.err) && !*abort_flag;
     if (done && (MODE == kDecode || MODE == kFlush) && h1 > h0) {
       const int b_first = (int)(h0 / p.H), b_last = (int)((h1 - 1) / p.H);
-      for (int b = b_first; b <= b_last; ++b) {
-        const long long lo = max(h0, (long long)b * p.H), hi = min(h1, (long long)(b + 1) * p.H);
+      for (int vb = b_first; vb <= b_last; ++vb) {
+        const long long lo = max(h0, (long long)vb * p.H), hi = min(h1, (long long)(vb + 1) * p.H);
         const int n_b = (int)(hi - lo);
+        const int b = seq_of(vb);
         int c, st;
         bool load, flush, bad;
         seq_plan(b, c, st, load, flush, bad);

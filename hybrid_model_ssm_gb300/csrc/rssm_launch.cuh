@@ -60,6 +60,9 @@ cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t s
 cudaError_t launch_sround_test(const float* x, uint16_t* y, long long n, long long base, uint32_t epoch,
                                unsigned long long seed, int sr, cudaStream_t st);
 cudaError_t launch_flush(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
+// The standalone flush's list of folding sequences (one block), before launch_flush.
+cudaError_t launch_flush_list(const int32_t* count, int B, int R, int min_count, int32_t* flist, int32_t* fcount,
+                              cudaStream_t st);
 cudaError_t launch_quant(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int rf);
 cudaError_t launch_conv(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
 cudaError_t launch_wait_selftest(uint32_t* err, cudaStream_t st);

@@ -111,8 +111,9 @@ typedef struct rssm_ctx* rssm_handle;
  *            pseudo-values w [B,H,R,P] fp32),
  *      K     [B,G,R,N] in_dtype at offset k_off (see rssm_ring_offsets).
  *  ptr_bytes: pointer block of int32 start[B], count[B], ticket[B], one
- *      uint32 error word (256 bytes) and int32 epoch[B] (flushes per sequence),
- *      each array 256-byte aligned.
+ *      uint32 error word (256 bytes), int32 epoch[B] (flushes per sequence),
+ *      then int32 flist[B] and one int32 (256 bytes), the standalone flush's
+ *      list of folding sequences; each array 256-byte aligned.
  *  read_copy_bytes: B*H*head_stride for a read copy, else 0.
  * Any output pointer may be NULL. Returns RSSM_EINVAL or RSSM_EUNSUPPORTED for
  * a bad configuration. */
@@ -194,7 +195,9 @@ rssm_status rssm_commit(rssm_handle h, const int32_t* accepted, void* stream);
 
 /* Fold every sequence that holds count >= min_count records (min_count >= 1)
  * into its checkpoint, write it once, refresh the read copy, and clear its
- * buffer. Pass min_count = L after a commit. Other sequences are not touched. */
+ * buffer. Pass min_count = L after a commit. Other sequences are not touched.
+ * Two launches on `stream`: a one-block kernel lists the folding sequences in
+ * the pointer block, then the fold runs over exactly their heads. */
 rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream);
 
 /* Copy start[B], count[B] (int32) and the error word to host memory,

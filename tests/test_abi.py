@@ -50,7 +50,7 @@ def test_workspace_layout_of_the_layer_workload(lib):
     assert k_off == v_off + 256 * 128 * R * 64 * 2
     assert ring == k_off + 256 * 8 * R * 128 * 2
     assert v_off % 256 == 0 and k_off % 256 == 0
-    assert ptrs == 4 * 1024 + 256  # start, count, ticket, error word (256 B), epoch
+    assert ptrs == 5 * 1024 + 512  # start, count, ticket, error word (256 B), epoch, flush list, its length
     assert copy == 0
 
 
