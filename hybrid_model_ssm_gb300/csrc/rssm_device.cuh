@@ -578,6 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr bool kF16 = (RF == kCkF16);                          // the checkpoint itself is FP16
   constexpr int CKES = kF16 ? 2 : 4;                             // checkpoint bytes per element
   constexpr bool kDel = (RF == kDelta);                          // gated delta-rule layer
+  // decode: the tile lane brings each head's new record into its slot (the gather
+  // lane, far ahead, the buffered ones); other modes: the gather lane brings all
+  constexpr bool kTileNew = (MODE == kDecode);
   constexpr int kSbOff = (kRMax + kTMax) * 4;                    // delta: slot offset of the write strengths
   constexpr int kCoefOff = 16;  // floats before the per-row coefficients
 
@@ -643,7 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       mbar_init(tempty0 + 8 * s, kNDW / lay.dgroups);  // the warps of the head's dot group
     }
     for (int s = 0; s < lay.slots; ++s) {
-      mbar_init(sfull0 + 8 * s, 2);  // the gather lane's expected bytes + its cp.async decays
+      // the gather lane's bytes, the new records' bytes and their cp.async decays
+      mbar_init(sfull0 + 8 * s, kTileNew ? 3 : 2);
       mbar_init(scoef0 + 8 * s, 1);
       mbar_init(sempty0 + 8 * s, kNDW / lay.dgroups + 1);  // the head's dot group + its coefficient warp
     }
@@ -706,18 +710,38 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   bool ok = true;
   if (warp == kTileWarp) {
     // ====================================================================== tile warp
+    // In decode it also brings each head's new record (from the call's inputs)
+    // into the head's record slot: the value row by bulk copy, the decay (and
+    // write strength) by 4-byte cp.async.
     if (lane == 0) {
       int li = 0, cur_b = -1, c = 0, st = 0;
       bool load = false, flush = false, bad = false;
+      const uint32_t rbytes = (uint32_t)p.P * ES;
       HeadIter it;
       it.init(h0, p.H, p.HPG);
       for (long long gh = h0; gh < h1; ++gh, it.next(p.H, p.HPG)) {
-        const int b = seq_of(it.b);
+        const int b = seq_of(it.b), hh = it.hh;
         if (b != cur_b) {
           cur_b = b;
           seq_plan(b, c, st, load, flush, bad);
         }
         if (!load) continue;
+        if constexpr (kTileNew) {
+          if (li >= lay.slots && !mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err)) { ok = false; break; }
+          const int nnew = records(c) - c;
+          const uint32_t sbar = sfull0 + 8 * rs;
+          const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
+          mbar_arrive_tx(sbar, (uint32_t)nnew * rbytes);
+          for (int t = 0; t < nnew; ++t) {
+            const size_t nrow = kDrafts ? ((size_t)b * p.T + t) * p.H + hh : (size_t)b * p.H + hh;
+            cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
+            if constexpr (kDel) cp_async4(sdst + kSbOff + 4 * (kRMax + t), p.beta + nrow);
+            const uint32_t vdst = kDel ? sdst + lay.nv_off + t * rbytes : sdst + lay.sv_off + (c + t) * rbytes;
+            tma_load_1d(vdst, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes, rbytes, sbar);
+          }
+          cp_async_arrive(sbar);  // completes with this lane's decay copies
+          slot_next();
+        }
         if (li >= lay.stages && !mbar_wait(tempty0 + 8 * ts, tph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const bool from_copy = kCopyRF && (MODE == kDecode) && !flush;
         const size_t hrow = (size_t)b * p.H + it.hh;
@@ -731,11 +755,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         tile_next();
         ++li;
       }
+      cp_async_wait_all();
       if (!ok) {  // drain the bulk copies still in flight (bounded), then leave
         volatile int dummy = 0;
         for (int k = 0; k < lay.stages && k < li; ++k) {
           const int i = li - 1 - k;
           mbar_wait(tfull0 + 8 * (i % lay.stages), (i / lay.stages) & 1, &dummy, p.err);
+        }
+        for (int k = 0; kTileNew && k <= lay.stages && k <= li; ++k) {  // its latest record-slot fills
+          const int i = li - k;
+          mbar_wait(sfull0 + 8 * (i % lay.slots), (i / lay.slots) & 1, &dummy, p.err);
         }
       }
     }
@@ -745,7 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     // into a slot. Committed records sit in the ring at slots st .. st + c - 1
     // (mod R), so their key rows, value rows and decays are at most two
     // contiguous runs each; every run is one bulk copy. New records come from
-    // the call's inputs: one bulk copy per row and a 4-byte cp.async per decay.
+    // the call's inputs: one bulk copy per row and a 4-byte cp.async per decay
+    // (in decode the tile lane brings the new record's value row and decay).
     if (lane == 0) {
       int li = 0, gi = 0, cur_b = -1, c = 0, st = 0, J = 0;
       long long cur_gg = -1;
@@ -798,11 +828,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         if (li >= lay.slots && !mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const uint32_t sbar = sfull0 + 8 * rs;
         const uint32_t sdst = smem_u32(smem + lay.slot_off + (size_t)rs * lay.slot_bytes);
-        // slot: decays at [ring slot] (committed) and kRMax + t (new); value rows in record order
-        // delta-rule layers: buffered records bring their pseudo-values (fp32) and
-        // the new record its v row, to nv_off
+        // slot: decays at [ring slot] (committed) and kRMax + t (new, from the tile
+        // lane); value rows in record order (delta-rule layers: the buffered
+        // records' pseudo-values (fp32), the new record's v row at nv_off)
         const uint32_t vb = kDel ? (uint32_t)p.P * 4 : rbytes;  // bytes of a buffered value row
-        mbar_arrive_tx(sbar, (uint32_t)c * vb + (uint32_t)nnew * rbytes + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
+        mbar_arrive_tx(sbar, (uint32_t)c * vb + (kTileNew ? 0u : (uint32_t)nnew * rbytes) + (c > 0 ? (uint32_t)p.Rp * 4 : 0u));
         if (c > 0) {
           tma_load_1d(sdst, p.ring_a + hrow * p.Rp, (uint32_t)p.Rp * 4, sbar);
           const int n1 = min(c, p.R - st);
@@ -810,14 +840,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           tma_load_1d(sdst + lay.sv_off, rv + (size_t)st * vb, (uint32_t)n1 * vb, sbar);
           if (c > n1) tma_load_1d(sdst + lay.sv_off + n1 * vb, rv, (uint32_t)(c - n1) * vb, sbar);
         }
-        for (int t = 0; t < nnew; ++t) {
-          const size_t nrow = kDrafts ? ((size_t)b * p.T + t) * p.H + hh : hrow;
-          cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
-          if constexpr (kDel) cp_async4(sdst + kSbOff + 4 * (kRMax + t), p.beta + nrow);
-          const uint32_t vdst = kDel ? sdst + lay.nv_off + t * rbytes : sdst + lay.sv_off + (c + t) * rbytes;
-          tma_load_1d(vdst, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes, rbytes, sbar);
+        if constexpr (!kTileNew) {
+          for (int t = 0; t < nnew; ++t) {
+            const size_t nrow = kDrafts ? ((size_t)b * p.T + t) * p.H + hh : hrow;
+            cp_async4(sdst + 4 * (kRMax + t), p.alpha + nrow);
+            if constexpr (kDel) cp_async4(sdst + kSbOff + 4 * (kRMax + t), p.beta + nrow);
+            const uint32_t vdst = kDel ? sdst + lay.nv_off + t * rbytes : sdst + lay.sv_off + (c + t) * rbytes;
+            tma_load_1d(vdst, reinterpret_cast<const uint8_t*>(p.v) + nrow * rbytes, rbytes, sbar);
+          }
+          cp_async_arrive(sbar);  // completes with this lane's decay copies
         }
-        cp_async_arrive(sbar);  // completes with this lane's decay copies
         slot_next();
         ++li;
       }

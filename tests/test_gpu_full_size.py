@@ -3,7 +3,8 @@
 Mamba-2 layer decode: B=256, H=128, P=64, N=128, G=8, L=16, bf16 inputs, 256
 steps from an N(0, 0.1^2) state. Speculative verify: the same layer at B=512,
 T=4, 64 rounds with seeded accepted lengths in 0..4, flushing every sequence
-that reaches 16 records. The GPU runs the whole batch; the float64 oracle
+that reaches 16 records. The same layer as a gated delta-rule layer: 64
+decode steps. The GPU runs the whole batch; the float64 oracle
 follows a sample of sequences (all heads) through every step. The pointers
 of every sequence are compared bit for bit against the oracle's bookkeeping.
 """
@@ -94,3 +95,40 @@ def test_mamba2_verify_b512_t4_64_rounds():
                 assert slice_rel_err(ck[i], orc.ckpt[i], 2) <= REL_TOL, f"round {r}"
     assert flushes > 0
     print(f"verify b512: worst output rel err {worst:.2e}, sampled flushes {flushes}")
+
+
+def test_delta_rule_layer_decode_b256_64_steps():
+    """The same layer shape as a gated delta-rule layer (bench.py --recurrence
+    delta): 64 steps (four flushes), a sample of sequences followed by the
+    delta-rule oracle, pointers of every sequence bit for bit."""
+    from hybrid_model_ssm_gb300 import LayerShape
+    require_gpu()
+    shape = synth.PRESETS["mamba2_layer_b256_l16"]
+    gen = synth.make_generator(shape.seed + 100)
+    S0 = synth.initial_state(shape, gen)
+    ls = LayerShape(B=shape.B, H=shape.H, P=shape.P, N=shape.N, G=shape.G, L=shape.L, in_dtype=shape.in_dtype,
+                    recurrence="delta")
+    model = ReplaySSM(ls, dev(S0))
+    sample = _sample(shape.B)
+    orc = oracle.DeltaReplayOracle(f64(S0[sample]), L=shape.L, R=shape.R, G=shape.G)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    del S0
+    idx = torch.as_tensor(sample, device="cuda")
+    worst_o = worst_s = 0.0
+    for t in range(64):
+        a, b, v, k, q = synth.delta_step_inputs(shape, gen)
+        o = model.decode_step(dev(a), dev(v), dev(k), dev(q), beta=dev(b))
+        o_ref, flushed = orc.decode(*(f64(x[sample]) for x in (a, b, v, k, q)))
+        shadow.decode()
+        e = slice_rel_err(o[idx].cpu(), o_ref, 1)
+        worst_o = max(worst_o, e)
+        assert e <= REL_TOL, f"step {t}: rel err {e:.3g}"
+        if flushed.any():
+            es = slice_rel_err(model.ckpt[idx].cpu(), orc.ckpt, 2)
+            worst_s = max(worst_s, es)
+            assert es <= REL_TOL, f"step {t}: checkpoint rel err {es:.3g}"
+        if t % 16 == 15 or t < 3:
+            start, count, err = model.read_pointers()
+            assert err == 0
+            assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count)
+    print(f"delta b256: worst output rel err {worst_o:.2e}, checkpoint {worst_s:.2e}")
