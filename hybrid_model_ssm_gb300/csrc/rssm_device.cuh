@@ -596,6 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 3 * kMaxSlots + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent of the previous kernel in the stream:
+  // the next launch may be scheduled now, and nothing here touches global
+  // memory before the previous grid has completed.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // kFlush with a list: heads are numbered over the listed sequences only
   const bool listed = (MODE == kFlush) && p.flist != nullptr;
   const long long total = listed ? (long long)min(max(*p.fcount, 0), p.B) * p.H : (long long)p.B * p.H;

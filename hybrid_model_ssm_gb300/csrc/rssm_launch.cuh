@@ -18,7 +18,20 @@ cudaError_t launch_one(const Params& p, int grid, size_t smem, cudaStream_t st) 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, kThreads, smem, st>>>(p);
+  // programmatic dependent launch: the kernel waits for the previous grid before
+  // its first global access, so it may be scheduled while that grid drains
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
