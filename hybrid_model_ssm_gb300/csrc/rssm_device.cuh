@@ -395,16 +395,9 @@ __device__ __forceinline__ f32x2 pk2(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float lo2(f32x2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return a;
-}
-__device__ __forceinline__ float hi2(f32x2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return b;
-}
+// the first element of a pair sits in the low 32 bits
+__device__ __forceinline__ float lo2(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
   f32x2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -569,7 +562,6 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   constexpr int RPI = 32 / LPR;  // rows per warp instruction
   static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "N must be 4..128, power of two");
   constexpr int ES = In<TIn>::kBytes;
-  constexpr int CHN = N * ES / 16;  // 16-byte chunks per k or q row
   constexpr bool kAppendMode = (MODE == kDecode || MODE == kVerify);
   constexpr bool kGroupData = (MODE != kQuant);
   constexpr bool kQuery = (MODE == kDecode || MODE == kVerify || MODE == kConv || MODE == kSnap);
