@@ -36,9 +36,6 @@ namespace rssm {
 #define RSSM_ROWS_PER_WARP 8
 #endif
 constexpr int kNDW = RSSM_DOT_WARPS;       // dot warps per CTA (stream the checkpoint tile)
-#ifndef RSSM_APPEND_BULK
-#define RSSM_APPEND_BULK 0  // ring appends: 16-byte stores (0) or one bulk store per row (1)
-#endif
 #ifndef RSSM_COEF_WARPS
 #define RSSM_COEF_WARPS 2
 #endif
@@ -1042,18 +1039,6 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       if constexpr (kAppendMode) {  // the new decays and value rows go to the ring
         // (delta-rule layers: the dot warps append the pseudo-value row instead)
         const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
-#if RSSM_APPEND_BULK
-        if (lane < na) {  // lane t: one bulk store per value row
-          const int slot_t = ring_slot(st, c + lane, p.R);
-          p.ring_a[hrow * p.Rp + slot_t] = sa[kRMax + lane];
-          if constexpr (!kDel) {
-            bulk_store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + slot_t) * p.P * ES,
-                       smem_u32(sv + (c + lane) * p.P * ES), p.P * ES);
-            bulk_commit();
-            bulk_wait_read();  // the slot may be refilled once its rows have been read
-          }
-        }
-#else
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[kRMax + lane];
         if constexpr (MODE == kVerify) {
           // the T value rows: one bulk store per contiguous ring run (at most two),
@@ -1075,7 +1060,6 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               *reinterpret_cast<uint4*>(dst + ch * 16) = *reinterpret_cast<const uint4*>(sv + (c + t) * p.P * ES + ch * 16);
           }
         }
-#endif
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty0 + 8 * rs);  // this warp is done with the slot
