@@ -47,6 +47,8 @@ DECODE_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_step_b256_l16.md")
 DELTA_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_delta.cu"]
 DELTA_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "delta_decode_step_b256_l16.md")
+VERIFY_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_verify.cu"]
+VERIFY_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_b512_t4.md")
 
 
 # ----------------------------------------------------------------- analytic bytes
@@ -616,14 +618,16 @@ def run_verify(args, world, rank, local):
                    "global_batch": s.B * world, "l2": "no flush needed: 2 GiB checkpoint per replica"},
         "seq_rounds_per_s": world * s.B * args.steps / elapsed,
         "roofline": {"bound": "hbm", "kernel": "verify", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": (profiled_traffic(VERIFY_TRAFFIC_FILE, VERIFY_KERNEL_SOURCES)
+                                 if args.batch is None else None),
                      "algorithmic_bytes_per_launch": vbytes / args.steps,
                      "mean_launch_ms": tv / args.steps * 1e3},
         "breakdown_ms_per_round": {"verify": tv / args.steps * 1e3, "commit": tc / args.steps * 1e3,
                                    "flush": tf / args.steps * 1e3,
                                    "flush_hbm_gbs": fbytes / tf / 1e9 if tf > 0 else None},
         "comparison": comp,
-        "clocks": clk.summary(), "gpu_launches": 3 * args.steps, "device_error_word": err,
+        "clocks": clk.summary(), "gpu_launches": 4 * args.steps,  # verify, commit, flush list, flush "device_error_word": err,
     }
 
 
