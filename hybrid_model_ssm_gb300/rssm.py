@@ -261,13 +261,17 @@ class ReplaySSM:
 
     # ------------------------------------------------------- ring inspection
     def ring_views(self):
-        """(alpha [B,H,Rp] f32, V [B,H,R,P], K [B,G,R,N]) views of the ring buffer (for tests)."""
+        """(alpha [B,H,Rp] f32, V [B,H,R,P], K [B,G,R,N]) views of the ring buffer (for tests).
+
+        V is in the input dtype; a delta-rule layer keeps its pseudo-values there, in f32.
+        """
         s = self.shape
         R, Rp = s.R, (s.R + 3) // 4 * 4
         v_off, k_off = ring_offsets(s)
         es = 4 if s.in_dtype == "f32" else 2
+        vdt, ves = (torch.float32, 4) if s.recurrence == "delta" else (s.torch_in_dtype, es)
         a = self.ring[: s.B * s.H * Rp * 4].view(torch.float32).view(s.B, s.H, Rp)
-        V = self.ring[v_off: v_off + s.B * s.H * R * s.P * es].view(s.torch_in_dtype).view(s.B, s.H, R, s.P)
+        V = self.ring[v_off: v_off + s.B * s.H * R * s.P * ves].view(vdt).view(s.B, s.H, R, s.P)
         K = self.ring[k_off: k_off + s.B * s.G * R * s.N * es].view(s.torch_in_dtype).view(s.B, s.G, R, s.N)
         return a, V, K
 
@@ -276,8 +280,7 @@ class ReplaySSM:
         s = self.shape
         if s.recurrence != "delta":
             raise ValueError("only delta-rule layers keep pseudo-values")
-        v_off, _ = ring_offsets(s)
-        return self.ring[v_off: v_off + s.B * s.H * s.R * s.P * 4].view(torch.float32).view(s.B, s.H, s.R, s.P)
+        return self.ring_views()[1]
 
 
 def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:
