@@ -1177,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           constexpr int LPV = N / 16, RPW = 32 / LPV, KWV = 2, JI = kRMax / LPV;
           const int cl = lane % LPV, rw = lane / LPV;
           for (int t0 = 0; t0 < p.T; t0 += kTQ) {
-            float qv[kTQ][16];
+            f32x2 qv[kTQ][8];  // the lane's 16 query columns as 8 column pairs
             float g[kTQ];
             float wv[JI][kTQ];  // this lane's record weights
 #pragma unroll
@@ -1188,7 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               for (int cc = 0; cc < 4; ++cc) {
                 const float4 qq = tv ? In<TIn>::lds4(gQ, (t0 + tt) * N + (cc * LPV + cl) * 4)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                qv[tt][4 * cc] = qq.x; qv[tt][4 * cc + 1] = qq.y; qv[tt][4 * cc + 2] = qq.z; qv[tt][4 * cc + 3] = qq.w;
+                qv[tt][2 * cc] = pk2(qq.x, qq.y);
+                qv[tt][2 * cc + 1] = pk2(qq.z, qq.w);
               }
 #pragma unroll
               for (int i = 0; i < JI; ++i) {
@@ -1206,19 +1207,20 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
                 for (int tt = 0; tt < kTQ; ++tt) a[tt] = 0.f;
                 if (row < p.P) {
                   const float* rp = tf + (size_t)row * N;
+                  f32x2 a2[kTQ];  // column-pair partial sums, packed fp32x2 FMAs
+#pragma unroll
+                  for (int tt = 0; tt < kTQ; ++tt) a2[tt] = 0ull;
 #pragma unroll
                   for (int cc = 0; cc < 4; ++cc) {
-                    const float4 x = lds4(rp + (cc * LPV + cl) * 4);
+                    const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(rp + (cc * LPV + cl) * 4);
 #pragma unroll
                     for (int tt = 0; tt < kTQ; ++tt) {
-                      a[tt] = fmaf(x.x, qv[tt][4 * cc], a[tt]);
-                      a[tt] = fmaf(x.y, qv[tt][4 * cc + 1], a[tt]);
-                      a[tt] = fmaf(x.z, qv[tt][4 * cc + 2], a[tt]);
-                      a[tt] = fmaf(x.w, qv[tt][4 * cc + 3], a[tt]);
+                      a2[tt] = fma2(x.x, qv[tt][2 * cc], a2[tt]);
+                      a2[tt] = fma2(x.y, qv[tt][2 * cc + 1], a2[tt]);
                     }
                   }
 #pragma unroll
-                  for (int tt = 0; tt < kTQ; ++tt) a[tt] *= g[tt];
+                  for (int tt = 0; tt < kTQ; ++tt) a[tt] = g[tt] * (lo2(a2[tt]) + hi2(a2[tt]));
 #pragma unroll
                   for (int i = 0; i < JI; ++i) {
                     const int j = cl + LPV * i;
