@@ -21,6 +21,12 @@ The checkpoint is read once per step, as for the outer-product recurrence;
 the extra work is O(h N) per head. A fold applies the records in order:
     S <- alpha_j S + beta_j (v_j - alpha_j S k_j) k_j^T.
 Flush policy and pointers are those of ``replay.ReplayOracle``.
+
+The write term of step j, w_j = beta_j (v_j - alpha_j S_{j-1} k_j) with
+S_{j-1} the state just before it (``delta_pseudo_value``), makes every step
+S_j = alpha_j S_{j-1} + w_j k_j^T: the outer-product recurrence with v_j
+replaced by w_j. A replay may therefore keep w_j per record instead of v_j.
+``tests/test_oracle_delta.py`` pins w_j to the step's own write term.
 """
 from __future__ import annotations
 
