@@ -507,6 +507,8 @@ def run_verify(args, world, rank, local):
 
     torch.cuda.set_device(local)
     s = VERIFY_WORKLOAD if args.batch is None else VERIFY_WORKLOAD.with_(B=args.batch)
+    if args.drafts is not None:
+        s = s.with_(T_max=args.drafts)
     T = s.T_max
     ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=T, in_dtype=s.in_dtype)
     dev = torch.device("cuda", local)
@@ -767,6 +769,8 @@ def main(argv=None):
                     help="non-flush steps read a low-precision copy of the checkpoint")
     ap.add_argument("--ckpt", choices=["f32", "f16_sr", "f16_rn"], default="f32",
                     help="checkpoint storage: FP32, or FP16 stored with stochastic / nearest rounding")
+    ap.add_argument("--drafts", type=int, default=None,
+                    help="verify: drafts per round T (1..8; default 4); other values are not the headline config")
     ap.add_argument("--recurrence", choices=["outer", "delta"], default="outer",
                     help="decode: the gated outer-product recurrence or the gated delta rule (beta inputs)")
     args = ap.parse_args(argv)
