@@ -50,6 +50,19 @@ def _rank(rank, world, port, results):
         dist.destroy_process_group()
 
 
+def test_window_bytes_of_a_delta_rule_layer():
+    """Delta-rule windows: the inputs carry beta (4 B per head) and the buffered
+    records hold fp32 pseudo-values instead of bf16 values (2 more bytes per
+    element), for the 120 buffered-record reads and 15 appends of a window."""
+    s = synth.PRESETS["mamba2_layer_b256_l16"]
+    outer, delta = bench.window_bytes(s), bench.window_bytes(s, delta=True)
+    beta_in = 16 * 4 * 128                      # one beta per head and step
+    ring_extra = (16 * 15 // 2 + 15) * 2 * 128 * 64  # record reads + appends, 2 B more per element
+    assert delta["replay_window"] - outer["replay_window"] == beta_in + ring_extra == 2220032
+    assert delta["state"] == outer["state"]
+    assert delta["replay_per_seq_step"] == 4808800
+
+
 def test_max_over_ranks_with_two_gloo_ranks():
     world = 2
     results = mp.Manager().dict()
