@@ -10,8 +10,12 @@ Each check rests on something other than the function it checks:
 - the replay formula and the fold, two different computations, against the
   step-by-step definition;
 - the pointer bookkeeping against the outer-product oracle's, bit for bit;
-- the pseudo-value w of a step against the step itself: S_t - alpha S = w k^T.
+- the pseudo-value w of a step against the step itself: S_t - alpha S = w k^T;
+- a two-step example worked by hand (tests/golden/hand_delta_two_step.txt), one
+  step with a key coupled to the earlier one.
 """
+import os
+
 import numpy as np
 
 import oracle
@@ -121,3 +125,45 @@ def test_pseudo_value_is_the_steps_write_term():
     w = delta.delta_pseudo_value(S, a, b, v, k)
     g = oracle.head_groups(H, G)
     assert np.allclose(S1 - a[:, :, None, None] * S, w[..., None] * k[:, g, None, :], atol=1e-12)
+
+
+def _golden_delta():
+    """name -> fields of tests/golden/hand_delta_two_step.txt."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "hand_delta_two_step.txt")
+    rows = {}
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            name, *rest = line.split()
+            rows[name] = rest
+    return rows
+
+
+def _step_inputs(fields):
+    """'alpha a beta b v v0 v1 k k0 k1 q q0 q1' -> the [1,1,...] arrays delta_step takes."""
+    d, i = {}, 0
+    while i < len(fields):
+        n = 2 if fields[i] in ("v", "k", "q") else 1
+        d[fields[i]] = np.array([float(x) for x in fields[i + 1: i + 1 + n]])
+        i += 1 + n
+    return (d["alpha"].reshape(1, 1), d["beta"].reshape(1, 1), d["v"][None, None], d["k"][None, None],
+            d["q"][None, None])
+
+
+def test_hand_computed_two_step_example():
+    """tests/golden/hand_delta_two_step.txt: steps, pseudo-values, replay output and fold."""
+    g = _golden_delta()
+    num = lambda xs: np.array([float(x) for x in xs])  # noqa: E731
+    S0 = num(g["S0"]).reshape(1, 1, 2, 2)
+    steps = [_step_inputs(g["step1"]), _step_inputs(g["step2"])]
+    S = S0
+    for n, (a, b, v, k, q) in enumerate(steps, 1):
+        w = delta.delta_pseudo_value(S, a, b, v, k)
+        assert np.allclose(w[0, 0], num(g[f"w{n}"]), atol=1e-12)
+        S, o = delta.delta_step(S, a, b, v, k, q)
+        assert np.allclose(S[0, 0].ravel(), num(g[f"S{n}"]), atol=1e-12)
+        assert np.allclose(o[0, 0], num(g[f"o{n}"]), atol=1e-12)
+    al, be = np.stack([x[0][0] for x in steps]), np.stack([x[1][0] for x in steps])
+    vs, ks = np.stack([x[2][0] for x in steps]), np.stack([x[3][0] for x in steps])
+    q2 = steps[1][4][0]
+    assert np.allclose(delta.delta_replay_output(S0[0], al, be, vs, ks, q2)[0], num(g["o2"]), atol=1e-12)
+    assert np.allclose(delta.delta_fold(S0[0], al, be, vs, ks)[0].ravel(), num(g["S2"]), atol=1e-12)
