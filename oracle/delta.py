@@ -20,7 +20,11 @@ so the output needs the query carried backwards through the records:
 The checkpoint is read once per step, as for the outer-product recurrence;
 the extra work is O(h N) per head. A fold applies the records in order:
     S <- alpha_j S + beta_j (v_j - alpha_j S k_j) k_j^T.
-Flush policy and pointers are those of ``replay.ReplayOracle``.
+Flush policy and pointers are those of ``replay.ReplayOracle``, and so are
+speculative verify (T drafts evaluated on a copy of the exact state, nothing
+changed) and commit (the first a drafts applied, count += a): the pages state
+rollback and output-only evaluation for the replay form in general ([RU] 05),
+and nothing in them is specific to the outer-product rule.
 
 The write term of step j, w_j = beta_j (v_j - alpha_j S_{j-1} k_j) with
 S_{j-1} the state just before it (``delta_pseudo_value``), makes every step
@@ -33,6 +37,7 @@ from __future__ import annotations
 import numpy as np
 
 from .recurrence import head_groups
+from .replay import CapacityError
 
 
 def delta_step(S, alpha, beta, v, k, q):
@@ -100,7 +105,7 @@ def delta_fold(S_ckpt, alphas, betas, vs, ks):
 
 
 class DeltaReplayOracle:
-    """Replay decoding of a gated delta-rule layer with an FP32 checkpoint.
+    """Replay decoding (and speculative verify / commit) of a gated delta-rule layer.
 
     The exact target is the definition, so ``S`` advances by ``delta_step``
     and the outputs are its outputs; ``ckpt`` is the exact state at each
@@ -116,17 +121,50 @@ class DeltaReplayOracle:
         self.L, self.R, self.G = L, R, G
         self.start = np.zeros(self.B, np.int64)
         self.count = np.zeros(self.B, np.int64)
+        self._drafts = None
 
     def decode(self, alpha, beta, v, k, q):
         h = self.count + 1
         if np.any(h > self.R):
-            raise ValueError("decode would exceed the ring capacity")
+            raise CapacityError("decode would exceed the ring capacity")
+        self._drafts = None
         self.S, o = delta_step(self.S, alpha, beta, v, k, q)
         flush = h >= self.L
         self.ckpt[flush] = self.S[flush]
         self.start = np.where(flush, (self.start + h) % self.R, self.start)
         self.count = np.where(flush, 0, h)
         return o, flush
+
+    def verify(self, alpha, beta, v, k, q):
+        """Speculative verify of T drafts: alpha, beta [B,T,H], v [B,T,H,P], k, q [B,T,G,N].
+
+        Output-only: the drafts run on a scratch copy of the exact state, so the
+        real state and the pointers stay unchanged. Returns O [B,T,H,P].
+        """
+        T = alpha.shape[1]
+        if np.any(self.count + T > self.R):
+            raise CapacityError("verify would exceed the ring capacity")
+        O = np.empty(v.shape)
+        Sc = self.S.copy()
+        for t in range(T):
+            Sc, O[:, t] = delta_step(Sc, alpha[:, t], beta[:, t], v[:, t], k[:, t], q[:, t])
+        self._drafts = (alpha.copy(), beta.copy(), v.copy(), k.copy(), q.copy(), T)
+        return O
+
+    def commit(self, accepted):
+        """Apply the first accepted[b] drafts of the last verify (count += a)."""
+        if self._drafts is None:
+            raise CapacityError("commit without a preceding verify")
+        alpha, beta, v, k, q, T = self._drafts
+        a = np.asarray(accepted, np.int64)
+        if np.any(a < 0) or np.any(a > T):
+            raise CapacityError("accepted length outside 0..T")
+        for t in range(T):
+            m = t < a
+            if np.any(m):
+                self.S[m], _ = delta_step(self.S[m], alpha[m, t], beta[m, t], v[m, t], k[m, t], q[m, t])
+        self.count = self.count + a
+        self._drafts = None
 
     def flush(self, min_count: int):
         mask = (self.count >= min_count) & (self.count > 0)

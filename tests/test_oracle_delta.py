@@ -12,11 +12,17 @@ Each check rests on something other than the function it checks:
 - the pointer bookkeeping against the outer-product oracle's, bit for bit;
 - the pseudo-value w of a step against the step itself: S_t - alpha S = w k^T;
 - a two-step example worked by hand (tests/golden/hand_delta_two_step.txt), one
-  step with a key coupled to the earlier one.
+  step with a key coupled to the earlier one;
+- speculative verify and commit: the hand example as two drafts, the projection
+  and associative-memory properties within a verify, each draft's output
+  against the replay formula, commit of an accepted prefix against the fold
+  (with junk in the rejected drafts), and the pointers against the
+  outer-product oracle's verify and commit.
 """
 import os
 
 import numpy as np
+import pytest
 
 import oracle
 from oracle import delta
@@ -167,3 +173,138 @@ def test_hand_computed_two_step_example():
     q2 = steps[1][4][0]
     assert np.allclose(delta.delta_replay_output(S0[0], al, be, vs, ks, q2)[0], num(g["o2"]), atol=1e-12)
     assert np.allclose(delta.delta_fold(S0[0], al, be, vs, ks)[0].ravel(), num(g["S2"]), atol=1e-12)
+
+
+# Speculative verify and commit on a gated delta-rule layer.
+
+
+def _drafts(rng, B, T, H, G, P, N):
+    return (rng.uniform(0.5, 1.0, (B, T, H)), rng.uniform(0.0, 1.0, (B, T, H)), rng.standard_normal((B, T, H, P)),
+            rng.standard_normal((B, T, G, N)), rng.standard_normal((B, T, G, N)))
+
+
+def test_verify_and_commit_of_the_hand_example():
+    """The two golden steps as two drafts: outputs o1, o2; commit(1) leaves S1, commit(2) S2."""
+    g = _golden_delta()
+    num = lambda xs: np.array([float(x) for x in xs])  # noqa: E731
+    S0 = num(g["S0"]).reshape(1, 1, 2, 2)
+    steps = [_step_inputs(g["step1"]), _step_inputs(g["step2"])]
+    drafts = [np.stack([s[i] for s in steps], axis=1) for i in range(5)]  # [1, T=2, ...]
+    for a, S_name in ((1, "S1"), (2, "S2")):
+        d = delta.DeltaReplayOracle(S0, L=4, R=4, G=1)
+        O = d.verify(*drafts)
+        assert np.allclose(O[0, 0, 0], num(g["o1"]), atol=1e-12)
+        assert np.allclose(O[0, 1, 0], num(g["o2"]), atol=1e-12)
+        assert np.array_equal(d.S, S0) and d.count[0] == 0
+        d.commit([a])
+        assert np.allclose(d.S[0, 0].ravel(), num(g[S_name]), atol=1e-12) and d.count[0] == a
+
+
+def test_verify_keeps_the_projection_and_memory_properties():
+    """beta = 1 and unit keys: draft t's output at q = k_t is v_t for any state and decay;
+    with alpha = 1 and orthonormal keys a later draft's query k_i reads back v_i."""
+    rng = np.random.default_rng(6)
+    B, T, H, G, P, N = 2, 4, 3, 1, 5, 8
+    d = delta.DeltaReplayOracle(rng.standard_normal((B, H, P, N)), L=8, R=8, G=G)
+    d.decode(rng.uniform(0.5, 1, (B, H)), rng.uniform(0, 1, (B, H)), rng.standard_normal((B, H, P)),
+             rng.standard_normal((B, G, N)), rng.standard_normal((B, G, N)))
+    alpha, _, v, _, _ = _drafts(rng, B, T, H, G, P, N)
+    k = rng.standard_normal((B, T, G, N))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    O = d.verify(alpha, np.ones((B, T, H)), v, k, k.copy())
+    assert np.allclose(O, v, atol=1e-12)
+    Q = np.stack([np.linalg.qr(rng.standard_normal((N, N)))[0][:, :T].T for _ in range(B)])  # [B, T, N]
+    kq = Q[:, :, None, :]
+    q = kq.copy()
+    q[:, 3] = kq[:, 0]  # the last draft reads back the first draft's value
+    O = d.verify(np.ones((B, T, H)), np.ones((B, T, H)), v, kq, q)
+    assert np.allclose(O[:, 3], v[:, 0], atol=1e-12)
+    assert np.allclose(O[:, :3], v[:, :3], atol=1e-12)
+
+
+def test_verify_matches_the_replay_formula():
+    """Draft t's output equals the backward query carry over the committed records and drafts 1..t."""
+    rng = np.random.default_rng(7)
+    B, T, H, G, P, N, L = 3, 3, 4, 2, 5, 6, 8
+    S0 = rng.standard_normal((B, H, P, N))
+    d = delta.DeltaReplayOracle(S0, L=L, R=L, G=G)
+    recs = []
+    for _ in range(2):
+        a, b, v, k, q = (x[:, 0] for x in _drafts(rng, B, 1, H, G, P, N))
+        d.decode(a, b, v, k, q)
+        recs.append((a, b, v, k))
+    dr = _drafts(rng, B, T, H, G, P, N)
+    O = d.verify(*dr)
+    for t in range(T):
+        rows = recs + [tuple(x[:, j] for x in dr[:4]) for j in range(t + 1)]
+        for bb in range(B):
+            al, be, vs, ks = (np.stack([r[i][bb] for r in rows]) for i in range(4))
+            o = delta.delta_replay_output(S0[bb], al, be, vs, ks, dr[4][bb, t])
+            assert np.allclose(O[bb, t], o, rtol=1e-11, atol=1e-11), (bb, t)
+
+
+def test_commit_applies_only_the_accepted_prefix():
+    """The rejected drafts' inputs do not reach the state; the state equals the fold of the accepted records."""
+    rng = np.random.default_rng(8)
+    B, T, H, G, P, N, L = 5, 4, 2, 1, 4, 6, 8
+    S0 = rng.standard_normal((B, H, P, N))
+    dr = _drafts(rng, B, T, H, G, P, N)
+    acc = np.array([0, 1, 2, 3, 4])
+    junk = [x.copy() for x in dr]
+    for bb, a in enumerate(acc):
+        for x in junk:
+            x[bb, a:] = rng.standard_normal(x[bb, a:].shape)
+    d1, d2 = (delta.DeltaReplayOracle(S0, L=L, R=L, G=G) for _ in range(2))
+    d1.verify(*dr)
+    d2.verify(*junk)
+    d1.commit(acc)
+    d2.commit(acc)
+    assert np.array_equal(d1.S, d2.S) and np.array_equal(d1.count, acc)
+    for bb, a in enumerate(acc):
+        al, be, vs, ks = (x[bb, :a] for x in dr[:4])
+        want = delta.delta_fold(S0[bb], al, be, vs, ks) if a else S0[bb]
+        assert np.allclose(d1.S[bb], want, rtol=1e-12, atol=1e-12), bb
+    assert np.array_equal(d1.S[0], S0[0])  # commit of 0 drafts leaves the state bit for bit
+
+
+def test_verify_commit_pointers_follow_the_outer_product_oracle():
+    rng = np.random.default_rng(9)
+    B, T, H, G, P, N, L = 4, 3, 2, 1, 3, 4, 6
+    S0 = rng.standard_normal((B, H, P, N))
+    d = delta.DeltaReplayOracle(S0, L=L, R=L + T, G=G)
+    r = oracle.ReplayOracle(S0, L=L, R=L + T, G=G)
+    for rnd in range(12):
+        a, b, v, k, q = _drafts(rng, B, T, H, G, P, N)
+        d.verify(a, b, v, k, q)
+        r.verify(a, v, k, q)
+        acc = rng.integers(0, T + 1, B)
+        d.commit(acc)
+        r.commit(acc)
+        assert np.array_equal(d.flush(L), r.flush(L))
+        assert np.array_equal(d.start, r.start) and np.array_equal(d.count, r.count), rnd
+
+
+def test_verify_and_commit_refusals():
+    rng = np.random.default_rng(10)
+    B, T, H, G, P, N = 2, 3, 2, 1, 3, 4
+    d = delta.DeltaReplayOracle(rng.standard_normal((B, H, P, N)), L=4, R=4, G=G)
+    dr = _drafts(rng, B, T, H, G, P, N)
+    with pytest.raises(oracle.CapacityError):
+        d.commit([0, 0])  # no verify yet
+    d.decode(*(x[:, 0] for x in dr))
+    d.decode(*(x[:, 1] for x in dr))
+    with pytest.raises(oracle.CapacityError):
+        d.verify(*dr)  # 2 + 3 records > R = 4
+    d.verify(*(x[:, :2] for x in dr))
+    with pytest.raises(oracle.CapacityError):
+        d.commit([3, 0])  # more than drafted
+    with pytest.raises(oracle.CapacityError):
+        d.commit([-1, 0])
+    d.commit([2, 1])
+    with pytest.raises(oracle.CapacityError):
+        d.commit([0, 0])  # a verify is committed once
+    d.flush(1)
+    d.verify(*(x[:, :2] for x in dr))
+    d.decode(*(x[:, 0] for x in dr))
+    with pytest.raises(oracle.CapacityError):
+        d.commit([1, 1])  # a decode step discards the pending drafts
