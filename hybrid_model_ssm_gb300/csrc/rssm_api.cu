@@ -115,7 +115,6 @@ struct Plan {
   rssm::Params p{};
 };
 
-// Tile stages, record slots and shared-memory carve for one launch (see Params in rssm_device.cuh).
 // Shared-memory plan of a head-kernel launch: the group areas, scratch and
 // barriers at the top of the CTA's shared memory, and below them two layouts of
 // tile stages and record slots (see rssm::Params). lay[0] fits every head.
@@ -140,9 +139,9 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   const size_t sc_off = align_up(nv_off + (delta ? P * es : 0), 16);
   // coefficients: 16 scalars, then the record weights [kRMax] (non-flush),
   // [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general, which
-  // also serves non-flush heads)
-  // delta layers: 16 scalars, the output weights and the new record's couplings
-  // [kRMax] each, then (general) the fold's scaled values [R][P]
+  // also serves non-flush heads). Delta layers: 16 scalars, the output weights
+  // and the new record's couplings [kRMax] each, then (general) the fold's
+  // scaled values [R][P].
   const size_t sc_floats = delta ? 16 + 2 * (size_t)kRMax + (nf ? 0 : R * P)
                          : nf    ? 16 + std::max(P, (size_t)kRMax)
                               : kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax
@@ -217,7 +216,7 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
 }
 
 int sm_count() {
-  static int cached_dev = -1, cached = 0;
+  thread_local int cached_dev = -1, cached = 0;  // per thread: no shared mutable state
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev != cached_dev) {

@@ -13,9 +13,11 @@
  *
  * Conventions for every call:
  *  - All tensors are caller-owned device memory in row-major layout with the
- *    last index contiguous. Base pointers must be 16-byte aligned. The library
- *    never allocates device memory. Its only allocation is the small host
- *    handle.
+ *    last index contiguous. Base pointers must be 16-byte aligned. No call
+ *    allocates device memory: the caller provides every buffer, and the
+ *    library's one piece of device memory of its own is the static ticket
+ *    array of rssm_decode_step_static_scratch. The only run-time allocation is
+ *    the small host handle.
  *  - Calls are asynchronous on the given stream (a cudaStream_t passed as
  *    void*; NULL means the legacy default stream). The one exception is
  *    rssm_read_pointers, which synchronizes the stream.
@@ -29,9 +31,13 @@
  *  - No C++ exception crosses this boundary. A handle is not thread safe: use
  *    one stream per handle at a time.
  *
+ * A second recurrence, the gated delta rule of Gated DeltaNet layers, is
+ * selected per handle by rssm_config.recurrence (see rssm_recurrence).
+ *
  * Supported sizes: N in {16, 32, 64, 128}; P a multiple of 8, at most 128;
- * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8. Read copies need
- * N in {64, 128}.
+ * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8. Read copies and
+ * FP16 checkpoints need N in {64, 128}. A delta-rule layer needs N in
+ * {64, 128}, an FP32 checkpoint, no read copy and T_max = 1.
  */
 #ifndef RSSM_H_
 #define RSSM_H_
