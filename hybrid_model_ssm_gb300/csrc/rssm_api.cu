@@ -215,6 +215,21 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   return RSSM_OK;
 }
 
+// derive() plus a check that every launch of a handle with this configuration
+// fits one CTA's shared memory, so that an unplaceable size is refused when the
+// buffers are sized and the handle is made, not at its first launch.
+rssm_status derive_placed(const rssm_config* c, Geom* g) {
+  rssm_status s = derive(c, g);
+  if (s != RSSM_OK) return s;
+  Plan pl;
+  s = plan_smem(c, *g, &pl);
+  if (s == RSSM_OK && c->T_max > 1) s = plan_smem(c, *g, &pl, LayoutKind::kVerify);
+  if (s != RSSM_OK)
+    return fail(s, "P=%d N=%d R=%d with %s inputs does not fit one CTA's shared memory (%s)", c->P, c->N, g->R,
+                c->in_dtype == RSSM_F32 ? "f32" : "bf16", g_msg.c_str());
+  return RSSM_OK;
+}
+
 int sm_count() {
   thread_local int cached_dev = -1, cached = 0;  // per thread: no shared mutable state
   int dev = 0;
@@ -277,7 +292,7 @@ const char* rssm_last_error(void) { return g_msg.c_str(); }
 rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* ring_bytes, size_t* ptr_bytes,
                                 size_t* read_copy_bytes) {
   Geom g;
-  const rssm_status s = derive(cfg, &g);
+  const rssm_status s = derive_placed(cfg, &g);
   if (s != RSSM_OK) return s;
   if (ring_bytes) *ring_bytes = g.ring_bytes;
   if (ptr_bytes) *ptr_bytes = g.ptr_bytes;
@@ -287,7 +302,7 @@ rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* ring_bytes, size
 
 rssm_status rssm_ring_offsets(const rssm_config* cfg, size_t* v_off, size_t* k_off) {
   Geom g;
-  const rssm_status s = derive(cfg, &g);
+  const rssm_status s = derive_placed(cfg, &g);
   if (s != RSSM_OK) return s;
   if (v_off) *v_off = g.v_off;
   if (k_off) *k_off = g.k_off;
@@ -297,7 +312,7 @@ rssm_status rssm_ring_offsets(const rssm_config* cfg, size_t* v_off, size_t* k_o
 rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, size_t* bscale_off,
                                   size_t* rscale_off) {
   Geom g;
-  const rssm_status s = derive(cfg, &g);
+  const rssm_status s = derive_placed(cfg, &g);
   if (s != RSSM_OK) return s;
   if (cfg->read_fmt == RSSM_READ_NONE) return fail(RSSM_EINVAL, "configuration has no read copy");
   if (head_stride) *head_stride = g.head_stride;
@@ -311,7 +326,7 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
   if (!out) return fail(RSSM_EINVAL, "out is NULL");
   *out = nullptr;
   Geom g;
-  rssm_status s = derive(cfg, &g);
+  rssm_status s = derive_placed(cfg, &g);
   if (s != RSSM_OK) return s;
   if (!ckpt || !ring || !ptrs) return fail(RSSM_EINVAL, "ckpt, ring and ptrs must be non-NULL");
   if (!aligned16(ckpt) || !aligned16(ring) || !aligned16(ptrs))

@@ -37,7 +37,13 @@
  * Supported sizes: N in {16, 32, 64, 128}; P a multiple of 8, at most 128;
  * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8. Read copies and
  * FP16 checkpoints need N in {64, 128}. A delta-rule layer needs N in
- * {64, 128}, an FP32 checkpoint, no read copy and T_max = 1.
+ * {64, 128}, an FP32 checkpoint, no read copy and T_max = 1. Every launch
+ * keeps two checkpoint tiles, two record slots and two groups' keys and
+ * queries in one CTA's shared memory; the one corner of the grid above where
+ * they do not fit is f32 inputs with P = N = 128 and R >= 30 (a delta-rule
+ * layer: L >= 29). rssm_workspace_size, rssm_ring_offsets,
+ * rssm_read_copy_layout and rssm_create return RSSM_EUNSUPPORTED for every
+ * size they cannot place.
  */
 #ifndef RSSM_H_
 #define RSSM_H_

@@ -76,6 +76,10 @@ def test_read_copy_layouts(lib):
     (dict(T_max=9), RSSM_EUNSUPPORTED),
     (dict(N=32, read_fmt="e2m1"), RSSM_EUNSUPPORTED),
     (dict(P=256, N=128), RSSM_EUNSUPPORTED),
+    # two f32 tiles of 128 x 128, two record slots and the group areas overflow shared memory
+    (dict(P=128, N=128, L=30, in_dtype="f32"), RSSM_EUNSUPPORTED),
+    (dict(P=128, N=128, L=27, T_max=4, in_dtype="f32"), RSSM_EUNSUPPORTED),
+    (dict(P=128, N=128, L=29, in_dtype="f32", recurrence="delta"), RSSM_EUNSUPPORTED),
 ])
 def test_invalid_configurations_are_rejected(lib, kw, status):
     base = dict(B=2, H=4, P=16, N=64, G=2, L=4, T_max=1)
@@ -83,6 +87,23 @@ def test_invalid_configurations_are_rejected(lib, kw, status):
     with pytest.raises(RssmError) as ei:
         workspace_size(LayerShape(**base))
     assert ei.value.status == status
+
+
+@pytest.mark.parametrize("kw", [
+    dict(P=128, N=128, L=29, in_dtype="f32"),
+    dict(P=128, N=128, L=26, T_max=4, in_dtype="f32"),
+    dict(P=128, N=128, L=28, in_dtype="f32", recurrence="delta"),
+    dict(P=128, N=128, L=32),
+    dict(P=128, N=128, L=25, T_max=8),
+    dict(P=128, N=128, L=32, recurrence="delta"),
+    dict(P=120, N=128, L=32, in_dtype="f32"),
+])
+def test_largest_placeable_configurations_are_accepted(lib, kw):
+    """The edge of the shared-memory plan: each of these still fits one CTA."""
+    base = dict(B=2, H=4, G=2, T_max=1)
+    base.update(kw)
+    ring, ptrs, _ = workspace_size(LayerShape(**base))
+    assert ring > 0 and ptrs > 0
 
 
 def test_null_config_and_handle(lib):
