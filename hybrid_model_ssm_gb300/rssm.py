@@ -163,13 +163,15 @@ def _stream_ptr(stream) -> int | None:
     return stream.cuda_stream
 
 
-def _expect(t: torch.Tensor, shape, dtype, name: str):
+def _expect(t: torch.Tensor, shape, dtype, name: str, device: torch.device | None = None):
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
     if t.dtype != dtype:
         raise ValueError(f"{name}: dtype {t.dtype} != {dtype}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the layer's state is on {device}")
 
 
 class ReplaySSM:
@@ -191,8 +193,9 @@ class ReplaySSM:
         self.copy = torch.empty(copy_b, dtype=torch.uint8, device=dev) if copy_b else None
         self._cfg = shape.config()
         h = ctypes.c_void_p()
-        _check(lib().rssm_create(ctypes.byref(self._cfg), _ptr(ckpt), _ptr(self.ring), _ptr(self.ptrs),
-                                 _ptr(self.copy), _stream_ptr(stream), ctypes.byref(h)))
+        with torch.cuda.device(dev):
+            _check(lib().rssm_create(ctypes.byref(self._cfg), _ptr(ckpt), _ptr(self.ring), _ptr(self.ptrs),
+                                     _ptr(self.copy), _stream_ptr(stream), ctypes.byref(h)))
         self._h = h
 
     def __del__(self):
@@ -204,45 +207,50 @@ class ReplaySSM:
     # ------------------------------------------------------------ decode path
     def decode_step(self, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:
         """One decode step; a delta-rule layer also takes beta [B,H] fp32."""
-        s = self.shape
-        _expect(alpha, (s.B, s.H), torch.float32, "alpha")
+        s, d = self.shape, self.ckpt.device
+        _expect(alpha, (s.B, s.H), torch.float32, "alpha", d)
         if (beta is None) != (s.recurrence == "outer"):
             raise ValueError("beta is required for (and only for) a delta-rule layer")
-        _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v")
-        _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k")
-        _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q")
+        _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v", d)
+        _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k", d)
+        _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q", d)
         if out is None:
-            out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=alpha.device)
-        _expect(out, (s.B, s.H, s.P), torch.float32, "out")
-        if beta is None:
-            _check(lib().rssm_decode_step(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
-                                          _stream_ptr(stream)))
-        else:
-            _expect(beta, (s.B, s.H), torch.float32, "beta")
-            _check(lib().rssm_decode_step_delta(self._h, _ptr(alpha), _ptr(beta), _ptr(v), _ptr(k), _ptr(q),
-                                                _ptr(out), _stream_ptr(stream)))
+            out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=d)
+        _expect(out, (s.B, s.H, s.P), torch.float32, "out", d)
+        with torch.cuda.device(d):
+            if beta is None:
+                _check(lib().rssm_decode_step(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
+                                              _stream_ptr(stream)))
+            else:
+                _expect(beta, (s.B, s.H), torch.float32, "beta", d)
+                _check(lib().rssm_decode_step_delta(self._h, _ptr(alpha), _ptr(beta), _ptr(v), _ptr(k), _ptr(q),
+                                                    _ptr(out), _stream_ptr(stream)))
         return out
 
     def verify(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
-        s = self.shape
+        s, d = self.shape, self.ckpt.device
         T = alpha.shape[1]
-        _expect(alpha, (s.B, T, s.H), torch.float32, "alpha")
-        _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v")
-        _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k")
-        _expect(q, (s.B, T, s.G, s.N), s.torch_in_dtype, "q")
+        _expect(alpha, (s.B, T, s.H), torch.float32, "alpha", d)
+        _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v", d)
+        _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k", d)
+        _expect(q, (s.B, T, s.G, s.N), s.torch_in_dtype, "q", d)
         if out is None:
-            out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=alpha.device)
-        _expect(out, (s.B, T, s.H, s.P), torch.float32, "out")
-        _check(lib().rssm_verify(self._h, T, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
-                                 _stream_ptr(stream)))
+            out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=d)
+        _expect(out, (s.B, T, s.H, s.P), torch.float32, "out", d)
+        with torch.cuda.device(d):
+            _check(lib().rssm_verify(self._h, T, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
+                                     _stream_ptr(stream)))
         return out
 
     def commit(self, accepted: torch.Tensor, stream=None):
-        _expect(accepted, (self.shape.B,), torch.int32, "accepted")
-        _check(lib().rssm_commit(self._h, _ptr(accepted), _stream_ptr(stream)))
+        _expect(accepted, (self.shape.B,), torch.int32, "accepted", self.ckpt.device)
+        with torch.cuda.device(self.ckpt.device):
+            _check(lib().rssm_commit(self._h, _ptr(accepted), _stream_ptr(stream)))
 
     def flush(self, min_count: int | None = None, stream=None):
-        _check(lib().rssm_flush(self._h, self.shape.L if min_count is None else int(min_count), _stream_ptr(stream)))
+        with torch.cuda.device(self.ckpt.device):
+            _check(lib().rssm_flush(self._h, self.shape.L if min_count is None else int(min_count),
+                                    _stream_ptr(stream)))
 
     def read_pointers(self, stream=None, check: bool = True):
         """(start, count, error word) as host int32 tensors and an int; synchronizes the stream."""
@@ -250,14 +258,16 @@ class ReplaySSM:
         start = (ctypes.c_int32 * B)()
         count = (ctypes.c_int32 * B)()
         err = ctypes.c_uint32()
-        st = lib().rssm_read_pointers(self._h, start, count, ctypes.byref(err), _stream_ptr(stream))
+        with torch.cuda.device(self.ckpt.device):
+            st = lib().rssm_read_pointers(self._h, start, count, ctypes.byref(err), _stream_ptr(stream))
         if check:
             _check(st)
         return (torch.tensor(list(start), dtype=torch.int32), torch.tensor(list(count), dtype=torch.int32),
                 int(err.value))
 
     def clear_error(self, stream=None):
-        _check(lib().rssm_clear_error(self._h, _stream_ptr(stream)))
+        with torch.cuda.device(self.ckpt.device):
+            _check(lib().rssm_clear_error(self._h, _stream_ptr(stream)))
 
     # ------------------------------------------------------- ring inspection
     def ring_views(self):
@@ -290,20 +300,23 @@ def conventional_step(shape: LayerShape, state, alpha, v, k, q, out=None, stream
     """
     s = shape
     _expect(state, (s.B, s.H, s.P, s.N), torch.float32, "state")
-    _expect(alpha, (s.B, s.H), torch.float32, "alpha")
-    _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v")
-    _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k")
-    _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q")
+    d = state.device
+    _expect(alpha, (s.B, s.H), torch.float32, "alpha", d)
+    _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v", d)
+    _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k", d)
+    _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q", d)
     if out is None:
-        out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=state.device)
+        out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=d)
+    _expect(out, (s.B, s.H, s.P), torch.float32, "out", d)
     cfg = s.config()
-    if beta is None:
-        _check(lib().rssm_conventional_step(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(v), _ptr(k), _ptr(q),
-                                            _ptr(out), _stream_ptr(stream)))
-    else:
-        _expect(beta, (s.B, s.H), torch.float32, "beta")
-        _check(lib().rssm_conventional_step_delta(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(beta), _ptr(v),
-                                                  _ptr(k), _ptr(q), _ptr(out), _stream_ptr(stream)))
+    with torch.cuda.device(d):
+        if beta is None:
+            _check(lib().rssm_conventional_step(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(v), _ptr(k),
+                                                _ptr(q), _ptr(out), _stream_ptr(stream)))
+        else:
+            _expect(beta, (s.B, s.H), torch.float32, "beta", d)
+            _check(lib().rssm_conventional_step_delta(ctypes.byref(cfg), _ptr(state), _ptr(alpha), _ptr(beta),
+                                                      _ptr(v), _ptr(k), _ptr(q), _ptr(out), _stream_ptr(stream)))
     return out
 
 
@@ -330,27 +343,29 @@ class ConventionalVerifier:
         self._last_T = 0
 
     def verify(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
-        s = self.shape
+        s, d = self.shape, self.states.device
         T = alpha.shape[1]
-        _expect(alpha, (s.B, T, s.H), torch.float32, "alpha")
-        _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v")
-        _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k")
-        _expect(q, (s.B, T, s.G, s.N), s.torch_in_dtype, "q")
+        _expect(alpha, (s.B, T, s.H), torch.float32, "alpha", d)
+        _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v", d)
+        _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k", d)
+        _expect(q, (s.B, T, s.G, s.N), s.torch_in_dtype, "q", d)
         if out is None:
-            out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=alpha.device)
-        _expect(out, (s.B, T, s.H, s.P), torch.float32, "out")
-        _check(lib().rssm_conventional_verify(ctypes.byref(self._cfg), _ptr(self.states), _ptr(self.cur), T,
-                                              _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out), _ptr(self.err),
-                                              _stream_ptr(stream)))
+            out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=d)
+        _expect(out, (s.B, T, s.H, s.P), torch.float32, "out", d)
+        with torch.cuda.device(d):
+            _check(lib().rssm_conventional_verify(ctypes.byref(self._cfg), _ptr(self.states), _ptr(self.cur), T,
+                                                  _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out), _ptr(self.err),
+                                                  _stream_ptr(stream)))
         self._last_T = T
         return out
 
     def commit(self, accepted: torch.Tensor, stream=None):
-        _expect(accepted, (self.shape.B,), torch.int32, "accepted")
+        _expect(accepted, (self.shape.B,), torch.int32, "accepted", self.states.device)
         if self._last_T < 1:
             raise ValueError("commit without a pending verify")
-        _check(lib().rssm_conventional_commit(ctypes.byref(self._cfg), _ptr(self.cur), _ptr(accepted), self._last_T,
-                                              _ptr(self.err), _stream_ptr(stream)))
+        with torch.cuda.device(self.states.device):
+            _check(lib().rssm_conventional_commit(ctypes.byref(self._cfg), _ptr(self.cur), _ptr(accepted),
+                                                  self._last_T, _ptr(self.err), _stream_ptr(stream)))
         self._last_T = 0
 
     def state(self) -> torch.Tensor:
