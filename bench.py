@@ -28,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -216,31 +217,75 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------- CPU oracle timing
-def time_oracle(shape, n_seq: int, n_steps: int, seed: int = 0, delta: bool = False) -> tuple[float, int]:
-    """Seconds for n_steps float64 steps of the oracle's recurrence (its definition) on n_seq sequences."""
-    import oracle
-    s = shape.with_(B=n_seq)
-    gen = synth.make_generator(seed)
-    S = oracle.to_f64(synth.initial_state(s, gen))
-    draw = synth.delta_step_inputs if delta else synth.decode_step_inputs
-    step = oracle.delta_step if delta else oracle.conventional_step
-    steps = [tuple(oracle.to_f64(x) for x in draw(s, gen)) for _ in range(min(n_steps, 4))]
-    t0 = time.perf_counter()
-    for i in range(n_steps):
-        S, o = step(S, *steps[i % len(steps)])
-    return time.perf_counter() - t0, n_seq * n_steps
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleSample:
+    """The float64 oracle's recurrence (its definition, as it stands) on a sample of
+    the workload: `threads` disjoint groups of `n_seq` sequences, each group with
+    its own seeded state and inputs, stepped by one host thread. numpy releases
+    the GIL inside its array loops, so the groups run on separate cores."""
+
+    def __init__(self, shape, n_seq: int, threads: int, delta: bool = False, seed: int = 0):
+        import oracle
+        self.step = oracle.delta_step if delta else oracle.conventional_step
+        self.n_seq, self.threads = n_seq, threads
+        draw = synth.delta_step_inputs if delta else synth.decode_step_inputs
+        s = shape.with_(B=n_seq)
+        self.parts = []
+        for t in range(threads):
+            gen = synth.make_generator(seed + 7919 * t)
+            S = oracle.to_f64(synth.initial_state(s, gen))
+            self.parts.append([S, [tuple(oracle.to_f64(x) for x in draw(s, gen)) for _ in range(4)]])
+        self.done = 0  # steps already taken by every group
+
+    def run(self, n_steps: int) -> float:
+        """Wall seconds for n_steps more steps of every group, the threads started together."""
+        start = threading.Barrier(self.threads + 1)
+        errors = []
+
+        def work(part):
+            start.wait()
+            try:
+                S, steps = part
+                for i in range(self.done, self.done + n_steps):
+                    S, _ = self.step(S, *steps[i % len(steps)])
+                part[0] = S
+            except Exception as e:  # surfaced below
+                errors.append(e)
+
+        ths = [threading.Thread(target=work, args=(p,)) for p in self.parts]
+        for th in ths:
+            th.start()
+        start.wait()
+        t0 = time.perf_counter()
+        for th in ths:
+            th.join()
+        t = time.perf_counter() - t0
+        if errors:
+            raise errors[0]
+        self.done += n_steps
+        return t
+
+    def units(self, n_steps: int) -> int:
+        return self.threads * self.n_seq * n_steps
 
 
 def cpu_baseline_line(shape, budget_s: float = 12.0, delta: bool = False) -> dict:
-    n_seq = 4
-    t, units = time_oracle(shape, n_seq, 2, delta=delta)  # calibrate
-    per_step = t / 2
+    n_seq, threads = 4, host_cores()
+    sample = OracleSample(shape, n_seq, threads, delta=delta)
+    sample.run(1)  # first touch of every group's arrays
+    per_step = sample.run(2) / 2
     steps = max(4, int(budget_s / max(per_step, 1e-6)))
-    t, units = time_oracle(shape, n_seq, steps, delta=delta)
+    t = sample.run(steps)
     what = "gated delta rule" if delta else "conventional recurrence"
-    return {"value": units / t, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"float64 {what}, {n_seq} of {shape.B} sequences x all {shape.H} heads, "
-                      f"{steps} steps ({t:.1f} s); numpy elementwise, one thread"}
+    return {"value": sample.units(steps) / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"float64 {what}, {threads} threads x {n_seq} sequences (of {shape.B}) x all {shape.H} "
+                      f"heads, {steps} steps ({t:.1f} s); numpy elementwise, one thread per sequence group"}
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -450,30 +495,21 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     s = WORKLOAD
-    import oracle
-    n_seq = 2
-    sub = s.with_(B=n_seq)
-    gen = synth.make_generator(s.seed)
-    S = oracle.to_f64(synth.initial_state(sub, gen))
-    steps = [tuple(oracle.to_f64(x) for x in synth.decode_step_inputs(sub, gen)) for _ in range(4)]
-    for w in range(args.warmup):
-        for j in range(s.L):
-            S, _ = oracle.conventional_step(S, *steps[j % 4])
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        for j in range(s.L):
-            S, _ = oracle.conventional_step(S, *steps[j % 4])
-    t = time.perf_counter() - t0
-    value = n_seq * s.L * args.steps / t
-    sample = (f"float64 oracle (conventional recurrence), {n_seq} of {s.B} sequences x {s.H} heads, "
-              f"one window of {s.L} decode steps per bench step")
+    n_seq, threads = 1, host_cores()
+    oracle_sample = OracleSample(s, n_seq, threads, seed=s.seed)
+    if args.warmup:
+        oracle_sample.run(args.warmup * s.L)
+    t = oracle_sample.run(args.steps * s.L)
+    value = oracle_sample.units(args.steps * s.L) / t
+    sample = (f"float64 oracle (conventional recurrence), {threads} threads x {n_seq} sequence (of {s.B}) x "
+              f"{s.H} heads, one window of {s.L} decode steps per bench step")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": f"ReplaySSM decode, B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
-                                   f"(oracle sample of {n_seq} sequences)"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+                                   f"(oracle sample of {threads} x {n_seq} sequences)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -3,6 +3,7 @@
 - The analytic HBM bytes per window, against the closed forms worked out by hand.
 - The multi-rank timing path: two gloo ranks on the CPU take the max over ranks,
   the way torchrun replicas do on GPUs.
+- The CPU baseline's threaded oracle sample and the reference arm.
 """
 import os
 import socket
@@ -85,3 +86,24 @@ def test_reference_arm_runs_on_cpu(capsys):
     if not torch.cuda.is_available():
         with pytest.raises(SystemExit):
             bench.main(["--steps", "1", "--warmup", "3"])
+
+
+def test_oracle_sample_threads_step_their_own_groups():
+    """The CPU baseline's threads each step their own seeded group: the states they
+    reach equal a plain sequential run of the same groups, over two calls."""
+    import numpy as np
+
+    import oracle
+    s = synth.PRESETS["tiny_b2_h2_p16_n16_l4"]
+    sample = bench.OracleSample(s, n_seq=2, threads=3, seed=5)
+    sample.run(3)
+    sample.run(2)
+    assert sample.units(5) == 3 * 2 * 5 and sample.done == 5
+    sub = s.with_(B=2)
+    for t, (S_thread, _) in enumerate(sample.parts):
+        gen = synth.make_generator(5 + 7919 * t)
+        S = oracle.to_f64(synth.initial_state(sub, gen))
+        steps = [tuple(oracle.to_f64(x) for x in synth.decode_step_inputs(sub, gen)) for _ in range(4)]
+        for i in range(5):
+            S, _ = oracle.conventional_step(S, *steps[i % 4])
+        assert np.array_equal(S_thread, S), t
