@@ -18,6 +18,11 @@ Each check rests on something other than the function it checks:
   against the replay formula, commit of an accepted prefix against the fold
   (with junk in the rejected drafts), and the pointers against the
   outer-product oracle's verify and commit.
+
+Planted mistakes (an undecayed or sign-flipped erase, no erase, a write
+without beta, an erase along the query, the old state's output, swapped k and
+q, interleaved groups, and wrong orders in the replay and the fold) are each
+caught by at least one of these pins.
 """
 import os
 
@@ -308,3 +313,130 @@ def test_verify_and_commit_refusals():
     d.decode(*(x[:, 0] for x in dr))
     with pytest.raises(oracle.CapacityError):
         d.commit([1, 1])  # a decode step discards the pending drafts
+
+
+# Planted mistakes: each plausible slip in the step, the replay formula or the
+# fold, substituted into the oracle module, must fail at least one pin above.
+
+_STEP = delta.delta_step
+_REPLAY = delta.delta_replay_output
+_FOLD = delta.delta_fold
+
+
+def _parts(S, k, q):
+    g = oracle.head_groups(S.shape[1], k.shape[1])
+    kh, qh = k[:, g, :], q[:, g, :]
+    return kh, qh, np.einsum("bhpn,bhn->bhp", S, kh)
+
+
+def _finish(S_new, qh):
+    return S_new, np.einsum("bhpn,bhn->bhp", S_new, qh)
+
+
+def _m_erase_not_decayed(S, a, b, v, k, q):  # alpha S - beta (S k) k^T + beta v k^T
+    kh, qh, Sk = _parts(S, k, q)
+    a4, b4 = a[:, :, None, None], b[:, :, None, None]
+    return _finish(a4 * S - b4 * Sk[..., None] * kh[:, :, None, :] + b4 * v[..., None] * kh[:, :, None, :], qh)
+
+
+def _m_no_erase(S, a, b, v, k, q):  # the outer-product rule with a write strength
+    kh, qh, _ = _parts(S, k, q)
+    return _finish(a[:, :, None, None] * S + b[:, :, None, None] * v[..., None] * kh[:, :, None, :], qh)
+
+
+def _m_erase_sign(S, a, b, v, k, q):
+    kh, qh, Sk = _parts(S, k, q)
+    a4, b4 = a[:, :, None, None], b[:, :, None, None]
+    return _finish(a4 * (S + b4 * Sk[..., None] * kh[:, :, None, :]) + b4 * v[..., None] * kh[:, :, None, :], qh)
+
+
+def _m_write_without_beta(S, a, b, v, k, q):
+    kh, qh, Sk = _parts(S, k, q)
+    a4, b4 = a[:, :, None, None], b[:, :, None, None]
+    return _finish(a4 * (S - b4 * Sk[..., None] * kh[:, :, None, :]) + v[..., None] * kh[:, :, None, :], qh)
+
+
+def _m_erase_along_query(S, a, b, v, k, q):  # (S q) k^T in place of (S k) k^T
+    kh, qh, _ = _parts(S, k, q)
+    Sq = np.einsum("bhpn,bhn->bhp", S, qh)
+    a4, b4 = a[:, :, None, None], b[:, :, None, None]
+    return _finish(a4 * (S - b4 * Sq[..., None] * kh[:, :, None, :]) + b4 * v[..., None] * kh[:, :, None, :], qh)
+
+
+def _m_old_state_output(S, a, b, v, k, q):
+    S_new, _ = _STEP(S, a, b, v, k, q)
+    _, qh, _ = _parts(S, k, q)
+    return S_new, np.einsum("bhpn,bhn->bhp", S, qh)
+
+
+def _m_swap_kq(S, a, b, v, k, q):
+    return _STEP(S, a, b, v, q, k)
+
+
+def _m_interleaved_groups(S, a, b, v, k, q):
+    H, G = S.shape[1], k.shape[1]
+    g = np.arange(H) % G
+    kh, qh = k[:, g, :], q[:, g, :]
+    Sk = np.einsum("bhpn,bhn->bhp", S, kh)
+    a4, b4 = a[:, :, None, None], b[:, :, None, None]
+    return _finish(a4 * (S - b4 * Sk[..., None] * kh[:, :, None, :]) + b4 * v[..., None] * kh[:, :, None, :], qh)
+
+
+def _m_replay_forward_order(S_ckpt, alphas, betas, vs, ks, q):  # the query carried through the records forwards
+    return _REPLAY(S_ckpt, alphas[::-1], betas[::-1], vs[::-1], ks[::-1], q)
+
+
+def _m_replay_decay_before_erase(S_ckpt, alphas, betas, vs, ks, q):  # u <- alpha u - c k
+    H = S_ckpt.shape[0]
+    g = oracle.head_groups(H, q.shape[0])
+    o = np.empty((H, S_ckpt.shape[1]))
+    for head in range(H):
+        u, val = np.array(q[g[head]], np.float64), np.zeros(S_ckpt.shape[1])
+        for j in range(len(alphas) - 1, -1, -1):
+            kj = ks[j, g[head]]
+            c = betas[j, head] * float(kj @ u)
+            val += c * vs[j, head]
+            u = alphas[j, head] * u - c * kj
+        o[head] = S_ckpt[head] @ u + val
+    return o
+
+
+def _m_fold_reversed(S_ckpt, alphas, betas, vs, ks):
+    return _FOLD(S_ckpt, alphas[::-1], betas[::-1], vs[::-1], ks[::-1])
+
+
+STEP_MUTANTS = [_m_erase_not_decayed, _m_no_erase, _m_erase_sign, _m_write_without_beta, _m_erase_along_query,
+                _m_old_state_output, _m_swap_kq, _m_interleaved_groups]
+FORM_MUTANTS = [("delta_replay_output", _m_replay_forward_order), ("delta_replay_output", _m_replay_decay_before_erase),
+                ("delta_fold", _m_fold_reversed)]
+PINS = [test_associative_memory_with_orthonormal_keys, test_full_strength_write_is_exact_for_any_decay,
+        test_zero_write_strength_is_pure_decay, test_scalar_case_by_hand, test_replay_formula_and_fold_match_the_definition,
+        test_pseudo_value_is_the_steps_write_term, test_hand_computed_two_step_example,
+        test_verify_and_commit_of_the_hand_example, test_verify_keeps_the_projection_and_memory_properties,
+        test_verify_matches_the_replay_formula, test_commit_applies_only_the_accepted_prefix]
+
+
+def _caught(monkeypatch, name, fn):
+    monkeypatch.setattr(delta, name, fn)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+            caught.append(False)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(True)  # a failed pin, or a shape error, catches the mistake
+    return caught
+
+
+@pytest.mark.parametrize("mutant", STEP_MUTANTS, ids=lambda m: m.__name__)
+def test_pins_catch_planted_mistakes_in_the_step(monkeypatch, mutant):
+    assert any(_caught(monkeypatch, "delta_step", mutant)), f"no pin catches {mutant.__name__}"
+
+
+@pytest.mark.parametrize("name,mutant", FORM_MUTANTS, ids=lambda x: getattr(x, "__name__", x))
+def test_pins_catch_planted_mistakes_in_replay_and_fold(monkeypatch, name, mutant):
+    assert any(_caught(monkeypatch, name, mutant)), f"no pin catches {mutant.__name__}"
+
+
+def test_the_unmutated_oracle_passes_every_pin(monkeypatch):
+    assert not any(_caught(monkeypatch, "delta_step", _STEP))
