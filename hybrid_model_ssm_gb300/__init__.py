@@ -10,6 +10,7 @@ from .rssm import (  # noqa: F401
     ReplaySSM,
     RssmError,
     conventional_step,
+    launch_plan,
     read_copy_layout,
     round_f16,
     ring_offsets,

@@ -321,6 +321,32 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
   return RSSM_OK;
 }
 
+rssm_status rssm_launch_plan(const rssm_config* cfg, int32_t kind, rssm_launch_plan_info* out) {
+  if (!out) return fail(RSSM_EINVAL, "out is NULL");
+  if (kind < 0 || kind > 2) return fail(RSSM_EINVAL, "kind=%d (0 flush, 1 decode, 2 verify)", kind);
+  Geom g;
+  rssm_status s = derive(cfg, &g);
+  if (s != RSSM_OK) return s;
+  if (kind == 2 && (cfg->T_max < 2 || cfg->recurrence != RSSM_GATED_OUTER))
+    return fail(RSSM_EINVAL, "verify launches need T_max > 1 and the outer-product recurrence");
+  const LayoutKind lk = kind == 0 ? LayoutKind::kGeneral : kind == 1 ? LayoutKind::kNonFlush : LayoutKind::kVerify;
+  Plan pl;
+  s = plan_smem(cfg, g, &pl, lk);
+  if (s != RSSM_OK) return s;
+  *out = rssm_launch_plan_info{};
+  out->smem_bytes = (int64_t)pl.smem;
+  out->nonflush_layout = pl.p.nf_ok;
+  for (int i = 0; i < 2; ++i) {
+    const rssm::Layout& L = pl.p.lay[i];
+    out->stages[i] = L.stages;
+    out->stage_bytes[i] = L.stage_bytes;
+    out->slots[i] = L.slots;
+    out->slot_bytes[i] = L.slot_bytes;
+    out->dgroups[i] = L.dgroups;
+  }
+  return RSSM_OK;
+}
+
 rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* ptrs, void* read_copy,
                         void* stream, rssm_handle* out) {
   if (!out) return fail(RSSM_EINVAL, "out is NULL");

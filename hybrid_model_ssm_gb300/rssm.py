@@ -40,11 +40,17 @@ class Config(ctypes.Structure):
                                               "ckpt_fmt")] + [("seed", ctypes.c_uint64), ("recurrence", ctypes.c_int32)]
 
 
+class LaunchPlanInfo(ctypes.Structure):
+    _fields_ = [("smem_bytes", ctypes.c_int64), ("nonflush_layout", ctypes.c_int32)] + [
+        (n, ctypes.c_int32 * 2) for n in ("stages", "stage_bytes", "slots", "slot_bytes", "dgroups")]
+
+
 _Cfg_p = ctypes.POINTER(Config)
 SIGNATURES = {
     "rssm_workspace_size": [_Cfg_p, _c_size_p, _c_size_p, _c_size_p],
     "rssm_ring_offsets": [_Cfg_p, _c_size_p, _c_size_p],
     "rssm_read_copy_layout": [_Cfg_p, _c_size_p, _c_size_p, _c_size_p],
+    "rssm_launch_plan": [_Cfg_p, ctypes.c_int32, ctypes.POINTER(LaunchPlanInfo)],
     "rssm_create": [_Cfg_p, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)],
     "rssm_decode_step": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_decode_step_static_scratch": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -151,6 +157,21 @@ def read_copy_layout(shape: LayerShape) -> tuple[int, int, int]:
     a, b, d = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
     _check(lib().rssm_read_copy_layout(ctypes.byref(c), ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
     return a.value, b.value, d.value
+
+
+LAUNCH_KINDS = {"flush": 0, "decode": 1, "verify": 2}
+
+
+def launch_plan(shape: LayerShape, kind: str) -> dict:
+    """Shared-memory plan of a launch kind ("flush", "decode", "verify"): smem bytes
+    and, per layout, stages, stage bytes, slots, slot bytes and dot-warp groups."""
+    c = shape.config()
+    info = LaunchPlanInfo()
+    _check(lib().rssm_launch_plan(ctypes.byref(c), LAUNCH_KINDS[kind], ctypes.byref(info)))
+    layouts = 2 if kind == "decode" and info.nonflush_layout else 1
+    return {"smem_bytes": info.smem_bytes,
+            "layouts": [{f: getattr(info, f)[i] for f in ("stages", "stage_bytes", "slots", "slot_bytes", "dgroups")}
+                        for i in range(layouts)]}
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:

@@ -151,6 +151,28 @@ rssm_status rssm_ring_offsets(const rssm_config* cfg, size_t* v_off, size_t* k_o
 rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, size_t* bscale_off,
                                   size_t* rscale_off);
 
+/* Shared-memory plan of the head kernel's launches for a configuration (no
+ * counterpart in the paper: introspection of this library's launch shapes).
+ * Host only; makes no CUDA call. Every launch runs one CTA per SM with the
+ * layouts below:
+ *   kind 0: flush and read-copy refresh (layout 0 only);
+ *   kind 1: decode (layout 0 for any head, layout 1 for steps in which none of
+ *           a CTA's sequences folds; nonflush_layout = 0 when only layout 0 fits);
+ *   kind 2: verify (layout 0 only; needs T_max > 1).
+ * Per layout: checkpoint tile stages (stage_bytes each), record slots
+ * (slot_bytes each) and the number of dot-warp groups, i.e. heads in flight.
+ * Both ring lengths are multiples of the number of consumers that take their
+ * entries in turn (stages of dgroups, slots of max(2, dgroups)). smem_bytes is
+ * the dynamic shared memory of the launch, at most 227 KiB. Returns
+ * RSSM_EINVAL for a bad kind or configuration, RSSM_EUNSUPPORTED when the
+ * sizes cannot be placed. */
+typedef struct {
+  int64_t smem_bytes;
+  int32_t nonflush_layout;
+  int32_t stages[2], stage_bytes[2], slots[2], slot_bytes[2], dgroups[2];
+} rssm_launch_plan_info;
+rssm_status rssm_launch_plan(const rssm_config* cfg, int32_t kind, rssm_launch_plan_info* out);
+
 /* Bind a decoding context to caller memory.
  *  ckpt      [B,H,P,N] device: the initial state, fp32, or fp16 (binary16) when
  *            ckpt_fmt is an FP16 format. It becomes the checkpoint and is

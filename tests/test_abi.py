@@ -106,6 +106,58 @@ def test_largest_placeable_configurations_are_accepted(lib, kw):
     assert ring > 0 and ptrs > 0
 
 
+def test_launch_plans_keep_the_ring_rule_over_the_size_grid(lib):
+    """Host planner over a grid of sizes, formats and recurrences (no CUDA call).
+
+    Every plan fits 227 KiB and keeps each shared-memory ring's length a multiple
+    of the consumers that take its entries in turn (stages: the dot groups;
+    slots: max(2, dot groups)), the rule that keeps an mbarrier parity wait from
+    matching the previous phase. A configuration is accepted by the sizing call
+    exactly when all of its launches can be planned."""
+    from hybrid_model_ssm_gb300 import launch_plan
+    smem_max = 227 * 1024
+    windows = [(1, 1), (2, 1), (4, 1), (16, 1), (29, 1), (32, 1), (2, 2), (4, 4), (16, 4), (27, 4), (8, 8), (25, 8)]
+    planned = refused = 0
+    for N in (16, 32, 64, 128):
+        for P in (8, 24, 64, 120, 128):
+            for L, T in windows:
+                for dt in ("f32", "bf16"):
+                    for rf, ck, rec in (("none", "f32", "outer"), ("e4m3", "f32", "outer"), ("e2m1", "f32", "outer"),
+                                        ("none", "f16_sr", "outer"), ("none", "f32", "delta")):
+                        shape = LayerShape(B=3, H=4, P=P, N=N, G=2, L=L, T_max=T, in_dtype=dt, read_fmt=rf, ckpt=ck,
+                                           recurrence=rec)
+                        kinds = ["flush", "decode"] + (["verify"] if T > 1 else [])
+                        plans = {}
+                        for kind in kinds:
+                            try:
+                                plans[kind] = launch_plan(shape, kind)
+                            except RssmError:
+                                pass
+                        try:
+                            workspace_size(shape)
+                            accepted = True
+                        except RssmError:
+                            accepted = False
+                        assert accepted == (len(plans) == len(kinds)), (shape, sorted(plans))
+                        if not accepted:
+                            refused += 1
+                            continue
+                        planned += 1
+                        ck_es = 2 if ck != "f32" else 4
+                        for kind, plan in plans.items():
+                            assert 0 < plan["smem_bytes"] <= smem_max
+                            for i, lay in enumerate(plan["layouts"]):
+                                d = lay["dgroups"]
+                                assert d in (1, 2, 4, 8) and lay["stages"] >= 2
+                                assert lay["stages"] % d == 0 and lay["slots"] % max(2, d) == 0, (shape, kind, lay)
+                                assert lay["stage_bytes"] % 128 == 0 and lay["slot_bytes"] % 128 == 0
+                                assert lay["stages"] * lay["stage_bytes"] + lay["slots"] * lay["slot_bytes"] \
+                                    <= plan["smem_bytes"]
+                                if i == 0:  # the general layout holds a whole checkpoint tile
+                                    assert lay["stage_bytes"] >= P * N * ck_es
+    assert planned > 500 and refused > 100
+
+
 def test_null_config_and_handle(lib):
     lib.rssm_workspace_size.restype = ctypes.c_int
     assert lib.rssm_workspace_size(None, None, None, None) == RSSM_EINVAL
