@@ -440,3 +440,51 @@ def test_pins_catch_planted_mistakes_in_replay_and_fold(monkeypatch, name, mutan
 
 def test_the_unmutated_oracle_passes_every_pin(monkeypatch):
     assert not any(_caught(monkeypatch, "delta_step", _STEP))
+
+
+def test_pseudo_value_verify_form_matches_the_oracle():
+    """The verify form a kernel evaluates from the checkpoint, the buffered pseudo-values
+    and the drafts (checkpoint dots with each draft key and query, then a chain over the
+    drafts) gives the oracle's verify outputs, and its w are the ones decode would write."""
+    rng = np.random.default_rng(11)
+    B, T, H, G, P, N, L = 2, 4, 4, 2, 5, 6, 8
+    S0 = rng.standard_normal((B, H, P, N))
+    d = delta.DeltaReplayOracle(S0, L=L, R=L + T, G=G)
+    g = oracle.head_groups(H, G)
+    recs = []  # committed (alpha, w, k) per step, w from the state before the step
+    for _ in range(3):
+        a, b, v, k, q = (x[:, 0] for x in _drafts(rng, B, 1, H, G, P, N))
+        recs.append((a, delta.delta_pseudo_value(d.S, a, b, v, k), k))
+        d.decode(a, b, v, k, q)
+    al, be, v, k, q = _drafts(rng, B, T, H, G, P, N)
+    O = d.verify(al, be, v, k, q)
+    alphas = [r[0] for r in recs] + [al[:, t] for t in range(T)]  # [B,H] per record m = 1..c+T
+    keys = [r[2] for r in recs] + [k[:, t] for t in range(T)]     # [B,G,N]
+    ws = [r[1] for r in recs]                                      # grows by one per draft
+    c = len(recs)
+
+    def decay(i, m):  # product of alphas of records i+1..m (1-based; empty = 1)
+        out = np.ones((B, H))
+        for j in range(i + 1, m + 1):
+            out = out * alphas[j - 1]
+        return out
+
+    def dot(x, y):  # group dots x_g . y_g, spread to the group's heads: [B,H]
+        return np.einsum("bgn,bgn->bg", x, y)[:, g]
+
+    for t in range(T):
+        m = c + t + 1
+        y = decay(0, m - 1)[..., None] * np.einsum("bhpn,bhn->bhp", S0, k[:, t][:, g])
+        for i in range(1, m):
+            y = y + (decay(i, m - 1) * dot(keys[i - 1], k[:, t]))[..., None] * ws[i - 1]
+        ws.append(be[:, t][..., None] * (v[:, t] - al[:, t][..., None] * y))
+        o = decay(0, m)[..., None] * np.einsum("bhpn,bhn->bhp", S0, q[:, t][:, g])
+        for i in range(1, m + 1):
+            o = o + (decay(i, m) * dot(keys[i - 1], q[:, t]))[..., None] * ws[i - 1]
+        assert np.allclose(o, O[:, t], rtol=1e-11, atol=1e-11), t
+    d.commit(np.array([2, 4]))
+    for bb, a in enumerate((2, 4)):
+        S_fold = S0[bb].copy()
+        for i in range(c + a):
+            S_fold = alphas[i][bb][:, None, None] * S_fold + ws[i][bb][..., None] * keys[i][bb][g][:, None, :]
+        assert np.allclose(d.S[bb], S_fold, rtol=1e-11, atol=1e-11), bb
