@@ -26,6 +26,9 @@ DECODE_CASES = [
     ("every_step_flushes_l1", S(B=2, H=2, P=16, N=16, G=1, L=1, in_dtype="f32", seed=9), 6),
     ("window_32_b2_h2_p16_n64", S(B=2, H=2, P=16, N=64, G=1, L=32, seed=10), 70),
     ("one_sequence_b1_h1", S(B=1, H=1, P=8, N=16, G=1, L=4, in_dtype="f32", seed=11), 9),
+    # the largest sizes: P = N = 128 with the longest ring that fits f32 inputs, and R = 32 with bf16
+    ("largest_f32_p128_n128_l29", S(B=2, H=2, P=128, N=128, G=1, L=29, in_dtype="f32", seed=14), 60),
+    ("largest_ring_p128_n128_l32_bf16", S(B=2, H=2, P=128, N=128, G=1, L=32, seed=15), 66),
 ]
 
 

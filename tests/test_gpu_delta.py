@@ -31,6 +31,8 @@ CASES = [
     ("every_step_flushes_l1_n64_f32", S(B=2, H=2, P=16, N=64, G=1, L=1, in_dtype="f32", seed=34), 6),
     ("window_32_b2_h2_p16_n64", S(B=2, H=2, P=16, N=64, G=1, L=32, seed=35), 70),
     ("ragged_rows_p8_n64_b3_h4_g2", S(B=3, H=4, P=8, N=64, G=2, L=3, seed=36), 20),
+    ("largest_f32_p128_n128_l28", S(B=2, H=2, P=128, N=128, G=1, L=28, in_dtype="f32", seed=39), 58),
+    ("largest_ring_p128_n128_l32_bf16", S(B=2, H=2, P=128, N=128, G=1, L=32, seed=40), 66),
 ]
 
 

@@ -23,6 +23,7 @@ VERIFY_CASES = [
     ("b4_h16_g2_p64_n128_l16_t4", S(B=4, H=16, P=64, N=128, G=2, L=16, T_max=4, seed=31), 30),
     ("t8_two_query_blocks_n64", S(B=3, H=4, P=24, N=64, G=2, L=8, T_max=8, seed=32), 16),
     ("t5_partial_block_n32", S(B=5, H=6, P=16, N=32, G=3, L=6, T_max=5, seed=33), 16),
+    ("largest_ring_p128_n128_l25_t8", S(B=3, H=2, P=128, N=128, G=1, L=25, T_max=8, seed=35), 24),
 ]
 
 
