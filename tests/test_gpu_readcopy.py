@@ -132,3 +132,78 @@ def test_decode_with_read_copy(fmt, N):
                 if fmt == "e2m1":
                     assert np.array_equal(bcodes[b], b_ref[b])
     assert worst > 0.0
+
+
+def _unit_scale_rows(fmt, N):
+    """Rows whose scales come out exactly 1, so that each element's code is the
+    format's own conversion of the element itself. They hold every finite code
+    value, every midpoint between neighbouring codes (a tie, resolved to the even
+    code) and the binary32 neighbours of each midpoint, with both signs.
+
+    E4M3: a row whose max |x| is 448 gets inv = 448/448 = 1.
+    E2M1: a row whose max |x| is 2688 gets s_r = 1 and d6 = 6; a block of 16 whose
+    max |x| is 6 then gets the block code of 1.0, so d = r = 1.
+    """
+    f32 = np.float32
+    if fmt == "e4m3":
+        vals = quant.e4m3_value(np.arange(0x7F)).astype(f32)  # 0 .. 448, every finite non-negative code
+        top = f32(448.0)
+    else:
+        vals = np.array(sorted(set(quant.e2m1_value(np.arange(8)).tolist())), f32)  # 0, 0.5, .., 6
+        top = f32(6.0)
+    mids = ((vals[:-1].astype(np.float64) + vals[1:]) / 2).astype(f32)
+    tests = np.concatenate([vals, mids, np.nextafter(mids, f32(np.inf)), np.nextafter(mids, f32(0))])
+    tests = np.concatenate([tests, -tests])
+    if fmt == "e4m3":
+        per_row = N - 1
+        rows = []
+        for i in range(0, len(tests), per_row):
+            r = np.zeros(N, f32)
+            r[0] = top
+            chunk = tests[i:i + per_row]
+            r[1:1 + len(chunk)] = chunk
+            rows.append(r)
+        return np.stack(rows)
+    per_block, nblk = 15, N // 16
+    blocks = [tests[i:i + per_block] for i in range(0, len(tests), per_block)]
+    nrows = -(-len(blocks) // (nblk - 1))
+    rows = np.zeros((nrows, N), f32)
+    for i in range(nrows * (nblk - 1)):  # every block after block 0 filled (the values repeat to fill the last row)
+        r, bi = divmod(i, nblk - 1)
+        blk = blocks[i % len(blocks)]
+        base = 16 * (bi + 1)
+        rows[r, base] = top
+        rows[r, base + 1: base + 1 + len(blk)] = blk
+    rows[:, 0] = f32(2688.0)  # block 0 pins the row scale
+    return rows
+
+
+def _saturation_row(N):
+    """E4M3 row with a scale other than 1 whose largest elements scale to the top code or just below it."""
+    r = np.zeros(N, np.float32)
+    r[:6] = [1000.0, 999.0, -1000.0, 1000.0 * 448.5 / 448, 1000.0 * 463.9 / 448, 1000.0 * 464.0 / 448]
+    return r
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_copy_codes_of_every_code_value_and_midpoint(fmt):
+    """The device quantizer (the CUDA conversions) against the oracle encoder, bit for
+    bit, on every code value, every tie between neighbouring codes and their binary32
+    neighbours (unit scales), plus (E4M3) a row whose largest elements scale to the top code."""
+    require_gpu()
+    shape = S(B=1, H=2, P=64, N=128, G=1, L=4, seed=52)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    rows = _unit_scale_rows(fmt, shape.N)
+    assert len(rows) < shape.P
+    S0[0, 0, : len(rows)] = torch.from_numpy(rows)
+    if fmt == "e4m3":
+        S0[0, 0, len(rows)] = torch.from_numpy(_saturation_row(shape.N))
+    c_ref, b_ref, s_ref = _oracle_codes(S0.numpy(), fmt)
+    # the crafted rows really have unit scales: their codes are the conversion of x itself
+    assert np.all(s_ref[0, 0, : len(rows)] == 1.0)
+    if fmt == "e2m1":
+        assert np.all(quant.e4m3_value(b_ref[0, 0, : len(rows), 1:]) == 1.0)
+    model = ReplaySSM(layer_shape(shape, fmt), dev(S0))
+    torch.cuda.synchronize()
+    _assert_copy_matches(model.copy, S0.numpy(), shape, fmt, "every code and midpoint")
