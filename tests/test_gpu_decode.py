@@ -94,6 +94,72 @@ def test_zero_initial_state_and_zero_inputs():
     assert torch.count_nonzero(model.ckpt) == 0
 
 
+def test_unit_keys_with_no_decay_are_exact():
+    """Brute force: alpha = 1, every key a unit vector e_c and small-integer values
+    and state. Then S_t = S_0 + sum_j v_j e_{c_j}^T, and a unit query e_i reads column
+    i: o_t = S_0[:, i] + sum of the v_j written to column i. Every term is a small
+    integer, so the replay (decode and flush) must reproduce it exactly."""
+    require_gpu()
+    B, H, P, N, G, L = 2, 4, 16, 64, 2, 4
+    shape = S(B=B, H=H, P=P, N=N, G=G, L=L, seed=16)
+    rng = np.random.default_rng(16)
+    S0 = rng.integers(-4, 5, (B, H, P, N)).astype(np.float32)
+    model = ReplaySSM(layer_shape(shape), dev(torch.from_numpy(S0)))
+    S_int = S0.astype(np.int64)
+    g = oracle.head_groups(H, G)
+    ones = torch.ones((B, H), device="cuda")
+    for t in range(3 * L + 2):
+        col = rng.integers(0, N, (B, G))  # key e_col per (sequence, group)
+        qi = rng.integers(0, N, (B, G))   # query e_qi
+        v = rng.integers(-3, 4, (B, H, P))
+        k = np.zeros((B, G, N), np.float32)
+        q = np.zeros((B, G, N), np.float32)
+        for b in range(B):
+            for gg in range(G):
+                k[b, gg, col[b, gg]] = 1.0
+                q[b, gg, qi[b, gg]] = 1.0
+        o = model.decode_step(ones, dev(torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)),
+                              dev(torch.from_numpy(k).to(torch.bfloat16)),
+                              dev(torch.from_numpy(q).to(torch.bfloat16))).cpu().numpy()
+        for b in range(B):
+            for h in range(H):
+                S_int[b, h, :, col[b, g[h]]] += v[b, h]
+        want = np.stack([[S_int[b, h, :, qi[b, g[h]]] for h in range(H)] for b in range(B)])
+        assert np.array_equal(o, want.astype(np.float32)), f"step {t}"
+        if (t + 1) % L == 0:  # a flush step: the checkpoint now holds S_t exactly
+            assert np.array_equal(model.ckpt.cpu().numpy(), S_int.astype(np.float32)), f"step {t}"
+    _, count, err = model.read_pointers()
+    assert err == 0 and np.array_equal(count.numpy(), np.full(B, (3 * L + 2) % L))
+
+
+def test_zero_decay_keeps_only_the_last_record():
+    """alpha = 0 forgets everything before the step: o_t = v_t (k_t . q_t), whatever
+    the checkpoint and the buffered records hold, in decode and at a flush."""
+    require_gpu()
+    shape = S(B=3, H=4, P=32, N=64, G=2, L=4, seed=17)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    orc = oracle.ReplayOracle(f64(S0), L=shape.L, R=shape.R, G=shape.G)
+    model = ReplaySSM(layer_shape(shape), dev(S0))
+    g = oracle.head_groups(shape.H, shape.G)
+    for t in range(10):
+        a, v, k, q = synth.decode_step_inputs(shape, gen)
+        if t in (2, 3, 6):  # steps 3 and 7 flush (L = 4); step 6 is mid-window
+            a = torch.zeros_like(a)
+        elif t == 5:
+            a[:, ::2] = 0.0  # half of the heads forget
+        o = model.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu()
+        o_ref, _ = orc.decode(f64(a), f64(v), f64(k), f64(q))
+        assert slice_rel_err(o, o_ref, 1) <= REL_TOL, f"step {t}"
+        zero = (a == 0).numpy()
+        if zero.any():
+            kq = np.einsum("bgn,bgn->bg", f64(k), f64(q))[:, g]  # [B,H]
+            last = f64(v) * kq[..., None]
+            assert slice_rel_err(o.numpy()[zero], last[zero], 1) <= REL_TOL, f"step {t}: not the last record alone"
+    _, _, err = model.read_pointers()
+    assert err == 0
+
+
 @pytest.mark.parametrize("shape", [
     S(B=2, H=2, P=16, N=16, G=1, L=4, in_dtype="f32", seed=20),
     S(B=3, H=8, P=64, N=128, G=2, L=16, seed=21),
