@@ -215,8 +215,10 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
  * not move. Each draft's output uses the checkpoint once for all T queries:
  *     O = S_ckpt Q D + V (W ⊙ (K^T Q)),  D = diag(gamma_{1:c+tau}),
  *     W[j,tau] = gamma_{j+1:c+tau} for j <= c+tau, else 0.
- * Verify always reads the FP32 checkpoint. A sequence with c + T > R sets
- * RSSM_ECAPACITY and is skipped. */
+ * Verify reads the checkpoint itself (FP32, or FP16 with an FP16 ckpt_fmt),
+ * never the read copy. A sequence with c + T > R sets RSSM_ECAPACITY and is
+ * skipped. T outside 1..T_max returns RSSM_EINVAL; a delta-rule handle returns
+ * RSSM_EUNSUPPORTED. */
 rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k,
                         const void* q, float* o, void* stream);
 
@@ -224,7 +226,9 @@ rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void
  * (aikraft.ru page §05; records past the pointer are ignored and later
  * overwritten). accepted [B] int32 device, each in 0..T of the last verify.
  * A value outside that range sets RSSM_ECAPACITY and leaves the sequence
- * unchanged. Nothing else moves. */
+ * unchanged. Nothing else moves. Returns RSSM_EINVAL when no verify is pending
+ * (none since the handle was made, it was committed already, or a decode step
+ * or flush came after it). */
 rssm_status rssm_commit(rssm_handle h, const int32_t* accepted, void* stream);
 
 /* Fold every sequence that holds count >= min_count records (min_count >= 1)
