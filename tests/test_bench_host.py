@@ -107,3 +107,21 @@ def test_oracle_sample_threads_step_their_own_groups():
         for i in range(5):
             S, _ = oracle.conventional_step(S, *steps[i % 4])
         assert np.array_equal(S_thread, S), t
+
+
+def test_verify_round_bytes_of_the_verify_workload():
+    """Verify-round byte model on four sequences of the B=512 T=4 workload's shape,
+    with the numbers worked out by hand: a 4 MiB checkpoint, 18,944-byte records,
+    20,992 bytes of draft inputs (a record plus its bf16 query) and 32,768-byte
+    outputs per sequence."""
+    import numpy as np
+    s = synth.PRESETS["mamba2_verify_b512_t4"].with_(B=4)
+    counts, accepted = np.array([0, 5, 15, 12]), np.array([4, 0, 1, 4])
+    vb, fb, after = bench.verify_round_bytes(s, 4, counts, accepted)
+    # each sequence: checkpoint once, its committed records, and per draft its inputs,
+    # its appended record and its output: 4194304 + c*18944 + 4*(20992 + 18944 + 32768)
+    assert vb == 4 * 4194304 + 32 * 18944 + 4 * 4 * 72704 == 18_546_688
+    # commit leaves 4, 5, 16, 16 records; the last two fold (read and write the
+    # checkpoint, read 16 records); commit moves 12 bytes per sequence
+    assert after.tolist() == [4, 5, 0, 0]
+    assert fb == 2 * (2 * 4194304 + 16 * 18944) + 12 * 4 == 17_383_472
