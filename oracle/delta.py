@@ -41,7 +41,9 @@ from .replay import CapacityError
 
 
 def delta_step(S, alpha, beta, v, k, q):
-    """One step of the definition for every (sequence, head).
+    """One step of the definition for every (sequence, head): the gated delta rule,
+    this build's reading of the Gated DeltaNet layers the pages name ([RU]
+    introduction; [ZH] 事件概述或研究问题).
 
     S [B,H,P,N], alpha and beta [B,H], v [B,H,P], k and q [B,G,N] (float64).
     Returns (S_t, o_t [B,H,P]).
@@ -60,7 +62,8 @@ def delta_step(S, alpha, beta, v, k, q):
 
 def delta_pseudo_value(S, alpha, beta, v, k):
     """The write term of one step: w = beta (v - alpha S k), so that
-    S_t = alpha S + w k^T. S [B,H,P,N] is the state before the step, alpha and
+    S_t = alpha S + w k^T (derived here for the pages' claim that GDN can use the
+    same replay form, [ZH] 待核实 list). S [B,H,P,N] is the state before the step, alpha and
     beta [B,H], v [B,H,P], k [B,G,N]. Returns w [B,H,P]."""
     S = np.asarray(S, np.float64)
     g = head_groups(S.shape[1], k.shape[1])
@@ -69,7 +72,9 @@ def delta_pseudo_value(S, alpha, beta, v, k):
 
 
 def delta_replay_output(S_ckpt, alphas, betas, vs, ks, q):
-    """Output-only evaluation for one sequence after h records (form above).
+    """Output-only evaluation for one sequence after h records (form above): the
+    pages' output-only evaluation ([RU] §05; [ZH] 方法/产品要点) carried to the
+    delta rule.
 
     S_ckpt [H,P,N]; alphas, betas [h,H]; vs [h,H,P]; ks [h,G,N]; q [G,N].
     Returns o [H,P].
@@ -92,7 +97,7 @@ def delta_replay_output(S_ckpt, alphas, betas, vs, ks, q):
 
 
 def delta_fold(S_ckpt, alphas, betas, vs, ks):
-    """The state after h records, applied in order (one sequence)."""
+    """The state after h records, applied in order (one sequence): the flush fold ([RU] §03)."""
     S = np.array(S_ckpt, np.float64)
     H = S.shape[0]
     g = head_groups(H, ks.shape[1])
@@ -105,7 +110,8 @@ def delta_fold(S_ckpt, alphas, betas, vs, ks):
 
 
 class DeltaReplayOracle:
-    """Replay decoding (and speculative verify / commit) of a gated delta-rule layer.
+    """Replay decoding (and speculative verify / commit) of a gated delta-rule layer
+    ([RU] §03 and §05, with the delta rule in place of the outer product).
 
     The exact target is the definition, so ``S`` advances by ``delta_step``
     and the outputs are its outputs; ``ckpt`` is the exact state at each
@@ -124,6 +130,7 @@ class DeltaReplayOracle:
         self._drafts = None
 
     def decode(self, alpha, beta, v, k, q):
+        """One decode step ([RU] §03 non-flush / flush policy). Returns (o [B,H,P], flushed mask [B])."""
         h = self.count + 1
         if np.any(h > self.R):
             raise CapacityError("decode would exceed the ring capacity")
@@ -139,7 +146,7 @@ class DeltaReplayOracle:
         """Speculative verify of T drafts: alpha, beta [B,T,H], v [B,T,H,P], k, q [B,T,G,N].
 
         Output-only: the drafts run on a scratch copy of the exact state, so the
-        real state and the pointers stay unchanged. Returns O [B,T,H,P].
+        real state and the pointers stay unchanged ([RU] §05). Returns O [B,T,H,P].
         """
         T = alpha.shape[1]
         if np.any(self.count + T > self.R):
@@ -152,7 +159,7 @@ class DeltaReplayOracle:
         return O
 
     def commit(self, accepted):
-        """Apply the first accepted[b] drafts of the last verify (count += a)."""
+        """Apply the first accepted[b] drafts of the last verify (count += a; [RU] §05)."""
         if self._drafts is None:
             raise CapacityError("commit without a preceding verify")
         alpha, beta, v, k, q, T = self._drafts
@@ -167,6 +174,7 @@ class DeltaReplayOracle:
         self._drafts = None
 
     def flush(self, min_count: int):
+        """Fold every sequence holding at least min_count records ([RU] §03). Returns the mask."""
         mask = (self.count >= min_count) & (self.count > 0)
         self.ckpt[mask] = self.S[mask]
         self.start = np.where(mask, (self.start + self.count) % self.R, self.start)

@@ -93,12 +93,14 @@ def _rne_to_grid(y, mags: np.ndarray, sign_bit: int) -> np.ndarray:
 
 
 def e4m3_encode(y) -> np.ndarray:
-    """binary32 values -> E4M3 codes, round to nearest even, saturating to +-448."""
+    """binary32 values -> E4M3 codes, round to nearest even, saturating to +-448
+    (OCP 8-bit floating point specification, E4M3 with saturating conversion)."""
     return _rne_to_grid(y, _E4M3_MAG, 7)
 
 
 def e2m1_encode(y) -> np.ndarray:
-    """binary32 values -> E2M1 codes (low nibble), round to nearest even, saturating to +-6."""
+    """binary32 values -> E2M1 codes (low nibble), round to nearest even, saturating to +-6
+    (OCP Microscaling specification, FP4 E2M1 elements)."""
     return _rne_to_grid(y, _E2M1_MAG, 3)
 
 
@@ -107,7 +109,10 @@ def _rn32(x) -> np.ndarray:
 
 
 def quantize_rows_e4m3(X):
-    """Rows of fp32 values [..., N] -> (codes uint8 [..., N], scale fp32 [...])."""
+    """Rows of fp32 values [..., N] -> (codes uint8 [..., N], scale fp32 [...]).
+
+    The E4M3 row recipe of the module docstring: this build's reading of the
+    pages' FP8 read copy, refreshed from the checkpoint at each flush ([RU] §06)."""
     X = np.asarray(X, dtype=np.float32)
     a = np.abs(X).max(axis=-1)
     live = a > ZERO_ROW_AMAX
@@ -120,12 +125,16 @@ def quantize_rows_e4m3(X):
 
 
 def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
+    """x_hat = value(code) * s per row: what a non-flush step reads in place of the checkpoint ([RU] §06)."""
     return e4m3_value(codes) * np.asarray(scale, np.float64)[..., None]
 
 
 def quantize_rows_e2m1(X):
     """Rows of fp32 values [..., N] (N a multiple of 16) ->
-    (codes uint8 [..., N] one nibble each, block codes uint8 [..., N/16], row scale fp32 [...])."""
+    (codes uint8 [..., N] one nibble each, block codes uint8 [..., N/16], row scale fp32 [...]).
+
+    The E2M1 recipe of the module docstring: this build's NVFP4-style reading of
+    the pages' 4-bit read copy ([RU] §06; [AR] "الحد من خطأ التكميم")."""
     X = np.asarray(X, dtype=np.float32)
     N = X.shape[-1]
     if N % BLOCK:
@@ -149,6 +158,7 @@ def quantize_rows_e2m1(X):
 
 
 def dequantize_rows_e2m1(codes, bcodes, rscale) -> np.ndarray:
+    """x_hat = value(code) * value(block code) * s_r: the 4-bit read copy as a non-flush step reads it ([RU] §06)."""
     codes = np.asarray(codes)
     N = codes.shape[-1]
     vb = e2m1_value(codes).reshape(codes.shape[:-1] + (N // BLOCK, BLOCK))
@@ -159,6 +169,10 @@ def dequantize_rows_e2m1(codes, bcodes, rscale) -> np.ndarray:
 
 def element_error_bound(fmt: str, X) -> np.ndarray:
     """Per-element bound on |x_hat - x| for the read-copy formats.
+
+    The pages ask that the read copy's error stay that of one quantization
+    ([RU] §06; [AR] "الحد من خطأ التكميم") but state no bound; this one is
+    derived here from the format definitions.
 
     E4M3: round to nearest gives relative error <= 2^-4 for normal codes and an
     absolute error <= 2^-10 (in units of the row scale s) for subnormal codes.
@@ -212,6 +226,7 @@ class FullyQuantizedState:
         raise ValueError(self.fmt)
 
     def step(self, alpha, v, k, q):
+        """One step of the quantized-state recurrence ([RU] §02 item 3); returns o."""
         S_pre, o = conventional_step(self.S, alpha, v, k, q)
         self.S = self._roundtrip(S_pre)
         return o

@@ -18,7 +18,8 @@ import numpy as np
 
 
 def to_f64(x) -> np.ndarray:
-    """Exact up-cast of a torch tensor (fp32/bf16) or array to a float64 ndarray."""
+    """Exact up-cast of a torch tensor (fp32/bf16) or array to a float64 ndarray
+    (no passage: the oracle works in float64 on the stored inputs)."""
     try:
         import torch
 

@@ -42,10 +42,16 @@ from . import quant
 
 
 class CapacityError(RuntimeError):
-    """A request would hold more records than the ring has slots, or commit more than was drafted."""
+    """A request would hold more records than the ring has slots, or commit more than was drafted
+    (no passage: the ring capacity R = L + T_max - 1 is this build's reading)."""
 
 
 class ReplayOracle:
+    """Exact float64 state of every (sequence, head) plus the window bookkeeping
+    of replay decoding: start, count and the records since the last flush
+    ([RU] §03 unrolled window; [ZH] 方法/产品要点, core representation), the
+    checkpoint at each flush, and the read copy made from it ([RU] §06)."""
+
     def __init__(self, S0, L: int, R: int, G: int, read_fmt: str | None = None):
         S0 = np.asarray(S0, np.float64)
         self.B, self.H, self.P, self.N = S0.shape
@@ -96,7 +102,9 @@ class ReplayOracle:
 
     # ------------------------------------------------------------------ steps
     def decode(self, alpha, v, k, q):
-        """One decode step. Returns (o [B,H,P], flushed mask [B])."""
+        """One decode step ([RU] §03: a non-flush step appends its record and
+        outputs only; the step that fills the window folds and writes the
+        checkpoint). Returns (o [B,H,P], flushed mask [B])."""
         h = self.count + 1
         if np.any(h > self.R):
             raise CapacityError("decode would exceed the ring capacity")
@@ -138,7 +146,8 @@ class ReplayOracle:
         return O
 
     def commit(self, accepted):
-        """Commit the first accepted[b] drafts of the last verify (count += a)."""
+        """Commit the first accepted[b] drafts of the last verify (count += a):
+        rollback is a pointer move ([RU] §05; [AR] "تقليل حركة الحالة وتبسيط rollback")."""
         if self._drafts is None:
             raise CapacityError("commit without a preceding verify")
         alpha, v, k, q, T = self._drafts
@@ -158,7 +167,9 @@ class ReplayOracle:
         self.events += 1
 
     def flush(self, min_count: int):
-        """Fold every sequence holding at least min_count (>= 1) records. Returns the mask."""
+        """Fold every sequence holding at least min_count (>= 1) records ([RU] §03
+        flush; after a commit, this build's reading of where the flush goes).
+        Returns the mask."""
         if min_count < 1:
             raise ValueError("min_count must be >= 1")
         mask = self.count >= min_count

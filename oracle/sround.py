@@ -45,7 +45,9 @@ _MASK32 = np.uint64(0xFFFFFFFF)
 
 
 def philox4x32_10(counter, key):
-    """counter: uint32 array [..., 4]; key: uint32 array [..., 2] (broadcast). Returns uint32 [..., 4]."""
+    """Philox4x32-10 (Salmon et al., SC'11), the rounds as the module docstring states them.
+
+    counter: uint32 array [..., 4]; key: uint32 array [..., 2] (broadcast). Returns uint32 [..., 4]."""
     c = np.asarray(counter, dtype=np.uint64)
     k = np.broadcast_to(np.asarray(key, dtype=np.uint64), c.shape[:-1] + (2,)).copy()
     c0, c1, c2, c3 = (c[..., i].copy() for i in range(4))
@@ -63,7 +65,8 @@ def philox4x32_10(counter, key):
 
 
 def sr_words(n_elements: int, base_index: int, epoch: int, seed: int) -> np.ndarray:
-    """The 32-bit words of elements base_index .. base_index + n - 1 (base_index a multiple of 4)."""
+    """The 32-bit words of elements base_index .. base_index + n - 1 (base_index a multiple of 4),
+    from this build's counter layout (module docstring; the pages name no generator)."""
     assert base_index % 4 == 0 and n_elements % 4 == 0
     g = np.arange(base_index // 4, (base_index + n_elements) // 4, dtype=np.uint64)
     ctr = np.stack([g & _MASK32, g >> np.uint64(32), np.full_like(g, epoch), np.zeros_like(g)], axis=-1)
@@ -72,7 +75,8 @@ def sr_words(n_elements: int, base_index: int, epoch: int, seed: int) -> np.ndar
 
 
 def f16_toward_zero(x32) -> np.ndarray:
-    """binary32 -> binary16 rounded toward zero (finite inputs with |x| < 65520), as float32 values."""
+    """binary32 -> binary16 rounded toward zero (finite inputs with |x| < 65520), as float32 values
+    (IEEE 754 binary16; the lower neighbour of the stochastic rounding)."""
     x = np.asarray(x32, dtype=np.float32)
     near = x.astype(np.float16)  # round to nearest even
     over = np.abs(near.astype(np.float32)) > np.abs(x)
@@ -81,7 +85,8 @@ def f16_toward_zero(x32) -> np.ndarray:
 
 
 def stochastic_round_f16(x32, words) -> np.ndarray:
-    """Stochastic rounding of binary32 values to binary16 with one 32-bit word per value."""
+    """Stochastic rounding of binary32 values to binary16 with one 32-bit word per value: the
+    FP16 checkpoint store of [RU] §06, with the rounding rule read in the module docstring."""
     x = np.asarray(x32, dtype=np.float32)
     r = np.asarray(words, dtype=np.uint64)
     ax = np.abs(x)
@@ -100,7 +105,7 @@ def stochastic_round_f16(x32, words) -> np.ndarray:
 
 
 def nearest_f16(x32) -> np.ndarray:
-    """Round-to-nearest-even binary16 storage with saturation (the comparison mode)."""
+    """Round-to-nearest-even binary16 storage with saturation (the comparison mode; IEEE 754 binary16)."""
     x = np.asarray(x32, dtype=np.float32)
     y = np.clip(x, -F16_MAX, F16_MAX).astype(np.float16)
     return np.where(np.isnan(x), np.float16(np.nan), y)
@@ -155,6 +160,8 @@ class ReplayOracleF16:
         return unrolled_state(self.ckpt[b], a_, v_, k_)
 
     def decode(self, alpha, v, k, q):
+        """One decode step over the FP16 checkpoint ([RU] §03 non-flush / flush steps;
+        §06 FP16 storage). Returns (o [B,H,P], flushed mask [B])."""
         from .recurrence import conventional_step, replay_output
 
         h = self.count + 1
@@ -181,6 +188,8 @@ class ReplayOracleF16:
         return o, flush
 
     def verify(self, alpha, v, k, q):
+        """Output-only evaluation of T drafts from the stored checkpoint ([RU] §05;
+        [ZH] 方法/产品要点, verify formula). Returns O [B,T,H,P]."""
         from .recurrence import verify_outputs
 
         T = alpha.shape[1]
@@ -195,6 +204,7 @@ class ReplayOracleF16:
         return O
 
     def commit(self, accepted):
+        """Keep the first accepted[b] drafts as records (count += a; [RU] §05)."""
         from .recurrence import conventional_step
 
         alpha, v, k, q, T = self._drafts
@@ -212,6 +222,7 @@ class ReplayOracleF16:
         self._drafts = None
 
     def flush(self, min_count: int):
+        """Fold and store (rounded) every sequence holding at least min_count records ([RU] §03, §06)."""
         mask = (self.count >= min_count) & (self.count > 0)
         for b in np.nonzero(mask)[0]:
             self._store(b, self._fold(b, self.records[b]))
