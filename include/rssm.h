@@ -116,7 +116,9 @@ typedef struct {
 
 typedef struct rssm_ctx* rssm_handle;
 
-/* Byte sizes of the three caller-allocated buffers that rssm_create binds.
+/* Byte sizes of the three caller-allocated buffers that rssm_create binds
+ * (no counterpart in the pages: they hold the pages' checkpoint-plus-window
+ * representation, aikraft.ru page §03, in this library's layout).
  *  ring_bytes: the record ring, made of
  *      alpha [B,H,Rp] fp32 (Rp = R rounded up to 4) at offset 0,
  *      V     [B,H,R,P] in_dtype at offset v_off (delta layers: the
@@ -132,10 +134,12 @@ typedef struct rssm_ctx* rssm_handle;
 rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* ring_bytes, size_t* ptr_bytes,
                                 size_t* read_copy_bytes);
 
-/* Byte offsets of the V and K arrays inside the ring buffer (both 256-aligned). */
+/* Byte offsets of the V and K arrays inside the ring buffer (both 256-aligned;
+ * a layout query with no counterpart in the pages). */
 rssm_status rssm_ring_offsets(const rssm_config* cfg, size_t* v_off, size_t* k_off);
 
-/* Read-copy layout. Each (sequence, head) owns head_stride bytes at
+/* Read-copy layout (the read copy of aikraft.ru page §06; the byte layout is
+ * this library's). Each (sequence, head) owns head_stride bytes at
  * (b*H + h)*head_stride. Inside it:
  *   codes at 0: [P][N] bytes (E4M3) or [P][N/2] bytes (E2M1, element 2i in the low nibble);
  *   block scales at bscale_off: [P][N/16] E4M3 bytes (E2M1 only);
@@ -233,20 +237,23 @@ rssm_status rssm_commit(rssm_handle h, const int32_t* accepted, void* stream);
 
 /* Fold every sequence that holds count >= min_count records (min_count >= 1)
  * into its checkpoint, write it once, refresh the read copy, and clear its
- * buffer. Pass min_count = L after a commit. Other sequences are not touched.
+ * buffer (aikraft.ru page §03, the flush step; the pages do not say where the
+ * flush goes in speculative decoding, and this library places it after the
+ * commit). Pass min_count = L after a commit. Other sequences are not touched.
  * Two launches on `stream`: a one-block kernel lists the folding sequences in
  * the pointer block, then the fold runs over exactly their heads. */
 rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream);
 
 /* Copy start[B], count[B] (int32) and the error word to host memory,
- * synchronizing the stream first. Any output may be NULL. Error word bits:
+ * synchronizing the stream first (library plumbing; no counterpart in the
+ * pages). Any output may be NULL. Error word bits:
  * 1 ring overflow, 2 bad accepted length, 4 a bounded wait expired, 8 a kernel
  * refused its launch plan. Returns RSSM_OK, RSSM_EUNSUPPORTED (bit 8),
  * RSSM_ETIMEOUT (bit 4) or RSSM_ECAPACITY (bits 1|2). */
 rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* count_host,
                                uint32_t* err_host, void* stream);
 
-/* Clear the device error word (asynchronous). */
+/* Clear the device error word (asynchronous; library plumbing, no counterpart in the pages). */
 rssm_status rssm_clear_error(rssm_handle h, void* stream);
 
 /* Self-test of the kernels' bounded waits (no counterpart in the paper). It
@@ -256,10 +263,10 @@ rssm_status rssm_clear_error(rssm_handle h, void* stream);
  * fault: the context stays usable. Asynchronous on `stream`. */
 rssm_status rssm_selftest_bounded_wait(uint32_t* err_word, void* stream);
 
-/* Release the host handle. Caller memory is not touched. */
+/* Release the host handle. Caller memory is not touched (no counterpart in the pages). */
 rssm_status rssm_destroy(rssm_handle h);
 
-/* Message of the last error on the calling thread (never NULL). */
+/* Message of the last error on the calling thread, never NULL (no counterpart in the pages). */
 const char* rssm_last_error(void);
 
 /* Decode step that allocates nothing (no counterpart in the paper: a library
@@ -281,9 +288,10 @@ const char* rssm_last_error(void);
 rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, const void* v, const void* k,
                                             const void* q, float* o, void* stream);
 
-/* One decode step of a gated delta-rule layer (recurrence RSSM_GATED_DELTA):
- * rssm_decode_step plus beta [B,H] fp32 (16-byte aligned), the write strength
- * of each head's record. Non-flush steps read the checkpoint once, append the
+/* One decode step of a gated delta-rule layer (recurrence RSSM_GATED_DELTA;
+ * the replay form that ai.cheesepanini.fun page's 待核实 list says Gated
+ * DeltaNet can use, derived under rssm_recurrence): rssm_decode_step plus
+ * beta [B,H] fp32 (16-byte aligned), the write strength of each head's record. Non-flush steps read the checkpoint once, append the
  * record's pseudo-value and compute the output (the form above); the step
  * whose append brings the count to L folds all records and writes the
  * checkpoint once. RSSM_EINVAL on a handle of the other recurrence (and
@@ -299,8 +307,9 @@ rssm_status rssm_conventional_step(const rssm_config* cfg, float* state, const f
                                    const void* v, const void* k, const void* q, float* o,
                                    void* stream);
 
-/* Comparison kernel for gated delta-rule layers: the conventional step of that
- * recurrence, S <- alpha S (I - beta k k^T) + beta v k^T, o = S q, reading and
+/* Comparison kernel for gated delta-rule layers (the recurrence read under
+ * rssm_recurrence for the Gated DeltaNet layers that aikraft.ru page's
+ * introduction names): the conventional step of that recurrence, S <- alpha S (I - beta k k^T) + beta v k^T, o = S q, reading and
  * writing the full fp32 state every step. cfg->recurrence must be
  * RSSM_GATED_DELTA (and rssm_conventional_step refuses such a cfg); beta [B,H]
  * fp32, 16-byte aligned; the other arguments as for rssm_conventional_step. */
