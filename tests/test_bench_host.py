@@ -125,3 +125,20 @@ def test_verify_round_bytes_of_the_verify_workload():
     # checkpoint, read 16 records); commit moves 12 bytes per sequence
     assert after.tolist() == [4, 5, 0, 0]
     assert fb == 2 * (2 * 4194304 + 16 * 18944) + 12 * 4 == 17_383_472
+
+
+def test_window_bytes_with_read_copies():
+    """Read-copy windows of the B=256 L=16 layer, worked out by hand. A head's E4M3
+    copy is 64 x 128 codes + 64 fp32 row scales = 8,448 B; an E2M1 copy is 4,096 B
+    of codes + 512 block scales + 256 B of row scales = 4,864 B. The 15 non-flush
+    steps read the copy; the flush step reads and writes the 4 MiB checkpoint and
+    writes the copy; records, inputs and outputs are as without a copy:
+    120 buffered-record reads and 15 appends of 18,944 B, 16 x (20,992 + 32,768)."""
+    s = synth.PRESETS["mamba2_layer_b256_l16"]
+    rest = 2 * 4194304 + 135 * 18944 + 16 * (20992 + 32768)
+    e4 = bench.window_bytes(s, "e4m3")
+    assert e4["replay_window"] == 16 * 128 * 8448 + rest == 29_107_712
+    assert e4["replay_per_seq_step"] == 1_819_232
+    e2 = bench.window_bytes(s, "e2m1")
+    assert e2["replay_window"] == 16 * 128 * 4864 + rest == 21_767_680
+    assert e2["replay_per_seq_step"] == 1_360_480
