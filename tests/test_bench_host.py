@@ -142,3 +142,12 @@ def test_window_bytes_with_read_copies():
     e2 = bench.window_bytes(s, "e2m1")
     assert e2["replay_window"] == 16 * 128 * 4864 + rest == 21_767_680
     assert e2["replay_per_seq_step"] == 1_360_480
+
+
+def test_window_bytes_with_an_fp16_checkpoint():
+    """FP16 checkpoint (2 MiB per sequence): 16 reads and one write of it per window,
+    the same records, inputs and outputs as the FP32 layer."""
+    s = synth.PRESETS["mamba2_layer_b256_l16"]
+    wb = bench.window_bytes(s, None, ckpt_bytes=2)
+    assert wb["replay_window"] == 17 * 2097152 + 135 * 18944 + 16 * (20992 + 32768) == 39_069_184
+    assert wb["replay_per_seq_step"] == 2_441_824
