@@ -185,6 +185,24 @@ def test_config_struct_matches_the_header(tmp_path):
     assert got[1:] == [getattr(Config, f).offset for f in fields]
 
 
+def test_launch_plan_struct_matches_the_header(tmp_path):
+    """ctypes' LaunchPlanInfo against the C compiler's layout of rssm_launch_plan_info."""
+    import subprocess
+
+    from hybrid_model_ssm_gb300.rssm import LaunchPlanInfo
+    fields = [f for f, _ in LaunchPlanInfo._fields_]
+    src = tmp_path / "plan_layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "rssm.h"\nint main(void) {\n'
+                   '  printf("%zu", sizeof(rssm_launch_plan_info));\n'
+                   + "".join(f'  printf(" %zu", offsetof(rssm_launch_plan_info, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "plan_layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(LaunchPlanInfo)
+    assert got[1:] == [getattr(LaunchPlanInfo, f).offset for f in fields]
+
+
 def test_delta_rule_ring_layout(lib):
     """Delta-rule layers keep fp32 pseudo-values [B,H,R,P] where V sits."""
     s = LayerShape(B=3, H=4, P=64, N=128, G=2, L=5, recurrence="delta")
