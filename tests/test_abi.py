@@ -236,3 +236,14 @@ def test_unknown_recurrence_is_rejected(lib):
     lib.rssm_workspace_size.restype = ctypes.c_int
     assert lib.rssm_workspace_size(ctypes.byref(cfg), ctypes.byref(r), ctypes.byref(p), ctypes.byref(q)) == RSSM_EINVAL
     assert isinstance(cfg, Config)
+
+
+@pytest.mark.parametrize("compiler,std", [("gcc", "-std=c99"), ("g++", "-std=c++17")])
+def test_header_compiles_cleanly(tmp_path, compiler, std):
+    """include/rssm.h is plain C: it compiles as C99 and as C++17 with every warning an error."""
+    import subprocess
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "rssm.h"\nint main(void) { return (int)(sizeof(rssm_config) + sizeof(rssm_launch_plan_info)) == 0; }\n')
+    lang = ["-x", "c++"] if compiler == "g++" else []
+    subprocess.run([compiler, std, "-Wall", "-Wextra", "-pedantic", "-Werror", *lang, "-I",
+                    os.path.join(ROOT, "include"), str(src), "-o", str(tmp_path / "use_header")], check=True)
