@@ -217,11 +217,16 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------- CPU oracle timing
+MAX_ORACLE_THREADS = 64  # bounds the sample's host memory (about 160 MB per thread of 4 sequences)
+
+
 def host_cores() -> int:
+    """Threads for the CPU oracle sample: the cores this process may use, at most MAX_ORACLE_THREADS."""
     try:
-        return len(os.sched_getaffinity(0))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count() or 1
+        n = os.cpu_count() or 1
+    return max(1, min(n, MAX_ORACLE_THREADS))
 
 
 class OracleSample:
