@@ -3,7 +3,10 @@
 The quantizers are checked against the format definitions (golden code
 tables), an independent library conversion (torch's float8_e4m3fn cast, below
 its saturation point), exhaustive round trips and tie cases, native binary32
-arithmetic, and the stated per-element error bound.
+arithmetic, and the stated per-element error bound. The read-copy branch of
+ReplayOracle and the fully quantized comparator are pinned by hand-worked
+examples in tests/golden/ (dyadic values, exact in E4M3), and planted slips in
+copies of both (on the CPU) must fail those examples.
 """
 import numpy as np
 import pytest
@@ -11,7 +14,7 @@ import torch
 
 import oracle
 from oracle import quant
-from tests.golden_io import read_codes
+from tests.golden_io import read_codes, read_keyed
 
 
 def test_golden_code_tables():
@@ -141,3 +144,118 @@ def test_split_precision_error_does_not_grow_but_quantized_state_does():
     e_split, e_full = np.array(e_split), np.array(e_full)
     assert e_split[-100:].max() <= 2.0 * e_split[:100].max()
     assert np.median(e_full[-100:]) > 2.0 * np.median(e_split[-100:])
+
+
+# ----------------------------------------------------------- hand-worked read-copy goldens
+def _read_copy_golden_holds(cls) -> bool:
+    """Three decode steps of tests/golden/hand_read_copy_e4m3.txt through a ReplayOracle
+    class (L = 2): the copy at creation, the non-flush outputs read from the copy, the flush
+    output from the exact state, and the copy refreshed from the folded state."""
+    g = read_keyed("hand_read_copy_e4m3.txt")
+    orc = cls(g["S0"].reshape(1, 1, 1, 2), L=2, R=2, G=1, read_fmt="e4m3")
+    ok = np.array_equal(orc.copy.ravel(), g["copy0"])
+    for i in (1, 2, 3):
+        a = np.array([[g["alpha"][i - 1]]])
+        o, _ = orc.decode(a, g[f"v{i}"].reshape(1, 1, 1), g[f"k{i}"].reshape(1, 1, 2), g[f"q{i}"].reshape(1, 1, 2))
+        ok &= np.array_equal(o.ravel(), g[f"o{i}"]) and np.array_equal(orc.S.ravel(), g[f"S{i}"])
+        if i == 2:
+            ok &= np.array_equal(orc.copy.ravel(), g["copy2"])
+    return bool(ok)
+
+
+def _fully_quantized_golden_holds(cls) -> bool:
+    """Two steps of tests/golden/hand_fully_quantized_e4m3.txt through a FullyQuantizedState class."""
+    g = read_keyed("hand_fully_quantized_e4m3.txt")
+    f = cls(g["S0"].reshape(1, 1, 2, 2), "e4m3")
+    ok = np.array_equal(f.S.ravel(), g["S0"])
+    for i in (1, 2):
+        o = f.step(np.array([[g[f"alpha{i}"][0]]]), g[f"v{i}"].reshape(1, 1, 2), g[f"k{i}"].reshape(1, 1, 2),
+                   g[f"q{i}"].reshape(1, 1, 2))
+        ok &= np.array_equal(o.ravel(), g[f"o{i}"]) and np.array_equal(f.S.ravel(), g[f"Sq{i}"])
+    return bool(ok)
+
+
+def test_hand_worked_read_copy_codes():
+    g = read_keyed("hand_read_copy_e4m3.txt")
+    codes, scale = quant.quantize_rows_e4m3(np.array([g["S0"]], np.float32))
+    assert list(codes.ravel()) == [int(x) for x in g["copy_codes0"]]
+    assert float(scale[0]) == g["copy_scale0"][0]
+
+
+def test_hand_worked_read_copy_replay():
+    assert _read_copy_golden_holds(oracle.ReplayOracle)
+
+
+def test_hand_worked_fully_quantized_steps():
+    assert _fully_quantized_golden_holds(oracle.FullyQuantizedState)
+
+
+# Planted mistakes in copies of the read-copy branch and of the quantized-state step (CPU only).
+class _FlushReadsCopy(oracle.ReplayOracle):
+    """Slip: the flush step's output also comes from the read copy."""
+
+    def decode(self, alpha, v, k, q):
+        copy_before = self.copy.copy()
+        recs = [list(r) for r in self.records]
+        o, flush = super().decode(alpha, v, k, q)
+        for b in np.nonzero(flush)[0]:
+            a_, v_, k_ = (np.stack(x) for x in zip(*(recs[b] + [(alpha[b], v[b], k[b])])))
+            o[b] = oracle.replay_output(copy_before[b], a_, v_, k_, q[b])
+        return o, flush
+
+
+class _CopyNotRefreshed(oracle.ReplayOracle):
+    """Slip: the flush folds the checkpoint but keeps the old read copy."""
+
+    def _fold(self, mask, n_records):
+        old = None if self.copy is None else self.copy.copy()
+        idx = super()._fold(mask, n_records)
+        if old is not None:
+            self.copy = old
+        return idx
+
+
+class _CopyNotQuantized(oracle.ReplayOracle):
+    """Slip: the copy is the exact state (no quantization)."""
+
+    def _quantize(self, X):
+        return np.array(X, np.float64)
+
+
+class _NonFlushReadsExact(oracle.ReplayOracle):
+    """Slip: non-flush outputs come from the exact state instead of the copy."""
+
+    def decode(self, alpha, v, k, q):
+        S_before = self.S.copy()
+        o, flush = super().decode(alpha, v, k, q)
+        _, o_exact = oracle.conventional_step(S_before, alpha, v, k, q)
+        return o_exact, flush
+
+
+class _OutputFromQuantized(oracle.FullyQuantizedState):
+    """Slip: the output reads the re-quantized state instead of the fresh update."""
+
+    def step(self, alpha, v, k, q):
+        super().step(alpha, v, k, q)
+        g = oracle.head_groups(self.S.shape[1], q.shape[1])
+        return (self.S * q[:, g][:, :, None, :]).sum(-1)
+
+
+class _StateKeptExact(oracle.FullyQuantizedState):
+    """Slip: the updated state is stored without re-quantization."""
+
+    def step(self, alpha, v, k, q):
+        S_pre, o = oracle.conventional_step(self.S, alpha, v, k, q)
+        self.S = S_pre
+        return o
+
+
+@pytest.mark.parametrize("mutant", [_FlushReadsCopy, _CopyNotRefreshed, _CopyNotQuantized, _NonFlushReadsExact],
+                         ids=lambda m: m.__name__)
+def test_read_copy_golden_catches_planted_mistakes(mutant):
+    assert not _read_copy_golden_holds(mutant)
+
+
+@pytest.mark.parametrize("mutant", [_OutputFromQuantized, _StateKeptExact], ids=lambda m: m.__name__)
+def test_fully_quantized_golden_catches_planted_mistakes(mutant):
+    assert not _fully_quantized_golden_holds(mutant)
