@@ -15,7 +15,15 @@ Prints one JSON line. Keys beyond the driver contract:
   e2e           the same metric with inputs copied from pinned host memory and
                 outputs copied back inside the timed region
   comparison    the conventional read-update-write kernel on the same workload
+  verify_b512_t4, read_copy_e4m3, read_copy_e2m1, delta_rule
+                the secondary arms of the path, each with its own roofline
+                block: speculative rounds (verify + commit + flush, B=512,
+                T=4) against the snapshot comparator, decode windows reading
+                an E4M3 or E2M1 copy of the checkpoint, and decode windows of
+                a gated delta-rule layer of the same shape
 
+The timed region covers at least --min-seconds of windows (default 1 s), and
+at least --steps of them, so that the clock sampler sees several samples.
 `--impl reference` times the CPU oracle instead (rank 0 only).
 """
 from __future__ import annotations
@@ -44,12 +52,9 @@ METRIC = "SSM decode seq-steps/s at B=256, L=16; achieved HBM GB/s vs GB300 peak
 UNIT = "seq-steps/s"
 WORKLOAD = synth.PRESETS["mamba2_layer_b256_l16"]
 FALLBACK_HBM_GBS = 6800.0
-DECODE_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_decode.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_step_b256_l16.md")
-DELTA_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_delta.cu"]
-DELTA_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "delta_decode_step_b256_l16.md")
-VERIFY_KERNEL_SOURCES = ["hybrid_model_ssm_gb300/csrc/rssm_device.cuh", "hybrid_model_ssm_gb300/csrc/k_verify.cu"]
-VERIFY_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_b512_t4.md")
+# DRAM bytes per launch from ncu captures, keyed by workload, each with the hash
+# of the kernel sources it was taken on (written beside the summaries).
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 # ----------------------------------------------------------------- analytic bytes
@@ -92,8 +97,12 @@ def window_bytes(s, read_fmt=None, ckpt_bytes: int = 4, delta: bool = False) -> 
     reads = (L - 1) * (C if read_fmt else S) + S
     total = reads + S + C + ring_rec * L * (L - 1) // 2 + L * (inp + out) + (L - 1) * ring_rec
     conv = L * (2 * 4 * s.H * s.P * s.N + inp + out)
+    # per launch: a non-flush step at window position t reads t buffered records and
+    # appends one (averaged over t = 0..L-2); the flush step reads L-1 records
+    nonflush = (C if read_fmt else S) + ring_rec * (L - 2) / 2 + inp + out + ring_rec if L > 1 else 0.0
+    flush = 2 * S + C + ring_rec * (L - 1) + inp + out
     return {"replay_window": total, "replay_per_seq_step": total / L, "conventional_per_seq_step": conv / L,
-            "state": S}
+            "state": S, "nonflush_per_seq_launch": nonflush, "flush_per_seq_launch": flush}
 
 
 # ----------------------------------------------------------------- environment
@@ -106,27 +115,24 @@ def measured_peak_gbs() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash(sources=None) -> str:
+def kernel_source_hash(sources) -> str:
     h = hashlib.sha256()
-    for rel in sources or DECODE_KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic(path: str = TRAFFIC_FILE, sources=None) -> float | None:
-    """DRAM bytes per decode launch from a committed ncu summary, if it was taken on this kernel source."""
+def profiled_traffic(key: str) -> float | None:
+    """DRAM bytes per launch of a workload from profiles/traffic.json, while the kernel
+    sources still hash to the value recorded with the capture; else None."""
     try:
-        kv = {}
-        with open(path) as f:
-            for line in f:
-                if ":" in line and line.strip().startswith("- "):
-                    k, v = line.strip()[2:].split(":", 1)
-                    kv[k.strip()] = v.strip().strip("`")
-        if kv.get("kernel_source_sha256") != kernel_source_hash(sources):
+        with open(TRAFFIC_JSON) as f:
+            entry = json.load(f)[key]
+        if entry["kernel_source_sha256"] != kernel_source_hash(entry["kernel_sources"]):
             return None
-        return float(kv["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        return float(entry["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
@@ -220,13 +226,17 @@ def max_over_ranks(x: float, world: int) -> float:
 MAX_ORACLE_THREADS = 64  # bounds the sample's host memory (about 160 MB per thread of 4 sequences)
 
 
-def host_cores() -> int:
-    """Threads for the CPU oracle sample: the cores this process may use, at most MAX_ORACLE_THREADS."""
+def usable_cores() -> int:
+    """Host cores this process may run on."""
     try:
-        n = len(os.sched_getaffinity(0))
+        return max(1, len(os.sched_getaffinity(0)))
     except AttributeError:
-        n = os.cpu_count() or 1
-    return max(1, min(n, MAX_ORACLE_THREADS))
+        return os.cpu_count() or 1
+
+
+def host_cores() -> int:
+    """Threads for the CPU oracle sample: the usable cores, at most MAX_ORACLE_THREADS."""
+    return max(1, min(usable_cores(), MAX_ORACLE_THREADS))
 
 
 class OracleSample:
@@ -288,29 +298,18 @@ def cpu_baseline_line(shape, budget_s: float = 12.0, delta: bool = False) -> dic
     steps = max(4, int(budget_s / max(per_step, 1e-6)))
     t = sample.run(steps)
     what = "gated delta rule" if delta else "conventional recurrence"
-    return {"value": sample.units(steps) / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+    return {"value": sample.units(steps) / t, "unit": UNIT, "cores": usable_cores(), "threads": threads,
+            "kind": "oracle",
             "sample": f"float64 {what}, {threads} threads x {n_seq} sequences (of {shape.B}) x all {shape.H} "
                       f"heads, {steps} steps ({t:.1f} s); numpy elementwise, one thread per sequence group"}
 
 
 # ----------------------------------------------------------------- GPU arm
-def run_ours(args, world, rank, local):
-    from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM, conventional_step
-
-    torch.cuda.set_device(local)
-    s = WORKLOAD if args.batch is None else WORKLOAD.with_(B=args.batch)
-    delta = args.recurrence == "delta"
-    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype, read_fmt=args.read_fmt,
-                    ckpt=args.ckpt, seed=s.seed, recurrence=args.recurrence)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(s.seed + 1000 * rank)
-    ckpt = (torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev, dtype=torch.float32) * 0.1)
-    model = ReplaySSM(ls, ckpt.to(ls.torch_ckpt_dtype))
+def decode_pool(s, ls, dev, gen, delta: bool, n: int = 16):
+    """n resident steps of seeded inputs (alpha, v, k, q[, beta]) on the device."""
     pool = []
     sc = 1.0 / math.sqrt(s.N)
-    for _ in range(16):  # 16 resident steps of inputs, cycled
+    for _ in range(n):
         u = torch.randn((s.B, s.H), generator=gen, device=dev)
         alpha = torch.exp(-torch.nn.functional.softplus(u)).float()
         v = (torch.randn((s.B, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
@@ -323,71 +322,145 @@ def run_ours(args, world, rank, local):
             pool.append((alpha, v, k, q, beta))
         else:
             pool.append((alpha, v, k, q))
-    out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=dev)
-    L = s.L
+    return pool
 
-    def step(x, o, st=None):
-        if delta:
-            model.decode_step(*x[:4], out=o, beta=x[4], stream=st)
+
+class DecodeArm:
+    """Decode windows of one layer: the model, its resident inputs and the timing loops."""
+
+    def __init__(self, s, local: int, rank: int, read_fmt=None, ckpt: str = "f32", recurrence: str = "outer"):
+        from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM
+
+        self.s, self.read_fmt, self.ckpt_fmt = s, read_fmt, ckpt
+        self.delta = recurrence == "delta"
+        self.ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=1, in_dtype=s.in_dtype,
+                             read_fmt=read_fmt, ckpt=ckpt, seed=s.seed, recurrence=recurrence)
+        self.dev = torch.device("cuda", local)
+        self.stream = torch.cuda.current_stream()
+        gen = torch.Generator(device=self.dev)
+        gen.manual_seed(s.seed + 1000 * rank)
+        self.ckpt0 = torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=self.dev, dtype=torch.float32) * 0.1
+        self.model = ReplaySSM(self.ls, self.ckpt0.to(self.ls.torch_ckpt_dtype))
+        self.pool = decode_pool(s, self.ls, self.dev, gen, self.delta)
+        self.out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=self.dev)
+        self.launches = 0
+
+    def step(self, x, o, st=None):
+        if self.delta:
+            self.model.decode_step(*x[:4], out=o, beta=x[4], stream=st)
         else:
-            model.decode_step(*x, out=o, stream=st)
+            self.model.decode_step(*x, out=o, stream=st)
+        self.launches += 1
 
-    def window(i0: int, ev: list | None = None):
-        for j in range(L):
-            x = pool[(i0 + j) % len(pool)]
+    def window(self, i0: int, ev: list | None = None):
+        for j in range(self.s.L):
+            x = self.pool[(i0 + j) % len(self.pool)]
             if ev is not None:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                step(x, out)
-                e1.record(stream)
+                e0.record(self.stream)
+                self.step(x, self.out)
+                e1.record(self.stream)
                 ev.append((e0, e1))
             else:
-                step(x, out)
+                self.step(x, self.out)
 
-    # warm-up (whole windows keep every sequence aligned on the window)
-    for w in range(args.warmup):
-        window(w * L)
-    torch.cuda.synchronize()
-    model.read_pointers()  # raises on any device error
-
-    # timed region: K windows
-    evs: list = []
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(args.steps):
-            window(i * L, evs)
-        t1.record(stream)
+    def warm(self, warmup: int) -> float:
+        """warmup whole windows (every sequence stays aligned on the window); returns s per window."""
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.window(0)
+        w0.record(self.stream)
+        for w in range(1, max(2, warmup)):
+            self.window(w * self.s.L)
+        w1.record(self.stream)
         torch.cuda.synchronize()
-    barrier(world)
-    elapsed = t0.elapsed_time(t1) / 1e3
-    launch_s = [a.elapsed_time(b) / 1e3 for a, b in evs]
-    start, count, err = model.read_pointers()
+        self.model.read_pointers()  # raises on any device error
+        return w0.elapsed_time(w1) / 1e3 / max(1, max(2, warmup) - 1)
+
+    def timed(self, n_windows: int, world: int, clock=None):
+        """n_windows timed windows with per-launch events; returns (elapsed s, per-launch s)."""
+        evs: list = []
+        barrier(world)
+        torch.cuda.synchronize()
+        ctx = clock if clock is not None else _Null()
+        with ctx:
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(self.stream)
+            for i in range(n_windows):
+                self.window(i * self.s.L, evs)
+            t1.record(self.stream)
+            torch.cuda.synchronize()
+        barrier(world)
+        return t0.elapsed_time(t1) / 1e3, [a.elapsed_time(b) / 1e3 for a, b in evs]
+
+    def roofline(self, launch_s: list, peak: float, peak_kind: str, traffic) -> dict:
+        s, L = self.s, self.s.L
+        wb = window_bytes(s, self.read_fmt, 4 if self.ckpt_fmt == "f32" else 2, self.delta)
+        alg = wb["replay_per_seq_step"] * s.B
+        mean = sum(launch_s) / len(launch_s)
+        flush_s = [launch_s[i] for i in range(len(launch_s)) if i % L == L - 1]
+        nonflush_s = [launch_s[i] for i in range(len(launch_s)) if i % L != L - 1]
+        nf = sum(nonflush_s) / max(1, len(nonflush_s))
+        fl = sum(flush_s) / max(1, len(flush_s))
+        achieved = alg / mean / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes_per_launch": alg,
+                "mean_launch_ms": mean * 1e3, "mean_nonflush_launch_ms": nf * 1e3, "mean_flush_launch_ms": fl * 1e3,
+                "nonflush_frac": wb["nonflush_per_seq_launch"] * s.B / nf / 1e9 / peak if nf > 0 else None,
+                "flush_frac": wb["flush_per_seq_launch"] * s.B / fl / 1e9 / peak if fl > 0 else None,
+                "frac_of_nominal_8tbs": achieved / 8000.0}
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+    def summary(self):
+        return None
+
+
+def windows_for(args_steps: int, per_window_s: float, min_seconds: float) -> int:
+    """Timed windows: at least --steps, and enough to fill min_seconds."""
+    return max(args_steps, int(math.ceil(min_seconds / max(per_window_s, 1e-6))))
+
+
+def run_ours(args, world, rank, local):
+    from hybrid_model_ssm_gb300 import conventional_step
+
+    torch.cuda.set_device(local)
+    s = WORKLOAD if args.batch is None else WORKLOAD.with_(B=args.batch)
+    delta = args.recurrence == "delta"
+    arm = DecodeArm(s, local, rank, args.read_fmt, args.ckpt, args.recurrence)
+    L = s.L
+    per_window = arm.warm(args.warmup)
+    n_windows = windows_for(args.steps, per_window, args.min_seconds)
+    with ClockSampler(local) as clk:
+        elapsed, launch_s = arm.timed(n_windows, world, clk)
+    timed_launches = len(launch_s)
+    start, count, err = arm.model.read_pointers()
     elapsed_max = max_over_ranks(elapsed, world)
-    seq_steps = world * s.B * L * args.steps
+    seq_steps = world * s.B * L * n_windows
     value = seq_steps / elapsed_max
-    mean_launch = sum(launch_s) / len(launch_s)
+    peak, peak_kind = measured_peak_gbs()
+    default_case = not (args.read_fmt or args.ckpt != "f32" or args.batch is not None)
+    traffic = (profiled_traffic("delta_decode_b256_l16" if delta else "decode_b256_l16") if default_case else None)
+    roof = arm.roofline(launch_s, peak, peak_kind, traffic)
     ckpt_es = 4 if args.ckpt == "f32" else 2
     wb = window_bytes(s, args.read_fmt, ckpt_es, delta)
-    alg_bytes_launch = wb["replay_per_seq_step"] * s.B
-    achieved = alg_bytes_launch / mean_launch / 1e9
-    peak, peak_kind = measured_peak_gbs()
-
-    # flush launch vs non-flush launches (launch index within the window)
-    flush_s = [launch_s[i] for i in range(len(launch_s)) if i % L == L - 1]
-    nonflush_s = [launch_s[i] for i in range(len(launch_s)) if i % L != L - 1]
+    model, pool, out, stream = arm.model, arm.pool, arm.out, arm.stream
 
     # in-run comparison: the conventional kernel on the same workload
     comp = None
     if not args.no_conventional:
-        state = ckpt.clone()
-        n_conv = max(1, min(args.steps, 50))
+        state = arm.ckpt0.clone()
+        n_conv = max(1, min(n_windows, 50))
+
         def conv(x):
-            conventional_step(ls, state, *x[:4], out=out, beta=x[4] if delta else None)
+            conventional_step(arm.ls, state, *x[:4], out=out, beta=x[4] if delta else None)
 
         for i in range(L):
             conv(pool[i % len(pool)])
@@ -426,7 +499,7 @@ def run_ours(args, world, rank, local):
         ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer j landed
         ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on buffer j finished
         ev_out = [torch.cuda.Event() for _ in range(2)]   # output j copied out
-        n_e2e = max(1, min(args.steps, 60))
+        n_e2e = max(1, min(n_windows, 120))
         torch.cuda.synchronize()
         barrier(world)
         tw0 = time.perf_counter()
@@ -441,7 +514,7 @@ def run_ours(args, world, rank, local):
             stream.wait_event(ev_in[j])
             if i >= 2:
                 stream.wait_event(ev_out[j])  # step i-2's output has been copied out
-            step(dpool[j], dout[j], stream)
+            arm.step(dpool[j], dout[j], stream)
             ev_done[j].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(ev_done[j])
@@ -454,6 +527,13 @@ def run_ours(args, world, rank, local):
                "note": "pinned host inputs copied in and outputs copied out every decode step; the copies run "
                        "on an input and an output copy stream, overlapping the neighbouring steps' kernels "
                        "(double-buffered device inputs and outputs)"}
+    del arm, model, pool, out
+    torch.cuda.empty_cache()
+
+    # the path's other arms, each with its own roofline block (default case only)
+    extras = {}
+    if default_case and not delta and not args.no_extras:
+        extras = secondary_arms(args, world, rank, local)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -464,7 +544,7 @@ def run_ours(args, world, rank, local):
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / n_windows * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.ckpt == "f32" else "f32 (fp16 checkpoint)",
         "data": "synthetic",
         "config": {"workload": f"ReplaySSM decode, one {'gated delta-rule' if delta else 'Mamba-2-shaped'} layer: "
@@ -473,25 +553,52 @@ def run_ours(args, world, rank, local):
                                f"of {L} decode launches ({L - 1} non-flush + 1 flush)",
                    "global_batch": s.B * world, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush needed: the 1 GiB checkpoint per replica is 8x the 129 MB L2",
-                   "inputs": "16 resident steps of seeded inputs, cycled"},
-        "hbm_gbs_achieved": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": (None if (args.read_fmt or args.ckpt != "f32" or args.batch is not None)
-                                 else profiled_traffic(DELTA_TRAFFIC_FILE, DELTA_KERNEL_SOURCES) if delta
-                                 else profiled_traffic()),
-                     "algorithmic_bytes_per_launch": alg_bytes_launch,
-                     "mean_launch_ms": mean_launch * 1e3,
-                     "mean_nonflush_launch_ms": 1e3 * sum(nonflush_s) / max(1, len(nonflush_s)),
-                     "mean_flush_launch_ms": 1e3 * sum(flush_s) / max(1, len(flush_s)),
-                     "frac_of_nominal_8tbs": achieved / 8000.0},
+                   "inputs": "16 resident steps of seeded inputs, cycled",
+                   "windows_timed": n_windows,
+                   "timed_region": f"max(--steps, enough windows for {args.min_seconds:g} s) = {n_windows} windows"},
+        "hbm_gbs_achieved": roof["achieved"],
+        "roofline": roof,
         "comparison": comp,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": len(evs),
+        "gpu_launches": timed_launches,
         "device_error_word": err,
     }
+    line.update(extras)
     return line
+
+
+def secondary_arms(args, world, rank, local) -> dict:
+    """The verify round, the two read-copy decodes and the delta-rule decode, each timed
+    for at least --extra-seconds, with the roofline of its dominant launch."""
+    out = {}
+    peak, peak_kind = measured_peak_gbs()
+    vargs = argparse.Namespace(**vars(args))
+    vargs.batch, vargs.drafts = None, None
+    vargs.min_seconds = args.extra_seconds
+    v = run_verify(vargs, world, rank, local, print_line=False)
+    if v is not None:
+        out["verify_b512_t4"] = {k: v[k] for k in ("metric", "value", "unit", "ms_per_step", "roofline",
+                                                  "breakdown_ms_per_round", "comparison", "gpu_launches",
+                                                  "device_error_word") if k in v}
+        out["verify_b512_t4"]["rounds_timed"] = v["config"]["rounds_timed"]
+    for key, kw in (("read_copy_e4m3", {"read_fmt": "e4m3"}), ("read_copy_e2m1", {"read_fmt": "e2m1"}),
+                    ("delta_rule", {"recurrence": "delta"})):
+        arm = DecodeArm(WORKLOAD, local, rank, **kw)
+        per_window = arm.warm(args.warmup)
+        n = windows_for(args.steps, per_window, args.extra_seconds)
+        elapsed, launch_s = arm.timed(n, world)
+        err = arm.model.read_pointers()[2]
+        traffic = profiled_traffic("delta_decode_b256_l16") if key == "delta_rule" else None
+        elapsed = max_over_ranks(elapsed, world)
+        out[key] = {"value": world * WORKLOAD.B * WORKLOAD.L * n / elapsed, "unit": UNIT,
+                    "ms_per_window": elapsed / n * 1e3, "windows_timed": n,
+                    "roofline": arm.roofline(launch_s, peak, peak_kind, traffic), "gpu_launches": len(launch_s),
+                    "device_error_word": err}
+        del arm
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_reference(args, world, rank):
@@ -514,7 +621,8 @@ def run_reference(args, world, rank):
             "data": "synthetic",
             "config": {"workload": f"ReplaySSM decode, B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
                                    f"(oracle sample of {threads} x {n_seq} sequences)"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": usable_cores(), "threads": threads,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -543,7 +651,7 @@ def verify_round_bytes(s, T: int, counts: np.ndarray, accepted: np.ndarray):
     return vb, fb, np.where(fl, 0, c2)
 
 
-def run_verify(args, world, rank, local):
+def run_verify(args, world, rank, local, print_line: bool = True):
     from hybrid_model_ssm_gb300 import ConventionalVerifier, LayerShape, ReplaySSM
 
     torch.cuda.set_device(local)
@@ -566,9 +674,14 @@ def run_verify(args, world, rank, local):
                      (torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
                      (torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)))
     cgen = synth.make_generator(s.seed + 7)
-    rounds = args.warmup + args.steps
-    acc_host = [synth.accepted_lengths(s.B, T, cgen) for _ in range(rounds)]
-    acc_dev = [a.to(dev) for a in acc_host]
+    acc_host: list = []
+    acc_dev: list = []
+
+    def draw(n):
+        for _ in range(n):
+            acc_host.append(synth.accepted_lengths(s.B, T, cgen))
+            acc_dev.append(acc_host[-1].to(dev))
+
     out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=dev)
 
     def one_round(i, ev=None):
@@ -583,11 +696,20 @@ def run_verify(args, world, rank, local):
         if e: e[3].record(stream); ev.append(e)
 
     counts = np.zeros(s.B, np.int64)
+    draw(args.warmup)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup):
+        if i == 1:
+            w0.record(stream)
         one_round(i)
         _, _, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64))
+    w1.record(stream)
     torch.cuda.synchronize()
     model.read_pointers()
+    per_round = w0.elapsed_time(w1) / 1e3 / max(1, args.warmup - 1)
+    n_rounds = windows_for(args.steps, per_round, args.min_seconds)
+    draw(n_rounds)
+    rounds = args.warmup + n_rounds
     ev = []
     vbytes = fbytes = 0
     for i in range(args.warmup, rounds):
@@ -626,9 +748,10 @@ def run_verify(args, world, rank, local):
             conv.verify(a, v, k, q, out=out)
             conv.commit(acc_dev[i])
         torch.cuda.synchronize()
+        n_conv = min(n_rounds, max(args.steps, 20))
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record(stream)
-        for i in range(args.warmup, rounds):
+        for i in range(args.warmup, args.warmup + n_conv):
             a, v, k, q = pool[i % len(pool)]
             conv.verify(a, v, k, q, out=out)
             conv.commit(acc_dev[i])
@@ -640,37 +763,40 @@ def run_verify(args, world, rank, local):
         Sb = 4 * s.H * s.P * s.N
         inp = record_bytes(s) + es * s.G * s.N
         conv_round = s.B * ((1 + T) * Sb + T * (inp + 4 * s.H * s.P)) + 8 * s.B
-        comp = {"conventional_draft_tokens_per_s": s.B * T * args.steps / ct,
-                "conventional_ms_per_round": ct / args.steps * 1e3,
-                "conventional_hbm_gbs": conv_round * args.steps / ct / 1e9,
-                "replay_speedup": (world * s.B * T * args.steps / elapsed) / (s.B * T * args.steps / ct),
-                "algorithmic_bytes_replay_over_conventional": (vbytes + fbytes) / (conv_round * args.steps),
+        replay_per_round = elapsed / n_rounds
+        comp = {"conventional_draft_tokens_per_s": s.B * T * n_conv / ct,
+                "conventional_ms_per_round": ct / n_conv * 1e3,
+                "conventional_hbm_gbs": conv_round * n_conv / ct / 1e9,
+                "replay_speedup": (ct / n_conv) / replay_per_round,
+                "algorithmic_bytes_replay_over_conventional": (vbytes + fbytes) / n_rounds / conv_round,
+                "rounds_timed": n_conv,
                 "method": "every draft advances the full fp32 state and writes a snapshot; commit selects the "
                           "accepted snapshot by a per-sequence slot index"}
         del conv
     if rank != 0:
         return None
     return {
-        "metric": VERIFY_METRIC, "value": world * s.B * T * args.steps / elapsed, "unit": "draft-tokens/s",
+        "metric": VERIFY_METRIC, "value": world * s.B * T * n_rounds / elapsed, "unit": "draft-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": elapsed / n_rounds * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"ReplaySSM speculative round: B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
                                f"T={T}, bf16 inputs; one step = verify + commit (seeded accepted lengths "
                                f"0..{T}) + flush of sequences at {s.L} records",
-                   "global_batch": s.B * world, "l2": "no flush needed: 2 GiB checkpoint per replica"},
-        "seq_rounds_per_s": world * s.B * args.steps / elapsed,
+                   "global_batch": s.B * world, "l2": "no flush needed: 2 GiB checkpoint per replica",
+                   "rounds_timed": n_rounds},
+        "seq_rounds_per_s": world * s.B * n_rounds / elapsed,
         "roofline": {"bound": "hbm", "kernel": "verify", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": (profiled_traffic(VERIFY_TRAFFIC_FILE, VERIFY_KERNEL_SOURCES)
-                                 if args.batch is None else None),
-                     "algorithmic_bytes_per_launch": vbytes / args.steps,
-                     "mean_launch_ms": tv / args.steps * 1e3},
-        "breakdown_ms_per_round": {"verify": tv / args.steps * 1e3, "commit": tc / args.steps * 1e3,
-                                   "flush": tf / args.steps * 1e3,
+                     "traffic": (profiled_traffic(f"verify_b512_t{T}") if args.batch is None else None),
+                     "algorithmic_bytes_per_launch": vbytes / n_rounds,
+                     "mean_launch_ms": tv / n_rounds * 1e3},
+        "breakdown_ms_per_round": {"verify": tv / n_rounds * 1e3, "commit": tc / n_rounds * 1e3,
+                                   "flush": tf / n_rounds * 1e3,
                                    "flush_hbm_gbs": fbytes / tf / 1e9 if tf > 0 else None},
         "comparison": comp,
-        "clocks": clk.summary(), "gpu_launches": 4 * args.steps,  # verify, commit, flush list, flush "device_error_word": err,
+        "clocks": clk.summary(), "gpu_launches": 4 * n_rounds,  # verify, commit, flush list, flush
+        "device_error_word": err,
     }
 
 
@@ -814,6 +940,12 @@ def main(argv=None):
                     help="verify: drafts per round T (1..8; default 4); other values are not the headline config")
     ap.add_argument("--recurrence", choices=["outer", "delta"], default="outer",
                     help="decode: the gated outer-product recurrence or the gated delta rule (beta inputs)")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="the timed region covers at least this long (and at least --steps steps)")
+    ap.add_argument("--extra-seconds", type=float, default=0.3,
+                    help="timed length of each secondary arm of the default line")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="leave out the secondary arms (verify, read copies, delta rule) of the default line")
     args = ap.parse_args(argv)
     if args.recurrence == "delta" and (args.workload != "decode" or args.read_fmt or args.ckpt != "f32"):
         ap.error("--recurrence delta: decode workload, FP32 checkpoint, no read copy")

@@ -46,9 +46,9 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, verbose: bool, build_dir: str = BUILD, defines: tuple = ()) -> str:
-    obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
-    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c", src, "-o", obj]
+def _compile(src: str, verbose: bool) -> str:
+    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,20 +59,15 @@ def _compile(src: str, verbose: bool, build_dir: str = BUILD, defines: tuple = (
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, out: str | None = None, defines: tuple = ()) -> str:
-    """Compile every CUDA source for sm_103a and link librssm.so. Returns its path.
-
-    `out` and `defines` build a variant (extra -D macros) into another file,
-    which RSSM_LIB can then select; the default is the in-tree library.
-    """
-    lib = out or LIB
-    if not force and out is None and not defines and up_to_date():
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every CUDA source for sm_103a and link librssm.so in-tree. Returns its path."""
+    lib = LIB
+    if not force and up_to_date():
         return LIB
-    build_dir = BUILD if out is None else lib + ".objs"
-    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose, build_dir, tuple(defines)), srcs))
+        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     tmp = lib + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -156,9 +156,6 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   // verify heads are compute-heavier (T queries): one stage per dot group measured best
   if (kind == LayoutKind::kVerify)
     while (dgroups < 8 && stages >= 2 * dgroups && slots >= 4 * dgroups) dgroups *= 2;
-#ifdef RSSM_DGROUPS  // build-time override for tuning
-  dgroups = RSSM_DGROUPS;
-#endif
   while (dgroups > 1 && (stages < dgroups || slots < dgroups)) dgroups /= 2;
   // Every ring's length must be a multiple of the number of consumers that take
   // its entries in turn. Then the previous use of an entry belongs to the same
@@ -518,7 +515,12 @@ rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* coun
 
 rssm_status rssm_clear_error(rssm_handle h, void* stream) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");
-  const cudaError_t e = cudaMemsetAsync(h->ptrs + h->g.off_err, 0, 4, static_cast<cudaStream_t>(stream));
+  // A launch that gave up on a wait leaves the per-sequence tickets of its
+  // sequences part-counted (the aborted CTA never adds its share), so the
+  // tickets are reset together with the error word.
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(h->ptrs + h->g.off_ticket, 0, (size_t)h->cfg.B * sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->ptrs + h->g.off_err, 0, 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "clear error");
   return RSSM_OK;
 }
@@ -670,16 +672,25 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(RSSM_EUNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   int32_t* tickets = nullptr;
   {
-    // Set-up, once per device with that device current: the host-side name of
-    // the array is not a device address, so ask the runtime for the real one.
+    // The host-side name of the array is not a device address: ask the runtime
+    // for the real one, with the device current. Outside a stream capture this
+    // is done on every call, so a context that was reset and reloaded the
+    // module gets its new address. Inside a capture the address found by an
+    // earlier call on this device is used.
     std::lock_guard<std::mutex> lock(g_static_ticket_mu);
-    if (!g_static_ticket_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
       void* ptr = nullptr;
       e = cudaGetSymbolAddress(&ptr, g_static_tickets);
       if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static tickets)");
       g_static_ticket_addr[dev] = static_cast<int32_t*>(ptr);
+    } else if (!g_static_ticket_addr[dev]) {
+      return fail(RSSM_EINVAL, "the first static-scratch call on device %d must come before any stream capture", dev);
     }
     tickets = g_static_ticket_addr[dev];
   }
@@ -689,7 +700,6 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
   fill_common(h, &pl.p);
   pl.p.ticket = tickets;
   pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The array keeps the last call's contents; the tickets must start at zero.
   e = cudaMemsetAsync(tickets, 0, (size_t)h->cfg.B * sizeof(int32_t), st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static tickets)");

@@ -29,24 +29,15 @@
 
 namespace rssm {
 
-#ifndef RSSM_DOT_WARPS
-#define RSSM_DOT_WARPS 8
-#endif
-#ifndef RSSM_ROWS_PER_WARP
-#define RSSM_ROWS_PER_WARP 8
-#endif
-constexpr int kNDW = RSSM_DOT_WARPS;       // dot warps per CTA (stream the checkpoint tile)
-#ifndef RSSM_COEF_WARPS
-#define RSSM_COEF_WARPS 2
-#endif
-constexpr int kNCoef = RSSM_COEF_WARPS;    // warps computing the per-head decay terms (alternate heads)
+constexpr int kNDW = 8;                    // dot warps per CTA (stream the checkpoint tile)
+constexpr int kNCoef = 2;                  // warps computing the per-head decay terms (alternate heads)
 static_assert((kNCoef & (kNCoef - 1)) == 0, "coefficient warps: a power of two");
 constexpr int kTileWarp = kNDW;            // warp that issues the bulk tile copies
 constexpr int kCoef0 = kNDW + 1;           // first coefficient warp
 constexpr int kGatherWarp = kNDW + 1 + kNCoef;  // warp that gathers the records, keys and queries
 constexpr int kThreads = (kNDW + 2 + kNCoef) * 32;
 constexpr int kMaxSlots = 32;              // largest record-slot ring
-constexpr int kKR = RSSM_ROWS_PER_WARP;    // FP32-tile row-instructions per warp per pass (multiple of 4)
+constexpr int kKR = 8;                     // FP32-tile row-instructions per warp per pass (multiple of 4)
 static_assert(kKR % 4 == 0, "rows per warp must be a multiple of 4");
 constexpr int kTQ = 4;                     // verify queries per pass over the tile
 constexpr int kTMax = 8;                   // largest draft count
@@ -202,26 +193,11 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // Bounded wait on an mbarrier phase. Returns false (after flagging the CTA and
 // the device error word) when the wait runs out or another thread aborted.
-// try_wait with a suspend-time hint: the thread sleeps until the phase completes
-// or about `ns` nanoseconds pass, instead of spinning on issue slots.
-__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
-#ifndef RSSM_WAIT_HINT_NS
-#define RSSM_WAIT_HINT_NS 0  // 0: plain try_wait (the hardware's own suspend limit)
-#endif
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                    uint32_t* err) {
   const unsigned long long t0 = gtimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (RSSM_WAIT_HINT_NS ? mbar_try_sleep(bar, parity, RSSM_WAIT_HINT_NS) : mbar_try(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (gtimer() - t0 > kWaitLimitNs) break;

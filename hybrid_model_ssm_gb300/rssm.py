@@ -16,8 +16,8 @@ from dataclasses import dataclass
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-# The in-tree build; RSSM_LIB may name another build of the same library.
-LIB_PATH = os.environ.get("RSSM_LIB") or os.path.join(_HERE, "librssm.so")
+# The in-tree build (hybrid_model_ssm_gb300.build).
+LIB_PATH = os.path.join(_HERE, "librssm.so")
 
 RSSM_OK, RSSM_EINVAL, RSSM_ECAPACITY, RSSM_ECUDA, RSSM_EUNSUPPORTED, RSSM_ETIMEOUT = range(6)
 STATUS_NAMES = {0: "RSSM_OK", 1: "RSSM_EINVAL", 2: "RSSM_ECAPACITY", 3: "RSSM_ECUDA", 4: "RSSM_EUNSUPPORTED",

@@ -253,7 +253,11 @@ rssm_status rssm_flush(rssm_handle h, int32_t min_count, void* stream);
 rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* count_host,
                                uint32_t* err_host, void* stream);
 
-/* Clear the device error word (asynchronous; library plumbing, no counterpart in the pages). */
+/* Clear the device error word and reset the per-sequence ticket counters of the
+ * pointer block (asynchronous, two memsets on `stream`; library plumbing, no
+ * counterpart in the pages). A launch whose bounded wait expired (bit 4) can
+ * leave the tickets of its sequences part-counted; call this before the next
+ * decode step or flush on the handle, with no launch of the handle in flight. */
 rssm_status rssm_clear_error(rssm_handle h, void* stream);
 
 /* Self-test of the kernels' bounded waits (no counterpart in the paper). It
@@ -278,9 +282,11 @@ const char* rssm_last_error(void);
  * more device memory once decoding runs: a fixed arena planned at start-up, an
  * allocator owned by another component, or a stream being captured.
  *  - B above 8192 returns RSSM_EUNSUPPORTED.
- *  - The first call on a device looks up the array's device address with that
- *    device current (cudaGetSymbolAddress). Make that first call before any
- *    stream capture.
+ *  - Each call outside a stream capture looks up the array's device address
+ *    with the device current (cudaGetSymbolAddress); a call inside a capture
+ *    reuses the address an earlier call found on that device. So make the
+ *    first call on a device before any stream capture (a capture without one
+ *    returns RSSM_EINVAL).
  *  - Each call clears the counters it uses with cudaMemsetAsync on `stream`.
  *    It calls no cudaMalloc or cudaFree.
  *  - Every call shares the one array: calls that overlap on the GPU (other

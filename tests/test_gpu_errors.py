@@ -128,3 +128,31 @@ def test_bounded_wait_expires_and_reports():
     model.decode_step(a, v, k, q)
     assert model.read_pointers()[2] == 0
 
+
+
+def test_clear_error_resets_part_counted_tickets():
+    """A launch that gives up on a wait leaves its sequences' tickets part-counted.
+    The host plants that state (nonzero tickets and the timeout bit) in the pointer
+    block; after rssm_clear_error the next decode steps must advance the pointers
+    exactly as the oracle's bookkeeping does."""
+    require_gpu()
+    from hybrid_model_ssm_gb300.rssm import ERR_TIMEOUT
+    from tests.gpu_helpers import PointerShadow, check_pointers
+
+    shape = S(B=5, H=6, P=16, N=32, G=2, L=3, seed=44)
+    model, gen = _model(shape)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    nb = -(-shape.B * 4 // 256) * 256  # each pointer-block array is 256-byte aligned
+    tickets = model.ptrs[2 * nb: 2 * nb + 4 * shape.B].view(torch.int32)
+    err = model.ptrs[3 * nb: 3 * nb + 4].view(torch.int32)
+    tickets.copy_(torch.tensor([3, 0, 5, 1, 2], dtype=torch.int32, device="cuda"))
+    err.fill_(ERR_TIMEOUT)
+    model.clear_error()
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(tickets).item() == 0 and int(err.item()) == 0
+    for _ in range(2 * shape.L + 1):
+        a, v, k, q = (dev(x) for x in synth.decode_step_inputs(shape, gen))
+        model.decode_step(a, v, k, q)
+        shadow.decode()
+        check_pointers(model, shadow)
+    assert torch.count_nonzero(tickets).item() == 0
