@@ -14,8 +14,11 @@
 #include <mutex>
 #include <string>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/rssm.h"
 #include "rssm_launch.cuh"
+#include "rssm_verify_tc.cuh"
 
 namespace {
 
@@ -38,8 +41,12 @@ rssm_status cuda_fail(cudaError_t e, const char* what) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensor-core verify: used from this many drafts up when the handle qualifies.
+constexpr int kTcAutoMinT = 5;
+
 struct Geom {
   int R = 0, Rp = 0, esize = 0, ck_es = 4, rf = 0;  // ck_es: checkpoint bytes per element; rf: tile format
+  bool tc_ok = false;  // the tensor-core verify serves this configuration
   size_t v_off = 0, k_off = 0, ring_bytes = 0;
   size_t off_count = 0, off_ticket = 0, off_err = 0, off_epoch = 0, off_flist = 0, off_fcount = 0, ptr_bytes = 0;
   size_t head_stride = 0, bsc_off = 0, rsc_off = 0, copy_bytes = 0;
@@ -60,7 +67,17 @@ rssm_status derive(const rssm_config* c, Geom* g) {
   if (c->P % 8) return fail(RSSM_EUNSUPPORTED, "P=%d must be a multiple of 8", c->P);
   if ((size_t)c->P * c->N * 4 > 64 * 1024) return fail(RSSM_EUNSUPPORTED, "P*N*4 > 64 KiB");
   if (c->P > 128) return fail(RSSM_EUNSUPPORTED, "P=%d > 128", c->P);
-  if (c->T_max > rssm::kTMax) return fail(RSSM_EUNSUPPORTED, "T_max=%d > %d", c->T_max, rssm::kTMax);
+  // The tensor-core verify: bf16 inputs, an FP32 checkpoint of the outer-product
+  // recurrence, N in {64, 128}, and 128 checkpoint rows holding whole heads of one group.
+  g->tc_ok = c->in_dtype == RSSM_BF16 && c->ckpt_fmt == RSSM_CKPT_F32 && c->recurrence == RSSM_GATED_OUTER &&
+             (c->N == 64 || c->N == 128) && (c->P == 32 || c->P == 64 || c->P == 128) && c->G > 0 &&
+             c->H % c->G == 0 && (c->H / c->G) % (128 / c->P) == 0;
+  if (c->T_max > rssm::kTcT) return fail(RSSM_EUNSUPPORTED, "T_max=%d > %d", c->T_max, rssm::kTcT);
+  if (c->T_max > rssm::kTMax && !g->tc_ok)
+    return fail(RSSM_EUNSUPPORTED,
+                "T_max=%d > %d needs the tensor-core verify (bf16 inputs, FP32 checkpoint, outer-product recurrence, "
+                "N in {64, 128}, P in {32, 64, 128}, H/G a multiple of 128/P)",
+                c->T_max, rssm::kTMax);
   const int R = c->L + c->T_max - 1;
   if (R > rssm::kRMax) return fail(RSSM_EUNSUPPORTED, "R = L + T_max - 1 = %d > %d", R, rssm::kRMax);
   if (c->read_fmt != RSSM_READ_NONE && c->N < 64)
@@ -212,6 +229,51 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   return RSSM_OK;
 }
 
+// Shared-memory plan of the tensor-core verify for T drafts: 16 KiB K-block
+// stages from the 1024-aligned base, two B operands, record slots, two group
+// areas, the coefficient scratch and the barriers.
+rssm_status plan_tc(const rssm_config* c, const Geom& g, int T, rssm::TcParams* tp, size_t* smem) {
+  using namespace rssm;
+  auto a128 = [](size_t x) { return align_up(x, 128); };
+  const size_t N = c->N, P = c->P, R = g.R, Rp = g.Rp, IH = 128 / P, NKB = N / kTcKB;
+  if (T < 1 || T > kTcT || (size_t)T > R) return fail(RSSM_EINVAL, "T=%d for the tensor-core verify", T);
+  const size_t qop = NKB * 2048;
+  const size_t sv = IH * Rp * 4;
+  const size_t sd = sv + IH * (R - T) * P * 2;
+  const size_t scf = sd + (size_t)T * IH * P * 2;
+  const size_t slot = a128(scf + IH * (size_t)kTcCoefFloats * 4);
+  const size_t gq = R * N * 2;
+  const size_t gb = a128(gq + (size_t)kTcT * N * 2);
+  const size_t wsc = (size_t)kTcCoefWarps * kTcT * kRMax * 4;
+  const size_t bars = a128((3 * (size_t)kTcMaxStages + 3 * (size_t)kTcMaxSlots + 13) * 8);
+  const size_t fixed = 2 * qop + 2 * gb + wsc + bars;
+  if (fixed + NKB * (size_t)kTcStageBytes + 2 * slot > (size_t)kSmemMax)
+    return fail(RSSM_EUNSUPPORTED, "the tensor-core verify does not fit shared memory");
+  const size_t budget = (size_t)kSmemMax - fixed;
+  size_t slots = 4;
+  size_t stages = std::min<size_t>(kTcMaxStages, budget >= slots * slot ? (budget - slots * slot) / kTcStageBytes : 0);
+  if (stages < 2 * NKB) {
+    slots = 2;
+    stages = std::min<size_t>(kTcMaxStages, (budget - slots * slot) / kTcStageBytes);
+  }
+  if (stages < NKB) return fail(RSSM_EUNSUPPORTED, "the tensor-core verify does not fit shared memory");
+  tp->stages = (int)stages;
+  tp->slots = (int)slots;
+  size_t off = stages * kTcStageBytes;
+  tp->qop_off = (int)off; tp->qop_bytes = (int)qop; off += 2 * qop;
+  tp->slot_off = (int)off; tp->slot_bytes = (int)slot; off += slots * slot;
+  tp->sv_off = (int)sv; tp->sd_off = (int)sd; tp->sc_off = (int)scf;
+  tp->gb_off = (int)off; tp->gb_bytes = (int)gb; tp->gq_off = (int)gq; off += 2 * gb;
+  tp->wsc_off = (int)off; off += wsc;
+  off = align_up(off, 16);
+  tp->bar_off = (int)off; off += bars;
+  if (off > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "tensor-core verify plan too large");
+  // more than half of the shared memory: one CTA per SM, so a CTA never waits
+  // for tensor memory held by another CTA of the same kernel
+  *smem = std::max<size_t>(off, (size_t)kSmemMax / 2 + 1024);
+  return RSSM_OK;
+}
+
 // derive() plus a check that every launch of a handle with this configuration
 // fits one CTA's shared memory, so that an unplaceable size is refused when the
 // buffers are sized and the handle is made, not at its first launch.
@@ -221,6 +283,11 @@ rssm_status derive_placed(const rssm_config* c, Geom* g) {
   Plan pl;
   s = plan_smem(c, *g, &pl);
   if (s == RSSM_OK && c->T_max > 1) s = plan_smem(c, *g, &pl, LayoutKind::kVerify);
+  if (s == RSSM_OK && c->T_max > 1 && g->tc_ok) {
+    rssm::TcParams tp{};
+    size_t smem = 0;
+    s = plan_tc(c, *g, c->T_max, &tp, &smem);
+  }
   if (s != RSSM_OK)
     return fail(s, "P=%d N=%d R=%d with %s inputs does not fit one CTA's shared memory (%s)", c->P, c->N, g->R,
                 c->in_dtype == RSSM_F32 ? "f32" : "bf16", g_msg.c_str());
@@ -243,13 +310,15 @@ int sm_count() {
 }  // namespace
 
 struct rssm_ctx {
+  CUtensorMap tmap;  // the checkpoint as rows of N fp32, 32 x P boxes, 128-byte swizzle (tensor-core verify)
   rssm_config cfg;
   Geom g;
   void* ckpt;  // fp32 or fp16 [B,H,P,N]
   uint8_t* ring;
   uint8_t* ptrs;
   uint8_t* copy;
-  int last_T;  // draft count of the last verify, 0 when none is pending
+  int last_T;         // draft count of the last verify, 0 when none is pending
+  int verify_kernel;  // 0 automatic, 1 CUDA cores, 2 tensor cores
 };
 
 namespace {
@@ -278,6 +347,43 @@ void fill_common(const rssm_ctx* h, rssm::Params* p) {
 int persistent_grid(long long heads) {
   const int sms = sm_count();
   return (int)std::max(1ll, std::min<long long>(heads, sms > 0 ? sms : 1));
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The checkpoint [B,H,P,N] fp32 as a 2-D tensor of B*H*P rows of N elements,
+// read in boxes of 32 columns x P rows (one head's K-block) with the 128-byte swizzle.
+rssm_status make_ckpt_tensor_map(const rssm_config* c, void* ckpt, CUtensorMap* out) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(RSSM_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)c->N, (cuuint64_t)c->B * c->H * c->P};
+  const cuuint64_t strides[1] = {(cuuint64_t)c->N * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)c->P};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ckpt, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RSSM_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return RSSM_OK;
+}
+
+// Which verify kernel a launch of T drafts takes: 2 tensor cores, 1 CUDA cores.
+int verify_kernel_for(const rssm_ctx* h, int T) {
+  if (!h->g.tc_ok) return 1;
+  if (h->verify_kernel == 1 && T <= rssm::kTMax) return 1;
+  if (h->verify_kernel == 2) return 2;
+  return (T >= kTcAutoMinT || T > rssm::kTMax) ? 2 : 1;
 }
 
 }  // namespace
@@ -320,12 +426,30 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
 
 rssm_status rssm_launch_plan(const rssm_config* cfg, int32_t kind, rssm_launch_plan_info* out) {
   if (!out) return fail(RSSM_EINVAL, "out is NULL");
-  if (kind < 0 || kind > 2) return fail(RSSM_EINVAL, "kind=%d (0 flush, 1 decode, 2 verify)", kind);
+  if (kind < 0 || kind > 3)
+    return fail(RSSM_EINVAL, "kind=%d (0 flush, 1 decode, 2 verify, 3 tensor-core verify)", kind);
   Geom g;
   rssm_status s = derive(cfg, &g);
   if (s != RSSM_OK) return s;
-  if (kind == 2 && (cfg->T_max < 2 || cfg->recurrence != RSSM_GATED_OUTER))
+  if (kind >= 2 && (cfg->T_max < 2 || cfg->recurrence != RSSM_GATED_OUTER))
     return fail(RSSM_EINVAL, "verify launches need T_max > 1 and the outer-product recurrence");
+  if (kind == 3) {
+    if (!g.tc_ok) return fail(RSSM_EUNSUPPORTED, "this configuration has no tensor-core verify");
+    rssm::TcParams tp{};
+    size_t smem = 0;
+    s = plan_tc(cfg, g, cfg->T_max, &tp, &smem);
+    if (s != RSSM_OK) return s;
+    *out = rssm_launch_plan_info{};
+    out->smem_bytes = (int64_t)smem;
+    out->stages[0] = tp.stages;
+    out->stage_bytes[0] = rssm::kTcStageBytes;
+    out->slots[0] = tp.slots;
+    out->slot_bytes[0] = tp.slot_bytes;
+    out->dgroups[0] = 0;
+    return RSSM_OK;
+  }
+  if (kind == 2 && cfg->T_max > rssm::kTMax)
+    return fail(RSSM_EUNSUPPORTED, "the CUDA-core verify takes at most %d drafts", rssm::kTMax);
   const LayoutKind lk = kind == 0 ? LayoutKind::kGeneral : kind == 1 ? LayoutKind::kNonFlush : LayoutKind::kVerify;
   Plan pl;
   s = plan_smem(cfg, g, &pl, lk);
@@ -365,6 +489,15 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
   h->ptrs = static_cast<uint8_t*>(ptrs);
   h->copy = cfg->read_fmt != RSSM_READ_NONE ? static_cast<uint8_t*>(read_copy) : nullptr;
   h->last_T = 0;
+  h->verify_kernel = 0;
+  std::memset(&h->tmap, 0, sizeof(h->tmap));
+  if (g.tc_ok && cfg->T_max > 1) {
+    s = make_ckpt_tensor_map(cfg, ckpt, &h->tmap);
+    if (s != RSSM_OK) {
+      delete h;
+      return s;
+    }
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ptrs, 0, g.ptr_bytes, st);
   if (e != cudaSuccess) {
@@ -439,6 +572,32 @@ rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void
   if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
+  if (verify_kernel_for(h, T) == 2) {
+    rssm::TcParams tp{};
+    size_t smem = 0;
+    const rssm_status s = plan_tc(&h->cfg, h->g, T, &tp, &smem);
+    if (s != RSSM_OK) return s;
+    const rssm_config& c = h->cfg;
+    tp.B = c.B; tp.H = c.H; tp.G = c.G; tp.L = c.L; tp.R = h->g.R; tp.Rp = h->g.Rp; tp.HPG = c.H / c.G; tp.T = T;
+    tp.alpha = alpha;
+    tp.v = static_cast<const __nv_bfloat16*>(v);
+    tp.k = static_cast<const __nv_bfloat16*>(k);
+    tp.q = static_cast<const __nv_bfloat16*>(q);
+    tp.o = o;
+    tp.ring_a = reinterpret_cast<float*>(h->ring);
+    tp.ring_v = reinterpret_cast<__nv_bfloat16*>(h->ring + h->g.v_off);
+    tp.ring_k = reinterpret_cast<__nv_bfloat16*>(h->ring + h->g.k_off);
+    tp.start = reinterpret_cast<const int32_t*>(h->ptrs);
+    tp.count = reinterpret_cast<const int32_t*>(h->ptrs + h->g.off_count);
+    tp.err = reinterpret_cast<uint32_t*>(h->ptrs + h->g.off_err);
+    const long long items = (long long)c.B * c.H / (128 / c.P);
+    const cudaError_t e = rssm::launch_verify_tc(tp, h->tmap, persistent_grid(items), smem,
+                                                 static_cast<cudaStream_t>(stream), c.N, c.P);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core verify launch");
+    h->last_T = T;
+    return RSSM_OK;
+  }
+  if (T > rssm::kTMax) return fail(RSSM_EUNSUPPORTED, "T=%d > %d needs the tensor-core verify", T, rssm::kTMax);
   Plan pl;
   const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kVerify);
   if (s != RSSM_OK) return s;
@@ -452,6 +611,23 @@ rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void
                                             h->cfg.N, h->cfg.in_dtype, vrf);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   h->last_T = T;
+  return RSSM_OK;
+}
+
+rssm_status rssm_set_verify_kernel(rssm_handle h, int32_t kind) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (kind < 0 || kind > 2) return fail(RSSM_EINVAL, "kind=%d (0 automatic, 1 CUDA cores, 2 tensor cores)", kind);
+  if (kind == 2 && !h->g.tc_ok)
+    return fail(RSSM_EUNSUPPORTED, "this configuration has no tensor-core verify");
+  if (kind == 2 && h->cfg.T_max < 2) return fail(RSSM_EUNSUPPORTED, "T_max = 1: no verify");
+  h->verify_kernel = kind;
+  return RSSM_OK;
+}
+
+rssm_status rssm_get_verify_kernel(rssm_handle h, int32_t T, int32_t* kind) {
+  if (!h || !kind) return fail(RSSM_EINVAL, "NULL argument");
+  if (T < 1 || T > h->cfg.T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, h->cfg.T_max);
+  *kind = verify_kernel_for(h, T);
   return RSSM_OK;
 }
 
@@ -593,6 +769,7 @@ rssm_status rssm_conventional_verify(const rssm_config* cfg, float* states, cons
   g.rf = rssm::kRfNone;
   if (cfg->recurrence != RSSM_GATED_OUTER) return fail(RSSM_EUNSUPPORTED, "the snapshot comparator is outer-product only");
   if (T < 1 || T > cfg->T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, cfg->T_max);
+  if (T > rssm::kTMax) return fail(RSSM_EUNSUPPORTED, "the snapshot comparator takes at most %d drafts", rssm::kTMax);
   if (!states || !cur || !alpha || !v || !k || !q || !o || !err_word) return fail(RSSM_EINVAL, "NULL pointer");
   if (!aligned16(states) || !aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");

@@ -1,6 +1,7 @@
 // rssm_launch.cuh - host-side dispatch from runtime sizes to kernel instantiations.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "rssm_device.cuh"
@@ -84,5 +85,9 @@ cudaError_t launch_commit(int B, int T, int R, const int32_t* accepted, int32_t*
 cudaError_t launch_snap(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
 cudaError_t launch_snap_commit(int B, int T, int nslot, const int32_t* accepted, int32_t* cur, uint32_t* err,
                                cudaStream_t st);
+struct TcParams;
+// Tensor-core verify (bf16 inputs, FP32 checkpoint): N in {64, 128}, P in {32, 64, 128}.
+cudaError_t launch_verify_tc(const TcParams& p, const CUtensorMap& tmap, int grid, size_t smem, cudaStream_t st,
+                             int N, int P);
 
 }  // namespace rssm

@@ -1,0 +1,116 @@
+// rssm_tc.cuh - 5th-generation tensor-core primitives (tcgen05, tensor memory,
+// TMA tensor copies) for sm_103a, written as inline PTX.
+//
+// Conventions used by the verify kernel:
+//  - Operands in shared memory are K-major with the 128-byte swizzle: a row of
+//    32 fp32 (128 B) per matrix row, 8-row atoms of 1024 B, and inside an atom
+//    the 16-byte chunk c of row r stored at chunk c ^ (r % 8). A TMA tensor copy
+//    with the 128-byte swizzle writes exactly this layout, and threads address
+//    it with swz128().
+//  - Tensor memory addresses carry the lane in bits 31..16 and the column in
+//    bits 15..0. An M = 128 accumulator keeps row i in lane i; a warp reaches
+//    only the 32 lanes of its quarter (warp index % 4).
+#pragma once
+
+#include <cstdint>
+
+namespace rssm {
+namespace tc {
+
+// Byte offset of fp32 element (row r, column c) of a K-major, 128-byte swizzled
+// block of 32 columns (rows 128 B apart, 8-row atoms 1024 B apart).
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+  return (uint32_t)(r * 128 + ((((c >> 2) ^ (r & 7)) << 4) | ((c & 3) << 2)));
+}
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte swizzle:
+// start address >> 4 in bits 0..13, leading byte offset (unused for this
+// layout, set to 16 B) in 16..29, stride byte offset (1024 B between 8-row
+// atoms) >> 4 in 32..45, descriptor version 1 in 46..47, base offset 0, and the
+// layout type 2 (128-byte swizzle) in 61..63. The operand block must be 1024-byte
+// aligned; `saddr` may point 32 B steps into it to select the K slice.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+         ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+// Instruction descriptor of a dense kind::tf32 MMA: fp32 accumulator (bits 4..5 =
+// 1), A and B in TF32 (bits 7..9 and 10..12 = 2), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17..22 and M >> 4 in bits 24..28.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- tensor memory
+// Allocate `ncols` columns (a power of two >= 32) for this CTA; the base address
+// is written to shared memory at `dst`. Executed by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+// Free them again (the same warp, the same column count).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Generic-proxy writes to shared memory become visible to the tensor cores and TMA.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 16 consecutive columns of this warp's 32 lanes: thread i writes lane base+i.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 8 consecutive columns of this warp's 32 lanes: thread i reads lane base+i.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- MMA (one thread)
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::tf32.
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)acc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::tf32 (A: row i in lane i, K along the columns).
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p; }" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"((uint32_t)acc)
+      : "memory");
+}
+// The mbarrier at `bar` receives one arrival once every earlier MMA of this thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------- TMA tensor copy
+// 2-D tile of the tensor map at (x = innermost coordinate, y) into shared memory,
+// completing its bytes on `bar`. x * element size must be a multiple of 16 B.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmap_prefetch(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+}  // namespace tc
+}  // namespace rssm

@@ -56,6 +56,8 @@ SIGNATURES = {
     "rssm_decode_step_static_scratch": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_decode_step_delta": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_verify": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_set_verify_kernel": [_vp, ctypes.c_int32],
+    "rssm_get_verify_kernel": [_vp, ctypes.c_int32, _c_i32_p],
     "rssm_commit": [_vp, _vp, _vp],
     "rssm_flush": [_vp, ctypes.c_int32, _vp],
     "rssm_read_pointers": [_vp, _c_i32_p, _c_i32_p, _c_u32_p, _vp],
@@ -159,12 +161,13 @@ def read_copy_layout(shape: LayerShape) -> tuple[int, int, int]:
     return a.value, b.value, d.value
 
 
-LAUNCH_KINDS = {"flush": 0, "decode": 1, "verify": 2}
+LAUNCH_KINDS = {"flush": 0, "decode": 1, "verify": 2, "verify_tc": 3}
+VERIFY_KERNELS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 
 
 def launch_plan(shape: LayerShape, kind: str) -> dict:
-    """Shared-memory plan of a launch kind ("flush", "decode", "verify"): smem bytes
-    and, per layout, stages, stage bytes, slots, slot bytes and dot-warp groups."""
+    """Shared-memory plan of a launch kind ("flush", "decode", "verify", "verify_tc"): smem
+    bytes and, per layout, stages, stage bytes, slots, slot bytes and dot-warp groups."""
     c = shape.config()
     info = LaunchPlanInfo()
     _check(lib().rssm_launch_plan(ctypes.byref(c), LAUNCH_KINDS[kind], ctypes.byref(info)))
@@ -262,6 +265,16 @@ class ReplaySSM:
             _check(lib().rssm_verify(self._h, T, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
                                      _stream_ptr(stream)))
         return out
+
+    def set_verify_kernel(self, kind: str):
+        """Kernel of the verify launches: "auto", "cuda_cores" (T <= 8) or "tensor_cores"."""
+        _check(lib().rssm_set_verify_kernel(self._h, VERIFY_KERNELS[kind]))
+
+    def verify_kernel(self, T: int) -> str:
+        """The kernel a verify of T drafts launches: "cuda_cores" or "tensor_cores"."""
+        k = ctypes.c_int32()
+        _check(lib().rssm_get_verify_kernel(self._h, int(T), ctypes.byref(k)))
+        return {1: "cuda_cores", 2: "tensor_cores"}[k.value]
 
     def commit(self, accepted: torch.Tensor, stream=None):
         _expect(accepted, (self.shape.B,), torch.int32, "accepted", self.ckpt.device)

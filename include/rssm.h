@@ -35,7 +35,10 @@
  * selected per handle by rssm_config.recurrence (see rssm_recurrence).
  *
  * Supported sizes: N in {16, 32, 64, 128}; P a multiple of 8, at most 128;
- * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8. Read copies and
+ * H a multiple of G; R = L + T_max - 1 <= 32; T_max <= 8, or T_max <= 16 for
+ * configurations that the tensor-core verify serves (bf16 inputs, an FP32
+ * checkpoint of the outer-product recurrence, N in {64, 128}, P in {32, 64,
+ * 128} and H/G a multiple of 128/P; see rssm_set_verify_kernel). Read copies and
  * FP16 checkpoints need N in {64, 128}. A delta-rule layer needs N in
  * {64, 128}, an FP32 checkpoint, no read copy and T_max = 1. Every launch
  * keeps two checkpoint tiles, two record slots and two groups' keys and
@@ -162,7 +165,11 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
  *   kind 0: flush and read-copy refresh (layout 0 only);
  *   kind 1: decode (layout 0 for any head, layout 1 for steps in which none of
  *           a CTA's sequences folds; nonflush_layout = 0 when only layout 0 fits);
- *   kind 2: verify (layout 0 only; needs T_max > 1).
+ *   kind 2: verify on the CUDA cores (layout 0 only; needs 1 < T_max <= 8);
+ *   kind 3: verify on the tensor cores at T = T_max (needs T_max > 1 and a
+ *           configuration it serves): stages[0] K-block stages of
+ *           stage_bytes[0] = 16 KiB (32 checkpoint columns of 128 rows),
+ *           slots[0] record slots of slot_bytes[0], dgroups[0] = 0.
  * Per layout: checkpoint tile stages (stage_bytes each), record slots
  * (slot_bytes each) and the number of dot-warp groups, i.e. heads in flight.
  * Both ring lengths are multiples of the number of consumers that take their
@@ -222,9 +229,28 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
  * Verify reads the checkpoint itself (FP32, or FP16 with an FP16 ckpt_fmt),
  * never the read copy. A sequence with c + T > R sets RSSM_ECAPACITY and is
  * skipped. T outside 1..T_max returns RSSM_EINVAL; a delta-rule handle returns
- * RSSM_EUNSUPPORTED. */
+ * RSSM_EUNSUPPORTED.
+ * Two kernels compute it (rssm_set_verify_kernel chooses; by default the
+ * tensor-core one from 5 drafts up where it applies, the CUDA-core one below):
+ *  - CUDA cores: FP32 FMAs over the checkpoint tile, T <= 8.
+ *  - Tensor cores: S_ckpt Q as kind::tf32 MMAs (tcgen05, accumulator in tensor
+ *    memory) with the checkpoint split into hi (its top 11 significant bits,
+ *    exact in TF32) and lo = S - hi, each multiplied by the exact bf16 queries:
+ *    about 5e-7 relative error against the FP32 product, T <= 16. The value
+ *    term V (W ⊙ K^T Q) stays on the CUDA cores in FP32. */
 rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k,
                         const void* q, float* o, void* stream);
+
+/* Choose the kernel of this handle's verify launches (library control, no
+ * counterpart in the pages): 0 automatic (the default), 1 the CUDA cores (for
+ * T <= 8; more drafts still take the tensor cores), 2 the tensor cores.
+ * RSSM_EUNSUPPORTED for 2 on a configuration the tensor-core verify does not
+ * serve (see the supported sizes above) or with T_max = 1. Host only. */
+rssm_status rssm_set_verify_kernel(rssm_handle h, int32_t kind);
+
+/* The kernel (1 CUDA cores, 2 tensor cores) that a verify of T drafts on this
+ * handle launches, into *kind (host only; RSSM_EINVAL for T outside 1..T_max). */
+rssm_status rssm_get_verify_kernel(rssm_handle h, int32_t T, int32_t* kind);
 
 /* Commit the accepted prefix of the last verify: count[b] += accepted[b]
  * (aikraft.ru page §05; records past the pointer are ignored and later

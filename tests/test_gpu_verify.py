@@ -27,12 +27,20 @@ VERIFY_CASES = [
 ]
 
 
-def run_verify_parity(shape: synth.Shape, rounds: int, decode_every: int = 3, vary_T: bool = True):
+def run_verify_parity(shape: synth.Shape, rounds: int, decode_every: int = 3, vary_T: bool = True,
+                      verify_kernel: str = "auto", check_ring: bool = False):
+    """Rounds of (decode every few rounds,) verify, commit and flush against the oracle.
+
+    verify_kernel picks the verify launches' kernel ("auto", "cuda_cores",
+    "tensor_cores"). check_ring also checks, after every verify, that the drafts'
+    decays, values and keys sit in the ring slots after the committed records, bit for bit.
+    """
     require_gpu()
     gen = synth.make_generator(shape.seed)
     S0 = synth.initial_state(shape, gen)
     orc = oracle.ReplayOracle(f64(S0), L=shape.L, R=shape.R, G=shape.G)
     model = ReplaySSM(layer_shape(shape), dev(S0))
+    model.set_verify_kernel(verify_kernel)
     for r in range(rounds):
         if decode_every and r % decode_every == 0:
             a, v, k, q = synth.decode_step_inputs(shape, gen)
@@ -45,6 +53,13 @@ def run_verify_parity(shape: synth.Shape, rounds: int, decode_every: int = 3, va
         O_ref = orc.verify(f64(a), f64(v), f64(k), f64(q))
         e = slice_rel_err(O, O_ref, 1)
         assert e <= REL_TOL, f"round {r}: verify rel err {e:.3g}"
+        if check_ring:
+            ra, rv, rk = (x.cpu() for x in model.ring_views())
+            for b in range(shape.B):
+                slots = [(int(orc.start[b]) + int(orc.count[b]) + t) % shape.R for t in range(T)]
+                assert torch.equal(ra[b][:, slots], a[b].T), f"round {r} seq {b}: draft decays in the ring"
+                assert torch.equal(rv[b][:, slots], v[b].transpose(0, 1)), f"round {r} seq {b}: draft values"
+                assert torch.equal(rk[b][:, slots], k[b].transpose(0, 1)), f"round {r} seq {b}: draft keys"
         acc = synth.accepted_lengths(shape.B, T, gen)
         ck_before = model.ckpt.clone()
         model.commit(dev(acc))
