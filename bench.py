@@ -579,7 +579,7 @@ def secondary_arms(args, world, rank, local) -> dict:
     vargs.min_seconds = args.extra_seconds
     v = run_verify(vargs, world, rank, local, print_line=False)
     if v is not None:
-        out["verify_b512_t4"] = {k: v[k] for k in ("metric", "value", "unit", "ms_per_step", "roofline",
+        out["verify_b512_t4"] = {k: v[k] for k in ("metric", "value", "unit", "ms_per_step", "verify_kernel", "roofline",
                                                   "breakdown_ms_per_round", "comparison", "gpu_launches",
                                                   "device_error_word") if k in v}
         out["verify_b512_t4"]["rounds_timed"] = v["config"]["rounds_timed"]
@@ -665,6 +665,8 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     gen = torch.Generator(device=dev)
     gen.manual_seed(s.seed + 1000 * rank)
     model = ReplaySSM(ls, torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev) * 0.1)
+    model.set_verify_kernel(args.verify_kernel)
+    vkernel = model.verify_kernel(T)
     sc = 1.0 / math.sqrt(s.N)
     pool = []
     for _ in range(8):
@@ -739,7 +741,7 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     # in-run comparison: conventional verify with per-draft snapshots (one state
     # read and T writes per round, commit by slot index), same inputs and accepts
     comp = None
-    if not args.no_conventional:
+    if not args.no_conventional and T <= 8:  # the snapshot comparator takes at most 8 drafts
         del model
         torch.cuda.empty_cache()
         conv = ConventionalVerifier(ls, torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev) * 0.1)
@@ -786,7 +788,9 @@ def run_verify(args, world, rank, local, print_line: bool = True):
                    "global_batch": s.B * world, "l2": "no flush needed: 2 GiB checkpoint per replica",
                    "rounds_timed": n_rounds},
         "seq_rounds_per_s": world * s.B * n_rounds / elapsed,
-        "roofline": {"bound": "hbm", "kernel": "verify", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "verify_kernel": vkernel,
+        "roofline": {"bound": "hbm", "kernel": f"verify ({vkernel.replace('_', ' ')})", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": (profiled_traffic(f"verify_b512_t{T}") if args.batch is None else None),
                      "algorithmic_bytes_per_launch": vbytes / n_rounds,
@@ -937,9 +941,12 @@ def main(argv=None):
     ap.add_argument("--ckpt", choices=["f32", "f16_sr", "f16_rn"], default="f32",
                     help="checkpoint storage: FP32, or FP16 stored with stochastic / nearest rounding")
     ap.add_argument("--drafts", type=int, default=None,
-                    help="verify: drafts per round T (1..8; default 4); other values are not the headline config")
+                    help="verify: drafts per round T (1..16; default 4); other values are not the headline config")
     ap.add_argument("--recurrence", choices=["outer", "delta"], default="outer",
                     help="decode: the gated outer-product recurrence or the gated delta rule (beta inputs)")
+    ap.add_argument("--verify-kernel", choices=["auto", "cuda_cores", "tensor_cores"], default="auto",
+                    help="verify: the kernel of the verify launches (auto: CUDA cores up to 8 drafts, tensor "
+                         "cores above)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="the timed region covers at least this long (and at least --steps steps)")
     ap.add_argument("--extra-seconds", type=float, default=0.3,

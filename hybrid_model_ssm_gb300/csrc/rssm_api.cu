@@ -41,8 +41,9 @@ rssm_status cuda_fail(cudaError_t e, const char* what) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Tensor-core verify: used from this many drafts up when the handle qualifies.
-constexpr int kTcAutoMinT = 5;
+// Tensor-core verify: used by default from this many drafts up (more than the
+// CUDA-core verify takes); below it the CUDA-core verify measures faster.
+constexpr int kTcAutoMinT = 9;
 
 struct Geom {
   int R = 0, Rp = 0, esize = 0, ck_es = 4, rf = 0;  // ck_es: checkpoint bytes per element; rf: tile format
@@ -245,7 +246,7 @@ rssm_status plan_tc(const rssm_config* c, const Geom& g, int T, rssm::TcParams* 
   const size_t gq = R * N * 2;
   const size_t gb = a128(gq + (size_t)kTcT * N * 2);
   const size_t wsc = (size_t)kTcCoefWarps * kTcT * kRMax * 4;
-  const size_t bars = a128((3 * (size_t)kTcMaxStages + 3 * (size_t)kTcMaxSlots + 13) * 8);
+  const size_t bars = a128((3 * (size_t)kTcMaxStages + 3 * (size_t)kTcMaxSlots + 15) * 8);
   const size_t fixed = 2 * qop + 2 * gb + wsc + bars;
   if (fixed + NKB * (size_t)kTcStageBytes + 2 * slot > (size_t)kSmemMax)
     return fail(RSSM_EUNSUPPORTED, "the tensor-core verify does not fit shared memory");

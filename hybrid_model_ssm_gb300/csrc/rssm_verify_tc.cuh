@@ -88,15 +88,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* const smem = tc_smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   // tfull, tempty, sdone [kTcMaxStages]; sfull, scoef, sempty [kTcMaxSlots]; dfull[2],
-  // gfull[2], gempty[2], qfull[2], qempty[2], drain; then the abort flag and the
-  // tensor-memory base address
+  // gfull[2], gempty[2], qfull[2], qempty[2], kqdone[2], drain; then the abort flag
+  // and the tensor-memory base address
   const uint32_t tfull0 = smem_u32(bars), tempty0 = tfull0 + 8 * kTcMaxStages, sdone0 = tempty0 + 8 * kTcMaxStages;
   const uint32_t sfull0 = sdone0 + 8 * kTcMaxStages, scoef0 = sfull0 + 8 * kTcMaxSlots;
   const uint32_t sempty0 = scoef0 + 8 * kTcMaxSlots, dfull0 = sempty0 + 8 * kTcMaxSlots;
   const uint32_t gfull0 = dfull0 + 16, gempty0 = gfull0 + 16, qfull0 = gempty0 + 16, qempty0 = qfull0 + 16;
-  const uint32_t drain_bar = qempty0 + 16;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kTcMaxStages + 3 * kTcMaxSlots + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kTcMaxStages + 3 * kTcMaxSlots + 12);
+  const uint32_t kqdone0 = qempty0 + 16, drain_bar = kqdone0 + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kTcMaxStages + 3 * kTcMaxSlots + 13);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kTcMaxStages + 3 * kTcMaxSlots + 14);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(tfull0 + 8 * s, 1);
       mbar_init(tempty0 + 8 * s, 1);             // the MMA commit
-      mbar_init(sdone0 + 8 * s, kTcRowWarps);
+      mbar_init(sdone0 + 8 * s, 4);              // the four row warps (one per lane quarter) of its K-block
     }
     for (int s = 0; s < p.slots; ++s) {
       mbar_init(sfull0 + 8 * s, 1);
@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(gempty0 + 8 * s, kTcCoefWarps);
       mbar_init(qfull0 + 8 * s, 1);
       mbar_init(qempty0 + 8 * s, 1);
+      mbar_init(kqdone0 + 8 * s, kTcCoefWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -322,7 +323,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= kTcCoef0) {
     // ====================================================================== coefficient warps
     const int cwi = warp - kTcCoef0;
-    float* skq = reinterpret_cast<float*>(smem + p.wsc_off) + cwi * kTcT * kRMax;  // [t][j] k_j^T q_t
+    float* const skq0 = reinterpret_cast<float*>(smem + p.wsc_off);  // [2 groups][t][j] k_j^T q_t, shared
+    const float* skq = skq0;
     int li = 0, gi = 0, cur_b = -1, c = 0, st = 0;
     long long cur_gg = -1;
     bool load = false;
@@ -344,20 +346,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!__all_sync(kFull, mbar_wait(gfull0 + 8 * gs, (gi >> 1) & 1, abort_flag, p.err))) { ok = false; break; }
         const uint8_t* gK = smem + p.gb_off + gs * p.gb_bytes;
         const uint8_t* gQ = gK + p.gq_off;
-        // k_j^T q_t, one (j, t) pair per lane, N/4 chunks from a lane-dependent start
-        const int npair = J * p.T;
-        for (int pr = lane; pr < npair; pr += 32) {
-          const int t = pr / J, j = pr - t * J;
-          float acc = 0.f;
-#pragma unroll 8
-          for (int i = 0; i < N / 4; ++i) {
-            const int c4 = (i + lane) & (N / 4 - 1);
-            acc += dot4(In<__nv_bfloat16>::lds4(gK, j * N + 4 * c4), In<__nv_bfloat16>::lds4(gQ, t * N + 4 * c4));
-          }
-          skq[t * kRMax + j] = acc;
-        }
         if (cwi == 0) {
-          // the queries as the MMA's B operand: fp32 (exact from bf16), [kTcT x N], K-major swizzled
+          // first the queries as the MMA's B operand: fp32 (exact from bf16), [kTcT x N], K-major swizzled
           if (gi >= 2 && !__all_sync(kFull, mbar_wait(qempty0 + 8 * gs, ((gi >> 1) - 1) & 1, abort_flag, p.err))) {
             ok = false;
             break;
@@ -379,7 +369,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bulk_commit();
           }
         }
+        // k_j^T q_t, the two warps taking alternate (j, t) pairs, N/4 chunks from a lane-dependent start
+        float* kq = skq0 + gs * kTcT * kRMax;
+        const int npair = J * p.T;
+        for (int pr = cwi * 32 + lane; pr < npair; pr += 32 * kTcCoefWarps) {
+          const int t = pr / J, j = pr - t * J;
+          float acc = 0.f;
+#pragma unroll 8
+          for (int i = 0; i < N / 4; ++i) {
+            const int c4 = (i + lane) & (N / 4 - 1);
+            acc += dot4(In<__nv_bfloat16>::lds4(gK, j * N + 4 * c4), In<__nv_bfloat16>::lds4(gQ, t * N + 4 * c4));
+          }
+          kq[t * kRMax + j] = acc;
+        }
         __syncwarp();
+        if (lane == 0) mbar_arrive(kqdone0 + 8 * gs);
+        if (!__all_sync(kFull, mbar_wait(kqdone0 + 8 * gs, (gi >> 1) & 1, abort_flag, p.err))) { ok = false; break; }
+        skq = kq;
         ++gi;
       }
       const int sl = li % p.slots;
@@ -444,13 +450,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int t0 = 8 * half;
       float acc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = (t0 + i < p.T) ? sc[t0 + i] * __uint_as_float(dv[i]) : 0.f;
-      for (int jj = 0; jj < J; ++jj) {
-        const float vj = jj < pc ? In<__nv_bfloat16>::lds(svh, jj * P + pr)
-                                 : In<__nv_bfloat16>::lds(sdr, (jj - pc) * IH * P + pr);
-        const float* w = sc + kTcT + t0 * kRMax + jj;
+      for (int i = 0; i < 8; ++i) acc[i] = sc[t0 + i] * __uint_as_float(dv[i]);
+      // value term: records in fours, each weight row of a query read as float4
+      // (the weights past c + t are zero, and records past J read as zero)
+      for (int j0 = 0; j0 < J; j0 += 4) {
+        float v4[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[i * kRMax], vj, acc[i]);
+        for (int u = 0; u < 4; ++u) {
+          const int jj = j0 + u;
+          v4[u] = jj >= J ? 0.f
+                  : jj < pc ? In<__nv_bfloat16>::lds(svh, jj * P + pr)
+                            : In<__nv_bfloat16>::lds(sdr, (jj - pc) * IH * P + pr);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 w = *reinterpret_cast<const float4*>(sc + kTcT + (t0 + i) * kRMax + j0);
+          acc[i] = fmaf(w.x, v4[0], fmaf(w.y, v4[1], fmaf(w.z, v4[2], fmaf(w.w, v4[3], acc[i]))));
+        }
       }
       const size_t hh = (size_t)phh + hj;
 #pragma unroll
@@ -474,33 +490,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       item_of(it, b, hh0, g);
       if (b != cur_b) { cur_b = b; seq_plan(b, c, st, load); }
       if (!load) continue;
-      // ---- split: hi back in place, lo into this item's tensor-memory buffer
+      // ---- split: hi back in place, lo into this item's tensor-memory buffer. The
+      // four warps of a half take K-blocks half, half + 2, ...: whole 128-byte rows,
+      // one 32-column store to tensor memory each, one fence sequence per item.
       const uint32_t lo0 = tbase + tl + (uint32_t)(ii & 1) * 256u;
-      for (int kb = 0; kb < NKB; ++kb, ++li) {
-        const int s = li % p.stages;
-        if (!__all_sync(kFull, mbar_wait(tfull0 + 8 * s, (li / p.stages) & 1, abort_flag, p.err))) { ok = false; break; }
+      for (int kb = half; kb < NKB; kb += 2) {
+        const int lk = li + kb, s = lk % p.stages;
+        if (!__all_sync(kFull, mbar_wait(tfull0 + 8 * s, (lk / p.stages) & 1, abort_flag, p.err))) { ok = false; break; }
         uint8_t* tile = smem + (size_t)s * kTcStageBytes + row * 128;
-        uint32_t lo[16];
+        uint32_t lo[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = 4 * half + i;
+        for (int ch = 0; ch < 8; ++ch) {
           uint4* ptr = reinterpret_cast<uint4*>(tile + ((ch ^ (row & 7)) << 4));
-          uint4 x = *ptr;
-          uint4 h = make_uint4(x.x & 0xFFFFE000u, x.y & 0xFFFFE000u, x.z & 0xFFFFE000u, x.w & 0xFFFFE000u);
+          const uint4 x = *ptr;
+          const uint4 h = make_uint4(x.x & 0xFFFFE000u, x.y & 0xFFFFE000u, x.z & 0xFFFFE000u, x.w & 0xFFFFE000u);
           *ptr = h;
-          lo[4 * i + 0] = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(h.x));
-          lo[4 * i + 1] = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(h.y));
-          lo[4 * i + 2] = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(h.z));
-          lo[4 * i + 3] = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(h.w));
+          lo[4 * ch + 0] = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(h.x));
+          lo[4 * ch + 1] = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(h.y));
+          lo[4 * ch + 2] = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(h.z));
+          lo[4 * ch + 3] = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(h.w));
         }
-        tc::tmem_st16(lo0 + kb * kTcKB + 16 * half, lo);
-        tc::tmem_st_wait();
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sdone0 + 8 * s);
+        tc::tmem_st32(lo0 + kb * kTcKB, lo);
       }
       if (!ok) break;
+      tc::tmem_st_wait();
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0)
+        for (int kb = half; kb < NKB; kb += 2) mbar_arrive(sdone0 + 8 * ((li + kb) % p.stages));
+      li += NKB;
       // ---- the previous item's epilogue (its MMAs ran while this item was split)
       if (pend && !epilogue()) { ok = false; break; }
       pend = true;

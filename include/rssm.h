@@ -231,7 +231,7 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
  * skipped. T outside 1..T_max returns RSSM_EINVAL; a delta-rule handle returns
  * RSSM_EUNSUPPORTED.
  * Two kernels compute it (rssm_set_verify_kernel chooses; by default the
- * tensor-core one from 5 drafts up where it applies, the CUDA-core one below):
+ * CUDA-core one up to 8 drafts and the tensor-core one above, where it applies):
  *  - CUDA cores: FP32 FMAs over the checkpoint tile, T <= 8.
  *  - Tensor cores: S_ckpt Q as kind::tf32 MMAs (tcgen05, accumulator in tensor
  *    memory) with the checkpoint split into hi (its top 11 significant bits,
