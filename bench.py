@@ -15,10 +15,11 @@ Prints one JSON line. Keys beyond the driver contract:
   e2e           the same metric with inputs copied from pinned host memory and
                 outputs copied back inside the timed region
   comparison    the conventional read-update-write kernel on the same workload
-  verify_b512_t4, read_copy_e4m3, read_copy_e2m1, delta_rule
+  verify_b512_t4, delta_verify_b512_t4, read_copy_e4m3, read_copy_e2m1, delta_rule
                 the secondary arms of the path, each with its own roofline
                 block: speculative rounds (verify + commit + flush, B=512,
-                T=4) against the snapshot comparator, decode windows reading
+                T=4) against the snapshot comparator, the same rounds of a
+                gated delta-rule layer, decode windows reading
                 an E4M3 or E2M1 copy of the checkpoint, and decode windows of
                 a gated delta-rule layer of the same shape
 
@@ -577,12 +578,15 @@ def secondary_arms(args, world, rank, local) -> dict:
     vargs = argparse.Namespace(**vars(args))
     vargs.batch, vargs.drafts = None, None
     vargs.min_seconds = args.extra_seconds
-    v = run_verify(vargs, world, rank, local, print_line=False)
-    if v is not None:
-        out["verify_b512_t4"] = {k: v[k] for k in ("metric", "value", "unit", "ms_per_step", "verify_kernel", "roofline",
-                                                  "breakdown_ms_per_round", "comparison", "gpu_launches",
-                                                  "device_error_word") if k in v}
-        out["verify_b512_t4"]["rounds_timed"] = v["config"]["rounds_timed"]
+    for key, rec in (("verify_b512_t4", "outer"), ("delta_verify_b512_t4", "delta")):
+        vargs.recurrence = rec
+        v = run_verify(vargs, world, rank, local, print_line=False)
+        torch.cuda.empty_cache()
+        if v is not None:
+            out[key] = {k: v[k] for k in ("metric", "value", "unit", "ms_per_step", "verify_kernel", "roofline",
+                                          "breakdown_ms_per_round", "comparison", "gpu_launches",
+                                          "device_error_word") if k in v}
+            out[key]["rounds_timed"] = v["config"]["rounds_timed"]
     for key, kw in (("read_copy_e4m3", {"read_fmt": "e4m3"}), ("read_copy_e2m1", {"read_fmt": "e2m1"}),
                     ("delta_rule", {"recurrence": "delta"})):
         arm = DecodeArm(WORKLOAD, local, rank, **kw)
@@ -630,19 +634,20 @@ VERIFY_WORKLOAD = synth.PRESETS["mamba2_verify_b512_t4"]
 VERIFY_METRIC = "speculative verify draft-tokens/s at B=512, T=4, L=16 (verify + commit + flush per round)"
 
 
-def verify_round_bytes(s, T: int, counts: np.ndarray, accepted: np.ndarray):
+def verify_round_bytes(s, T: int, counts: np.ndarray, accepted: np.ndarray, delta: bool = False):
     """Algorithmic HBM bytes of one speculative round for the whole batch.
 
     verify: per sequence |S| + c|r| + T(|in| + |r| + |o|): the checkpoint once, the
     c committed records, the T drafts' records and queries, T outputs and the T
     appended records. commit: 12 B per sequence. flush: every sequence that
-    reaches L records reads |S| and its c records and writes |S| once.
-    Returns (verify_bytes, flush_bytes, counts_after).
+    reaches L records reads |S| and its c records and writes |S| once. A
+    delta-rule layer's ring records hold the fp32 pseudo-value w in place of v,
+    and its inputs carry beta. Returns (verify_bytes, flush_bytes, counts_after).
     """
     es = 2 if s.in_dtype == "bf16" else 4
     S = 4 * s.H * s.P * s.N
-    r = record_bytes(s)
-    inp = r + es * s.G * s.N
+    r = 4 * s.H + (4 if delta else es) * s.H * s.P + es * s.G * s.N  # a ring record
+    inp = record_bytes(s, delta) + es * s.G * s.N                    # a draft's inputs
     out = 4 * s.H * s.P
     vb = int(np.sum(S + counts * r + T * (inp + r + out)))
     c2 = counts + accepted
@@ -659,7 +664,9 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     if args.drafts is not None:
         s = s.with_(T_max=args.drafts)
     T = s.T_max
-    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=T, in_dtype=s.in_dtype)
+    delta = args.recurrence == "delta"
+    ls = LayerShape(B=s.B, H=s.H, P=s.P, N=s.N, G=s.G, L=s.L, T_max=T, in_dtype=s.in_dtype,
+                    recurrence=args.recurrence)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev)
@@ -671,10 +678,16 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     pool = []
     for _ in range(8):
         u = torch.randn((s.B, T, s.H), generator=gen, device=dev)
-        pool.append((torch.exp(-torch.nn.functional.softplus(u)).float(),
-                     (torch.randn((s.B, T, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
-                     (torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype),
-                     (torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)))
+        a = torch.exp(-torch.nn.functional.softplus(u)).float()
+        v = (torch.randn((s.B, T, s.H, s.P), generator=gen, device=dev) * sc).to(ls.torch_in_dtype)
+        k = torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc
+        q = torch.randn((s.B, T, s.G, s.N), generator=gen, device=dev) * sc
+        if delta:  # write strengths in (0, 1); unit-norm keys and queries
+            beta = torch.sigmoid(torch.randn((s.B, T, s.H), generator=gen, device=dev)).float()
+            k, q = k / k.norm(dim=-1, keepdim=True), q / q.norm(dim=-1, keepdim=True)
+            pool.append((a, v, k.to(ls.torch_in_dtype), q.to(ls.torch_in_dtype), beta))
+        else:
+            pool.append((a, v, k.to(ls.torch_in_dtype), q.to(ls.torch_in_dtype)))
     cgen = synth.make_generator(s.seed + 7)
     acc_host: list = []
     acc_dev: list = []
@@ -687,10 +700,10 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=dev)
 
     def one_round(i, ev=None):
-        a, v, k, q = pool[i % len(pool)]
+        x = pool[i % len(pool)]
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if ev is not None else None
         if e: e[0].record(stream)
-        model.verify(a, v, k, q, out=out)
+        model.verify(*x[:4], out=out, beta=x[4] if delta else None)
         if e: e[1].record(stream)
         model.commit(acc_dev[i])
         if e: e[2].record(stream)
@@ -704,7 +717,7 @@ def run_verify(args, world, rank, local, print_line: bool = True):
         if i == 1:
             w0.record(stream)
         one_round(i)
-        _, _, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64))
+        _, _, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64), delta)
     w1.record(stream)
     torch.cuda.synchronize()
     model.read_pointers()
@@ -715,7 +728,7 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     ev = []
     vbytes = fbytes = 0
     for i in range(args.warmup, rounds):
-        vb, fb, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64))
+        vb, fb, counts = verify_round_bytes(s, T, counts, acc_host[i].numpy().astype(np.int64), delta)
         vbytes += vb
         fbytes += fb
     barrier(world)
@@ -741,7 +754,7 @@ def run_verify(args, world, rank, local, print_line: bool = True):
     # in-run comparison: conventional verify with per-draft snapshots (one state
     # read and T writes per round, commit by slot index), same inputs and accepts
     comp = None
-    if not args.no_conventional and T <= 8:  # the snapshot comparator takes at most 8 drafts
+    if not args.no_conventional and T <= 8 and not delta:  # the snapshot comparator: outer product, T <= 8
         del model
         torch.cuda.empty_cache()
         conv = ConventionalVerifier(ls, torch.randn((s.B, s.H, s.P, s.N), generator=gen, device=dev) * 0.1)
@@ -782,7 +795,8 @@ def run_verify(args, world, rank, local, print_line: bool = True):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed / n_rounds * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"ReplaySSM speculative round: B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
+        "config": {"workload": f"ReplaySSM speculative round{' (gated delta-rule layer)' if delta else ''}: "
+                               f"B={s.B} H={s.H} P={s.P} N={s.N} G={s.G} L={s.L} "
                                f"T={T}, bf16 inputs; one step = verify + commit (seeded accepted lengths "
                                f"0..{T}) + flush of sequences at {s.L} records",
                    "global_batch": s.B * world, "l2": "no flush needed: 2 GiB checkpoint per replica",
@@ -792,7 +806,8 @@ def run_verify(args, world, rank, local, print_line: bool = True):
         "roofline": {"bound": "hbm", "kernel": f"verify ({vkernel.replace('_', ' ')})", "achieved": achieved,
                      "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": (profiled_traffic(f"verify_b512_t{T}") if args.batch is None else None),
+                     "traffic": (profiled_traffic(f"{'delta_' if delta else ''}verify_b512_t{T}")
+                                 if args.batch is None else None),
                      "algorithmic_bytes_per_launch": vbytes / n_rounds,
                      "mean_launch_ms": tv / n_rounds * 1e3},
         "breakdown_ms_per_round": {"verify": tv / n_rounds * 1e3, "commit": tc / n_rounds * 1e3,
@@ -954,8 +969,8 @@ def main(argv=None):
     ap.add_argument("--no-extras", action="store_true",
                     help="leave out the secondary arms (verify, read copies, delta rule) of the default line")
     args = ap.parse_args(argv)
-    if args.recurrence == "delta" and (args.workload != "decode" or args.read_fmt or args.ckpt != "f32"):
-        ap.error("--recurrence delta: decode workload, FP32 checkpoint, no read copy")
+    if args.recurrence == "delta" and (args.workload == "multilayer" or args.read_fmt or args.ckpt != "f32"):
+        ap.error("--recurrence delta: decode or verify workload, FP32 checkpoint, no read copy")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

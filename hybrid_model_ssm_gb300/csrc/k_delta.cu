@@ -1,6 +1,6 @@
 // Instantiations of the head kernel for gated delta-rule layers (FP32
-// checkpoint, N in {64, 128}): the decode step, the standalone flush and the
-// conventional read-update-write step used for comparison.
+// checkpoint, N in {64, 128}): the decode step, the speculative verify, the
+// standalone flush and the conventional read-update-write step used for comparison.
 #include "rssm_launch.cuh"
 
 namespace rssm {
@@ -15,6 +15,8 @@ cudaError_t launch_delta(int mode, const Params& p, int grid, size_t smem, cudaS
                                          : delta_n<kDecode, __nv_bfloat16>(p, grid, smem, st, N);
   if (mode == kFlush) return dtype == 0 ? delta_n<kFlush, float>(p, grid, smem, st, N)
                                         : delta_n<kFlush, __nv_bfloat16>(p, grid, smem, st, N);
+  if (mode == kVerify) return dtype == 0 ? delta_n<kVerify, float>(p, grid, smem, st, N)
+                                         : delta_n<kVerify, __nv_bfloat16>(p, grid, smem, st, N);
   if (mode == kConv) return dtype == 0 ? delta_n<kConv, float>(p, grid, smem, st, N)
                                        : delta_n<kConv, __nv_bfloat16>(p, grid, smem, st, N);
   return cudaErrorInvalidValue;

@@ -17,6 +17,7 @@ __global__ void commit_kernel(int B, int T, int R, const int32_t* __restrict__ a
 }
 
 cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf) {
+  if (rf == kDelta) return launch_delta(kVerify, p, grid, smem, st, N, dtype);
   return dtype == 0 ? dispatch_n<kVerify, float>(p, grid, smem, st, N, rf)
                     : dispatch_n<kVerify, __nv_bfloat16>(p, grid, smem, st, N, rf);
 }

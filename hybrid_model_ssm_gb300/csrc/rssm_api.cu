@@ -41,6 +41,9 @@ rssm_status cuda_fail(cudaError_t e, const char* what) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Delta-rule layers verify at most this many drafts (2 T vectors per row).
+constexpr int kDeltaTMax = 4;
+
 // Tensor-core verify: used by default from this many drafts up (more than the
 // CUDA-core verify takes); below it the CUDA-core verify measures faster.
 constexpr int kTcAutoMinT = 9;
@@ -89,8 +92,9 @@ rssm_status derive(const rssm_config* c, Geom* g) {
   if (c->recurrence != RSSM_GATED_OUTER && c->recurrence != RSSM_GATED_DELTA)
     return fail(RSSM_EINVAL, "recurrence %d", c->recurrence);
   if (c->recurrence == RSSM_GATED_DELTA &&
-      (c->N < 64 || c->read_fmt != RSSM_READ_NONE || c->ckpt_fmt != RSSM_CKPT_F32 || c->T_max != 1))
-    return fail(RSSM_EUNSUPPORTED, "a delta-rule layer needs N in {64, 128}, an FP32 checkpoint, no read copy and T_max = 1");
+      (c->N < 64 || c->read_fmt != RSSM_READ_NONE || c->ckpt_fmt != RSSM_CKPT_F32 || c->T_max > kDeltaTMax))
+    return fail(RSSM_EUNSUPPORTED,
+                "a delta-rule layer needs N in {64, 128}, an FP32 checkpoint, no read copy and T_max <= %d", kDeltaTMax);
   if ((long long)c->B * c->H > (1ll << 30)) return fail(RSSM_EUNSUPPORTED, "B*H too large");
   g->R = R;
   g->Rp = (R + 3) / 4 * 4;
@@ -154,13 +158,16 @@ rssm_status plan_layout(const rssm_config* c, const Geom& g, LayoutKind kind, si
   const bool delta = g.rf == rssm::kDelta;
   const size_t sv_off = (size_t)(kRMax + kTMax) * 4 * (delta ? 2 : 1);
   const size_t nv_off = sv_off + vrows * P * (delta ? 4 : es);
-  const size_t sc_off = align_up(nv_off + (delta ? P * es : 0), 16);
+  const size_t sc_off = align_up(nv_off + (delta ? (size_t)c->T_max * P * es : 0), 16);
   // coefficients: 16 scalars, then the record weights [kRMax] (non-flush),
   // [kTMax][kRMax] (verify), or the fold's scaled values [R][P] (general, which
   // also serves non-flush heads). Delta layers: 16 scalars, the output weights
   // and the new record's couplings [kRMax] each, then (general) the fold's
   // scaled values [R][P].
-  const size_t sc_floats = delta ? 16 + 2 * (size_t)kRMax + (nf ? 0 : R * P)
+  // Delta-rule verify: 16 scalars, the committed weights [kTMax][kRMax] of 2T vectors,
+  // then the drafts' couplings E and F [4][4] each.
+  const size_t sc_floats = delta ? (kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax + 32
+                                                                : 16 + 2 * (size_t)kRMax + (nf ? 0 : R * P))
                          : nf    ? 16 + std::max(P, (size_t)kRMax)
                               : kind == LayoutKind::kVerify ? 16 + (size_t)kTMax * kRMax
                                                             : 16 + std::max({(size_t)kRMax, R * P, (size_t)c->T_max * P});
@@ -205,8 +212,9 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   const size_t gq_off = R * N * es;
   const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
   const size_t wsc = a128((size_t)kNCoef * kTMax * kRMax * 4);
+  const size_t dsc = (g.rf == kDelta && kind == LayoutKind::kVerify) ? (size_t)kNDW * 16 * 2 * kTMax * 4 : 0;
   const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6) * 8);
-  const size_t fixed = 2 * gb + wsc + bars;
+  const size_t fixed = 2 * gb + wsc + dsc + bars;
   if (fixed >= (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "group areas too large for shared memory");
   const size_t budget = ((size_t)kSmemMax - fixed) / 128 * 128;
   rssm::Params& p = pl->p;
@@ -223,6 +231,7 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   p.gb_bytes = (int)gb;
   p.gq_off = (int)gq_off;
   p.wsc_off = (int)off; off += wsc;
+  p.dsc_off = (int)off; off += dsc;
   p.bar_off = (int)off; off += bars;
   if (off > (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "shared memory plan too large");
   pl->stages = p.lay[0].stages;
@@ -381,7 +390,7 @@ rssm_status make_ckpt_tensor_map(const rssm_config* c, void* ckpt, CUtensorMap* 
 
 // Which verify kernel a launch of T drafts takes: 2 tensor cores, 1 CUDA cores.
 int verify_kernel_for(const rssm_ctx* h, int T) {
-  if (!h->g.tc_ok) return 1;
+  if (!h->g.tc_ok || h->g.rf == rssm::kDelta) return 1;
   if (h->verify_kernel == 1 && T <= rssm::kTMax) return 1;
   if (h->verify_kernel == 2) return 2;
   return (T >= kTcAutoMinT || T > rssm::kTMax) ? 2 : 1;
@@ -432,8 +441,9 @@ rssm_status rssm_launch_plan(const rssm_config* cfg, int32_t kind, rssm_launch_p
   Geom g;
   rssm_status s = derive(cfg, &g);
   if (s != RSSM_OK) return s;
-  if (kind >= 2 && (cfg->T_max < 2 || cfg->recurrence != RSSM_GATED_OUTER))
-    return fail(RSSM_EINVAL, "verify launches need T_max > 1 and the outer-product recurrence");
+  if (kind >= 2 && cfg->T_max < 2) return fail(RSSM_EINVAL, "verify launches need T_max > 1");
+  if (kind == 3 && cfg->recurrence != RSSM_GATED_OUTER)
+    return fail(RSSM_EINVAL, "the tensor-core verify serves the outer-product recurrence");
   if (kind == 3) {
     if (!g.tc_ok) return fail(RSSM_EUNSUPPORTED, "this configuration has no tensor-core verify");
     rssm::TcParams tp{};
@@ -565,10 +575,30 @@ rssm_status decode_impl(rssm_handle h, const float* alpha, const float* beta, co
 }
 }  // namespace
 
+namespace {
+rssm_status verify_impl(rssm_handle h, int32_t T, const float* alpha, const float* beta, const void* v,
+                        const void* k, const void* q, float* o, void* stream);
+}
+
 rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k, const void* q,
                         float* o, void* stream) {
+  if (h && h->cfg.recurrence == RSSM_GATED_DELTA)
+    return fail(RSSM_EINVAL, "a delta-rule layer verifies with rssm_verify_delta");
+  return verify_impl(h, T, alpha, nullptr, v, k, q, o, stream);
+}
+
+rssm_status rssm_verify_delta(rssm_handle h, int32_t T, const float* alpha, const float* beta, const void* v,
+                              const void* k, const void* q, float* o, void* stream) {
+  if (h && h->cfg.recurrence != RSSM_GATED_DELTA)
+    return fail(RSSM_EINVAL, "rssm_verify_delta needs a delta-rule layer");
+  if (!beta || !aligned16(beta)) return fail(RSSM_EINVAL, "beta must be a 16-byte aligned device pointer");
+  return verify_impl(h, T, alpha, beta, v, k, q, o, stream);
+}
+
+namespace {
+rssm_status verify_impl(rssm_handle h, int32_t T, const float* alpha, const float* beta, const void* v,
+                        const void* k, const void* q, float* o, void* stream) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");
-  if (h->cfg.recurrence == RSSM_GATED_DELTA) return fail(RSSM_EUNSUPPORTED, "verify is not offered for delta-rule layers");
   if (T < 1 || T > h->cfg.T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, h->cfg.T_max);
   if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
@@ -604,16 +634,17 @@ rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.T = T;
-  pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
+  pl.p.alpha = alpha; pl.p.beta = beta; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
   const long long heads = (long long)h->cfg.B * h->cfg.H;
   // verify reads the checkpoint itself, never a read copy
-  const int vrf = h->g.rf == rssm::kCkF16 ? (int)rssm::kCkF16 : (int)rssm::kRfNone;
+  const int vrf = h->g.rf == rssm::kCkF16 || h->g.rf == rssm::kDelta ? h->g.rf : (int)rssm::kRfNone;
   const cudaError_t e = rssm::launch_verify(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
                                             h->cfg.N, h->cfg.in_dtype, vrf);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   h->last_T = T;
   return RSSM_OK;
 }
+}  // namespace
 
 rssm_status rssm_set_verify_kernel(rssm_handle h, int32_t kind) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");

@@ -100,6 +100,7 @@ struct Params {
   int nf_ok;  // lay[1] is valid
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
+  int dsc_off;           // delta-rule verify: per dot warp [16 rows][2 kTMax] row sums
 };
 
 // ----------------------------------------------------------------- input types
@@ -895,7 +896,22 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
             }
             __syncwarp();
           }
-          if constexpr (kDel && MODE != kFlush) {  // lane j < c: k_j^T k_c, the new key against the buffered ones
+          if constexpr (kDel && MODE == kVerify) {
+            // k_j^T k_{c+t}: every record's key against each draft key, rows T..2T-1 of the scratch
+            const int npk = J * nq;
+            for (int pr = lane; pr < npk; pr += 32) {
+              const int t = pr / J, j = pr - t * J;
+              float acc = 0.f;
+#pragma unroll 8
+              for (int i = 0; i < N / 4; ++i) {
+                const int c4 = (i + lane) & (N / 4 - 1);
+                acc += dot4(In<TIn>::lds4(gK, j * N + 4 * c4), In<TIn>::lds4(gK, (c + t) * N + 4 * c4));
+              }
+              skq_w[(nq + t) * kRMax + j] = acc;
+            }
+            __syncwarp();
+          }
+          if constexpr (kDel && (MODE == kDecode || MODE == kConv)) {  // lane j < c: k_j^T k_c, the new key against the buffered ones
             float acc = 0.f;
             if (lane < c) {
 #pragma unroll 8
@@ -931,7 +947,45 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
       float* sc = reinterpret_cast<float*>(slot + lay.sc_off);    // coefficients
       // lane j holds alpha of record j
       const float aj = (lane < c) ? sa[ring_slot(st, lane, p.R)] : (lane < J) ? sa[kRMax + lane - c] : 1.f;
-      if constexpr (MODE == kVerify) {
+      if constexpr (MODE == kVerify && kDel) {
+        // Gated delta rule, T drafts after c committed records (draft t is record c + t):
+        //   y_t = P_t (S k_{c+t}) + sum_{i<c} D_it (k_i^T k_{c+t}) w_i + sum_{s<t} E_ts w'_s
+        //   w'_t = beta_t (v_t - alpha_{c+t} y_t)
+        //   o_t = G_t (S q_t) + sum_{i<c} W_it (k_i^T q_t) w_i + sum_{s<=t} F_ts w'_s
+        // with P_t = alpha_0 .. alpha_{c+t-1}, G_t = alpha_0 .. alpha_{c+t}, D_it and W_it the
+        // decays strictly after record i up to c+t-1 and c+t, E_ts = (alpha_{c+s+1} .. alpha_{c+t-1})
+        // (k_{c+s}^T k_{c+t}) and F_ts = (alpha_{c+s+1} .. alpha_{c+t}) (k_{c+s}^T q_t).
+        // sc: [t] G_t, [T + t] P_t; [16 + v kRMax + i] the committed weights of vector v
+        // (v < T: query t with W_it; v >= T: draft key v - T with D_it); then E [t][4], F [t][4].
+        const float sfx = suffix_prod((lane < c) ? aj : 1.f, lane);  // alpha_lane .. alpha_{c-1}
+        const float dn = __shfl_down_sync(kFull, sfx, 1);
+        const float dpart = (lane < 31) ? dn : 1.f;                  // alpha_{lane+1} .. alpha_{c-1}
+        const float call = __shfl_sync(kFull, sfx, 0);                // alpha_0 .. alpha_{c-1}
+        float pre = 1.f;                                               // alpha_c .. alpha_{c+t-1}
+        for (int t = 0; t < p.T; ++t) {
+          const float inc = pre * sa[kRMax + t];
+          if (lane == 0) {
+            sc[t] = call * inc;
+            sc[p.T + t] = call * pre;
+          }
+          const bool com = lane < c;
+          sc[kCoefOff + t * kRMax + lane] = com ? dpart * inc * skq_w[t * kRMax + lane] : 0.f;
+          sc[kCoefOff + (p.T + t) * kRMax + lane] = com ? dpart * pre * skq_w[(p.T + t) * kRMax + lane] : 0.f;
+          pre = inc;
+        }
+        if (lane < 16) {  // (t, s) = (lane / 4, lane % 4)
+          const int t = lane >> 2, s = lane & 3;
+          float e = 0.f, f = 0.f;
+          if (t < p.T && s <= t) {
+            float pe = 1.f;
+            for (int u = s + 1; u < t; ++u) pe *= sa[kRMax + u];
+            if (s < t) e = pe * skq_w[(p.T + t) * kRMax + c + s];
+            f = (s < t ? pe * sa[kRMax + t] : 1.f) * skq_w[t * kRMax + c + s];
+          }
+          sc[kCoefOff + kTMax * kRMax + lane] = e;
+          sc[kCoefOff + kTMax * kRMax + 16 + lane] = f;
+        }
+      } else if constexpr (MODE == kVerify) {
         // Per query t (records 0 .. c + t): g_{1:c+t+1} into sc[t] and the record
         // weights g_{j+2:c+t+1} (k_j^T q_t) into sc[kCoefOff + t kRMax + j]. One scan
         // covers the committed records; the drafts' decays enter as per-lane running
@@ -1016,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         // (delta-rule layers: the dot warps append the pseudo-value row instead)
         const int na = (MODE == kVerify) ? p.T : (flush ? 0 : 1);
         if (lane < na) p.ring_a[hrow * p.Rp + ring_slot(st, c + lane, p.R)] = sa[kRMax + lane];
-        if constexpr (MODE == kVerify) {
+        if constexpr (MODE == kVerify && !kDel) {
           // the T value rows: one bulk store per contiguous ring run (at most two),
           // issued by one lane; the slot is released once the copies have read it
           if (lane == 0 && na > 0) {
@@ -1147,7 +1201,115 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         // add their share to the scaled dot before the row reduction, so the value
         // term costs no shuffles. w_tj = 0 for records that query t does not see.
         const float* cw = sc + kCoefOff;  // [kTMax][kRMax]
-        if constexpr (N >= 64 && !kF16) {
+        if constexpr (kDel) {
+          // Gated delta rule. Per row, 2T sums as the outer-product verify forms them,
+          // over the vectors q_0 .. q_{T-1}, k_c .. k_{c+T-1} (scales and committed
+          // weights from the coefficient warps); then, one lane per row, the chain over
+          // the drafts that forms each draft's pseudo-value w'_t (appended to the ring)
+          // and its output.
+          constexpr int LPV = N / 16, RPW = 32 / LPV, KWV = 2, JI = kRMax / LPV, ROWS = KWV * RPW;
+          static_assert(ROWS <= 16, "the per-warp scratch holds 16 rows");
+          const int cl = lane % LPV, rw = lane / LPV;
+          const int nvec = 2 * p.T;
+          float* dsc = reinterpret_cast<float*>(smem + p.dsc_off) + warp * 16 * 2 * kTMax;
+          const float* sw = reinterpret_cast<const float*>(sv);  // committed pseudo-values [c][P]
+          const float* ef = cw + kTMax * kRMax;                  // E [t][4], then F [t][4]
+          const float* sa = reinterpret_cast<const float*>(slot);
+          const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
+          for (int r0 = wr * ROWS; r0 < p.P; r0 += wpg * ROWS) {
+            for (int t0 = 0; t0 < nvec; t0 += kTQ) {
+              f32x2 qv[kTQ][8];
+              float g[kTQ];
+              float wv[JI][kTQ];
+#pragma unroll
+              for (int tt = 0; tt < kTQ; ++tt) {
+                const int v = t0 + tt;
+                const bool tv = v < nvec;
+                const uint8_t* vec = v < p.T ? gQ + (size_t)v * N * ES : gK + (size_t)(c + v - p.T) * N * ES;
+                g[tt] = tv ? sc[v] : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                  const float4 qq = tv ? In<TIn>::lds4(vec, (cc * LPV + cl) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  qv[tt][2 * cc] = pk2(qq.x, qq.y);
+                  qv[tt][2 * cc + 1] = pk2(qq.z, qq.w);
+                }
+#pragma unroll
+                for (int i = 0; i < JI; ++i) {
+                  const int j = cl + LPV * i;
+                  wv[i][tt] = (tv && j < c) ? cw[v * kRMax + j] : 0.f;
+                }
+              }
+              float part[KWV * kTQ];
+#pragma unroll
+              for (int kk = 0; kk < KWV; ++kk) {
+                const int row = r0 + kk * RPW + rw;
+                float a[kTQ];
+#pragma unroll
+                for (int tt = 0; tt < kTQ; ++tt) a[tt] = 0.f;
+                if (row < p.P) {
+                  const float* rp = tf + (size_t)row * N;
+                  f32x2 a2[kTQ];
+#pragma unroll
+                  for (int tt = 0; tt < kTQ; ++tt) a2[tt] = 0ull;
+#pragma unroll
+                  for (int cc = 0; cc < 4; ++cc) {
+                    const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(rp + (cc * LPV + cl) * 4);
+#pragma unroll
+                    for (int tt = 0; tt < kTQ; ++tt) {
+                      a2[tt] = fma2(x.x, qv[tt][2 * cc], a2[tt]);
+                      a2[tt] = fma2(x.y, qv[tt][2 * cc + 1], a2[tt]);
+                    }
+                  }
+#pragma unroll
+                  for (int tt = 0; tt < kTQ; ++tt) a[tt] = g[tt] * (lo2(a2[tt]) + hi2(a2[tt]));
+#pragma unroll
+                  for (int i = 0; i < JI; ++i) {
+                    const int j = cl + LPV * i;
+                    if (j < c) {
+                      const float wj = sw[j * p.P + row];
+#pragma unroll
+                      for (int tt = 0; tt < kTQ; ++tt) a[tt] = fmaf(wv[i][tt], wj, a[tt]);
+                    }
+                  }
+                }
+#pragma unroll
+                for (int tt = 0; tt < kTQ; ++tt) part[kk * kTQ + tt] = a[tt];
+              }
+              int off = 0;
+              TRed<KWV * kTQ, LPV / 2>::run(part, lane, off);
+              constexpr int KF = (KWV * kTQ / LPV) > 0 ? (KWV * kTQ / LPV) : 1;
+              constexpr int D = (LPV / (KWV * kTQ)) > 0 ? (LPV / (KWV * kTQ)) : 1;
+#pragma unroll
+              for (int i = 0; i < KF; ++i) {
+                const int kk = (off + i) / kTQ, v = t0 + (off + i) % kTQ;
+                if ((cl & (D - 1)) == 0 && v < nvec) dsc[(kk * RPW + rw) * 2 * kTMax + v] = part[i];
+              }
+            }
+            __syncwarp();
+            if (lane < ROWS && r0 + lane < p.P) {
+              const int row = r0 + lane;
+              const float* rs = dsc + lane * 2 * kTMax;
+              const uint8_t* nv = slot + lay.nv_off;
+              float wd[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                wd[t] = 0.f;
+                if (t < p.T) {
+                  float y = rs[p.T + t];
+#pragma unroll
+                  for (int s2 = 0; s2 < t; ++s2) y = fmaf(ef[t * 4 + s2], wd[s2], y);
+                  wd[t] = sbeta[kRMax + t] * fmaf(-sa[kRMax + t], y, In<TIn>::lds(nv, t * p.P + row));
+                  float o = rs[t];
+#pragma unroll
+                  for (int s2 = 0; s2 <= t; ++s2) o = fmaf(ef[16 + t * 4 + s2], wd[s2], o);
+                  p.o[(((size_t)b * p.T + t) * p.H + hh) * p.P + row] = o;
+                  reinterpret_cast<float*>(p.ring_v)[(hrow * p.R + ring_slot(st, c + t, p.R)) * p.P + row] = wd[t];
+                }
+              }
+            }
+            __syncwarp();
+          }
+        } else if constexpr (N >= 64 && !kF16) {
           // LPV lanes per row, 16 columns per lane in 4 interleaved chunks (as the
           // wide non-flush rows); KWV row instructions x kTQ queries per pass.
           constexpr int LPV = N / 16, RPW = 32 / LPV, KWV = 2, JI = kRMax / LPV;

@@ -68,7 +68,7 @@ cudaError_t dispatch_n(const Params& p, int grid, size_t smem, cudaStream_t st, 
 }
 
 cudaError_t launch_decode(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
-// Gated delta-rule layers (rf = kDelta): mode kDecode, kFlush or kConv, N in {64, 128}.
+// Gated delta-rule layers (rf = kDelta): mode kDecode, kVerify, kFlush or kConv, N in {64, 128}.
 cudaError_t launch_delta(int mode, const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
 cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
 cudaError_t launch_sround_test(const float* x, uint16_t* y, long long n, long long base, uint32_t epoch,

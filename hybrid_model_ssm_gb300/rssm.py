@@ -56,6 +56,7 @@ SIGNATURES = {
     "rssm_decode_step_static_scratch": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_decode_step_delta": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_verify": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_verify_delta": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_set_verify_kernel": [_vp, ctypes.c_int32],
     "rssm_get_verify_kernel": [_vp, ctypes.c_int32, _c_i32_p],
     "rssm_commit": [_vp, _vp, _vp],
@@ -251,9 +252,12 @@ class ReplaySSM:
                                                     _ptr(out), _stream_ptr(stream)))
         return out
 
-    def verify(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+    def verify(self, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:
+        """Speculative verify of T drafts; a delta-rule layer also takes beta [B,T,H] fp32."""
         s, d = self.shape, self.ckpt.device
         T = alpha.shape[1]
+        if (beta is None) != (s.recurrence == "outer"):
+            raise ValueError("beta is required for (and only for) a delta-rule layer")
         _expect(alpha, (s.B, T, s.H), torch.float32, "alpha", d)
         _expect(v, (s.B, T, s.H, s.P), s.torch_in_dtype, "v", d)
         _expect(k, (s.B, T, s.G, s.N), s.torch_in_dtype, "k", d)
@@ -262,8 +266,13 @@ class ReplaySSM:
             out = torch.empty((s.B, T, s.H, s.P), dtype=torch.float32, device=d)
         _expect(out, (s.B, T, s.H, s.P), torch.float32, "out", d)
         with torch.cuda.device(d):
-            _check(lib().rssm_verify(self._h, T, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
-                                     _stream_ptr(stream)))
+            if beta is None:
+                _check(lib().rssm_verify(self._h, T, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
+                                         _stream_ptr(stream)))
+            else:
+                _expect(beta, (s.B, T, s.H), torch.float32, "beta", d)
+                _check(lib().rssm_verify_delta(self._h, T, _ptr(alpha), _ptr(beta), _ptr(v), _ptr(k), _ptr(q),
+                                               _ptr(out), _stream_ptr(stream)))
         return out
 
     def set_verify_kernel(self, kind: str):

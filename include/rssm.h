@@ -104,8 +104,8 @@ typedef enum {
  * step that appends record c forms y_c = P_c S_ckpt k_c + sum_{i<c} D_ic
  * (k_i^T k_c) w_i (P_c the decays before c, D_ic those strictly between i and
  * c) while it reads the checkpoint anyway. Delta layers decode with
- * rssm_decode_step_delta; they need ckpt_fmt F32, read_fmt NONE, T_max = 1 and
- * N in {64, 128} (verify is not offered for them). */
+ * rssm_decode_step_delta and verify with rssm_verify_delta; they need ckpt_fmt
+ * F32, read_fmt NONE, T_max <= 4 and N in {64, 128}. */
 typedef enum { RSSM_GATED_OUTER = 0, RSSM_GATED_DELTA = 1 } rssm_recurrence;
 
 typedef struct {
@@ -165,7 +165,8 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
  *   kind 0: flush and read-copy refresh (layout 0 only);
  *   kind 1: decode (layout 0 for any head, layout 1 for steps in which none of
  *           a CTA's sequences folds; nonflush_layout = 0 when only layout 0 fits);
- *   kind 2: verify on the CUDA cores (layout 0 only; needs 1 < T_max <= 8);
+ *   kind 2: verify on the CUDA cores (layout 0 only; needs 1 < T_max <= 8;
+ *           a delta-rule configuration gives the plan of rssm_verify_delta);
  *   kind 3: verify on the tensor cores at T = T_max (needs T_max > 1 and a
  *           configuration it serves): stages[0] K-block stages of
  *           stage_bytes[0] = 16 KiB (32 checkpoint columns of 128 rows),
@@ -228,8 +229,8 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
  *     W[j,tau] = gamma_{j+1:c+tau} for j <= c+tau, else 0.
  * Verify reads the checkpoint itself (FP32, or FP16 with an FP16 ckpt_fmt),
  * never the read copy. A sequence with c + T > R sets RSSM_ECAPACITY and is
- * skipped. T outside 1..T_max returns RSSM_EINVAL; a delta-rule handle returns
- * RSSM_EUNSUPPORTED.
+ * skipped. T outside 1..T_max returns RSSM_EINVAL; so does a delta-rule handle
+ * (it verifies with rssm_verify_delta).
  * Two kernels compute it (rssm_set_verify_kernel chooses; by default the
  * CUDA-core one up to 8 drafts and the tensor-core one above, where it applies):
  *  - CUDA cores: FP32 FMAs over the checkpoint tile, T <= 8.
@@ -240,6 +241,28 @@ rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, c
  *    term V (W ⊙ K^T Q) stays on the CUDA cores in FP32. */
 rssm_status rssm_verify(rssm_handle h, int32_t T, const float* alpha, const void* v, const void* k,
                         const void* q, float* o, void* stream);
+
+/* Speculative verify of T <= T_max (<= 4) drafts of a gated delta-rule layer
+ * (the pages' output-only verify, ai.cheesepanini.fun page, 方法/产品要点, which
+ * its 待核实 list says Gated DeltaNet can use; the form is derived under
+ * rssm_recurrence). rssm_verify's arguments plus beta [B,T,H] fp32, the drafts'
+ * write strengths (16-byte aligned). Draft t is record c + t after the c
+ * committed records. Per row, with P_t the decays before record c + t, G_t
+ * those up to and including it, the committed records' pseudo-values w_i from
+ * the ring and the drafts' own w'_s formed here:
+ *     y_t  = P_t S_ckpt k_{c+t} + sum_{i<c} (decays after i, before c+t) (k_i^T k_{c+t}) w_i
+ *            + sum_{s<t} (decays after c+s, before c+t) (k_{c+s}^T k_{c+t}) w'_s
+ *     w'_t = beta_t (v_t - alpha_{c+t} y_t)
+ *     o_t  = G_t S_ckpt q_t + sum_{i<c} (decays after i, to c+t) (k_i^T q_t) w_i
+ *            + sum_{s<=t} (decays after c+s, to c+t) (k_{c+s}^T q_t) w'_s
+ * The checkpoint is read once for the 2T vectors. Each w'_t is appended to the
+ * ring (with alpha and k), and a later rssm_commit keeps the accepted prefix:
+ * an accepted draft's w' depends only on the state before it, so it is the
+ * pseudo-value a decode step would have written. Pointers do not move. A
+ * sequence with c + T > R sets RSSM_ECAPACITY and is skipped. RSSM_EINVAL on a
+ * handle of the other recurrence or for T outside 1..T_max. */
+rssm_status rssm_verify_delta(rssm_handle h, int32_t T, const float* alpha, const float* beta, const void* v,
+                              const void* k, const void* q, float* o, void* stream);
 
 /* Choose the kernel of this handle's verify launches (library control, no
  * counterpart in the pages): 0 automatic (the default), 1 the CUDA cores (for

@@ -11,6 +11,7 @@ from .inputs import (  # noqa: F401
     initial_state,
     decode_step_inputs,
     delta_step_inputs,
+    delta_verify_round_inputs,
     verify_round_inputs,
     accepted_lengths,
 )

@@ -136,3 +136,19 @@ def delta_step_inputs(shape: Shape, gen: torch.Generator, mu: float = 0.0):
     k = (k / k.norm(dim=-1, keepdim=True)).to(shape.torch_dtype)
     q = (q / q.norm(dim=-1, keepdim=True)).to(shape.torch_dtype)
     return alpha, beta, v, k, q
+
+
+def delta_verify_round_inputs(shape: Shape, T: int, gen: torch.Generator, mu: float = 0.0):
+    """T draft records and queries of a gated delta-rule layer: the recipe of
+    ``delta_step_inputs`` with a draft axis T after B, drawn in the same order.
+    Returns (alpha [B,T,H], beta [B,T,H], v [B,T,H,P], k [B,T,G,N], q [B,T,G,N])."""
+    B, H, P, N, G = shape.B, shape.H, shape.P, shape.N, shape.G
+    u = torch.randn((B, T, H), generator=gen, dtype=torch.float32) + mu
+    alpha = _decay_from_normal(u)
+    beta = torch.sigmoid(torch.randn((B, T, H), generator=gen, dtype=torch.float32))
+    v = (torch.randn((B, T, H, P), generator=gen, dtype=torch.float32) / math.sqrt(N)).to(shape.torch_dtype)
+    k = torch.randn((B, T, G, N), generator=gen, dtype=torch.float32)
+    q = torch.randn((B, T, G, N), generator=gen, dtype=torch.float32)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(shape.torch_dtype)
+    q = (q / q.norm(dim=-1, keepdim=True)).to(shape.torch_dtype)
+    return alpha, beta, v, k, q

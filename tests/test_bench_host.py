@@ -127,6 +127,20 @@ def test_verify_round_bytes_of_the_verify_workload():
     assert fb == 2 * (2 * 4194304 + 16 * 18944) + 12 * 4 == 17_383_472
 
 
+def test_verify_round_bytes_of_a_delta_rule_layer():
+    """The same four sequences as a gated delta-rule layer, worked out by hand: a ring
+    record holds alpha (512 B), the fp32 pseudo-value w (32,768 B) and the bf16 key
+    (2,048 B), 35,328 bytes; a draft's inputs are alpha and beta (512 B each), v (16,384 B),
+    k and q (2,048 B each), 21,504 bytes."""
+    import numpy as np
+    s = synth.PRESETS["mamba2_verify_b512_t4"].with_(B=4)
+    counts, accepted = np.array([0, 5, 15, 12]), np.array([4, 0, 1, 4])
+    vb, fb, after = bench.verify_round_bytes(s, 4, counts, accepted, delta=True)
+    assert vb == 4 * 4194304 + 32 * 35328 + 4 * 4 * (21504 + 35328 + 32768) == 19_341_312
+    assert after.tolist() == [4, 5, 0, 0]
+    assert fb == 2 * (2 * 4194304 + 16 * 35328) + 12 * 4 == 17_907_760
+
+
 def test_window_bytes_with_read_copies():
     """Read-copy windows of the B=256 L=16 layer, worked out by hand. A head's E4M3
     copy is 64 x 128 codes + 64 fp32 row scales = 8,448 B; an E2M1 copy is 4,096 B

@@ -18,7 +18,7 @@ import torch
 import oracle
 import synth
 from hybrid_model_ssm_gb300 import LayerShape, ReplaySSM, RssmError, conventional_step
-from hybrid_model_ssm_gb300.rssm import RSSM_EINVAL, RSSM_EUNSUPPORTED, lib
+from hybrid_model_ssm_gb300.rssm import RSSM_EINVAL, lib
 from tests.gpu_helpers import REL_TOL, dev, f64, require_gpu, slice_rel_err
 
 pytestmark = pytest.mark.gpu
@@ -174,8 +174,9 @@ def test_entry_points_that_do_not_apply_refuse_delta_layers():
         conventional_step(delta_shape(shape), dev(S0), a, v, k, q)
     assert ei.value.status == RSSM_EINVAL
     cfg = delta_shape(shape).config()
+    # a delta-rule layer verifies with rssm_verify_delta (tests/test_gpu_delta_verify.py)
     assert L.rssm_verify(model._h, 1, a.data_ptr(), v.data_ptr(), k.data_ptr(), q.data_ptr(), o.data_ptr(),
-                         None) == RSSM_EUNSUPPORTED
+                         None) == RSSM_EINVAL
     assert isinstance(cfg, ctypes.Structure)
     torch.cuda.synchronize()
     assert model.read_pointers()[2] == 0 and plain.read_pointers()[2] == 0

@@ -4,7 +4,8 @@ Mamba-2 layer decode: B=256, H=128, P=64, N=128, G=8, L=16, bf16 inputs, 256
 steps from an N(0, 0.1^2) state. Speculative verify: the same layer at B=512,
 T=4, 64 rounds with seeded accepted lengths in 0..4, flushing every sequence
 that reaches 16 records. The same layer as a gated delta-rule layer: 64
-decode steps. The GPU runs the whole batch; the float64 oracle
+decode steps, and 32 speculative rounds at B=512, T=4. The outer-product layer
+at T=16 on the tensor-core verify: 24 rounds. The GPU runs the whole batch; the float64 oracle
 follows a sample of sequences (all heads) through every step. The pointers
 of every sequence are compared bit for bit against the oracle's bookkeeping.
 """
@@ -132,3 +133,87 @@ def test_delta_rule_layer_decode_b256_64_steps():
             assert err == 0
             assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count)
     print(f"delta b256: worst output rel err {worst_o:.2e}, checkpoint {worst_s:.2e}")
+
+
+def test_delta_rule_verify_b512_t4_32_rounds():
+    """Speculative rounds on the full-size layer as a gated delta-rule layer (B=512, T=4,
+    verify + commit + flush at 16), a sample of sequences followed by the delta-rule
+    oracle, pointers of every sequence bit for bit."""
+    from hybrid_model_ssm_gb300 import LayerShape
+    require_gpu()
+    shape = synth.PRESETS["mamba2_verify_b512_t4"]
+    T = shape.T_max
+    gen = synth.make_generator(shape.seed + 100)
+    S0 = synth.initial_state(shape, gen)
+    ls = LayerShape(B=shape.B, H=shape.H, P=shape.P, N=shape.N, G=shape.G, L=shape.L, T_max=T,
+                    in_dtype=shape.in_dtype, recurrence="delta")
+    model = ReplaySSM(ls, dev(S0))
+    sample = _sample(shape.B)
+    sidx = torch.as_tensor(sample, device="cuda")
+    orc = oracle.DeltaReplayOracle(f64(S0[sample]), L=shape.L, R=shape.R, G=shape.G)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    del S0
+    worst = 0.0
+    flushes = 0
+    for r in range(32):
+        a, b, v, k, q = synth.delta_verify_round_inputs(shape, T, gen)
+        O = model.verify(dev(a), dev(v), dev(k), dev(q), beta=dev(b))
+        O_ref = orc.verify(*(f64(x[sample]) for x in (a, b, v, k, q)))
+        shadow.verify(T)
+        e = slice_rel_err(O[sidx].cpu(), O_ref, 1)
+        worst = max(worst, e)
+        assert e <= REL_TOL, f"round {r}: verify rel err {e:.3g}"
+        acc = synth.accepted_lengths(shape.B, T, gen)
+        model.commit(dev(acc))
+        orc.commit(acc.numpy()[sample])
+        shadow.commit(acc.numpy())
+        model.flush(shape.L)
+        fl = orc.flush(shape.L)
+        shadow.flush(shape.L)
+        start, count, err = model.read_pointers()
+        assert err == 0
+        assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count), f"round {r}"
+        if fl.any():
+            flushes += int(fl.sum())
+            ck = model.ckpt[sidx].cpu()
+            for i in np.nonzero(fl)[0]:
+                assert slice_rel_err(ck[i], orc.ckpt[i], 2) <= REL_TOL, f"round {r}"
+    assert flushes > 0
+    print(f"delta verify b512: worst output rel err {worst:.2e}, sampled flushes {flushes}")
+
+
+def test_tensor_core_verify_b512_t16_24_rounds():
+    """The speculative workload at T=16 (L=16, R=31) on the tensor-core verify, a sample of
+    sequences followed by the oracle, pointers of every sequence bit for bit."""
+    require_gpu()
+    shape = synth.PRESETS["mamba2_verify_b512_t4"].with_(T_max=16)
+    T = shape.T_max
+    gen = synth.make_generator(shape.seed + 200)
+    S0 = synth.initial_state(shape, gen)
+    model = ReplaySSM(layer_shape(shape), dev(S0))
+    assert model.verify_kernel(T) == "tensor_cores"
+    sample = _sample(shape.B)
+    sidx = torch.as_tensor(sample, device="cuda")
+    orc = oracle.ReplayOracle(f64(S0[sample]), L=shape.L, R=shape.R, G=shape.G)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    del S0
+    worst = 0.0
+    for r in range(24):
+        a, v, k, q = synth.verify_round_inputs(shape, T, gen)
+        O = model.verify(dev(a), dev(v), dev(k), dev(q))
+        O_ref = orc.verify(f64(a[sample]), f64(v[sample]), f64(k[sample]), f64(q[sample]))
+        shadow.verify(T)
+        e = slice_rel_err(O[sidx].cpu(), O_ref, 1)
+        worst = max(worst, e)
+        assert e <= REL_TOL, f"round {r}: verify rel err {e:.3g}"
+        acc = synth.accepted_lengths(shape.B, T, gen)
+        model.commit(dev(acc))
+        orc.commit(acc.numpy()[sample])
+        shadow.commit(acc.numpy())
+        model.flush(shape.L)
+        orc.flush(shape.L)
+        shadow.flush(shape.L)
+        start, count, err = model.read_pointers()
+        assert err == 0
+        assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count), f"round {r}"
+    print(f"tensor-core verify b512 t16: worst output rel err {worst:.2e}")
