@@ -138,7 +138,10 @@ def profiled_traffic(key: str) -> float | None:
 
 
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    """nvidia-smi clock and throttle-reason samples during the timed region
+    (off with --no-clocks, e.g. under a profiler, which would attach to the sampler)."""
+
+    enabled = True
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -150,6 +153,8 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
+        if not ClockSampler.enabled:
+            return self
         try:
             import tempfile
             fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -966,6 +971,8 @@ def main(argv=None):
                     help="the timed region covers at least this long (and at least --steps steps)")
     ap.add_argument("--extra-seconds", type=float, default=0.3,
                     help="timed length of each secondary arm of the default line")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="do not sample clocks with nvidia-smi (profiler runs)")
     ap.add_argument("--no-extras", action="store_true",
                     help="leave out the secondary arms (verify, read copies, delta rule) of the default line")
     args = ap.parse_args(argv)
@@ -973,6 +980,7 @@ def main(argv=None):
         ap.error("--recurrence delta: decode or verify workload, FP32 checkpoint, no read copy")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    ClockSampler.enabled = not args.no_clocks
     world, rank, local = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, world, rank)
