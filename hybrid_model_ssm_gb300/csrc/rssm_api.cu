@@ -212,7 +212,8 @@ rssm_status plan_smem(const rssm_config* c, const Geom& g, Plan* pl, LayoutKind 
   const size_t gq_off = R * N * es;
   const size_t gb = a128(gq_off + (size_t)kTMax * N * es);
   const size_t wsc = a128((size_t)kNCoef * kTMax * kRMax * 4);
-  const size_t dsc = (g.rf == kDelta && kind == LayoutKind::kVerify) ? (size_t)kNDW * 16 * 2 * kTMax * 4 : 0;
+  // delta-rule verify: per dot warp, 32 rows of 2T <= 8 sums
+  const size_t dsc = (g.rf == kDelta && kind == LayoutKind::kVerify) ? (size_t)kNDW * 32 * 8 * 4 : 0;
   const size_t bars = a128((2 * kMaxStages + 3 * kMaxSlots + 6) * 8);
   const size_t fixed = 2 * gb + wsc + dsc + bars;
   if (fixed >= (size_t)kSmemMax) return fail(RSSM_EUNSUPPORTED, "group areas too large for shared memory");

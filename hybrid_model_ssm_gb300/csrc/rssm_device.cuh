@@ -100,7 +100,7 @@ struct Params {
   int nf_ok;  // lay[1] is valid
   int gb_off, gb_bytes, gq_off;
   int wsc_off, bar_off;  // coefficient-warp scratch (kTMax x kRMax fp32), barriers
-  int dsc_off;           // delta-rule verify: per dot warp [16 rows][2 kTMax] row sums
+  int dsc_off;           // delta-rule verify: per dot warp [32 rows][8] row sums
 };
 
 // ----------------------------------------------------------------- input types
@@ -1204,19 +1204,23 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         if constexpr (kDel) {
           // Gated delta rule. Per row, 2T sums as the outer-product verify forms them,
           // over the vectors q_0 .. q_{T-1}, k_c .. k_{c+T-1} (scales and committed
-          // weights from the coefficient warps); then, one lane per row, the chain over
-          // the drafts that forms each draft's pseudo-value w'_t (appended to the ring)
-          // and its output.
+          // weights from the coefficient warps), kept in a per-warp scratch of 32 rows;
+          // then, one lane per row for 32 rows at a time, the chain over the drafts that
+          // forms each draft's pseudo-value w'_t (appended to the ring) and its output.
           constexpr int LPV = N / 16, RPW = 32 / LPV, KWV = 2, JI = kRMax / LPV, ROWS = KWV * RPW;
-          static_assert(ROWS <= 16, "the per-warp scratch holds 16 rows");
+          constexpr int MB = 32 / ROWS;  // row groups per chain batch
+          constexpr int SROW = 8;        // scratch floats per row: 2T <= 8
+          static_assert(MB * ROWS == 32, "a chain batch is 32 rows");
           const int cl = lane % LPV, rw = lane / LPV;
           const int nvec = 2 * p.T;
-          float* dsc = reinterpret_cast<float*>(smem + p.dsc_off) + warp * 16 * 2 * kTMax;
+          float* dsc = reinterpret_cast<float*>(smem + p.dsc_off) + warp * 32 * SROW;
           const float* sw = reinterpret_cast<const float*>(sv);  // committed pseudo-values [c][P]
           const float* ef = cw + kTMax * kRMax;                  // E [t][4], then F [t][4]
           const float* sa = reinterpret_cast<const float*>(slot);
           const float* sbeta = reinterpret_cast<const float*>(slot + kSbOff);
-          for (int r0 = wr * ROWS; r0 < p.P; r0 += wpg * ROWS) {
+          int m = 0;  // row group of this warp
+          for (int r0 = wr * ROWS; r0 < p.P; r0 += wpg * ROWS, ++m) {
+            const int mb = m % MB;
             for (int t0 = 0; t0 < nvec; t0 += kTQ) {
               f32x2 qv[kTQ][8];
               float g[kTQ];
@@ -1282,13 +1286,14 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 #pragma unroll
               for (int i = 0; i < KF; ++i) {
                 const int kk = (off + i) / kTQ, v = t0 + (off + i) % kTQ;
-                if ((cl & (D - 1)) == 0 && v < nvec) dsc[(kk * RPW + rw) * 2 * kTMax + v] = part[i];
+                if ((cl & (D - 1)) == 0 && v < nvec) dsc[(mb * ROWS + kk * RPW + rw) * SROW + v] = part[i];
               }
             }
+            if (mb != MB - 1 && r0 + wpg * ROWS < p.P) continue;  // the batch is not full yet
             __syncwarp();
-            if (lane < ROWS && r0 + lane < p.P) {
-              const int row = r0 + lane;
-              const float* rs = dsc + lane * 2 * kTMax;
+            const int row = r0 - (mb - lane / ROWS) * (wpg * ROWS) + lane % ROWS;  // lane's row in the batch
+            if (lane < (mb + 1) * ROWS && row < p.P) {
+              const float* rs = dsc + lane * SROW;
               const uint8_t* nv = slot + lay.nv_off;
               float wd[4];
 #pragma unroll
