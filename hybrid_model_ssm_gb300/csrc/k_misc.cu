@@ -79,18 +79,14 @@ __global__ void sround_test_kernel(const float* __restrict__ x, uint16_t* __rest
                                    uint32_t epoch, unsigned long long seed, int sr) {
   const long long g4 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (g4 >= n) return;
-  const unsigned long long grp = (unsigned long long)(base + g4) >> 2;
-  const uint4 w = philox4x32_10(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), epoch, 0u),
-                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
-  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
   float xv[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) xv[e] = (g4 + e < n) ? x[g4 + e] : 0.f;
-  // the same two paths as the fold's store
-  const uint32_t h01 = sr ? ((uint32_t)to_f16_bits(xv[0], ww[0], true) | ((uint32_t)to_f16_bits(xv[1], ww[1], true) << 16))
-                          : rn_f16x2_sat(xv[0], xv[1]);
-  const uint32_t h23 = sr ? ((uint32_t)to_f16_bits(xv[2], ww[2], true) | ((uint32_t)to_f16_bits(xv[3], ww[3], true) << 16))
-                          : rn_f16x2_sat(xv[2], xv[3]);
+  const float4 a = make_float4(xv[0], xv[1], xv[2], xv[3]);
+  // the fold's store, in either mode
+  const uint2 h = sr ? sr_f16x4(a, sr_words((size_t)(base + g4), epoch, seed))
+                     : make_uint2(rn_f16x2_sat(a.x, a.y), rn_f16x2_sat(a.z, a.w));
+  const uint32_t h01 = h.x, h23 = h.y;
   const uint16_t hv[4] = {(uint16_t)h01, (uint16_t)(h01 >> 16), (uint16_t)h23, (uint16_t)(h23 >> 16)};
 #pragma unroll
   for (int e = 0; e < 4; ++e)

@@ -460,38 +460,48 @@ __device__ __forceinline__ void quantize_rows(const float4 (&x)[KR], int lane, i
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    const unsigned long long m0 = (unsigned long long)0xD2511F53u * c.x;  // one widening multiply each
+    const unsigned long long m1 = (unsigned long long)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(m1 >> 32) ^ c.y ^ k.x, (uint32_t)m1, (uint32_t)(m0 >> 32) ^ c.w ^ k.y, (uint32_t)m0);
     k.x += 0x9E3779B9u;
     k.y += 0xBB67AE85u;
   }
   return c;
 }
-// binary32 -> binary16 bits. Stochastic (sr): with lo = x rounded toward zero
-// and hi the next binary16 away from zero, hi is taken when r < floor(frac 2^32),
-// frac = (|x| - |lo|) / (|hi| - |lo|) (exact in binary32); otherwise round to
-// nearest even. Both saturate to +-65504 and keep the sign; NaN gives 0x7E00.
-__device__ __forceinline__ uint16_t to_f16_bits(float x, uint32_t r, bool sr) {
-  const float ax = fabsf(x);
-  const uint16_t sign = (uint16_t)((__float_as_uint(x) >> 16) & 0x8000u);
-  if (!(ax == ax)) return 0x7E00u;
-  if (ax >= 65504.f) return sign | 0x7BFFu;
-  uint16_t mag;
-  if (sr) {
-    const uint16_t lo = __half_as_ushort(__float2half_rz(ax));
-    const float lo_f = __half2float(__ushort_as_half(lo));
-    // the binary16 spacing above lo is 2^(max(E, 1) - 25), E = lo's exponent field, so
-    // frac 2^32 = (|x| - lo) 2^(57 - max(E, 1)): an exact power-of-two scaling
-    const uint32_t e16 = max((uint32_t)(lo >> 10), 1u);
-    const float scale = __uint_as_float((57u - e16 + 127u) << 23);
-    const uint32_t t = __float2uint_rz((ax - lo_f) * scale);  // floor(frac 2^32), exact
-    mag = (r < t) ? (uint16_t)(lo + 1) : lo;
-  } else {
-    mag = __half_as_ushort(__float2half_rn(ax));
-    if (mag > 0x7BFFu) mag = 0x7BFFu;
-  }
-  return sign | mag;
+// The generator words of the group of four checkpoint elements starting at
+// element e (a multiple of 4) at a flush epoch: counter (e / 4 low and high
+// words, epoch, 0), key the seed.
+__device__ __forceinline__ uint4 sr_words(size_t e, uint32_t epoch, unsigned long long seed) {
+  const unsigned long long grp = (unsigned long long)e >> 2;
+  return philox4x32_10(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), epoch, 0u),
+                       make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+// binary32 -> binary16 bits by stochastic rounding with the 32-bit word r: with
+// lo = |x| rounded toward zero and hi the next binary16 away from zero, hi is
+// taken when r < floor(frac 2^32), frac = (|x| - lo) / (hi - lo). The result
+// saturates to +-65504 and keeps the sign; NaN gives 0x7E00.
+// Branch-free on the bit pattern. With e the biased exponent and m the significand
+// with its leading one, Z = floor(m 2^(32 - s)), s = clamp(126 - e, 13, 63), is |x|
+// in units of the binary16 spacing at |x| (2^-24 below 2^-14, 2^(e - 137) above)
+// as a 32.32 fixed-point number, its low word floor(frac 2^32). Adding 2^32 - 1 - r
+// carries into the high word exactly when r < that fraction word, and the high word
+// plus (max(e, 113) - 113) 2^10 is the binary16 magnitude. For e = 0 (zero, binary32
+// subnormals) the shift of 63 leaves Z = 0, so the leading one added to m is harmless.
+__device__ __forceinline__ uint32_t sr_f16_bits(float x, uint32_t r) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t au = u & 0x7FFFFFFFu;
+  const uint32_t e = au >> 23;
+  const uint32_t m = (au & 0x7FFFFFu) | 0x800000u;
+  const int sh = min(max(126 - (int)e, 13), 63);
+  const unsigned long long Z = ((unsigned long long)m << 32) >> sh;
+  uint32_t mag = (uint32_t)((Z + (unsigned long long)(~r)) >> 32) + ((max(e, 113u) - 113u) << 10);
+  mag = min(mag, 0x7BFFu) | ((u >> 16) & 0x8000u);
+  return au > 0x7F800000u ? 0x7E00u : mag;
+}
+// Four values and the four words of one generator call -> two binary16x2 words.
+__device__ __forceinline__ uint2 sr_f16x4(const float4& a, const uint4& w) {
+  return make_uint2(sr_f16_bits(a.x, w.x) | (sr_f16_bits(a.y, w.y) << 16),
+                    sr_f16_bits(a.z, w.z) | (sr_f16_bits(a.w, w.w) << 16));
 }
 // Two binary32 values -> binary16x2 (lo in the low half), round to nearest even,
 // saturating to +-65504 (the round-to-nearest store, two elements per instruction).
@@ -1583,30 +1593,30 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
               }
             }
           }
-          if constexpr (MODE != kQuant) {
+          if constexpr (MODE != kQuant && kF16) {
+            uint8_t* ck = reinterpret_cast<uint8_t*>(p.ckpt);
+            if (p.sr) {
+#pragma unroll
+              for (int kk = 0; kk < kKR; ++kk) {
+                const int row = (rbase + kk) * RPI + rsub;
+                const size_t e = (hrow * p.P + row) * N + col4 * 4;  // first of the four elements
+                const uint2 h = sr_f16x4(acc[kk], sr_words(e, (uint32_t)ep, p.seed));
+                if (row < p.P) *reinterpret_cast<uint2*>(ck + e * 2) = h;
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < kKR; ++kk) {
+                const int row = (rbase + kk) * RPI + rsub;
+                if (row < p.P)
+                  *reinterpret_cast<uint2*>(ck + ((hrow * p.P + row) * N + col4 * 4) * 2) =
+                      make_uint2(rn_f16x2_sat(acc[kk].x, acc[kk].y), rn_f16x2_sat(acc[kk].z, acc[kk].w));
+              }
+            }
+          } else if constexpr (MODE != kQuant) {
 #pragma unroll
             for (int kk = 0; kk < kKR; ++kk) {
               const int row = (rbase + kk) * RPI + rsub;
-              if constexpr (kF16) {
-                if (row < p.P) {
-                  // counter: (element group e / 4, epoch of this flush, 0); key: the seed
-                  const size_t e = (hrow * p.P + row) * N + col4 * 4;  // first of the four elements
-                  const size_t grp = e >> 2;
-                  uint32_t h01, h23;
-                  if (p.sr) {
-                    const uint4 w = philox4x32_10(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)ep, 0u),
-                                                  make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
-                    h01 = (uint32_t)to_f16_bits(acc[kk].x, w.x, true) | ((uint32_t)to_f16_bits(acc[kk].y, w.y, true) << 16);
-                    h23 = (uint32_t)to_f16_bits(acc[kk].z, w.z, true) | ((uint32_t)to_f16_bits(acc[kk].w, w.w, true) << 16);
-                  } else {
-                    h01 = rn_f16x2_sat(acc[kk].x, acc[kk].y);
-                    h23 = rn_f16x2_sat(acc[kk].z, acc[kk].w);
-                  }
-                  *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.ckpt) + e * 2) = make_uint2(h01, h23);
-                }
-              } else {
-                if (row < p.P) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
-              }
+              if (row < p.P) *reinterpret_cast<float4*>(p.ckpt + (hrow * p.P + row) * N + col4 * 4) = acc[kk];
             }
           }
           if constexpr (kCopyRF && MODE != kConv) {

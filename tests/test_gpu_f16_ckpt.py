@@ -60,6 +60,34 @@ def test_store_rounding_is_bit_exact(stochastic):
     assert len(bad) == 0, f"{len(bad)} values differ, first x={x[~nan][bad[:3]]}"
 
 
+def _bit_patterns(rng):
+    """Random binary32 bit patterns over every exponent, and every finite binary16
+    value with its two binary32 neighbours, both signs."""
+    pat = rng.integers(0, 2 ** 32, 1 << 18, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    h = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float32)
+    grid = np.concatenate([h, np.nextafter(h, np.float32(np.inf)), np.nextafter(h, np.float32(0))])
+    return np.concatenate([pat, grid, -grid]).astype(np.float32)
+
+
+@pytest.mark.parametrize("stochastic", [True, False])
+def test_store_rounding_is_bit_exact_over_bit_patterns(stochastic):
+    require_gpu()
+    x = _bit_patterns(np.random.default_rng(62))
+    base, epoch, seed = 4 * 777, 3, 0x0F1E_2D3C_4B5A_6978
+    y = round_f16(torch.from_numpy(x).cuda(), base=base, epoch=epoch, seed=seed, stochastic=stochastic).cpu().numpy()
+    with np.errstate(invalid="ignore", over="ignore"):
+        if stochastic:
+            ref = sround.stochastic_round_f16(x, sround.sr_words(len(x), base, epoch, seed))
+        else:
+            ref = sround.nearest_f16(x)
+    nan = np.isnan(x)
+    assert np.all(np.isnan(y[nan]))
+    if stochastic:  # the stochastic store writes one NaN code
+        assert np.all(y[nan].view(np.uint16) == 0x7E00)
+    bad = np.nonzero(y[~nan].view(np.uint16) != ref[~nan].view(np.uint16))[0]
+    assert len(bad) == 0, f"{len(bad)} values differ, first x={x[~nan][bad[:3]]}"
+
+
 def _f16_model(shape, mode, seed):
     gen = synth.make_generator(shape.seed)
     S0 = synth.initial_state(shape, gen).to(torch.float16)
