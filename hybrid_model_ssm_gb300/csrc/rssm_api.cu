@@ -18,6 +18,7 @@
 
 #include "../../include/rssm.h"
 #include "rssm_launch.cuh"
+#include "rssm_nonflush.cuh"
 #include "rssm_verify_tc.cuh"
 
 namespace {
@@ -330,6 +331,7 @@ struct rssm_ctx {
   uint8_t* copy;
   int last_T;         // draft count of the last verify, 0 when none is pending
   int verify_kernel;  // 0 automatic, 1 CUDA cores, 2 tensor cores
+  int decode_kernel;  // 0 automatic, 1 the pipelined head kernel only, 2 warp-per-head non-flush step first
 };
 
 namespace {
@@ -395,6 +397,49 @@ int verify_kernel_for(const rssm_ctx* h, int T) {
   if (h->verify_kernel == 1 && T <= rssm::kTMax) return 1;
   if (h->verify_kernel == 2) return 2;
   return (T >= kTcAutoMinT || T > rssm::kTMax) ? 2 : 1;
+}
+
+// The warp-per-head non-flush step serves the small head tiles: an E4M3 or E2M1
+// read copy, or an FP16 checkpoint (N in {64, 128}, outer-product recurrence).
+bool nonflush_applies_fmt(const rssm_ctx* h) {
+  return h->g.rf == rssm::kRfE4m3 || h->g.rf == rssm::kRfE2m1 || h->g.rf == rssm::kCkF16;
+}
+
+// The per-warp stages of the warp-per-head step, and how many warps fit a CTA.
+rssm::NfStage nonflush_stage(const rssm_ctx* h) {
+  const rssm_config& c = h->cfg;
+  const int tile = h->g.rf == rssm::kCkF16 ? c.P * c.N * 2 : (int)h->g.head_stride;
+  return rssm::nf_stage(tile, h->g.R, h->g.Rp, c.P, h->g.esize);
+}
+int nonflush_warps(const rssm::NfStage& sg) {
+  return std::min(rssm::kNfMaxWarps, (rssm::kSmemMax - rssm::kNfCtaBytes) / rssm::nf_warp_bytes(sg));
+}
+
+bool nonflush_applies(const rssm_ctx* h) {
+  return nonflush_applies_fmt(h) && nonflush_warps(nonflush_stage(h)) >= 1;
+}
+
+// Which decode kernels a step launches: 2 the warp-per-head non-flush step and
+// then the head kernel for the flushing sequences, 1 the head kernel alone.
+int decode_kernel_for(const rssm_ctx* h) {
+  if (!nonflush_applies(h) || h->decode_kernel == 1) return 1;
+  return 2;
+}
+
+// Enqueue one decode step with the parameters in p (pointers, inputs, ticket block set).
+cudaError_t launch_decode_step(const rssm_ctx* h, rssm::Params& p, size_t smem, cudaStream_t st) {
+  const long long heads = (long long)h->cfg.B * h->cfg.H;
+  if (decode_kernel_for(h) == 2) {
+    const rssm::NfStage sg = nonflush_stage(h);
+    const int warps = nonflush_warps(sg);
+    const long long want = (heads + warps - 1) / warps;
+    const int grid = (int)std::max(1ll, std::min<long long>(want, (long long)std::max(1, sm_count())));
+    const size_t smem = rssm::kNfCtaBytes + (size_t)warps * rssm::nf_warp_bytes(sg);
+    const cudaError_t e = rssm::launch_nonflush(p, sg, grid, warps, smem, st, h->cfg.N, h->cfg.in_dtype, h->g.rf);
+    if (e != cudaSuccess) return e;
+    p.skip_nonflush = 1;
+  }
+  return rssm::launch_decode(p, persistent_grid(heads), smem, st, h->cfg.N, h->cfg.in_dtype, h->g.rf);
 }
 
 }  // namespace
@@ -502,6 +547,7 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
   h->copy = cfg->read_fmt != RSSM_READ_NONE ? static_cast<uint8_t*>(read_copy) : nullptr;
   h->last_T = 0;
   h->verify_kernel = 0;
+  h->decode_kernel = 0;
   std::memset(&h->tmap, 0, sizeof(h->tmap));
   if (g.tc_ok && cfg->T_max > 1) {
     s = make_ckpt_tensor_map(cfg, ckpt, &h->tmap);
@@ -567,9 +613,7 @@ rssm_status decode_impl(rssm_handle h, const float* alpha, const float* beta, co
   if (s != RSSM_OK) return s;
   fill_common(h, &pl.p);
   pl.p.alpha = alpha; pl.p.beta = beta; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
-  const long long heads = (long long)h->cfg.B * h->cfg.H;
-  const cudaError_t e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, static_cast<cudaStream_t>(stream),
-                                            h->cfg.N, h->cfg.in_dtype, h->g.rf);
+  const cudaError_t e = launch_decode_step(h, pl.p, pl.smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   h->last_T = 0;
   return RSSM_OK;
@@ -661,6 +705,22 @@ rssm_status rssm_get_verify_kernel(rssm_handle h, int32_t T, int32_t* kind) {
   if (!h || !kind) return fail(RSSM_EINVAL, "NULL argument");
   if (T < 1 || T > h->cfg.T_max) return fail(RSSM_EINVAL, "T=%d outside 1..T_max=%d", T, h->cfg.T_max);
   *kind = verify_kernel_for(h, T);
+  return RSSM_OK;
+}
+
+rssm_status rssm_set_decode_kernel(rssm_handle h, int32_t kind) {
+  if (!h) return fail(RSSM_EINVAL, "handle is NULL");
+  if (kind < 0 || kind > 2)
+    return fail(RSSM_EINVAL, "kind=%d (0 automatic, 1 head kernel only, 2 warp-per-head non-flush step)", kind);
+  if (kind == 2 && !nonflush_applies(h))
+    return fail(RSSM_EUNSUPPORTED, "the warp-per-head non-flush step serves read copies and FP16 checkpoints");
+  h->decode_kernel = kind;
+  return RSSM_OK;
+}
+
+rssm_status rssm_get_decode_kernel(rssm_handle h, int32_t* kind) {
+  if (!h || !kind) return fail(RSSM_EINVAL, "NULL argument");
+  *kind = decode_kernel_for(h);
   return RSSM_OK;
 }
 
@@ -913,8 +973,7 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
   // The array keeps the last call's contents; the tickets must start at zero.
   e = cudaMemsetAsync(tickets, 0, (size_t)h->cfg.B * sizeof(int32_t), st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static tickets)");
-  const long long heads = (long long)h->cfg.B * h->cfg.H;
-  e = rssm::launch_decode(pl.p, persistent_grid(heads), pl.smem, st, h->cfg.N, h->cfg.in_dtype, h->g.rf);
+  e = launch_decode_step(h, pl.p, pl.smem, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");
   h->last_T = 0;
   return RSSM_OK;

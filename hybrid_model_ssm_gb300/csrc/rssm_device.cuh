@@ -44,6 +44,10 @@ constexpr int kTMax = 8;                   // largest draft count
 constexpr int kRMax = 32;                  // largest ring (records per head)
 constexpr int kMaxStages = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+// The warp-per-head non-flush step (rssm_nonflush.cuh): at most this many warps per CTA,
+// one CTA per SM (the warps' shared-memory stages decide how many fit).
+constexpr int kNfMaxWarps = 16;
+constexpr int kNfMaxThreads = kNfMaxWarps * 32;
 constexpr unsigned kFull = 0xffffffffu;
 
 enum Mode : int { kDecode = 0, kVerify = 1, kFlush = 2, kQuant = 3, kConv = 4, kSnap = 5 };
@@ -77,6 +81,7 @@ struct Params {
   const int32_t* fcount;  // kFlush: their number
   unsigned long long seed;  // FP16 checkpoint: generator key
   int sr;              // FP16 checkpoint: 1 stochastic rounding, 0 round to nearest
+  int skip_nonflush;   // kDecode: leave non-flush sequences to the warp-per-head kernel (pointers still advance)
   const int32_t* cur;  // kSnap: [B] slot holding each sequence's state
   int nslot;           // kSnap: state slots (T_max + 1)
   uint32_t* err;       // error word
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     if constexpr (MODE == kDecode) {
       bad = (c + 1 > p.R) || c < 0;
       flush = !bad && (c + 1 >= p.L);
-      load = !bad;
+      load = !bad && (flush || !p.skip_nonflush);
     } else if constexpr (MODE == kVerify) {
       bad = (c + p.T > p.R) || c < 0;
       load = !bad;
@@ -677,6 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
     else if constexpr (MODE == kConv) return 1;
     else if constexpr (MODE == kSnap) return p.T;
     else return 0;
+  };
+
+  // Move a head loop past the rest of the current sequence (virtual index it.b):
+  // the loop's increment then lands on the next sequence's first head.
+  auto skip_seq = [&](long long& gh, HeadIter& it) {
+    gh = min(h1, (long long)(it.b + 1) * p.H) - 1;
+    it.init(gh, p.H, p.HPG);
   };
 
   // Ring positions (index, phase parity) of the tile stages and record slots.
@@ -706,7 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           cur_b = b;
           seq_plan(b, c, st, load, flush, bad);
         }
-        if (!load) continue;
+        if (!load) {  // past the rest of this sequence in one step
+          skip_seq(gh, it);
+          continue;
+        }
         if constexpr (kTileNew) {
           if (li >= lay.slots && !mbar_wait(sempty0 + 8 * rs, rph ^ 1, abort_flag, p.err)) { ok = false; break; }
           const int nnew = records(c) - c;
@@ -775,7 +790,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
           J = records(c);
           cur_gg = -1;
         }
-        if (!load) continue;
+        if (!load) {  // past the rest of this sequence in one step
+          skip_seq(gh, it);
+          continue;
+        }
         const int nnew = J - c;  // records that come from the call's inputs
         if constexpr (kGroupData) {
           if (gg != cur_gg) {
@@ -870,7 +888,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         J = records(c);
         cur_gg = -1;
       }
-      if (!load) continue;
+      if (!load) {  // past the rest of this sequence in one step
+        skip_seq(gh, it);
+        continue;
+      }
       if constexpr (kGroupData) {
         if (gg != cur_gg) {
           cur_gg = gg;
@@ -1146,7 +1167,10 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
         cur_gg = -1;
         if constexpr (kF16) ep = p.epoch[b];
       }
-      if (!load) continue;
+      if (!load) {  // past the rest of this sequence in one step
+        skip_seq(gh, it);
+        continue;
+      }
       if constexpr (kGroupData) {
         if (gg != cur_gg) {
           cur_gg = gg;
@@ -1864,13 +1888,16 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
 
   // ------------------------------------------------------------------ epilogue
   // Pointer updates: once every CTA covering a sequence has finished reading its
-  // pointers, the last one (ticket) advances them. Never a spin wait.
+  // pointers, the last one (ticket) advances them. Never a spin wait. Warp 0's
+  // lanes take the CTA's sequences in parallel (their fences and tickets overlap).
   mbar_arrive(end_bar);
-  if (threadIdx.x == 0) {
-    const bool done = mbar_wait(end_bar, 0, abort_flag, p.err) && !*abort_flag;
+  if (warp == 0) {
+    bool done = false;
+    if (lane == 0) done = mbar_wait(end_bar, 0, abort_flag, p.err) && !*abort_flag;
+    done = __shfl_sync(kFull, done, 0);
     if (done && (MODE == kDecode || MODE == kFlush) && h1 > h0) {
       const int b_first = (int)(h0 / p.H), b_last = (int)((h1 - 1) / p.H);
-      for (int vb = b_first; vb <= b_last; ++vb) {
+      for (int vb = b_first + lane; vb <= b_last; vb += 32) {
         const long long lo = max(h0, (long long)vb * p.H), hi = min(h1, (long long)(vb + 1) * p.H);
         const int n_b = (int)(hi - lo);
         const int b = seq_of(vb);

@@ -68,6 +68,11 @@ cudaError_t dispatch_n(const Params& p, int grid, size_t smem, cudaStream_t st, 
 }
 
 cudaError_t launch_decode(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);
+// The warp-per-head non-flush step (rf = kRfE4m3, kRfE2m1 or kCkF16; N in {64, 128}):
+// CTAs of `warps` warps with their stages (rssm_nonflush.cuh) in `smem` bytes.
+struct NfStage;
+cudaError_t launch_nonflush(const Params& p, const NfStage& sg, int grid, int warps, size_t smem, cudaStream_t st,
+                            int N, int dtype, int rf);
 // Gated delta-rule layers (rf = kDelta): mode kDecode, kVerify, kFlush or kConv, N in {64, 128}.
 cudaError_t launch_delta(int mode, const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype);
 cudaError_t launch_verify(const Params& p, int grid, size_t smem, cudaStream_t st, int N, int dtype, int rf);

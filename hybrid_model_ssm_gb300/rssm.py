@@ -57,6 +57,8 @@ SIGNATURES = {
     "rssm_decode_step_delta": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_verify": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp],
     "rssm_verify_delta": [_vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "rssm_set_decode_kernel": [_vp, ctypes.c_int32],
+    "rssm_get_decode_kernel": [_vp, _c_i32_p],
     "rssm_set_verify_kernel": [_vp, ctypes.c_int32],
     "rssm_get_verify_kernel": [_vp, ctypes.c_int32, _c_i32_p],
     "rssm_commit": [_vp, _vp, _vp],
@@ -164,6 +166,7 @@ def read_copy_layout(shape: LayerShape) -> tuple[int, int, int]:
 
 LAUNCH_KINDS = {"flush": 0, "decode": 1, "verify": 2, "verify_tc": 3}
 VERIFY_KERNELS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+DECODE_KERNELS = {"auto": 0, "head_kernel": 1, "warp_per_head": 2}
 
 
 def launch_plan(shape: LayerShape, kind: str) -> dict:
@@ -274,6 +277,17 @@ class ReplaySSM:
                 _check(lib().rssm_verify_delta(self._h, T, _ptr(alpha), _ptr(beta), _ptr(v), _ptr(k), _ptr(q),
                                                _ptr(out), _stream_ptr(stream)))
         return out
+
+    def set_decode_kernel(self, kind: str):
+        """Kernels of the decode steps: "auto", "head_kernel" (alone) or "warp_per_head"
+        (the non-flush step of read copies and FP16 checkpoints, then the head kernel)."""
+        _check(lib().rssm_set_decode_kernel(self._h, DECODE_KERNELS[kind]))
+
+    def decode_kernel(self) -> str:
+        """The kernels a decode step launches: "head_kernel" or "warp_per_head"."""
+        k = ctypes.c_int32()
+        _check(lib().rssm_get_decode_kernel(self._h, ctypes.byref(k)))
+        return {1: "head_kernel", 2: "warp_per_head"}[k.value]
 
     def set_verify_kernel(self, kind: str):
         """Kernel of the verify launches: "auto", "cuda_cores" (T <= 8) or "tensor_cores"."""

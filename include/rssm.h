@@ -216,9 +216,25 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
  * and writes no state. If h >= L it folds all h records into the checkpoint,
  * writes it once (and refreshes the read copy), outputs o = S_new q, and
  * clears the buffer (start += h mod R, count = 0). A sequence with h > R sets
- * RSSM_ECAPACITY in the error word and is left untouched. */
+ * RSSM_ECAPACITY in the error word and is left untouched.
+ * With an E4M3 or E2M1 read copy or an FP16 checkpoint the step is two kernels
+ * by default (rssm_set_decode_kernel): a warp-per-head kernel computes the
+ * non-flush sequences' outputs and appends their records, then the head kernel
+ * folds the flushing sequences and advances every sequence's pointers. Other
+ * configurations launch the head kernel alone. */
 rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, const void* k,
                              const void* q, float* o, void* stream);
+
+/* Choose the kernels of this handle's decode steps (library control, no
+ * counterpart in the pages): 0 automatic (the default), 1 the head kernel alone,
+ * 2 the warp-per-head non-flush kernel before it. RSSM_EUNSUPPORTED for 2
+ * unless the handle has an E4M3 or E2M1 read copy or an FP16 checkpoint.
+ * Both give the same outputs and state up to FP32 summation order. Host only. */
+rssm_status rssm_set_decode_kernel(rssm_handle h, int32_t kind);
+
+/* The decode kernels of this handle's steps into *kind: 1 the head kernel alone,
+ * 2 the warp-per-head non-flush kernel and then the head kernel. Host only. */
+rssm_status rssm_get_decode_kernel(rssm_handle h, int32_t* kind);
 
 /* Speculative verify of T <= T_max drafts (aikraft.ru page §05;
  * ai.cheesepanini.fun card, 方法/产品要点, verify formula). Inputs: alpha

@@ -1,0 +1,185 @@
+"""GPU parity of the two decode kernels of small head tiles.
+
+With an E4M3 or E2M1 read copy, or an FP16 checkpoint, a decode step runs a
+warp-per-head kernel for the non-flush sequences and then the head kernel for
+the flushing ones (which also advances every pointer); the head kernel alone
+is the other choice. Sequences are staggered (a verify and a commit of random
+accepted lengths) so that single steps mix flushing and non-flushing
+sequences.
+
+Bit-exact between the two choices: pointers, checkpoints, read copies and the
+live ring records (the appends are raw copies of the inputs, and the fold is
+the same kernel). Outputs agree to 1e-5 per (sequence, head) (FP32 summation
+order). Against the oracle (read copies): each non-flush output equals the
+oracle's output-only form on the device copy and the buffered records, and
+each flush output the exact recurrence, both within 1e-4.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from hybrid_model_ssm_gb300 import ReplaySSM, RssmError
+from hybrid_model_ssm_gb300.rssm import RSSM_EUNSUPPORTED
+from tests.gpu_helpers import REL_TOL, dev, f64, layer_shape, require_gpu, slice_rel_err
+from tests.test_gpu_readcopy import _dequantized_copy
+
+pytestmark = pytest.mark.gpu
+
+S = synth.Shape
+CASES = [("e4m3", 64, "bf16"), ("e4m3", 128, "f32"), ("e2m1", 64, "f32"), ("e2m1", 128, "bf16"),
+         ("f16_sr", 128, "bf16"), ("f16_rn", 64, "f32")]
+
+
+def _model(shape, fmt, S0, kernel):
+    if fmt.startswith("f16"):
+        ls = dataclasses.replace(layer_shape(shape), ckpt=fmt, seed=77)
+        m = ReplaySSM(ls, dev(S0.to(torch.float16)))
+    else:
+        m = ReplaySSM(layer_shape(shape, fmt), dev(S0))
+    m.set_decode_kernel(kernel)
+    return m
+
+
+def _live_ring(model, shape):
+    """The committed records of every sequence: (alpha [H], v [H,P], k [G,N]) per (b, j), raw bytes."""
+    a, V, K = model.ring_views()
+    start, count, _ = model.read_pointers()
+    out = []
+    for b in range(shape.B):
+        for j in range(int(count[b])):
+            s = (int(start[b]) + j) % shape.R
+            out.append((a[b, :, s].cpu().view(torch.int32), V[b, :, s].cpu().contiguous().view(torch.uint8),
+                        K[b, :, s].cpu().contiguous().view(torch.uint8)))
+    return out
+
+
+def _assert_same_state(m1, m2, shape, where):
+    s1, c1, e1 = m1.read_pointers()
+    s2, c2, e2 = m2.read_pointers()
+    assert e1 == 0 and e2 == 0, f"{where}: error word {e1} / {e2}"
+    assert torch.equal(s1, s2) and torch.equal(c1, c2), f"{where}: pointers differ"
+    assert torch.equal(m1.ckpt.view(torch.uint8), m2.ckpt.view(torch.uint8)), f"{where}: checkpoints differ"
+    if m1.copy is not None:
+        assert torch.equal(m1.copy, m2.copy), f"{where}: read copies differ"
+    for i, (x, y) in enumerate(zip(_live_ring(m1, shape), _live_ring(m2, shape))):
+        for part, name in zip(range(3), ("decays", "values", "keys")):
+            assert torch.equal(x[part], y[part]), f"{where}: live record {i}: {name} differ"
+
+
+def test_kernel_choice_and_refusal():
+    require_gpu()
+    shape = S(B=2, H=4, P=16, N=64, G=2, L=4, seed=90)
+    S0 = synth.initial_state(shape, synth.make_generator(shape.seed))
+    m = ReplaySSM(layer_shape(shape, "e4m3"), dev(S0))
+    assert m.decode_kernel() == "warp_per_head"
+    m.set_decode_kernel("head_kernel")
+    assert m.decode_kernel() == "head_kernel"
+    m.set_decode_kernel("auto")
+    assert m.decode_kernel() == "warp_per_head"
+    plain = ReplaySSM(layer_shape(shape), dev(S0))
+    assert plain.decode_kernel() == "head_kernel"
+    with pytest.raises(RssmError) as ei:
+        plain.set_decode_kernel("warp_per_head")
+    assert ei.value.status == RSSM_EUNSUPPORTED
+    assert plain.decode_kernel() == "head_kernel"
+
+
+@pytest.mark.parametrize("fmt,N,in_dtype", CASES)
+def test_staggered_steps_agree(fmt, N, in_dtype):
+    require_gpu()
+    shape = S(B=5, H=8, P=32, N=N, G=2, L=6, T_max=3, in_dtype=in_dtype, seed=91)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    mh = _model(shape, fmt, S0, "head_kernel")
+    mw = _model(shape, fmt, S0, "warp_per_head")
+    assert mh.decode_kernel() == "head_kernel" and mw.decode_kernel() == "warp_per_head"
+    rc = not fmt.startswith("f16")
+    orc = oracle.ReplayOracle(f64(S0), L=shape.L, R=shape.R, G=shape.G) if rc else None
+    mixed = 0
+    for rnd in range(3):
+        # stagger: a verify of T = 3 drafts and a commit of random accepted lengths
+        a, v, k, q = synth.verify_round_inputs(shape, 3, gen)
+        acc = synth.accepted_lengths(shape.B, 3, gen)
+        start, count, _ = mw.read_pointers()
+        if np.any(count.numpy() + 3 > shape.R):  # flush first where the drafts would not fit
+            for m in (mh, mw):
+                m.flush(1)
+            if orc is not None:
+                orc.flush(1)
+        for m in (mh, mw):
+            m.verify(dev(a), dev(v), dev(k), dev(q))
+            m.commit(dev(acc))
+        if orc is not None:
+            orc.verify(f64(a), f64(v), f64(k), f64(q))
+            orc.commit(acc.numpy())
+        _assert_same_state(mh, mw, shape, f"round {rnd} after commit")
+        for t in range(shape.L + 1):
+            a, v, k, q = synth.decode_step_inputs(shape, gen)
+            torch.cuda.synchronize()
+            copy_vals = _dequantized_copy(mw.copy, shape, fmt) if rc else None
+            recs_before = [list(r) for r in orc.records] if rc else None
+            oh = mh.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu().numpy().astype(np.float64)
+            ow = mw.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu().numpy().astype(np.float64)
+            where = f"round {rnd} step {t}"
+            assert slice_rel_err(ow, oh, 1) <= 1e-5, f"{where}: the two kernels' outputs differ"
+            _assert_same_state(mh, mw, shape, where)
+            if orc is None:
+                continue
+            o_ref, flushed = orc.decode(f64(a), f64(v), f64(k), f64(q))
+            mixed += int(flushed.any() and not flushed.all())
+            for b in range(shape.B):
+                if flushed[b]:
+                    assert slice_rel_err(ow[b], o_ref[b], 1) <= REL_TOL, f"{where} seq {b}: flush output"
+                    continue
+                alphas = np.stack([r[0] for r in recs_before[b]] + [f64(a)[b]])
+                vs = np.stack([r[1] for r in recs_before[b]] + [f64(v)[b]])
+                ks = np.stack([r[2] for r in recs_before[b]] + [f64(k)[b]])
+                o_copy = oracle.replay_output(copy_vals[b], alphas, vs, ks, f64(q)[b])
+                assert slice_rel_err(ow[b], o_copy, 1) <= REL_TOL, f"{where} seq {b}: non-flush output"
+    if orc is not None:
+        assert mixed > 0, "no step mixed flushing and non-flushing sequences"
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1", "f16_rn"])
+@pytest.mark.parametrize("qscale", [2.0 ** -100, 2.0 ** -60, 1.0, 2.0 ** 40, 2.0 ** 100, "spread"])
+def test_query_scales(fmt, qscale):
+    """bf16 queries from 2^-100 to 2^100: the warp-per-head step scales each group's query by a power
+    of two before its binary16 tile dot and back after, so its outputs agree with the head
+    kernel's FP32 dot (1e-5) and, for read copies, with the oracle's read-copy output (1e-4)."""
+    require_gpu()
+    shape = S(B=2, H=4, P=16, N=128, G=2, L=4, seed=92)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    mh = _model(shape, fmt, S0, "head_kernel")
+    mw = _model(shape, fmt, S0, "warp_per_head")
+    rc = not fmt.startswith("f16")
+    orc = oracle.ReplayOracle(f64(S0), L=shape.L, R=shape.R, G=shape.G) if rc else None
+    for t in range(shape.L - 1):  # non-flush steps only
+        a, v, k, q = synth.decode_step_inputs(shape, gen)
+        if qscale == "spread":  # elements from 2^-20 to 2^20 of each other in every group
+            mag = 2.0 ** torch.linspace(-20, 20, shape.N)
+            q = (q.float() * mag).to(q.dtype)
+        else:
+            q = (q.float() * qscale).to(q.dtype)
+        torch.cuda.synchronize()
+        copy_vals = _dequantized_copy(mw.copy, shape, fmt) if rc else None
+        recs_before = [list(r) for r in orc.records] if rc else None
+        oh = mh.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu().numpy().astype(np.float64)
+        ow = mw.decode_step(dev(a), dev(v), dev(k), dev(q)).cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(ow))
+        assert slice_rel_err(ow, oh, 1) <= 1e-5, f"step {t}: the two kernels' outputs differ"
+        _assert_same_state(mh, mw, shape, f"step {t}")
+        if orc is None:
+            continue
+        o_ref, flushed = orc.decode(f64(a), f64(v), f64(k), f64(q))
+        assert not flushed.any()
+        for b in range(shape.B):
+            alphas = np.stack([r[0] for r in recs_before[b]] + [f64(a)[b]])
+            vs = np.stack([r[1] for r in recs_before[b]] + [f64(v)[b]])
+            ks = np.stack([r[2] for r in recs_before[b]] + [f64(k)[b]])
+            o_copy = oracle.replay_output(copy_vals[b], alphas, vs, ks, f64(q)[b])
+            assert slice_rel_err(ow[b], o_copy, 1) <= REL_TOL, f"step {t} seq {b}"
