@@ -423,7 +423,10 @@ bool nonflush_applies(const rssm_ctx* h) {
 // then the head kernel for the flushing sequences, 1 the head kernel alone.
 int decode_kernel_for(const rssm_ctx* h) {
   if (!nonflush_applies(h) || h->decode_kernel == 1) return 1;
-  return 2;
+  if (h->decode_kernel == 2) return 2;
+  // automatic: the read copies; an FP16 checkpoint's 16 KiB tiles fit too few
+  // warps per SM, and the head kernel alone measures as fast there
+  return h->g.rf == rssm::kCkF16 ? 1 : 2;
 }
 
 // Enqueue one decode step with the parameters in p (pointers, inputs, ticket block set).

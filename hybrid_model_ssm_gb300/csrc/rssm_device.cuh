@@ -595,14 +595,38 @@ __global__ void __launch_bounds__(kThreads, 1) head_kernel(const Params p) {
   // before all CTAs of the sequence are done with them.
   bool lean = false;
   if constexpr (MODE == kDecode) {
-    if (p.nf_ok && h1 > h0) {
+    if (h1 > h0 && (p.nf_ok || p.skip_nonflush)) {
       bool need = false;
-      const int b_last = (int)((h1 - 1) / p.H);
-      for (int b = (int)(h0 / p.H) + lane; b <= b_last; b += 32) {
+      const int b_first = (int)(h0 / p.H), b_last = (int)((h1 - 1) / p.H);
+      for (int b = b_first + lane; b <= b_last; b += 32) {
         const int c = p.count[b];
         need |= (c >= 0 && c + 1 <= p.R && c + 1 >= p.L);
       }
-      lean = !__any_sync(kFull, need);
+      const bool none = !__any_sync(kFull, need);  // no sequence of this CTA flushes now
+      lean = p.nf_ok && none;
+      if (p.skip_nonflush && none) {
+        // Nothing to fold (the warp-per-head kernel took the outputs and appends):
+        // warp 0's lanes only advance the pointers, with the same tickets as below.
+        if (warp == 0) {
+          for (int b = b_first + lane; b <= b_last; b += 32) {
+            const int c = p.count[b];
+            if (c < 0 || c + 1 > p.R) {
+              atomicOr(p.err, kErrCapacity);
+              continue;
+            }
+            const long long lo = max(h0, (long long)b * p.H), hi = min(h1, (long long)(b + 1) * p.H);
+            const int n_b = (int)(hi - lo);
+            __threadfence();
+            const int prev = atomicAdd(p.ticket + b, n_b);
+            if (prev + n_b == p.H) {
+              __threadfence();
+              p.count[b] = c + 1;
+              p.ticket[b] = 0;
+            }
+          }
+        }
+        return;
+      }
     }
   }
   Layout lay;  // field by field, so that no copy goes through local memory

@@ -217,18 +217,19 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
  * writes it once (and refreshes the read copy), outputs o = S_new q, and
  * clears the buffer (start += h mod R, count = 0). A sequence with h > R sets
  * RSSM_ECAPACITY in the error word and is left untouched.
- * With an E4M3 or E2M1 read copy or an FP16 checkpoint the step is two kernels
- * by default (rssm_set_decode_kernel): a warp-per-head kernel computes the
- * non-flush sequences' outputs and appends their records, then the head kernel
- * folds the flushing sequences and advances every sequence's pointers. Other
- * configurations launch the head kernel alone. */
+ * With an E4M3 or E2M1 read copy the step is two kernels by default
+ * (rssm_set_decode_kernel; an FP16 checkpoint may choose them too): a
+ * warp-per-head kernel computes the non-flush sequences' outputs and appends
+ * their records, then the head kernel folds the flushing sequences and advances
+ * every sequence's pointers. Other configurations launch the head kernel alone. */
 rssm_status rssm_decode_step(rssm_handle h, const float* alpha, const void* v, const void* k,
                              const void* q, float* o, void* stream);
 
 /* Choose the kernels of this handle's decode steps (library control, no
- * counterpart in the pages): 0 automatic (the default), 1 the head kernel alone,
- * 2 the warp-per-head non-flush kernel before it. RSSM_EUNSUPPORTED for 2
- * unless the handle has an E4M3 or E2M1 read copy or an FP16 checkpoint.
+ * counterpart in the pages): 0 automatic (the default: 2 with a read copy, else
+ * 1), 1 the head kernel alone, 2 the warp-per-head non-flush kernel before it.
+ * RSSM_EUNSUPPORTED for 2 unless the handle has an E4M3 or E2M1 read copy or an
+ * FP16 checkpoint.
  * Both give the same outputs and state up to FP32 summation order. Host only. */
 rssm_status rssm_set_decode_kernel(rssm_handle h, int32_t kind);
 

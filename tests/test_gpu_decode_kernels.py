@@ -80,6 +80,10 @@ def test_kernel_choice_and_refusal():
     assert m.decode_kernel() == "head_kernel"
     m.set_decode_kernel("auto")
     assert m.decode_kernel() == "warp_per_head"
+    f16 = _model(shape, "f16_sr", S0, "auto")
+    assert f16.decode_kernel() == "head_kernel"  # automatic: FP16 checkpoints keep the head kernel
+    f16.set_decode_kernel("warp_per_head")
+    assert f16.decode_kernel() == "warp_per_head"
     plain = ReplaySSM(layer_shape(shape), dev(S0))
     assert plain.decode_kernel() == "head_kernel"
     with pytest.raises(RssmError) as ei:
