@@ -30,8 +30,9 @@ from tests.test_gpu_readcopy import _dequantized_copy
 pytestmark = pytest.mark.gpu
 
 S = synth.Shape
-CASES = [("e4m3", 64, "bf16"), ("e4m3", 128, "f32"), ("e2m1", 64, "f32"), ("e2m1", 128, "bf16"),
-         ("f16_sr", 128, "bf16"), ("f16_rn", 64, "f32")]
+# (format, N, input dtype, P): tiles from 2 KiB (E4M3 P=32 N=64) to 16 KiB (FP16)
+CASES = [("e4m3", 64, "bf16", 32), ("e4m3", 128, "f32", 32), ("e4m3", 128, "bf16", 64), ("e2m1", 64, "f32", 32),
+         ("e2m1", 128, "bf16", 64), ("e2m1", 128, "bf16", 128), ("f16_sr", 128, "bf16", 32), ("f16_rn", 64, "f32", 32)]
 
 
 def _model(shape, fmt, S0, kernel):
@@ -92,10 +93,10 @@ def test_kernel_choice_and_refusal():
     assert plain.decode_kernel() == "head_kernel"
 
 
-@pytest.mark.parametrize("fmt,N,in_dtype", CASES)
-def test_staggered_steps_agree(fmt, N, in_dtype):
+@pytest.mark.parametrize("fmt,N,in_dtype,P", CASES)
+def test_staggered_steps_agree(fmt, N, in_dtype, P):
     require_gpu()
-    shape = S(B=5, H=8, P=32, N=N, G=2, L=6, T_max=3, in_dtype=in_dtype, seed=91)
+    shape = S(B=5, H=8, P=P, N=N, G=2, L=6, T_max=3, in_dtype=in_dtype, seed=91)
     gen = synth.make_generator(shape.seed)
     S0 = synth.initial_state(shape, gen)
     mh = _model(shape, fmt, S0, "head_kernel")
@@ -114,12 +115,14 @@ def test_staggered_steps_agree(fmt, N, in_dtype):
                 m.flush(1)
             if orc is not None:
                 orc.flush(1)
-        for m in (mh, mw):
+        for m in (mh, mw):  # then fold the sequences that now hold L or more records
             m.verify(dev(a), dev(v), dev(k), dev(q))
             m.commit(dev(acc))
+            m.flush(shape.L)
         if orc is not None:
             orc.verify(f64(a), f64(v), f64(k), f64(q))
             orc.commit(acc.numpy())
+            orc.flush(shape.L)
         _assert_same_state(mh, mw, shape, f"round {rnd} after commit")
         for t in range(shape.L + 1):
             a, v, k, q = synth.decode_step_inputs(shape, gen)
