@@ -350,6 +350,10 @@ class DecodeArm:
         self.pool = decode_pool(s, self.ls, self.dev, gen, self.delta)
         self.out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=self.dev)
         self.launches = 0
+        # kernels per decode step: the warp-per-head non-flush kernel and the head kernel
+        # (read copies, by default), or the head kernel alone
+        self.decode_kernels = self.model.decode_kernel()
+        self.kernels_per_step = 2 if self.decode_kernels == "warp_per_head" else 1
 
     def step(self, x, o, st=None):
         if self.delta:
@@ -446,7 +450,8 @@ def run_ours(args, world, rank, local):
     n_windows = windows_for(args.steps, per_window, args.min_seconds)
     with ClockSampler(local) as clk:
         elapsed, launch_s = arm.timed(n_windows, world, clk)
-    timed_launches = len(launch_s)
+    timed_launches = len(launch_s) * arm.kernels_per_step
+    decode_kernels = arm.decode_kernels
     start, count, err = arm.model.read_pointers()
     elapsed_max = max_over_ranks(elapsed, world)
     seq_steps = world * s.B * L * n_windows
@@ -569,6 +574,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": timed_launches,
+        "decode_kernels": decode_kernels,
         "device_error_word": err,
     }
     line.update(extras)
@@ -603,8 +609,9 @@ def secondary_arms(args, world, rank, local) -> dict:
         elapsed = max_over_ranks(elapsed, world)
         out[key] = {"value": world * WORKLOAD.B * WORKLOAD.L * n / elapsed, "unit": UNIT,
                     "ms_per_window": elapsed / n * 1e3, "windows_timed": n,
-                    "roofline": arm.roofline(launch_s, peak, peak_kind, traffic), "gpu_launches": len(launch_s),
-                    "device_error_word": err}
+                    "roofline": arm.roofline(launch_s, peak, peak_kind, traffic),
+                    "decode_kernels": arm.decode_kernels,
+                    "gpu_launches": len(launch_s) * arm.kernels_per_step, "device_error_word": err}
         del arm
         torch.cuda.empty_cache()
     return out

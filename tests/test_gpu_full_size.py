@@ -217,3 +217,52 @@ def test_tensor_core_verify_b512_t16_24_rounds():
         assert err == 0
         assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count), f"round {r}"
     print(f"tensor-core verify b512 t16: worst output rel err {worst:.2e}")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+def test_read_copy_decode_b256_64_steps(fmt):
+    """The same Mamba-2 layer with a read copy, in bench.py's launch configuration (the
+    warp-per-head non-flush kernel, then the head kernel): every non-flush output of the
+    sampled sequences equals the oracle's output-only form on the device copy (1e-4), every
+    flush output the exact recurrence, and every sequence's pointers the oracle's."""
+    from tests.test_gpu_readcopy import _dequantized_copy
+
+    require_gpu()
+    shape = synth.PRESETS["mamba2_layer_b256_l16"]
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    model = ReplaySSM(layer_shape(shape, fmt), dev(S0))
+    assert model.decode_kernel() == "warp_per_head"
+    sample = _sample(shape.B)
+    sub = synth.Shape(B=len(sample), H=shape.H, P=shape.P, N=shape.N, G=shape.G, L=shape.L, seed=shape.seed)
+    orc = oracle.ReplayOracle(f64(S0[sample]), L=shape.L, R=shape.R, G=shape.G)
+    shadow = PointerShadow(shape.B, shape.L, shape.R)
+    del S0
+    idx = torch.as_tensor(sample, device="cuda")
+    worst = 0.0
+    for t in range(64):
+        a, v, k, q = synth.decode_step_inputs(shape, gen)
+        torch.cuda.synchronize()
+        copy_s = model.copy.view(shape.B, -1)[idx].reshape(-1)
+        copy_vals = _dequantized_copy(copy_s, sub, fmt)  # what this step's non-flush heads read
+        recs_before = [list(r) for r in orc.records]
+        o = model.decode_step(dev(a), dev(v), dev(k), dev(q))
+        o_s = o[idx].cpu().numpy().astype(np.float64)
+        a_s, v_s, k_s, q_s = (f64(x[sample]) for x in (a, v, k, q))
+        o_ref, flushed = orc.decode(a_s, v_s, k_s, q_s)
+        shadow.decode()
+        for i in range(len(sample)):
+            if flushed[i]:
+                e = slice_rel_err(o_s[i], o_ref[i], 1)
+            else:
+                alphas = np.stack([r[0] for r in recs_before[i]] + [a_s[i]])
+                vs = np.stack([r[1] for r in recs_before[i]] + [v_s[i]])
+                ks = np.stack([r[2] for r in recs_before[i]] + [k_s[i]])
+                e = slice_rel_err(o_s[i], oracle.replay_output(copy_vals[i], alphas, vs, ks, q_s[i]), 1)
+            worst = max(worst, e)
+            assert e <= REL_TOL, f"step {t} sequence {sample[i]}: rel err {e:.3g}"
+        if t % 16 == 15 or t < 3:
+            start, count, err = model.read_pointers()
+            assert err == 0
+            assert np.array_equal(start.numpy(), shadow.start) and np.array_equal(count.numpy(), shadow.count)
+    print(f"{fmt} read copy b256: worst output rel err {worst:.2e}")
