@@ -605,7 +605,7 @@ def secondary_arms(args, world, rank, local) -> dict:
         n = windows_for(args.steps, per_window, args.extra_seconds)
         elapsed, launch_s = arm.timed(n, world)
         err = arm.model.read_pointers()[2]
-        traffic = profiled_traffic("delta_decode_b256_l16") if key == "delta_rule" else None
+        traffic = profiled_traffic("delta_decode_b256_l16" if key == "delta_rule" else key + "_b256_l16")
         elapsed = max_over_ranks(elapsed, world)
         out[key] = {"value": world * WORKLOAD.B * WORKLOAD.L * n / elapsed, "unit": UNIT,
                     "ms_per_window": elapsed / n * 1e3, "windows_timed": n,
