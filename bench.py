@@ -595,7 +595,7 @@ def secondary_arms(args, world, rank, local) -> dict:
         torch.cuda.empty_cache()
         if v is not None:
             out[key] = {k: v[k] for k in ("metric", "value", "unit", "ms_per_step", "verify_kernel", "roofline",
-                                          "breakdown_ms_per_round", "comparison", "gpu_launches",
+                                          "breakdown_ms_per_round", "comparison", "clocks", "gpu_launches",
                                           "device_error_word") if k in v}
             out[key]["rounds_timed"] = v["config"]["rounds_timed"]
     for key, kw in (("read_copy_e4m3", {"read_fmt": "e4m3"}), ("read_copy_e2m1", {"read_fmt": "e2m1"}),
@@ -603,14 +603,15 @@ def secondary_arms(args, world, rank, local) -> dict:
         arm = DecodeArm(WORKLOAD, local, rank, **kw)
         per_window = arm.warm(args.warmup)
         n = windows_for(args.steps, per_window, args.extra_seconds)
-        elapsed, launch_s = arm.timed(n, world)
+        with ClockSampler(local) as clk:
+            elapsed, launch_s = arm.timed(n, world, clk)
         err = arm.model.read_pointers()[2]
         traffic = profiled_traffic("delta_decode_b256_l16" if key == "delta_rule" else key + "_b256_l16")
         elapsed = max_over_ranks(elapsed, world)
         out[key] = {"value": world * WORKLOAD.B * WORKLOAD.L * n / elapsed, "unit": UNIT,
                     "ms_per_window": elapsed / n * 1e3, "windows_timed": n,
                     "roofline": arm.roofline(launch_s, peak, peak_kind, traffic),
-                    "decode_kernels": arm.decode_kernels,
+                    "clocks": clk.summary(), "decode_kernels": arm.decode_kernels,
                     "gpu_launches": len(launch_s) * arm.kernels_per_step, "device_error_word": err}
         del arm
         torch.cuda.empty_cache()
