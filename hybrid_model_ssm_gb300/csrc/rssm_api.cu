@@ -264,11 +264,14 @@ rssm_status plan_tc(const rssm_config* c, const Geom& g, int T, rssm::TcParams* 
   const size_t budget = (size_t)kSmemMax - fixed;
   size_t slots = 4;
   size_t stages = std::min<size_t>(kTcMaxStages, budget >= slots * slot ? (budget - slots * slot) / kTcStageBytes : 0);
-  if (stages < 2 * NKB) {
+  if (stages < (size_t)kTcSets * NKB) {
     slots = 2;
     stages = std::min<size_t>(kTcMaxStages, (budget - slots * slot) / kTcStageBytes);
   }
-  if (stages < NKB) return fail(RSSM_EUNSUPPORTED, "the tensor-core verify does not fit shared memory");
+  // each row-warp set keeps its own stages: a multiple of kTcSets items' K-blocks
+  stages -= stages % ((size_t)kTcSets * NKB);
+  if (stages < (size_t)kTcSets * NKB)
+    return fail(RSSM_EUNSUPPORTED, "the tensor-core verify does not fit shared memory");
   tp->stages = (int)stages;
   tp->slots = (int)slots;
   size_t off = stages * kTcStageBytes;

@@ -25,10 +25,13 @@
 //   coefficients  per group: K^T Q and the queries as the B operand (fp32,
 //                 swizzled); per item: the decay products g_t and the record
 //                 weights, the appends of draft decays and keys
-//   row warps     thread = checkpoint row: split each K-block into hi (written
-//                 back in place) and lo (into tensor memory); after the MMAs,
-//                 the epilogue o[t] = g_t (S q_t) + sum_j w_tj v_j[row], the
-//                 output store and the appends of the draft value rows
+//   row warps     two sets of eight, taking alternate items (each set owns one
+//                 tensor-memory buffer, and its items' tile stages and record
+//                 slots), so that two items' chains overlap. Thread = checkpoint
+//                 row: split each K-block into hi (written back in place) and lo
+//                 (into tensor memory); after the MMAs, the epilogue
+//                 o[t] = g_t (S q_t) + sum_j w_tj v_j[row], the output store and
+//                 the appends of the draft value rows
 // Every wait is bounded (the same waits as the head kernel); a CTA that gives
 // up drains its copies and MMAs and frees its tensor memory before it returns.
 #pragma once
@@ -46,8 +49,11 @@ constexpr int kTcKB = 32;                // fp32 columns per K-block (128 bytes)
 constexpr int kTcStageBytes = kTcRows * kTcKB * 4;  // 16 KiB
 constexpr int kTcMaxStages = 12;
 constexpr int kTcMaxSlots = 8;
-constexpr int kTcRowWarps = 8;           // two per tensor-memory lane quarter
-constexpr int kTcTmaWarp = 8, kTcGatherWarp = 9, kTcMmaWarp = 10, kTcCoef0 = 11;
+constexpr int kTcSets = 2;               // row-warp sets, taking alternate items
+constexpr int kTcSetWarps = 8;           // row warps of a set: two per tensor-memory lane quarter
+constexpr int kTcRowWarps = kTcSets * kTcSetWarps;
+constexpr int kTcTmaWarp = kTcRowWarps, kTcGatherWarp = kTcRowWarps + 1, kTcMmaWarp = kTcRowWarps + 2;
+constexpr int kTcCoef0 = kTcRowWarps + 3;
 constexpr int kTcCoefWarps = 2;
 constexpr int kTcThreads = (kTcCoef0 + kTcCoefWarps) * 32;
 constexpr uint32_t kTcCols = 512;        // tensor memory: two buffers of 256 columns
@@ -106,9 +112,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const long long i0 = (long long)blockIdx.x * total / gridDim.x;
   const long long i1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
 
-  // The swizzled operands need a 1024-byte aligned base; refuse any other plan.
-  if ((smem_u32(smem) & 1023u) != 0 || p.stages < NKB || p.stages > kTcMaxStages || p.slots < 2 ||
-      p.slots > kTcMaxSlots || (p.slots % kTcCoefWarps) != 0 || p.T < 1 || p.T > kTcT) {
+  // The swizzled operands need a 1024-byte aligned base. Every tile stage and
+  // record slot must belong to one row-warp set for good (its items come every
+  // other item), so that a set never waits on an entry the other set still holds:
+  // stages a multiple of kTcSets K-blocks per item, slots a multiple of kTcSets.
+  // Refuse any other plan.
+  if ((smem_u32(smem) & 1023u) != 0 || p.stages < kTcSets * NKB || (p.stages % (kTcSets * NKB)) != 0 ||
+      p.stages > kTcMaxStages || p.slots < 2 || p.slots > kTcMaxSlots || (p.slots % kTcCoefWarps) != 0 ||
+      (p.slots % kTcSets) != 0 || p.T < 1 || p.T > kTcT) {
     if (threadIdx.x == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       atomicOr(p.err, kErrPlan);
@@ -124,7 +135,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < p.slots; ++s) {
       mbar_init(sfull0 + 8 * s, 1);
       mbar_init(scoef0 + 8 * s, 1);
-      mbar_init(sempty0 + 8 * s, kTcRowWarps);
+      mbar_init(sempty0 + 8 * s, kTcSetWarps);  // the row warps of the item's set
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(dfull0 + 8 * s, 1);
@@ -424,7 +435,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bulk_wait_all();
   } else {
     // ====================================================================== row warps
-    const int quarter = warp & 3, half = warp >> 2;
+    const int set = warp / kTcSetWarps, sw = warp - set * kTcSetWarps;  // this warp's set and rank in it
+    const int quarter = sw & 3, half = sw >> 2;
     const int row = 32 * quarter + lane;         // checkpoint row of the item (tensor-memory lane)
     const int hj = row / P, pr = row - hj * P;   // head within the item, row within the head
     const uint32_t tl = (uint32_t)(32 * quarter) << 16;
@@ -490,6 +502,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       item_of(it, b, hh0, g);
       if (b != cur_b) { cur_b = b; seq_plan(b, c, st, load); }
       if (!load) continue;
+      if ((ii % kTcSets) != set) {  // the other set's item: count its stages, buffer and slot
+        li += NKB;
+        ++ii;
+        ++si;
+        continue;
+      }
+      // ---- the set's previous item's epilogue first: its MMAs have completed once its
+      // accumulator is read (the wait inside), so this item's split may overwrite the
+      // buffer's lo columns and this item's MMAs its accumulator. The other set's
+      // work fills the SM meanwhile.
+      if (pend && !epilogue()) { ok = false; break; }
+      pend = false;
       // ---- split: hi back in place, lo into this item's tensor-memory buffer. The
       // four warps of a half take K-blocks half, half + 2, ...: whole 128-byte rows,
       // one 32-column store to tensor memory each, one fence sequence per item.
@@ -520,8 +544,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0)
         for (int kb = half; kb < NKB; kb += 2) mbar_arrive(sdone0 + 8 * ((li + kb) % p.stages));
       li += NKB;
-      // ---- the previous item's epilogue (its MMAs ran while this item was split)
-      if (pend && !epilogue()) { ok = false; break; }
       pend = true;
       pb = b; phh = hh0; pc = c; pst = st; pii = ii; psl = si % p.slots; puse = si / p.slots;
       ++ii;
