@@ -11,7 +11,8 @@
 // a 1e-4 tolerance, so the checkpoint is split S = hi + lo, hi = S with its low
 // 13 mantissa bits cleared (exact in TF32), lo = S - hi (exact in fp32, and its
 // own TF32 rounding costs only 2^-21 of S). bf16 queries are exact in TF32.
-// The product is hi Q + lo Q: hi from shared memory, lo from tensor memory.
+// The product is hi Q + lo Q: hi is the tile as it sits in shared memory (a
+// kind::tf32 operand's low 13 mantissa bits are ignored), lo from tensor memory.
 //
 // An item is 128 checkpoint rows: 128/P consecutive heads of one group, which
 // share their queries, so one M = 128 MMA serves them. Warp roles:
@@ -28,8 +29,8 @@
 //   row warps     two sets of eight, taking alternate items (each set owns one
 //                 tensor-memory buffer, and its items' tile stages and record
 //                 slots), so that two items' chains overlap. Thread = checkpoint
-//                 row: split each K-block into hi (written back in place) and lo
-//                 (into tensor memory); after the MMAs, the epilogue
+//                 row: form each K-block's lo = S - hi (into tensor memory; the
+//                 MMAs read hi from the tile as stored); after the MMAs, the epilogue
 //                 o[t] = g_t (S q_t) + sum_j w_tj v_j[row], the output store and
 //                 the appends of the draft value rows
 // Every wait is bounded (the same waits as the head kernel); a CTA that gives
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // work fills the SM meanwhile.
       if (pend && !epilogue()) { ok = false; break; }
       pend = false;
-      // ---- split: hi back in place, lo into this item's tensor-memory buffer. The
+      // ---- split: lo = S - hi into this item's tensor-memory buffer. The
       // four warps of a half take K-blocks half, half + 2, ...: whole 128-byte rows,
       // one 32-column store to tensor memory each, one fence sequence per item.
       const uint32_t lo0 = tbase + tl + (uint32_t)(ii & 1) * 256u;
@@ -525,10 +526,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t lo[32];
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          uint4* ptr = reinterpret_cast<uint4*>(tile + ((ch ^ (row & 7)) << 4));
-          const uint4 x = *ptr;
+          // kind::tf32 reads an fp32 operand's sign, exponent and top 10 mantissa bits
+          // and ignores the low 13: the MMA of the tile as stored is the MMA of hi
+          const uint4 x = *reinterpret_cast<const uint4*>(tile + ((ch ^ (row & 7)) << 4));
           const uint4 h = make_uint4(x.x & 0xFFFFE000u, x.y & 0xFFFFE000u, x.z & 0xFFFFE000u, x.w & 0xFFFFE000u);
-          *ptr = h;
           lo[4 * ch + 0] = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(h.x));
           lo[4 * ch + 1] = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(h.y));
           lo[4 * ch + 2] = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(h.z));

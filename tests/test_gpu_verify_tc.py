@@ -62,7 +62,10 @@ def test_kernel_choice():
 
 
 def test_tensor_core_and_cuda_core_verify_agree():
-    """Both kernels on the same state and drafts (T = 8): each within 1e-4 of the other."""
+    """Both kernels on the same state and drafts (T = 8): within 1e-5 of each other (1.9e-6
+    measured). The tensor-core kernel reads the checkpoint tile as stored and lets kind::tf32
+    ignore the low 13 mantissa bits (its hi part); a conversion that rounded instead would
+    leave about 1e-4 here."""
     require_gpu()
     shape = S(B=6, H=16, P=64, N=128, G=2, L=16, T_max=8, seed=68)
     gen = synth.make_generator(shape.seed)
@@ -74,7 +77,7 @@ def test_tensor_core_and_cuda_core_verify_agree():
         a, v, k, q = (dev(x) for x in synth.verify_round_inputs(shape, 8, gen))
         oa, ob = ma.verify(a, v, k, q).cpu().double(), mb.verify(a, v, k, q).cpu().double()
         rel = ((oa - ob).abs().amax(-1) / ob.abs().amax(-1).clamp_min(1e-30)).max().item()
-        assert rel <= 1e-4, f"round {r}: {rel:.3g}"
+        assert rel <= 1e-5, f"round {r}: {rel:.3g}"
         acc = dev(synth.accepted_lengths(shape.B, 8, gen))
         for m in (ma, mb):
             m.commit(acc)
