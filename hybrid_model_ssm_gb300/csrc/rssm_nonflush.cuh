@@ -373,6 +373,11 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
         volatile int dummy = 0;
         mbar_wait(bar0 + 8u * buf, (phase >> buf) & 1u, &dummy, p.err);
         if (more) mbar_wait(bar0 + 8u * (buf ^ 1), (phase >> (buf ^ 1)) & 1u, &dummy, p.err);
+        // The heads from here on get no output or append. Their sequences keep their
+        // pointers, as after an aborted head-kernel CTA: the head kernel advances a
+        // sequence only when its ticket reaches H, and rssm_clear_error resets tickets.
+        const int b_last = (int)((h1 - 1) / p.H);
+        for (int b = cur.b; b <= b_last; ++b) atomicAdd(p.ticket + b, -(1 << 20));
       }
       __syncwarp();
       return;

@@ -322,7 +322,9 @@ rssm_status rssm_read_pointers(rssm_handle h, int32_t* start_host, int32_t* coun
 /* Clear the device error word and reset the per-sequence ticket counters of the
  * pointer block (asynchronous, two memsets on `stream`; library plumbing, no
  * counterpart in the pages). A launch whose bounded wait expired (bit 4) can
- * leave the tickets of its sequences part-counted; call this before the next
+ * leave the tickets of its sequences part-counted, so that their pointers stay
+ * where they were (in a two-kernel decode step, the sequences whose heads the
+ * warp-per-head kernel did not finish as well); call this before the next
  * decode step or flush on the handle, with no launch of the handle in flight. */
 rssm_status rssm_clear_error(rssm_handle h, void* stream);
 
