@@ -1,6 +1,6 @@
 // rssm_nonflush.cuh - the non-flush decode step for small head tiles (an E4M3 or
-// E2M1 read copy, or an FP16 checkpoint): one warp per head, no shared-memory
-// pipeline and no waits.
+// E2M1 read copy, or an FP16 checkpoint): one warp per head, each warp with its
+// own double-buffered stages and nothing shared between the warps.
 //
 // The output-only step (aikraft.ru, "ReplaySSM: Революция в декодировании
 // гибридных моделей", §03 unrolled window, §05 output-only evaluation, §06 split
