@@ -190,3 +190,55 @@ def test_query_scales(fmt, qscale):
             ks = np.stack([r[2] for r in recs_before[b]] + [f64(k)[b]])
             o_copy = oracle.replay_output(copy_vals[b], alphas, vs, ks, f64(q)[b])
             assert slice_rel_err(ow[b], o_copy, 1) <= REL_TOL, f"step {t} seq {b}"
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+def test_read_copy_step_replayed_from_a_cuda_graph(fmt):
+    """A read-copy decode step (the warp-per-head kernel, then the head kernel) captured once
+    in a CUDA graph and replayed across flush boundaries: every output against the oracle's
+    read-copy form on the device copy (non-flush) or the exact recurrence (flush)."""
+    require_gpu()
+    shape = S(B=3, H=8, P=32, N=128, G=2, L=6, seed=93)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    model = ReplaySSM(layer_shape(shape, fmt), dev(S0))
+    assert model.decode_kernel() == "warp_per_head"
+    orc = oracle.ReplayOracle(f64(S0), L=shape.L, R=shape.R, G=shape.G)
+    buf = tuple(dev(x) for x in synth.decode_step_inputs(shape, synth.make_generator(0)))
+    out = torch.empty((shape.B, shape.H, shape.P), device="cuda")
+    graph, flushes = None, 0
+    for t in range(4 * shape.L):
+        a, v, k, q = synth.decode_step_inputs(shape, gen)
+        for d, h in zip(buf, (a, v, k, q)):
+            d.copy_(h)
+        torch.cuda.synchronize()
+        copy_vals = _dequantized_copy(model.copy, shape, fmt)
+        recs_before = [list(r) for r in orc.records]
+        if t < shape.L + 2:
+            model.decode_step(*buf, out=out)
+        else:
+            if graph is None:
+                graph = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(graph, stream=side):  # records the launches only
+                        model.decode_step(*buf, out=out)
+                torch.cuda.current_stream().wait_stream(side)
+            graph.replay()
+        o = out.cpu().numpy().astype(np.float64)
+        o_ref, flushed = orc.decode(f64(a), f64(v), f64(k), f64(q))
+        flushes += int(flushed.any())
+        for b in range(shape.B):
+            if flushed[b]:
+                assert slice_rel_err(o[b], o_ref[b], 1) <= REL_TOL, f"step {t} seq {b}: flush output"
+                continue
+            alphas = np.stack([r[0] for r in recs_before[b]] + [f64(a)[b]])
+            vs = np.stack([r[1] for r in recs_before[b]] + [f64(v)[b]])
+            ks = np.stack([r[2] for r in recs_before[b]] + [f64(k)[b]])
+            o_copy = oracle.replay_output(copy_vals[b], alphas, vs, ks, f64(q)[b])
+            assert slice_rel_err(o[b], o_copy, 1) <= REL_TOL, f"step {t} seq {b}: non-flush output"
+    assert flushes == 4
+    start, count, err = model.read_pointers()
+    assert err == 0
+    assert np.array_equal(start.numpy(), orc.start) and np.array_equal(count.numpy(), orc.count)
