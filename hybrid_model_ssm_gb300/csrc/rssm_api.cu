@@ -335,6 +335,7 @@ struct rssm_ctx {
   int last_T;         // draft count of the last verify, 0 when none is pending
   int verify_kernel;  // 0 automatic, 1 CUDA cores, 2 tensor cores
   int decode_kernel;  // 0 automatic, 1 the pipelined head kernel only, 2 warp-per-head non-flush step first
+  Plan dplan;         // the decode launch plan with the handle's buffers filled in (made once, at creation)
 };
 
 namespace {
@@ -554,6 +555,12 @@ rssm_status rssm_create(const rssm_config* cfg, void* ckpt, void* ring, void* pt
   h->last_T = 0;
   h->verify_kernel = 0;
   h->decode_kernel = 0;
+  s = plan_smem(cfg, g, &h->dplan, LayoutKind::kNonFlush);
+  if (s != RSSM_OK) {
+    delete h;
+    return s;
+  }
+  fill_common(h, &h->dplan.p);
   std::memset(&h->tmap, 0, sizeof(h->tmap));
   if (g.tc_ok && cfg->T_max > 1) {
     s = make_ckpt_tensor_map(cfg, ckpt, &h->tmap);
@@ -614,10 +621,7 @@ rssm_status decode_impl(rssm_handle h, const float* alpha, const float* beta, co
   if (!alpha || !v || !k || !q || !o) return fail(RSSM_EINVAL, "NULL tensor");
   if (!aligned16(alpha) || !aligned16(v) || !aligned16(k) || !aligned16(q) || !aligned16(o))
     return fail(RSSM_EINVAL, "tensors must be 16-byte aligned");
-  Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kNonFlush);
-  if (s != RSSM_OK) return s;
-  fill_common(h, &pl.p);
+  Plan pl = h->dplan;  // planned at creation; only the inputs change per step
   pl.p.alpha = alpha; pl.p.beta = beta; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
   const cudaError_t e = launch_decode_step(h, pl.p, pl.smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -970,10 +974,7 @@ rssm_status rssm_decode_step_static_scratch(rssm_handle h, const float* alpha, c
     }
     tickets = g_static_ticket_addr[dev];
   }
-  Plan pl;
-  const rssm_status s = plan_smem(&h->cfg, h->g, &pl, LayoutKind::kNonFlush);
-  if (s != RSSM_OK) return s;
-  fill_common(h, &pl.p);
+  Plan pl = h->dplan;
   pl.p.ticket = tickets;
   pl.p.alpha = alpha; pl.p.v = v; pl.p.k = k; pl.p.q = q; pl.p.o = o;
   // The array keeps the last call's contents; the tickets must start at zero.

@@ -9,6 +9,7 @@ the import raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from dataclasses import dataclass
@@ -220,11 +221,18 @@ class ReplaySSM:
         self.ptrs = torch.empty(ptr_b, dtype=torch.uint8, device=dev)
         self.copy = torch.empty(copy_b, dtype=torch.uint8, device=dev) if copy_b else None
         self._cfg = shape.config()
+        self._dev_index = dev.index if dev.index is not None else torch.cuda.current_device()
         h = ctypes.c_void_p()
         with torch.cuda.device(dev):
             _check(lib().rssm_create(ctypes.byref(self._cfg), _ptr(ckpt), _ptr(self.ring), _ptr(self.ptrs),
                                      _ptr(self.copy), _stream_ptr(stream), ctypes.byref(h)))
         self._h = h
+
+    def _on_device(self):
+        """The layer's device made current for a call (nothing to do when it already is)."""
+        if torch.cuda.current_device() == self._dev_index:
+            return contextlib.nullcontext()
+        return torch.cuda.device(self._dev_index)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -245,7 +253,7 @@ class ReplaySSM:
         if out is None:
             out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=d)
         _expect(out, (s.B, s.H, s.P), torch.float32, "out", d)
-        with torch.cuda.device(d):
+        with self._on_device():
             if beta is None:
                 _check(lib().rssm_decode_step(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q), _ptr(out),
                                               _stream_ptr(stream)))
