@@ -413,7 +413,7 @@ bool nonflush_applies_fmt(const rssm_ctx* h) {
 rssm::NfStage nonflush_stage(const rssm_ctx* h) {
   const rssm_config& c = h->cfg;
   const int tile = h->g.rf == rssm::kCkF16 ? c.P * c.N * 2 : (int)h->g.head_stride;
-  return rssm::nf_stage(tile, h->g.R, h->g.Rp, c.P, h->g.esize);
+  return rssm::nf_stage(tile, c.L, h->g.Rp, c.P, h->g.esize);
 }
 int nonflush_warps(const rssm::NfStage& sg) {
   return std::min(rssm::kNfMaxWarps, (rssm::kSmemMax - rssm::kNfCtaBytes) / rssm::nf_warp_bytes(sg));

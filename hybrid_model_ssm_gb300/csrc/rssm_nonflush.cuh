@@ -10,10 +10,11 @@
 // The pipelined head kernel pays a fixed cost per head (mbarrier round trips
 // between its roles, one gather lane) that a 4.9-16 KiB tile cannot hide. Here
 // each warp walks a contiguous run of heads on its own. One lane copies the next
-// head's tile, value rows and decays into the warp's other shared-memory stage
-// with bulk copies (an mbarrier per stage counts their bytes) while the warp
-// computes the current head, so every head costs one overlapped round trip
-// however many records it holds. The keys' dots with the query are computed
+// head's tile and decays into the warp's other tile stage with bulk copies (an
+// mbarrier per stage counts their bytes) while the warp computes the current
+// head; the value rows, needed only at the end of a head, have one stage that
+// is refilled for the next head as soon as the current head's value term is
+// done. Every head costs one overlapped round trip however many records it holds. The keys' dots with the query are computed
 // once per group, from registers. Every wait is bounded, as in the head kernel.
 //
 // Sequences that flush in this step, and sequences whose ring would overflow,
@@ -28,18 +29,21 @@ namespace rssm {
 
 constexpr int kNfBatch = 8;  // tile chunks per lane between row reductions
 
-// Per-warp shared memory of the warp-per-head step: two mbarriers (one per stage),
-// the tile dots (P <= 128 floats), then two stages of [tile | value rows in
-// record order (at most R) | the ring's decays (Rp)], each filled by bulk copies.
+// Per-warp shared memory of the warp-per-head step: three mbarriers (two tile
+// stages, one value stage), the tile dots (P floats), two tile stages of
+// [tile | the ring's decays (Rp)], and one value stage of the head's value rows
+// in record order (at most L - 1: a sequence with L - 1 buffered records folds).
 struct NfStage {
-  int tile_bytes, v_off, a_off, bytes;
+  int tile_bytes, a_off, tbytes, vbytes, rsum_bytes;
 };
-__host__ __device__ inline NfStage nf_stage(int tile_bytes, int R, int Rp, int P, int in_bytes) {
+__host__ __device__ inline NfStage nf_stage(int tile_bytes, int L, int Rp, int P, int in_bytes) {
   NfStage g;
   g.tile_bytes = tile_bytes;
-  g.v_off = (tile_bytes + 15) / 16 * 16;
-  g.a_off = g.v_off + R * P * in_bytes;
-  g.bytes = (g.a_off + Rp * 4 + 127) / 128 * 128;
+  g.a_off = (tile_bytes + 15) / 16 * 16;
+  g.tbytes = (g.a_off + Rp * 4 + 127) / 128 * 128;
+  const int vrows = L > 1 ? L - 1 : 1;
+  g.vbytes = (vrows * P * in_bytes + 127) / 128 * 128;
+  g.rsum_bytes = (P * 4 + 127) / 128 * 128;
   return g;
 }
 // Order this thread's earlier generic-proxy accesses to shared memory before its
@@ -47,10 +51,11 @@ __host__ __device__ inline NfStage nf_stage(int tile_bytes, int R, int Rp, int P
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-constexpr int kNfCtaBytes = 128;         // the CTA's abort flag, padded
-constexpr int kNfBarBytes = 128;         // the two stage barriers, padded
-constexpr int kNfRowSumBytes = 128 * 4;  // the tile dots
-__host__ __device__ inline int nf_warp_bytes(const NfStage& g) { return kNfBarBytes + kNfRowSumBytes + 2 * g.bytes; }
+constexpr int kNfCtaBytes = 128;  // the CTA's abort flag, padded
+constexpr int kNfBarBytes = 32;   // a warp's three stage barriers, padded (stages stay 16-byte aligned)
+__host__ __device__ inline int nf_warp_bytes(const NfStage& g) {
+  return kNfBarBytes + g.rsum_bytes + 2 * g.tbytes + g.vbytes;
+}
 
 // A head tile as rows of 16-byte chunks: CW columns per chunk, CPR chunks per row.
 template <int N, int RF>
@@ -226,12 +231,15 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
   volatile int* abort_flag = reinterpret_cast<volatile int*>(nf_smem);
   if (threadIdx.x == 0) *abort_flag = 0;
   uint8_t* wbase = nf_smem + kNfCtaBytes + (size_t)warp * nf_warp_bytes(sg);
-  const uint32_t bar0 = smem_u32(wbase);  // stage b's barrier at bar0 + 8 b
+  const uint32_t bar0 = smem_u32(wbase);  // tile stage b's barrier at bar0 + 8 b, the value stage's at bar0 + 16
+  const uint32_t vbar = bar0 + 16;
   float* rsum = reinterpret_cast<float*>(wbase + kNfBarBytes);
-  const uint32_t stage0 = smem_u32(wbase + kNfBarBytes + kNfRowSumBytes);
+  uint8_t* const tstage = wbase + kNfBarBytes + sg.rsum_bytes;  // tile stage b at tstage + b tbytes
+  const uint8_t* const sv = tstage + 2 * sg.tbytes;             // the value stage
   if (lane == 0) {
     mbar_init(bar0, 1);
     mbar_init(bar0 + 8, 1);
+    mbar_init(vbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -261,29 +269,64 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
     }
     return false;
   };
-  // Bulk-copy a head's tile, value rows (record order: the committed ones are at most
-  // two contiguous ring runs, then the step's own) and the ring's decays into stage
-  // `buf`; every lane returns the step's own decay (read now, used one head later).
-  auto issue = [&](const NfHead& r, int buf) -> float {
+  // Bulk-copy a head's tile and the ring's decays into tile stage `buf`; every lane
+  // returns the step's own decay (read now, used one head later).
+  auto issue_tile = [&](const NfHead& r, int buf) -> float {
     const size_t hrow = (size_t)r.b * p.H + r.hh;
     if (lane == 0) {
-      const uint32_t dst = stage0 + (uint32_t)buf * sg.bytes, bar = bar0 + 8u * buf;
+      const uint32_t dst = smem_u32(tstage + (size_t)buf * sg.tbytes), bar = bar0 + 8u * buf;
       const uint8_t* tile = (RF == kCkF16) ? reinterpret_cast<const uint8_t*>(p.ckpt) + hrow * (size_t)p.P * N * 2
                                            : p.copy + hrow * (size_t)p.head_stride;
-      const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * (size_t)vrow;
       fence_proxy_async_shared();  // the warp's earlier reads of this stage come first
-      mbar_arrive_tx(bar, (uint32_t)(sg.tile_bytes + (r.c + 1) * vrow + p.Rp * 4));
+      mbar_arrive_tx(bar, (uint32_t)(sg.tile_bytes + p.Rp * 4));
       tma_load_1d(dst, tile, (uint32_t)sg.tile_bytes, bar);
-      if (r.c > 0) {
-        const int n1 = min(r.c, p.R - r.st);
-        tma_load_1d(dst + sg.v_off, rv + (size_t)r.st * vrow, (uint32_t)(n1 * vrow), bar);
-        if (r.c > n1) tma_load_1d(dst + sg.v_off + n1 * vrow, rv, (uint32_t)((r.c - n1) * vrow), bar);
-      }
-      tma_load_1d(dst + sg.v_off + r.c * vrow, reinterpret_cast<const uint8_t*>(p.v) + hrow * (size_t)vrow,
-                  (uint32_t)vrow, bar);
       tma_load_1d(dst + sg.a_off, p.ring_a + hrow * p.Rp, (uint32_t)(p.Rp * 4), bar);
     }
     return p.alpha[hrow];
+  };
+  // Bulk-copy a head's value rows into the value stage, in record order: the
+  // committed ones are at most two contiguous ring runs, then the step's own.
+  auto issue_values = [&](const NfHead& r) {
+    if (lane == 0) {
+      const size_t hrow = (size_t)r.b * p.H + r.hh;
+      const uint32_t dst = smem_u32(sv);
+      const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + hrow * p.R * (size_t)vrow;
+      fence_proxy_async_shared();
+      mbar_arrive_tx(vbar, (uint32_t)((r.c + 1) * vrow));
+      if (r.c > 0) {
+        const int n1 = min(r.c, p.R - r.st);
+        tma_load_1d(dst, rv + (size_t)r.st * vrow, (uint32_t)(n1 * vrow), vbar);
+        if (r.c > n1) tma_load_1d(dst + n1 * vrow, rv, (uint32_t)((r.c - n1) * vrow), vbar);
+      }
+      tma_load_1d(dst + r.c * vrow, reinterpret_cast<const uint8_t*>(p.v) + hrow * (size_t)vrow, (uint32_t)vrow,
+                  vbar);
+    }
+  };
+  // Wait (bounded) for a barrier's next phase. On failure, lane 0 waits (bounded)
+  // for every copy still in flight into this warp's stages (bits of `pend`: tile
+  // stages 0 and 1, the value stage) and keeps the pointers of the sequences of
+  // the heads not done, and the warp leaves.
+  uint32_t phase = 0;  // bit i: the parity barrier i (tile 0, tile 1, values) completes next
+  uint32_t pend = 0;   // bit i: a copy issued on barrier i not yet waited for
+  auto wait_or_leave = [&](int i, int b_first) -> bool {
+    const uint32_t bar = bar0 + 8u * i;
+    if (__all_sync(kFull, mbar_wait(bar, (phase >> i) & 1u, abort_flag, p.err))) {
+      phase ^= 1u << i;
+      pend &= ~(1u << i);
+      return true;
+    }
+    if (lane == 0) {
+      volatile int dummy = 0;
+      for (int j = 0; j < 3; ++j)
+        if ((pend >> j) & 1u) mbar_wait(bar0 + 8u * j, (phase >> j) & 1u, &dummy, p.err);
+      // The heads from here on get no output or append. Their sequences keep their
+      // pointers, as after an aborted head-kernel CTA: the head kernel advances a
+      // sequence only when its ticket reaches H, and rssm_clear_error resets tickets.
+      const int b_last = (int)((h1 - 1) / p.H);
+      for (int b = b_first; b <= b_last; ++b) atomicAdd(p.ticket + b, -(1 << 20));
+    }
+    __syncwarp();
+    return false;
   };
 
   long long cur_g = -1;
@@ -293,12 +336,20 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
   float qs_lo = 1.f, qs_hi = 1.f;   // 2^-s in two exact factors (bf16 inputs)
   NfHead cur, nxt;
   bool have = find(cur);
-  float acur = have ? issue(cur, 0) : 1.f;  // the current head's own decay
+  float acur = 1.f;  // the current head's own decay
+  if (have) {
+    acur = issue_tile(cur, 0);
+    issue_values(cur);
+    pend = 1u | 4u;
+  }
   int buf = 0;
-  uint32_t phase = 0;  // bit b: the parity stage b's barrier completes next
   while (have) {
     const bool more = find(nxt);
-    const float anxt = more ? issue(nxt, buf ^ 1) : 1.f;
+    float anxt = 1.f;
+    if (more) {
+      anxt = issue_tile(nxt, buf ^ 1);
+      pend |= 1u << (buf ^ 1);
+    }
     const int c = cur.c, st = cur.st, J = c + 1;
     const size_t grow = (size_t)cur.b * p.G + cur.g;
     const size_t hrow = (size_t)cur.b * p.H + cur.hh;
@@ -366,26 +417,10 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
       if (cur.gpos == 0) kn.store(reinterpret_cast<uint8_t*>(p.ring_k) + (grow * p.R + snew) * N * ES, lane * NPL);
     }
 
-    // this head's copies have landed (the next head's may still be in flight)
-    if (!__all_sync(kFull, mbar_wait(bar0 + 8u * buf, (phase >> buf) & 1u, abort_flag, p.err))) {
-      // leave after the copies still in flight into this warp's stages (bounded waits)
-      if (lane == 0) {
-        volatile int dummy = 0;
-        mbar_wait(bar0 + 8u * buf, (phase >> buf) & 1u, &dummy, p.err);
-        if (more) mbar_wait(bar0 + 8u * (buf ^ 1), (phase >> (buf ^ 1)) & 1u, &dummy, p.err);
-        // The heads from here on get no output or append. Their sequences keep their
-        // pointers, as after an aborted head-kernel CTA: the head kernel advances a
-        // sequence only when its ticket reaches H, and rssm_clear_error resets tickets.
-        const int b_last = (int)((h1 - 1) / p.H);
-        for (int b = cur.b; b <= b_last; ++b) atomicAdd(p.ticket + b, -(1 << 20));
-      }
-      __syncwarp();
-      return;
-    }
-    phase ^= 1u << buf;
-    const uint8_t* stg = wbase + kNfBarBytes + kNfRowSumBytes + (size_t)buf * sg.bytes;
+    // this head's tile and decays have landed (the next head's may still be in flight)
+    if (!wait_or_leave(buf, cur.b)) return;
+    const uint8_t* stg = tstage + (size_t)buf * sg.tbytes;
     const float* sa = reinterpret_cast<const float*>(stg + sg.a_off);
-    const uint8_t* sv = stg + sg.v_off;
 
     // -------------------------------------------------- decays and record weights
     // lane j: alpha_j (committed records in ring order, then the step's own), 1 past J
@@ -427,6 +462,7 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
     __syncwarp();
 
     // -------------------------------------------------- o = g (S q) + sum_j c_j v_j, row pairs
+    if (!wait_or_leave(2, cur.b)) return;  // this head's value rows
     const float* rscale = reinterpret_cast<const float*>(stg + p.rsc_off);
     for (int r0 = 0; r0 < p.P; r0 += 64) {
       const int r = r0 + 2 * lane;
@@ -458,7 +494,11 @@ __global__ void __launch_bounds__(kNfMaxThreads, 1) nonflush_kernel(const Params
         vc.store(reinterpret_cast<uint8_t*>(p.ring_v) + (hrow * p.R + snew) * (size_t)vrow, r);
       }
     }
-    __syncwarp();  // the stage and the row sums are rewritten by later heads
+    __syncwarp();  // the stages and the row sums are rewritten by later heads
+    if (more) {  // the value stage is free: the next head's rows
+      issue_values(nxt);
+      pend |= 4u;
+    }
     cur = nxt;
     acur = anxt;
     have = more;
