@@ -102,6 +102,14 @@ struct Raw {
   }
 };
 
+// The two E4M3 block scales of a 32-column chunk (bytes 0 and 1 of bs) as floats,
+// with one conversion (E4M3 values are exact in binary16 and in binary32).
+__device__ __forceinline__ float2 dec_e4m3x2(uint32_t bs) {
+  uint32_t h;
+  asm("{ .reg .b16 lo; cvt.u16.u32 lo, %1; cvt.rn.f16x2.e4m3x2 %0, lo; }" : "=r"(h) : "r"(bs));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
 // c + a.lo b.lo + a.hi b.hi for binary16 pairs a and b, accumulated in FP32: each
 // fma.rn.f32.f16 multiplies two exact binary16 values (an exact product in FP32)
 // and rounds once, the same as an FP32 fma of the two values.
@@ -145,7 +153,8 @@ __device__ __forceinline__ float chunk_dot_h(const uint4 u, const uint32_t* qh, 
 #pragma unroll
       for (int e = 0; e < 4; ++e) blk[qd >> 1] = fma_h2(h[e], qh[qd * 4 + e], blk[qd >> 1]);
     }
-    return fmaf(dec_e4m3(bs & 0xffu), blk[0], dec_e4m3((bs >> 8) & 0xffu) * blk[1]);
+    const float2 sc = dec_e4m3x2(bs);
+    return fmaf(sc.x, blk[0], sc.y * blk[1]);
   } else {  // FP16 checkpoint: eight halves
     float a0 = fma_h2(ws[0], qh[0], 0.f);
     float a1 = fma_h2(ws[1], qh[1], 0.f);
@@ -181,7 +190,8 @@ __device__ __forceinline__ float chunk_dot(const uint4 u, const float* qt, uint3
 #pragma unroll
       for (int e = 0; e < 8; ++e) blk[qd >> 1] = fmaf(f[e], qt[qd * 8 + e], blk[qd >> 1]);
     }
-    return fmaf(dec_e4m3(bs & 0xffu), blk[0], dec_e4m3((bs >> 8) & 0xffu) * blk[1]);
+    const float2 sc = dec_e4m3x2(bs);
+    return fmaf(sc.x, blk[0], sc.y * blk[1]);
   } else {  // FP16 checkpoint: eight halves
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
