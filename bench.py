@@ -22,6 +22,10 @@ Prints one JSON line. Keys beyond the driver contract:
                 gated delta-rule layer, decode windows reading
                 an E4M3 or E2M1 copy of the checkpoint, and decode windows of
                 a gated delta-rule layer of the same shape
+  static_scratch
+                the headline windows through the entry point that keeps its
+                tickets in a static device array, timed in alternating blocks
+                with the ordinary decode step on one layer
 
 The timed region covers at least --min-seconds of windows (default 1 s), and
 at least --steps of them, so that the clock sampler sees several samples.
@@ -355,8 +359,12 @@ class DecodeArm:
         self.decode_kernels = self.model.decode_kernel()
         self.kernels_per_step = 2 if self.decode_kernels == "warp_per_head" else 1
 
+    static_scratch = False  # decode steps through rssm_decode_step_static_scratch
+
     def step(self, x, o, st=None):
-        if self.delta:
+        if self.static_scratch:
+            self.model.decode_step_static_scratch(*x, out=o, stream=st)
+        elif self.delta:
             self.model.decode_step(*x[:4], out=o, beta=x[4], stream=st)
         else:
             self.model.decode_step(*x, out=o, stream=st)
@@ -615,7 +623,33 @@ def secondary_arms(args, world, rank, local) -> dict:
                     "gpu_launches": len(launch_s) * arm.kernels_per_step, "device_error_word": err}
         del arm
         torch.cuda.empty_cache()
+    out["static_scratch"] = static_scratch_arm(args, world, rank, local)
+    torch.cuda.empty_cache()
     return out
+
+
+def static_scratch_arm(args, world, rank, local, blocks: int = 4) -> dict:
+    """The headline workload stepped through rssm_decode_step_static_scratch (tickets in the
+    library's static array, cleared by a memset before every launch) and through
+    rssm_decode_step, in alternating blocks of windows on one layer."""
+    arm = DecodeArm(WORKLOAD, local, rank)
+    per_window = arm.warm(args.warmup)
+    n = max(1, windows_for(args.steps, per_window, args.extra_seconds) // blocks)
+    t = {False: 0.0, True: 0.0}
+    with ClockSampler(local) as clk:
+        for b in range(2 * blocks):
+            arm.static_scratch = b % 2 == 1
+            elapsed, _ = arm.timed(n, world)
+            t[arm.static_scratch] += max_over_ranks(elapsed, world)
+    err = arm.model.read_pointers()[2]
+    units = world * WORKLOAD.B * WORKLOAD.L * n * blocks
+    res = {"value": units / t[True], "unit": UNIT, "windows_timed": n * blocks,
+           "ms_per_window": t[True] / (n * blocks) * 1e3,
+           "decode_step_ms_per_window": t[False] / (n * blocks) * 1e3,
+           "decode_step_value": units / t[False], "clocks": clk.summary(),
+           "gpu_launches": 2 * n * blocks * WORKLOAD.L * arm.kernels_per_step, "device_error_word": err}
+    del arm
+    return res
 
 
 def run_reference(args, world, rank):

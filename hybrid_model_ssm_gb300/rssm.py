@@ -263,6 +263,22 @@ class ReplaySSM:
                                                     _ptr(out), _stream_ptr(stream)))
         return out
 
+    def decode_step_static_scratch(self, alpha, v, k, q, out=None, stream=None) -> torch.Tensor:
+        """One decode step of an outer-product layer with its tickets in the library's
+        static device array instead of the pointer block (B <= 8192)."""
+        s, d = self.shape, self.ckpt.device
+        _expect(alpha, (s.B, s.H), torch.float32, "alpha", d)
+        _expect(v, (s.B, s.H, s.P), s.torch_in_dtype, "v", d)
+        _expect(k, (s.B, s.G, s.N), s.torch_in_dtype, "k", d)
+        _expect(q, (s.B, s.G, s.N), s.torch_in_dtype, "q", d)
+        if out is None:
+            out = torch.empty((s.B, s.H, s.P), dtype=torch.float32, device=d)
+        _expect(out, (s.B, s.H, s.P), torch.float32, "out", d)
+        with self._on_device():
+            _check(lib().rssm_decode_step_static_scratch(self._h, _ptr(alpha), _ptr(v), _ptr(k), _ptr(q),
+                                                         _ptr(out), _stream_ptr(stream)))
+        return out
+
     def verify(self, alpha, v, k, q, out=None, stream=None, beta=None) -> torch.Tensor:
         """Speculative verify of T drafts; a delta-rule layer also takes beta [B,T,H] fp32."""
         s, d = self.shape, self.ckpt.device

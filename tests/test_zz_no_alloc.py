@@ -101,3 +101,27 @@ def test_static_scratch_refusals():
     assert _static_step(dmodel, a, v, k, k, o) == RSSM_EUNSUPPORTED
     assert "outer-product" in lib().rssm_last_error().decode()
     torch.cuda.synchronize()
+
+
+def test_static_scratch_binding_read_copy_two_kernels():
+    """Through the Python binding, on an E4M3 read-copy layer with bf16 inputs (the
+    warp-per-head kernel, then the head kernel): a window, a flush and two more steps, with
+    outputs, pointers and checkpoint identical bit for bit to rssm_decode_step on a twin layer
+    (the two calls differ only in where the tickets live)."""
+    require_gpu()
+    shape = synth.Shape(B=6, H=8, P=64, N=128, G=2, L=4, in_dtype="bf16", seed=92)
+    gen = synth.make_generator(shape.seed)
+    S0 = synth.initial_state(shape, gen)
+    ref = ReplaySSM(layer_shape(shape, "e4m3"), dev(S0))
+    alt = ReplaySSM(layer_shape(shape, "e4m3"), dev(S0))
+    assert alt.decode_kernel() == "warp_per_head"
+    for t in range(shape.L + 2):
+        a, v, k, q = (dev(x) for x in synth.decode_step_inputs(shape, gen))
+        o_ref = ref.decode_step(a, v, k, q)
+        o_alt = alt.decode_step_static_scratch(a, v, k, q)
+        assert torch.equal(o_alt, o_ref), f"step {t}"
+        s_ref, c_ref, e_ref = ref.read_pointers()
+        s_alt, c_alt, e_alt = alt.read_pointers()
+        assert e_ref == 0 and e_alt == 0
+        assert torch.equal(s_ref, s_alt) and torch.equal(c_ref, c_alt), f"step {t}: pointers differ"
+    assert torch.equal(alt.ckpt, ref.ckpt)
