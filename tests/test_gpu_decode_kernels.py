@@ -30,9 +30,13 @@ from tests.test_gpu_readcopy import _dequantized_copy
 pytestmark = pytest.mark.gpu
 
 S = synth.Shape
-# (format, N, input dtype, P): tiles from 2 KiB (E4M3 P=32 N=64) to 16 KiB (FP16)
+# (format, N, input dtype, P): tiles from 0.5 KiB (E4M3 P=8 N=64) to 16 KiB (FP16), and head
+# dimensions that are no power of two (a row pass over 24 or 120 rows, one ragged
+# group of chunk rows, value rows of 48 or 240 bytes)
 CASES = [("e4m3", 64, "bf16", 32), ("e4m3", 128, "f32", 32), ("e4m3", 128, "bf16", 64), ("e2m1", 64, "f32", 32),
-         ("e2m1", 128, "bf16", 64), ("e2m1", 128, "bf16", 128), ("f16_sr", 128, "bf16", 32), ("f16_rn", 64, "f32", 32)]
+         ("e2m1", 128, "bf16", 64), ("e2m1", 128, "bf16", 128), ("f16_sr", 128, "bf16", 32), ("f16_rn", 64, "f32", 32),
+         ("e4m3", 64, "f32", 8), ("e4m3", 128, "bf16", 24), ("e2m1", 64, "bf16", 120), ("e2m1", 128, "f32", 40),
+         ("f16_rn", 64, "bf16", 24)]
 
 
 def _model(shape, fmt, S0, kernel):
