@@ -405,28 +405,30 @@ int verify_kernel_for(const rssm_ctx* h, int T) {
 
 // The warp-per-head non-flush step serves the small head tiles: an E4M3 or E2M1
 // read copy, or an FP16 checkpoint (N in {64, 128}, outer-product recurrence).
-bool nonflush_applies_fmt(const rssm_ctx* h) {
-  return h->g.rf == rssm::kRfE4m3 || h->g.rf == rssm::kRfE2m1 || h->g.rf == rssm::kCkF16;
+bool nonflush_applies_fmt(const Geom& g) {
+  return g.rf == rssm::kRfE4m3 || g.rf == rssm::kRfE2m1 || g.rf == rssm::kCkF16;
 }
 
 // The per-warp stages of the warp-per-head step, and how many warps fit a CTA.
-rssm::NfStage nonflush_stage(const rssm_ctx* h) {
-  const rssm_config& c = h->cfg;
-  const int tile = h->g.rf == rssm::kCkF16 ? c.P * c.N * 2 : (int)h->g.head_stride;
-  return rssm::nf_stage(tile, c.L, h->g.Rp, c.P, h->g.esize);
+rssm::NfStage nonflush_stage(const rssm_config& c, const Geom& g) {
+  const int tile = g.rf == rssm::kCkF16 ? c.P * c.N * 2 : (int)g.head_stride;
+  return rssm::nf_stage(tile, c.L, g.Rp, c.P, g.esize);
 }
 int nonflush_warps(const rssm::NfStage& sg) {
   return std::min(rssm::kNfMaxWarps, (rssm::kSmemMax - rssm::kNfCtaBytes) / rssm::nf_warp_bytes(sg));
 }
+size_t nonflush_smem(const rssm::NfStage& sg, int warps) {
+  return rssm::kNfCtaBytes + (size_t)warps * rssm::nf_warp_bytes(sg);
+}
 
-bool nonflush_applies(const rssm_ctx* h) {
-  return nonflush_applies_fmt(h) && nonflush_warps(nonflush_stage(h)) >= 1;
+bool nonflush_applies(const rssm_config& c, const Geom& g) {
+  return nonflush_applies_fmt(g) && nonflush_warps(nonflush_stage(c, g)) >= 1;
 }
 
 // Which decode kernels a step launches: 2 the warp-per-head non-flush step and
 // then the head kernel for the flushing sequences, 1 the head kernel alone.
 int decode_kernel_for(const rssm_ctx* h) {
-  if (!nonflush_applies(h) || h->decode_kernel == 1) return 1;
+  if (!nonflush_applies(h->cfg, h->g) || h->decode_kernel == 1) return 1;
   if (h->decode_kernel == 2) return 2;
   // automatic: the read copies; an FP16 checkpoint's 16 KiB tiles fit too few
   // warps per SM, and the head kernel alone measures as fast there
@@ -437,12 +439,12 @@ int decode_kernel_for(const rssm_ctx* h) {
 cudaError_t launch_decode_step(const rssm_ctx* h, rssm::Params& p, size_t smem, cudaStream_t st) {
   const long long heads = (long long)h->cfg.B * h->cfg.H;
   if (decode_kernel_for(h) == 2) {
-    const rssm::NfStage sg = nonflush_stage(h);
+    const rssm::NfStage sg = nonflush_stage(h->cfg, h->g);
     const int warps = nonflush_warps(sg);
     const long long want = (heads + warps - 1) / warps;
     const int grid = (int)std::max(1ll, std::min<long long>(want, (long long)std::max(1, sm_count())));
-    const size_t smem = rssm::kNfCtaBytes + (size_t)warps * rssm::nf_warp_bytes(sg);
-    const cudaError_t e = rssm::launch_nonflush(p, sg, grid, warps, smem, st, h->cfg.N, h->cfg.in_dtype, h->g.rf);
+    const cudaError_t e =
+        rssm::launch_nonflush(p, sg, grid, warps, nonflush_smem(sg, warps), st, h->cfg.N, h->cfg.in_dtype, h->g.rf);
     if (e != cudaSuccess) return e;
     p.skip_nonflush = 1;
   }
@@ -489,11 +491,27 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
 
 rssm_status rssm_launch_plan(const rssm_config* cfg, int32_t kind, rssm_launch_plan_info* out) {
   if (!out) return fail(RSSM_EINVAL, "out is NULL");
-  if (kind < 0 || kind > 3)
-    return fail(RSSM_EINVAL, "kind=%d (0 flush, 1 decode, 2 verify, 3 tensor-core verify)", kind);
+  if (kind < 0 || kind > 4)
+    return fail(RSSM_EINVAL, "kind=%d (0 flush, 1 decode, 2 verify, 3 tensor-core verify, 4 warp-per-head step)",
+                kind);
   Geom g;
   rssm_status s = derive(cfg, &g);
   if (s != RSSM_OK) return s;
+  if (kind == 4) {
+    if (!nonflush_applies_fmt(g))
+      return fail(RSSM_EUNSUPPORTED, "the warp-per-head non-flush step serves read copies and FP16 checkpoints");
+    const rssm::NfStage sg = nonflush_stage(*cfg, g);
+    const int warps = nonflush_warps(sg);
+    if (warps < 1) return fail(RSSM_EUNSUPPORTED, "one warp's stages do not fit a CTA's shared memory");
+    *out = rssm_launch_plan_info{};
+    out->smem_bytes = (int64_t)nonflush_smem(sg, warps);
+    out->stages[0] = 2;
+    out->stage_bytes[0] = sg.tbytes;
+    out->slots[0] = 1;
+    out->slot_bytes[0] = sg.vbytes;
+    out->dgroups[0] = warps;
+    return RSSM_OK;
+  }
   if (kind >= 2 && cfg->T_max < 2) return fail(RSSM_EINVAL, "verify launches need T_max > 1");
   if (kind == 3 && cfg->recurrence != RSSM_GATED_OUTER)
     return fail(RSSM_EINVAL, "the tensor-core verify serves the outer-product recurrence");
@@ -722,7 +740,7 @@ rssm_status rssm_set_decode_kernel(rssm_handle h, int32_t kind) {
   if (!h) return fail(RSSM_EINVAL, "handle is NULL");
   if (kind < 0 || kind > 2)
     return fail(RSSM_EINVAL, "kind=%d (0 automatic, 1 head kernel only, 2 warp-per-head non-flush step)", kind);
-  if (kind == 2 && !nonflush_applies(h))
+  if (kind == 2 && !nonflush_applies(h->cfg, h->g))
     return fail(RSSM_EUNSUPPORTED, "the warp-per-head non-flush step serves read copies and FP16 checkpoints");
   h->decode_kernel = kind;
   return RSSM_OK;

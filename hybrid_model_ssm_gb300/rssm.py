@@ -165,14 +165,16 @@ def read_copy_layout(shape: LayerShape) -> tuple[int, int, int]:
     return a.value, b.value, d.value
 
 
-LAUNCH_KINDS = {"flush": 0, "decode": 1, "verify": 2, "verify_tc": 3}
+LAUNCH_KINDS = {"flush": 0, "decode": 1, "verify": 2, "verify_tc": 3, "warp_per_head": 4}
 VERIFY_KERNELS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 DECODE_KERNELS = {"auto": 0, "head_kernel": 1, "warp_per_head": 2}
 
 
 def launch_plan(shape: LayerShape, kind: str) -> dict:
-    """Shared-memory plan of a launch kind ("flush", "decode", "verify", "verify_tc"): smem
-    bytes and, per layout, stages, stage bytes, slots, slot bytes and dot-warp groups."""
+    """Shared-memory plan of a launch kind ("flush", "decode", "verify", "verify_tc",
+    "warp_per_head"): smem bytes and, per layout, stages, stage bytes, slots, slot bytes and
+    dot-warp groups (for "warp_per_head": two tile stages and one value stage per warp, and
+    the warps per CTA in dgroups)."""
     c = shape.config()
     info = LaunchPlanInfo()
     _check(lib().rssm_launch_plan(ctypes.byref(c), LAUNCH_KINDS[kind], ctypes.byref(info)))

@@ -170,7 +170,14 @@ rssm_status rssm_read_copy_layout(const rssm_config* cfg, size_t* head_stride, s
  *   kind 3: verify on the tensor cores at T = T_max (needs T_max > 1 and a
  *           configuration it serves): stages[0] K-block stages of
  *           stage_bytes[0] = 16 KiB (32 checkpoint columns of 128 rows),
- *           slots[0] record slots of slot_bytes[0], dgroups[0] = 0.
+ *           slots[0] record slots of slot_bytes[0], dgroups[0] = 0;
+ *   kind 4: the warp-per-head non-flush decode step (read copies and FP16
+ *           checkpoints; RSSM_EUNSUPPORTED otherwise): dgroups[0] warps per
+ *           CTA, each with stages[0] = 2 tile stages of stage_bytes[0] (the
+ *           head's tile, then the ring's decays at the next 16-byte boundary)
+ *           and slots[0] = 1 value stage of slot_bytes[0] (the L - 1 value
+ *           rows a non-flush step can read); smem_bytes adds the CTA's abort
+ *           flag and each warp's barriers and row sums.
  * Per layout: checkpoint tile stages (stage_bytes each), record slots
  * (slot_bytes each) and the number of dot-warp groups, i.e. heads in flight.
  * Both ring lengths are multiples of the number of consumers that take their

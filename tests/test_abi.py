@@ -158,6 +158,51 @@ def test_launch_plans_keep_the_ring_rule_over_the_size_grid(lib):
     assert planned > 500 and refused > 100
 
 
+def test_warp_per_head_plans_over_the_size_grid(lib):
+    """Host planner of the warp-per-head non-flush step (no CUDA call): for every accepted
+    read-copy or FP16 configuration of the grid, each warp's two tile stages hold the head's
+    tile (the copy's head stride, or P x N binary16 values) and the ring's decays at the next
+    16-byte boundary, its value stage holds the L - 1 value rows a non-flush step can read,
+    and the CTA takes as many warps as 227 KiB allow, up to 16. Other layers have no such plan."""
+    from hybrid_model_ssm_gb300 import launch_plan
+    smem_max, cta_bytes, bar_bytes = 227 * 1024, 128, 32
+    planned = 0
+    for N in (64, 128):
+        for P in (8, 24, 64, 120, 128):
+            for L, T in ((1, 1), (2, 1), (4, 1), (16, 1), (32, 1), (16, 4), (25, 8)):
+                for dt, es in (("f32", 4), ("bf16", 2)):
+                    for fmt in ("e4m3", "e2m1", "f16_sr", "f16_rn"):
+                        kw = dict(ckpt=fmt) if fmt.startswith("f16") else dict(read_fmt=fmt)
+                        shape = LayerShape(B=3, H=4, P=P, N=N, G=2, L=L, T_max=T, in_dtype=dt, **kw)
+                        try:
+                            workspace_size(shape)
+                        except RssmError:
+                            continue
+                        plan = launch_plan(shape, "warp_per_head")
+                        (lay,) = plan["layouts"]
+                        tile = P * N * 2 if fmt.startswith("f16") else read_copy_layout(shape)[0]
+                        Rp = (L + T - 1 + 3) // 4 * 4
+                        warps = lay["dgroups"]
+                        assert lay["stages"] == 2 and lay["slots"] == 1
+                        assert lay["stage_bytes"] % 128 == 0 and lay["slot_bytes"] % 128 == 0
+                        assert lay["stage_bytes"] >= (tile + 15) // 16 * 16 + 4 * Rp
+                        assert lay["slot_bytes"] >= max(L - 1, 1) * P * es
+                        per_warp = bar_bytes + (P * 4 + 127) // 128 * 128 + 2 * lay["stage_bytes"] + lay["slot_bytes"]
+                        assert plan["smem_bytes"] == cta_bytes + warps * per_warp <= smem_max, (shape, plan)
+                        assert 1 <= warps <= 16
+                        assert warps == 16 or cta_bytes + (warps + 1) * per_warp > smem_max, (shape, plan)
+                        planned += 1
+    assert planned > 200
+    # the read-copy decode workload (B=256 H=128 P=64 N=128 G=8 L=16, bf16 inputs):
+    # 12 warps per CTA with an E4M3 copy, 16 with an E2M1 copy
+    for fmt, warps in (("e4m3", 12), ("e2m1", 16)):
+        shape = LayerShape(B=256, H=128, P=64, N=128, G=8, L=16, in_dtype="bf16", read_fmt=fmt)
+        assert launch_plan(shape, "warp_per_head")["layouts"][0]["dgroups"] == warps
+    for kw in (dict(), dict(recurrence="delta")):
+        with pytest.raises(RssmError, match="EUNSUPPORTED"):
+            launch_plan(LayerShape(B=2, H=4, P=64, N=128, G=2, L=16, **kw), "warp_per_head")
+
+
 def test_null_config_and_handle(lib):
     lib.rssm_workspace_size.restype = ctypes.c_int
     assert lib.rssm_workspace_size(None, None, None, None) == RSSM_EINVAL
