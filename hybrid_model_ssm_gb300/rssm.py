@@ -349,6 +349,8 @@ class ReplaySSM:
                 int(err.value))
 
     def clear_error(self, stream=None):
+        """Zero the device error word and the per-sequence tickets (after a launch that
+        gave up on a wait); enqueued on the stream."""
         with torch.cuda.device(self.ckpt.device):
             _check(lib().rssm_clear_error(self._h, _stream_ptr(stream)))
 
