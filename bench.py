@@ -15,13 +15,16 @@ Prints one JSON line. Keys beyond the driver contract:
   e2e           the same metric with inputs copied from pinned host memory and
                 outputs copied back inside the timed region
   comparison    the conventional read-update-write kernel on the same workload
-  verify_b512_t4, delta_verify_b512_t4, read_copy_e4m3, read_copy_e2m1, delta_rule
+  verify_b512_t4, delta_verify_b512_t4, read_copy_e4m3, read_copy_e2m1, delta_rule,
+  ckpt_f16_sr, ckpt_f16_rn
                 the secondary arms of the path, each with its own roofline
                 block: speculative rounds (verify + commit + flush, B=512,
                 T=4) against the snapshot comparator, the same rounds of a
                 gated delta-rule layer, decode windows reading
-                an E4M3 or E2M1 copy of the checkpoint, and decode windows of
-                a gated delta-rule layer of the same shape
+                an E4M3 or E2M1 copy of the checkpoint, decode windows of
+                a gated delta-rule layer of the same shape, and decode windows
+                with the checkpoint stored as binary16 (stochastic rounding,
+                or rounding to nearest)
   static_scratch
                 the headline windows through the entry point that keeps its
                 tickets in a static device array, timed in alternating blocks
@@ -590,8 +593,9 @@ def run_ours(args, world, rank, local):
 
 
 def secondary_arms(args, world, rank, local) -> dict:
-    """The verify round, the two read-copy decodes and the delta-rule decode, each timed
-    for at least --extra-seconds, with the roofline of its dominant launch."""
+    """The verify rounds, the read-copy, delta-rule and FP16-checkpoint decodes and the
+    static-scratch step, each timed for at least --extra-seconds, with the roofline of
+    its dominant launch."""
     out = {}
     peak, peak_kind = measured_peak_gbs()
     vargs = argparse.Namespace(**vars(args))
@@ -607,7 +611,8 @@ def secondary_arms(args, world, rank, local) -> dict:
                                           "device_error_word") if k in v}
             out[key]["rounds_timed"] = v["config"]["rounds_timed"]
     for key, kw in (("read_copy_e4m3", {"read_fmt": "e4m3"}), ("read_copy_e2m1", {"read_fmt": "e2m1"}),
-                    ("delta_rule", {"recurrence": "delta"})):
+                    ("delta_rule", {"recurrence": "delta"}), ("ckpt_f16_sr", {"ckpt": "f16_sr"}),
+                    ("ckpt_f16_rn", {"ckpt": "f16_rn"})):
         arm = DecodeArm(WORKLOAD, local, rank, **kw)
         per_window = arm.warm(args.warmup)
         n = windows_for(args.steps, per_window, args.extra_seconds)
@@ -1016,7 +1021,7 @@ def main(argv=None):
     ap.add_argument("--no-clocks", action="store_true",
                     help="do not sample clocks with nvidia-smi (profiler runs)")
     ap.add_argument("--no-extras", action="store_true",
-                    help="leave out the secondary arms (verify, read copies, delta rule) of the default line")
+                    help="leave out the secondary arms (verify, read copies, delta rule, FP16 checkpoints, static scratch) of the default line")
     args = ap.parse_args(argv)
     if args.recurrence == "delta" and (args.workload == "multilayer" or args.read_fmt or args.ckpt != "f32"):
         ap.error("--recurrence delta: decode or verify workload, FP32 checkpoint, no read copy")
