@@ -71,6 +71,31 @@ def test_max_over_ranks_with_two_gloo_ranks():
     assert dict(results) == {0: 20.0, 1: 20.0}
 
 
+def _reference_rank(rank, world, port, results):
+    import contextlib
+    import io
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), LOCAL_RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        bench.main(["--impl", "reference", "--gpus", str(world), "--steps", "1", "--warmup", "3"])
+    results[rank] = out.getvalue()
+
+
+def test_reference_arm_under_two_gloo_ranks():
+    """Launched as torchrun replicas, the reference arm runs on rank 0 alone, which prints
+    the one JSON line (n_gpus = world size); the other rank prints nothing and exits."""
+    import json
+    world = 2
+    results = mp.Manager().dict()
+    mp.start_processes(_reference_rank, args=(world, _free_port(), results), nprocs=world, start_method="spawn")
+    assert results[1] == ""
+    lines = results[0].strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == world and line["value"] > 0
+
+
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     bench.barrier(1)
